@@ -1,0 +1,216 @@
+"""Scheduler oracle: a plain restatement of the per-pass schedule() the pages describe.
+
+Test infrastructure only (see the package docstring).  Follows "Continuous Batching Is Not a Bigger
+Batch" (deepconcepts.dev), section "What the scheduler does on one step":
+
+* Phase one walks the running requests in arrival order.  Each wants num_tokens - num_computed_tokens
+  (one while decoding, the rest of the prompt while prefilling), capped by the pass's token budget:
+  chunked prefill, no separate prefill phase.
+* For each it allocates the blocks those tokens need.  On failure it pops the LAST running request
+  (the newest), frees its blocks, marks it PREEMPTED, resets num_computed_tokens to 0 and prepends it to
+  the waiting queue; then it retries.  If the popped request is the one being scheduled, phase one ends
+  (reading: the pages show only the pop; this is the plain consequence).
+* Phase two admits from the head of the waiting queue, only if the pass preempted nobody, while the
+  token budget lasts and while the running count is below max_num_seqs -- the cap is read only there
+  ("Saturation and Capacity", section "Runtime capacity control": lowering it drains, never evicts).
+* Blocks are 16-token units handed out on demand from a free list
+  (same page, sections "Where the batch size actually comes from" and "The allocator is the other half").
+
+Readings where the pages are silent (listed in the design notes): the waiting queue is strict FIFO with
+head-of-line blocking (an unallocatable head stops admission for the pass); a pass that computes a
+request's last known token yields one output token; a request finishes when its outputs reach its
+budget and frees its blocks the same pass; freed blocks go to the tail of the free list in block-table
+order; the token budget is shared by both phases.
+"""
+from __future__ import annotations
+
+import collections
+import dataclasses
+from typing import Deque, List, Optional, Sequence
+
+import numpy as np
+
+from .paging import slot_of
+
+WAITING, RUNNING, PREEMPTED, FINISHED = "WAITING", "RUNNING", "PREEMPTED", "FINISHED"
+
+
+@dataclasses.dataclass(eq=False)
+class Request:
+    req_id: int
+    prompt_len: int
+    max_output: int
+    num_computed: int = 0
+    num_output: int = 0
+    status: str = WAITING
+    blocks: List[int] = dataclasses.field(default_factory=list)
+
+    @property
+    def num_tokens(self) -> int:
+        """Tokens whose K/V the request needs: the prompt plus outputs generated so far."""
+        return self.prompt_len + self.num_output
+
+
+@dataclasses.dataclass
+class StepRows:
+    """The ragged batch one pass hands to the GPU, rows in scheduling order."""
+    req_ids: np.ndarray        # int64 [B]
+    q_lens: np.ndarray         # int32 [B]
+    context_lens: np.ndarray   # int32 [B]  num_computed before the pass + q_len
+    block_tables: np.ndarray   # int32 [B, max_blocks], -1 padded
+    slot_mapping: np.ndarray   # int64 [T]
+    preempted: List[int]
+    admitted: List[int]
+    finished: List[int]
+
+
+class Scheduler:
+    def __init__(self, max_num_seqs: int, token_budget: int, block_size: int, free_blocks: Sequence[int]):
+        if max_num_seqs < 1:
+            raise ValueError("max_num_seqs must be at least 1")
+        if token_budget < 1 or block_size < 1:
+            raise ValueError("token_budget and block_size must be positive")
+        self.max_num_seqs = max_num_seqs
+        self.token_budget = token_budget
+        self.block_size = block_size
+        self.num_blocks = len(free_blocks)
+        self.free: Deque[int] = collections.deque(int(b) for b in free_blocks)
+        self.running: List[Request] = []
+        self.waiting: Deque[Request] = collections.deque()
+        self.by_id = {}
+        # statistics
+        self.steps = 0
+        self.num_preemptions = 0
+        self.recomputed_tokens = 0
+        self.recomputed_prompt_tokens = 0
+        self.max_batch = 0
+        self.batch_sum = 0
+        self.tokens_scheduled = 0
+
+    # --- allocator -----------------------------------------------------------------------------------
+    def _allocate(self, req: Request, num_new: int) -> bool:
+        need = -(-(req.num_computed + num_new) // self.block_size) - len(req.blocks)
+        if need > len(self.free):
+            return False
+        for _ in range(max(need, 0)):
+            req.blocks.append(self.free.popleft())
+        return True
+
+    def _free(self, req: Request) -> None:
+        self.free.extend(req.blocks)
+        req.blocks = []
+
+    # --- requests ------------------------------------------------------------------------------------
+    def add(self, req_id: int, prompt_len: int, max_output: int) -> None:
+        if prompt_len < 1 or max_output < 1:
+            raise ValueError("prompt_len and max_output must be positive")
+        req = Request(req_id, prompt_len, max_output)
+        self.by_id[req_id] = req
+        self.waiting.append(req)
+
+    def abort(self, req_id: int) -> None:
+        """A cancelled request leaves no blocks behind ("An advertised batch limit proves nothing until
+        sampled", section "Counting jobs while they run")."""
+        req = self.by_id.pop(req_id)
+        if req in self.running:
+            self.running.remove(req)
+        if req in self.waiting:
+            self.waiting.remove(req)
+        self._free(req)
+        req.status = FINISHED
+
+    def set_max_num_seqs(self, n: int) -> None:
+        if n < 1:
+            raise ValueError("max_num_seqs must be at least 1")
+        self.max_num_seqs = n
+
+    def done(self) -> bool:
+        return not self.running and not self.waiting
+
+    # --- one pass ------------------------------------------------------------------------------------
+    def step(self) -> StepRows:
+        budget = self.token_budget
+        scheduled = []          # (request, num_new, num_computed before the pass)
+        preempted: List[Request] = []
+        admitted: List[int] = []
+
+        # phase one: running requests, arrival order
+        i = 0
+        while i < len(self.running) and budget > 0:
+            req = self.running[i]
+            num_new = min(req.num_tokens - req.num_computed, budget)
+            schedulable = True
+            while not self._allocate(req, num_new):
+                victim = self.running.pop()
+                self._free(victim)
+                victim.status = PREEMPTED
+                self.recomputed_tokens += victim.num_computed
+                self.recomputed_prompt_tokens += min(victim.num_computed, victim.prompt_len)
+                victim.num_computed = 0
+                self.waiting.appendleft(victim)
+                preempted.append(victim)
+                if victim is req:
+                    schedulable = False
+                    break
+            if not schedulable:
+                break
+            scheduled.append((req, num_new, req.num_computed))
+            budget -= num_new
+            i += 1
+
+        # phase two: admission, only when nothing was preempted
+        if not preempted:
+            while self.waiting and budget > 0:
+                if len(self.running) >= self.max_num_seqs:
+                    break
+                req = self.waiting[0]
+                num_new = min(req.num_tokens - req.num_computed, budget)
+                if not self._allocate(req, num_new):
+                    break
+                self.waiting.popleft()
+                req.status = RUNNING
+                self.running.append(req)
+                admitted.append(req.req_id)
+                scheduled.append((req, num_new, req.num_computed))
+                budget -= num_new
+
+        rows = self._rows(scheduled)
+        rows.preempted = [r.req_id for r in preempted]
+        rows.admitted = admitted
+        self.num_preemptions += len(preempted)
+
+        # the forward pass has run: advance each scheduled request
+        finished = []
+        for req, num_new, _ in scheduled:
+            req.num_computed += num_new
+            if req.num_computed == req.num_tokens:
+                req.num_output += 1
+                if req.num_output >= req.max_output:
+                    self.running.remove(req)
+                    self._free(req)
+                    req.status = FINISHED
+                    finished.append(req.req_id)
+        rows.finished = finished
+        self.steps += 1
+        self.max_batch = max(self.max_batch, len(scheduled))
+        self.batch_sum += len(scheduled)
+        self.tokens_scheduled += int(rows.q_lens.sum()) if len(scheduled) else 0
+        return rows
+
+    def _rows(self, scheduled) -> StepRows:
+        B = len(scheduled)
+        bs = self.block_size
+        max_blocks = max([len(r.blocks) for r, _, _ in scheduled] + [1])
+        req_ids = np.zeros(B, dtype=np.int64)
+        q_lens = np.zeros(B, dtype=np.int32)
+        ctx = np.zeros(B, dtype=np.int32)
+        bt = np.full((B, max_blocks), -1, dtype=np.int32)
+        slots = []
+        for b, (req, num_new, start) in enumerate(scheduled):
+            req_ids[b] = req.req_id
+            q_lens[b] = num_new
+            ctx[b] = start + num_new
+            bt[b, : len(req.blocks)] = req.blocks
+            for p in range(start, start + num_new):
+                slots.append(slot_of(req.blocks, p, bs))
+        return StepRows(req_ids, q_lens, ctx, bt, np.asarray(slots, dtype=np.int64), [], [], [])

@@ -1,0 +1,133 @@
+"""Pins for the scheduler oracle: hand-worked traces and the behaviour rules the pages state."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from continuous_batching_paged_ragged_gb300 import synth
+
+TRACES = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "sched_traces.json")))["traces"]
+
+
+def _run(trace):
+    s = oracle.Scheduler(trace["max_num_seqs"], trace["token_budget"], trace["block_size"], trace["free_blocks"])
+    for rid, p, o in trace["requests"]:
+        s.add(rid, p, o)
+    steps = []
+    while not s.done():
+        steps.append(s.step())
+        assert len(steps) < 1000
+    return s, steps
+
+
+@pytest.mark.parametrize("trace", TRACES, ids=[t["name"] for t in TRACES])
+def test_hand_worked_trace(trace):
+    s, steps = _run(trace)
+    assert len(steps) == len(trace["steps"])
+    for got, want in zip(steps, trace["steps"]):
+        rows = [[int(got.req_ids[b]), int(got.q_lens[b]), int(got.context_lens[b]),
+                 [int(x) for x in got.block_tables[b] if x >= 0]] for b in range(len(got.req_ids))]
+        assert rows == [r[:4] for r in want["rows"]]
+        assert got.slot_mapping.tolist() == [x for r in want["rows"] for x in r[4]]
+        assert got.preempted == want["preempted"]
+        assert sorted(got.finished) == sorted(want["finished"])
+    assert list(s.free) == trace["final_free"]
+    assert s.num_preemptions == trace["preemptions"]
+    assert s.recomputed_tokens == trace["recomputed"]
+
+
+def _trace_sched(num_blocks, cap, seed=0, n=64):
+    reqs = synth.trace_requests(seed, n=n)
+    s = oracle.Scheduler(cap, 8192, 16, synth.block_permutation(num_blocks, seed))
+    for r in reqs:
+        s.add(r.req_id, r.prompt_len, r.max_output)
+    return s, reqs
+
+
+def test_invariants_along_a_pressured_trace():
+    """Block conservation, budget, per-row block counts, exactly one output per finished token stream."""
+    s, reqs = _trace_sched(num_blocks=600, cap=64)
+    seen_preempt = 0
+    while not s.done():
+        running_before = list(s.running)
+        rows = s.step()
+        assert int(rows.q_lens.sum()) <= s.token_budget
+        held = [b for r in s.running for b in r.blocks] + [b for r in s.waiting for b in r.blocks]
+        assert len(held) == len(set(held))
+        assert len(held) + len(s.free) == s.num_blocks
+        assert not set(held) & set(s.free)
+        for r in s.running:
+            assert len(r.blocks) == -(-r.num_computed // 16)
+        for r in s.waiting:
+            assert r.blocks == [] and r.num_computed == 0
+        if rows.preempted:
+            seen_preempt += 1
+            assert rows.admitted == []                      # a preempting pass admits nobody
+            # victims are the newest running requests, taken from the back
+            tail = [r.req_id for r in running_before][-len(rows.preempted):][::-1]
+            assert rows.preempted == tail
+        assert s.steps < 100000
+    assert seen_preempt > 0
+    assert all(r.num_output == r.max_output for r in s.by_id.values())
+
+
+def test_preempted_request_restarts_from_zero():
+    s, _ = _trace_sched(num_blocks=600, cap=64)
+    while not s.done():
+        before = {r.req_id: r.num_output for r in s.running}
+        rows = s.step()
+        for rid in rows.preempted:
+            r = s.by_id[rid]
+            assert r.num_computed == 0 and r.status == "PREEMPTED"
+            assert r.num_output == before[rid]                # generated outputs are kept, K/V recomputed
+        # a readmitted request's first row re-prefills prompt + outputs from position 0
+        for b, rid in enumerate(rows.req_ids.tolist()):
+            if rid in rows.admitted:
+                assert rows.context_lens[b] == rows.q_lens[b]
+
+
+def test_cap_gates_admission_only_and_lowering_drains():
+    s, _ = _trace_sched(num_blocks=20000, cap=32)
+    for _ in range(5):
+        s.step()
+    assert len(s.running) == 32
+    s.set_max_num_seqs(8)
+    rows = s.step()
+    assert len(rows.req_ids) == 32 and rows.preempted == []   # nobody evicted
+    while len(s.running) > 8:
+        rows = s.step()
+        assert rows.admitted == []
+    with pytest.raises(ValueError):
+        s.set_max_num_seqs(0)
+
+
+def test_decode_wants_one_token_and_prefill_is_chunked():
+    s = oracle.Scheduler(8, 100, 16, list(range(100)))
+    s.add(0, 250, 3)
+    r1 = s.step()
+    r2 = s.step()
+    r3 = s.step()
+    assert (r1.q_lens.tolist(), r2.q_lens.tolist(), r3.q_lens.tolist()) == ([100], [100], [50])
+    r4 = s.step()
+    assert r4.q_lens.tolist() == [1] and r4.context_lens.tolist() == [251]
+
+
+def test_abort_frees_every_block():
+    s, _ = _trace_sched(num_blocks=3000, cap=64)
+    for _ in range(4):
+        s.step()
+    victim = s.running[3].req_id
+    s.abort(victim)
+    held = [b for r in s.running for b in r.blocks]
+    assert len(held) + len(s.free) == s.num_blocks
+    assert victim not in [r.req_id for r in s.running]
+
+
+def test_no_preemption_when_pool_is_large():
+    s, reqs = _trace_sched(num_blocks=20000, cap=256, n=256)
+    while not s.done():
+        s.step()
+    assert s.num_preemptions == 0
+    assert s.max_batch == 256
