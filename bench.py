@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Benchmark of one forward pass's hot path: per layer kv_append + ragged paged GQA attention.
+
+Default workload: the Qwen2.5-1.5B-shaped decode batch (28 layers, 12 q / 2 KV heads, head_dim 128,
+256 rows with contexts uniform in [256, 768] plus one new token, blocks of 16 scattered over a pool 1.25x
+the need, fp16 values from the seeded generator).  A step = one attention plan + 28 x (append + attention).
+
+Prints one JSON line (rank 0).  `value` is algorithmic HBM bytes per second of the whole step (K/V read
+once per row and layer, q read, output written, block tables, append traffic); `ctx_tokens_per_s` is the
+number of context tokens attended per second.  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import os
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")   # the oracle legs are single-threaded by design
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from continuous_batching_paged_ragged_gb300 import pkv, synth, workload  # noqa: E402
+
+CONFIGS = {
+    "qwen_decode": lambda: synth.qwen_decode(0),
+    "mixed_step": lambda: synth.mixed_step(0),
+    "long_gqa": lambda: synth.long_gqa(0),
+    "tiny_decode": lambda: synth.tiny_decode(0),
+}
+
+# DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
+# summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
+# source they were taken on; reported as null once the source changes.
+TRAFFIC = {}
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes(batch: synth.StepBatch):
+    """Per layer: (attention bytes, append bytes) -- each K/V element of a row read once (GQA grouping),
+    q read and output written once, 4 bytes per block-table entry; append reads k/v and writes them."""
+    s = batch.shape
+    ctx = batch.context_lens.astype(np.int64)
+    T = int(batch.q_lens.sum())
+    attn = (2 * int(ctx.sum()) * s.num_kv_heads * s.head_dim * 2 + T * s.num_q_heads * s.head_dim * 2 * 2
+            + 4 * int(((ctx + 15) // 16).sum()))
+    append = T * s.num_kv_heads * s.head_dim * 2 * 2 * 2 + 8 * T
+    return attn, append
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("attention.cu", "pkv_internal.cuh"):
+        with open(os.path.join(ROOT, "continuous_batching_paged_ragged_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return None
+        loaded = [s for s in sms if s > 0.5 * max(sms)] or sms
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------------------------------
+# CPU oracle legs (cpu_baseline and --impl reference)
+# ----------------------------------------------------------------------------------------------------
+
+def oracle_inputs(batch: synth.StepBatch, layer: int, rows):
+    s = batch.shape
+    items = []
+    for b in rows:
+        req, ctx = int(batch.req_ids[b]), int(batch.context_lens[b])
+        ql = int(batch.q_lens[b])
+        k, v = synth.sequence_kv(batch.seed, layer, req, ctx, s.num_kv_heads, s.head_dim)
+        q = synth.token_values(synth.KIND_Q, batch.seed, layer, np.full(ql, req), np.arange(ctx - ql, ctx),
+                               s.num_q_heads, s.head_dim)
+        items.append((q, k, v))
+    return items
+
+
+def oracle_bytes(batch, rows):
+    s = batch.shape
+    ctx = batch.context_lens[rows].astype(np.int64)
+    ql = batch.q_lens[rows].astype(np.int64)
+    return (2 * int(ctx.sum()) * s.num_kv_heads * s.head_dim * 2 + int(ql.sum()) * s.num_q_heads * s.head_dim * 4
+            + 4 * int(((ctx + 15) // 16).sum())), int(ctx.sum())
+
+
+def cpu_baseline(batch, budget_s: float = 12.0):
+    import oracle
+    rows = list(range(batch.num_seqs))
+    items = oracle_inputs(batch, 0, rows)
+    nbytes, nctx = oracle_bytes(batch, rows)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        for q, k, v in items:
+            oracle.attention_row(q, k, v)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return {"value": nbytes * reps / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "ctx_tokens_per_s": nctx * reps / el,
+            "sample": f"layer 0 of {batch.shape.num_layers}, all {batch.num_seqs} rows, repeated {reps}x "
+                      f"({el:.1f} s, fp64 NumPy, 1 thread of {os.cpu_count()} host cores)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    batch = CONFIGS[args.config]()
+    rows_all = list(range(batch.num_seqs))
+    probe = oracle_inputs(batch, 0, rows_all[:8])
+    t0 = time.perf_counter()
+    for q, k, v in probe:
+        oracle.attention_row(q, k, v)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    budget = 150.0 / (args.steps + args.warmup)
+    n = int(max(1, min(batch.num_seqs, budget / max(per_row, 1e-6))))
+    rows = rows_all[:n]
+    items = oracle_inputs(batch, 0, rows)
+    nbytes, nctx = oracle_bytes(batch, rows)
+    for _ in range(args.warmup):
+        for q, k, v in items:
+            oracle.attention_row(q, k, v)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for q, k, v in items:
+            oracle.attention_row(q, k, v)
+    el = time.perf_counter() - t0
+    value = nbytes * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": "paged ragged attention: achieved HBM GB/s (% of GB300 peak), ctx tokens/s",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": batch.name, "rows_per_step": n, "layers_per_step": 1},
+        "ctx_tokens_per_s": nctx * args.steps / el,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} of {batch.num_seqs} rows of layer 0 per step, fp64 NumPy, 1 thread"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------------------
+# GPU path
+# ----------------------------------------------------------------------------------------------------
+
+class RawStep:
+    """The timed step with every pointer resolved up front: plan + per layer (append, attention)."""
+
+    def __init__(self, pool, ds, attn, qs, ks, vs, outs, stream):
+        self.lib = pkv.load()
+        self.pool = pool.handle
+        self.ds = ds
+        self.ws = attn.workspace.data_ptr()
+        self.ws_bytes = attn.ws_bytes
+        self.q = [x.data_ptr() for x in qs]
+        self.k = [x.data_ptr() for x in ks]
+        self.v = [x.data_ptr() for x in vs]
+        self.o = [x.data_ptr() for x in outs]
+        self.stream = stream
+        self.bt = ds.block_tables.data_ptr()
+        self.ctx = ds.context_lens.data_ptr()
+        self.qsl = ds.query_start_loc.data_ptr()
+        self.slots = ds.slot_mapping.data_ptr()
+        self.launches = 0
+
+    def plan(self):
+        d = self.ds
+        st = self.lib.pkv_attention_plan(self.pool, self.ctx, self.qsl, d.num_seqs, d.num_tokens, d.max_blocks,
+                                         self.ws, self.ws_bytes, self.stream)
+        if st:
+            raise pkv.PkvError(st, "pkv_attention_plan", pkv.pkv_last_error())
+        self.launches += self.lib.pkv_last_launch_count(self.pool)
+
+    def append(self, i, layer):
+        st = self.lib.pkv_append(self.pool, layer, self.k[i], self.v[i], self.slots, self.ds.num_tokens, self.stream)
+        if st:
+            raise pkv.PkvError(st, "pkv_append", pkv.pkv_last_error())
+        self.launches += self.lib.pkv_last_launch_count(self.pool)
+
+    def attention(self, i, layer):
+        d = self.ds
+        st = self.lib.pkv_attention(self.pool, layer, self.q[i], self.bt, d.max_blocks, self.ctx, self.qsl,
+                                    d.num_seqs, d.num_tokens, self.o[i], self.ws, self.ws_bytes, self.stream)
+        if st:
+            raise pkv.PkvError(st, "pkv_attention", pkv.pkv_last_error())
+        self.launches += self.lib.pkv_last_launch_count(self.pool)
+
+    def __call__(self, layers):
+        self.plan()
+        for i, layer in enumerate(layers):
+            self.append(i, layer)
+            self.attention(i, layer)
+
+
+def run_pkv(args, rank, world, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    batch = CONFIGS[args.config]()
+    s = batch.shape
+    layers = list(range(s.num_layers))
+    pool = workload.make_pool(batch, split_blocks=args.split_blocks)
+    workload.prefill_cache(pool, batch, layers)
+    ds = workload.upload(batch, pool)
+    qs, ks, vs = workload.step_inputs(ds, layers)
+    outs = [torch.empty_like(q) for q in qs]
+    attn = workload.Attention(pool, ds)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    step = RawStep(pool, ds, attn, qs, ks, vs, outs, sp)
+    torch.cuda.synchronize()
+    assert pool.check() == 0
+
+    attn_bytes, append_bytes = algorithmic_bytes(batch)
+    step_bytes = (attn_bytes + append_bytes) * len(layers)
+    ctx_tokens = int(batch.context_lens.astype(np.int64).sum()) * len(layers)
+
+    # ---- device-resident timed region ----
+    for _ in range(args.warmup):
+        step(layers)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    step.launches = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(layers)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    launches = step.launches
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    assert pool.check() == 0
+
+    # ---- per-kernel timing of the dominant call (pkv_attention), events on its stream ----
+    kev = []
+    n_kernel_steps = max(3, min(args.steps, 200))
+    for _ in range(n_kernel_steps):
+        step.plan()
+        for i, layer in enumerate(layers):
+            step.append(i, layer)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step.attention(i, layer)
+            b.record(stream)
+            kev.append((a, b))
+    torch.cuda.synchronize()
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+
+    # ---- end to end through the public calls with host buffers ----
+    e2e = run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_bytes)
+
+    if rank != 0:
+        return
+    peak, peak_src = measured_peak()
+    achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+    sh = source_hash()
+    value = step_bytes * world / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "paged ragged attention: achieved HBM GB/s (% of GB300 peak), ctx tokens/s",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded Philox4x32-10, Irwin-Hall approx N(0,1) fp16)",
+        "config": {"workload": batch.name, "layers": s.num_layers, "num_q_heads": s.num_q_heads,
+                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
+                   "rows": batch.num_seqs, "new_tokens": batch.num_tokens,
+                   "context_tokens_per_layer": int(batch.context_lens.sum()), "pool_blocks": batch.num_blocks,
+                   "split_blocks": pool.cfg.split_blocks,
+                   "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of K/V per step rotating over "
+                         f"{s.num_layers} layer pools", "parallelism": f"replicas x{world}"},
+        "pct_of_peak": 100.0 * value / world / peak,
+        "ctx_tokens_per_s": ctx_tokens * world / (ms * 1e-3),
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": TRAFFIC.get(sh), "kernel": "pkv_attention (decode partials + merge)",
+                     "per_launch_bytes": attn_bytes, "avg_launch_ms": attn_ms, "peak_source": peak_src,
+                     "source": sh},
+        "e2e": e2e,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(batch)
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_bytes):
+    """Same metric with the step's inputs copied from pinned host memory and its outputs read back."""
+    L = len(layers)
+    h_q = torch.stack([q.cpu() for q in qs]).pin_memory()
+    h_k = torch.stack([k.cpu() for k in ks]).pin_memory()
+    h_v = torch.stack([v.cpu() for v in vs]).pin_memory()
+    h_out = torch.empty((L,) + tuple(outs[0].shape), dtype=torch.float16).pin_memory()
+    h_bt = ds.block_tables.cpu().pin_memory()
+    h_ctx = ds.context_lens.cpu().pin_memory()
+    h_qsl = ds.query_start_loc.cpu().pin_memory()
+    h_slots = ds.slot_mapping.cpu().pin_memory()
+    d_q = torch.stack(qs)
+    d_k = torch.stack(ks)
+    d_v = torch.stack(vs)
+    d_out = torch.stack(outs)
+    step = RawStep(pool, ds, attn, list(d_q), list(d_k), list(d_v), list(d_out), stream.cuda_stream)
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_bt, h_ctx, h_qsl, h_slots))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def one():
+        ds.block_tables.copy_(h_bt, non_blocking=True)
+        ds.context_lens.copy_(h_ctx, non_blocking=True)
+        ds.query_start_loc.copy_(h_qsl, non_blocking=True)
+        ds.slot_mapping.copy_(h_slots, non_blocking=True)
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        step(layers)
+        h_out.copy_(d_out, non_blocking=True)
+
+    n = max(3, min(args.steps, 200))
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"value": step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--config", default="qwen_decode", choices=sorted(CONFIGS))
+    ap.add_argument("--split-blocks", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        run_pkv(args, rank, world, local)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,174 @@
+// Internal helpers shared by libpkv's translation units: host-side error state, the pool handle,
+// launch helpers (programmatic dependent launch), and inline-PTX wrappers for mbarriers and the
+// bulk (TMA) copy engine on sm_103a.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <utility>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// ---- host-side error reporting -----------------------------------------------------------------
+void set_error(const std::string& msg);
+void clear_error();
+pkv_status fail(pkv_status code, const std::string& msg);
+pkv_status cuda_fail(cudaError_t e, const char* what);
+
+constexpr size_t kStatusBytes = 256;
+
+struct PlanKey {
+  const void* workspace = nullptr;
+  const int32_t* context_lens = nullptr;
+  const int32_t* query_start_loc = nullptr;
+  int32_t num_seqs = -1;
+  int32_t num_tokens = -1;
+  int32_t max_blocks_per_seq = -1;
+};
+
+}  // namespace pkv
+
+struct pkv_pool {
+  pkv_config cfg;
+  char* base = nullptr;        // device: cache, then the status area
+  size_t cache_bytes = 0;      // bytes of the fp16 cache region
+  int32_t* dev_error = nullptr;  // device error word (in the status area)
+  int32_t last_launches = 0;
+  int num_sms = 0;
+  int device = 0;
+  pkv::PlanKey plan;           // last plan issued through this pool
+};
+
+namespace pkv {
+
+// ---- launch with programmatic dependent launch (PDL) ---------------------------------------------
+// Every kernel of the library calls griddep_wait() before touching global memory written by earlier
+// work, so letting the next grid be scheduled early is always safe and hides launch latency.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace pkv
+
+// ---- device helpers ------------------------------------------------------------------------------
+#if defined(__CUDACC__)
+
+namespace pkv {
+namespace dev {
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: polls for at most ~1 s of wall time, then returns false; callers record
+// PKV_DEVERR_WAIT_TIMEOUT and unwind without touching the barrier again.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > 1000000000ull) return false;
+  }
+}
+
+// A pool whose error word records a wait timeout refuses further work until pkv_pool_check clears it.
+__device__ __forceinline__ bool pool_poisoned(const int32_t* err) {
+  return err && (*reinterpret_cast<const volatile int32_t*>(err) & PKV_DEVERR_WAIT_TIMEOUT) != 0;
+}
+
+// 1-D bulk copy global -> shared through the TMA engine, completion counted on `bar` in bytes.
+// Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_addr(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void set_error(int32_t* err, int32_t bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// Row of packed token t: the largest b with query_start_loc[b] <= t (query_start_loc has num_seqs + 1
+// entries).  Binary search; callers validate the row's bounds afterwards.
+__device__ __forceinline__ int row_of_token(const int32_t* __restrict__ qsl, int num_seqs, int t) {
+  int lo = 0, hi = num_seqs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(qsl + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace dev
+}  // namespace pkv
+
+#endif  // __CUDACC__

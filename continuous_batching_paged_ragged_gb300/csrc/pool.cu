@@ -1,0 +1,232 @@
+// Pool handle, error reporting, slot mapping and kv_append.
+//
+// kv_append follows "Continuous Batching Is Not a Bigger Batch" (opening section and "The allocator is
+// the other half"): every computed token's key and value are kept, one pair per token per layer, in the
+// slot of a 16-token block that was allocated as the token was computed.  It is a pure bit copy.
+#include <cuda_fp16.h>
+
+#include <cstring>
+#include <string>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+static thread_local std::string g_last_error;
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+void clear_error() { g_last_error.clear(); }
+pkv_status fail(pkv_status code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return PKV_ERR_CUDA;
+}
+
+static bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 6 || g == 8; }
+
+static pkv_status check_config(const pkv_config* c) {
+  if (!c) return fail(PKV_ERR_INVALID_ARG, "config is NULL");
+  if (c->num_layers < 1 || c->num_q_heads < 1 || c->num_kv_heads < 1 || c->num_blocks < 1)
+    return fail(PKV_ERR_INVALID_ARG, "layers, heads and blocks must be positive");
+  if (c->num_q_heads % c->num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+  if (c->block_size != 16) return fail(PKV_ERR_UNSUPPORTED, "block_size must be 16");
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+  if (!supported_group(c->num_q_heads / c->num_kv_heads))
+    return fail(PKV_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4, 6 or 8");
+  if (c->split_blocks < 0) return fail(PKV_ERR_INVALID_ARG, "split_blocks must be >= 0");
+  return PKV_OK;
+}
+
+static size_t cache_bytes_of(const pkv_config* c) {
+  return (size_t)2 * c->num_layers * (size_t)c->num_blocks * c->num_kv_heads * c->block_size * c->head_dim *
+         sizeof(__half);
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" const char* pkv_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" size_t pkv_pool_bytes(const pkv_config* cfg) {
+  if (check_config(cfg) != PKV_OK) return 0;
+  return cache_bytes_of(cfg) + kStatusBytes;
+}
+
+extern "C" pkv_status pkv_pool_init(const pkv_config* cfg, void* dev_cache, size_t bytes, pkv_pool** out) {
+  clear_error();
+  pkv_status st = check_config(cfg);
+  if (st != PKV_OK) return st;
+  if (!dev_cache || !out) return fail(PKV_ERR_INVALID_ARG, "dev_cache and out must be non-NULL");
+  if (reinterpret_cast<uintptr_t>(dev_cache) % 256 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "dev_cache must be 256-byte aligned");
+  size_t need = cache_bytes_of(cfg) + kStatusBytes;
+  if (bytes < need)
+    return fail(PKV_ERR_INVALID_ARG, "buffer too small: need " + std::to_string(need) + " bytes");
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, dev_cache);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return fail(PKV_ERR_INVALID_ARG, "dev_cache is not device memory");
+  pkv_pool* p = new pkv_pool();
+  p->cfg = *cfg;
+  if (p->cfg.split_blocks == 0) p->cfg.split_blocks = 16;
+  p->base = static_cast<char*>(dev_cache);
+  p->cache_bytes = cache_bytes_of(cfg);
+  p->dev_error = reinterpret_cast<int32_t*>(p->base + p->cache_bytes);
+  p->device = attr.device;
+  e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+  if (e != cudaSuccess) {
+    delete p;
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  }
+  e = cudaMemset(p->dev_error, 0, kStatusBytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    delete p;
+    return cuda_fail(e, "clearing the status area");
+  }
+  *out = p;
+  return PKV_OK;
+}
+
+extern "C" void pkv_pool_destroy(pkv_pool* pool) { delete pool; }
+
+extern "C" void* pkv_pool_layer_ptr(const pkv_pool* pool, int32_t layer, int32_t kv) {
+  if (!pool || layer < 0 || layer >= pool->cfg.num_layers || (kv != 0 && kv != 1)) return nullptr;
+  const pkv_config& c = pool->cfg;
+  size_t per = (size_t)c.num_blocks * c.num_kv_heads * c.block_size * c.head_dim * sizeof(__half);
+  return pool->base + ((size_t)layer * 2 + kv) * per;
+}
+
+extern "C" pkv_status pkv_pool_check(pkv_pool* pool, int32_t* bits, int32_t clear) {
+  clear_error();
+  if (!pool || !bits) return fail(PKV_ERR_INVALID_ARG, "pool and bits must be non-NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  e = cudaMemcpy(bits, pool->dev_error, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (clear) {
+    e = cudaMemset(pool->dev_error, 0, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+  }
+  return PKV_OK;
+}
+
+extern "C" int32_t pkv_last_launch_count(const pkv_pool* pool) { return pool ? pool->last_launches : 0; }
+
+// ---------------------------------------------------------------------------------------------------
+// Kernels
+// ---------------------------------------------------------------------------------------------------
+namespace pkv {
+
+// One thread per 16-byte chunk of one token's [Hkv][d] K (and the matching chunk of V).
+__global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                                        const int64_t* __restrict__ slot_mapping, int num_tokens,
+                                                        uint4* __restrict__ pool_k, uint4* __restrict__ pool_v,
+                                                        int num_kv_heads, int chunks_per_head, int64_t num_slots,
+                                                        int32_t* err) {
+  dev::griddep_wait();
+  dev::griddep_launch_dependents();
+  const int64_t per_token = (int64_t)num_kv_heads * chunks_per_head;
+  const int64_t total = (int64_t)num_tokens * per_token;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / per_token;
+    const int64_t rem = i - t * per_token;
+    const int64_t h = rem / chunks_per_head;
+    const int64_t c = rem - h * chunks_per_head;
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot == -1) continue;
+    if (slot < 0 || slot >= num_slots) {
+      if (c == 0 && h == 0) dev::set_error(err, PKV_DEVERR_SLOT_RANGE);
+      continue;
+    }
+    const int64_t blk = slot >> 4, off = slot & 15;
+    const int64_t dst = ((blk * num_kv_heads + h) * 16 + off) * chunks_per_head + c;
+    pool_k[dst] = __ldg(k + i);
+    pool_v[dst] = __ldg(v + i);
+  }
+}
+
+__global__ void __launch_bounds__(256) slot_mapping_kernel(const int32_t* __restrict__ block_tables, int max_blocks,
+                                                           const int32_t* __restrict__ context_lens,
+                                                           const int32_t* __restrict__ qsl, int num_seqs,
+                                                           int num_tokens, int num_blocks,
+                                                           int64_t* __restrict__ slot_mapping, int32_t* err) {
+  dev::griddep_wait();
+  dev::griddep_launch_dependents();
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < num_tokens; t += gridDim.x * blockDim.x) {
+    const int b = dev::row_of_token(qsl, num_seqs, t);
+    const int q0 = __ldg(qsl + b), q1 = __ldg(qsl + b + 1);
+    const int q_len = q1 - q0, ctx = __ldg(context_lens + b);
+    int64_t slot = -1;
+    if (t >= q1 || q_len < 1 || ctx < q_len || ctx > max_blocks * 16) {
+      dev::set_error(err, PKV_DEVERR_ROW_META);
+    } else {
+      const int p = ctx - q_len + (t - q0);
+      const int blk = __ldg(block_tables + (int64_t)b * max_blocks + (p >> 4));
+      if (blk < 0 || blk >= num_blocks) dev::set_error(err, PKV_DEVERR_BLOCK_RANGE);
+      else slot = (int64_t)blk * 16 + (p & 15);
+    }
+    slot_mapping[t] = slot;
+  }
+}
+
+}  // namespace pkv
+
+extern "C" pkv_status pkv_append(pkv_pool* pool, int32_t layer, const void* k, const void* v,
+                                 const int64_t* slot_mapping, int32_t num_tokens, void* stream) {
+  clear_error();
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  pool->last_launches = 0;
+  if (layer < 0 || layer >= pool->cfg.num_layers) return fail(PKV_ERR_OUT_OF_RANGE, "layer out of range");
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens must be >= 0");
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping) return fail(PKV_ERR_INVALID_ARG, "k, v and slot_mapping must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  const pkv_config& c = pool->cfg;
+  const int chunks = c.head_dim / 8;
+  const int64_t total = (int64_t)num_tokens * c.num_kv_heads * chunks;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = (int64_t)pool->num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  cudaError_t e = launch_pdl(kv_append_kernel, dim3((unsigned)blocks), dim3(threads), 0, (cudaStream_t)stream,
+                             static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, (int)num_tokens,
+                             static_cast<uint4*>(pkv_pool_layer_ptr(pool, layer, 0)),
+                             static_cast<uint4*>(pkv_pool_layer_ptr(pool, layer, 1)), (int)c.num_kv_heads, chunks,
+                             (int64_t)c.num_blocks * c.block_size, pool->dev_error);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  pool->last_launches = 1;
+  return PKV_OK;
+}
+
+extern "C" pkv_status pkv_slot_mapping(pkv_pool* pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, const int32_t* query_start_loc, int32_t num_seqs,
+                                       int32_t num_tokens, int64_t* slot_mapping, void* stream) {
+  clear_error();
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  pool->last_launches = 0;
+  if (num_tokens < 0 || num_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "sizes must be >= 0");
+  if (num_tokens == 0) return PKV_OK;
+  if (num_seqs < 1) return fail(PKV_ERR_INVALID_ARG, "tokens without rows");
+  if (max_blocks_per_seq < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
+  if (!block_tables || !context_lens || !query_start_loc || !slot_mapping)
+    return fail(PKV_ERR_INVALID_ARG, "metadata pointers must be non-NULL");
+  const int threads = 256;
+  int blocks = (num_tokens + threads - 1) / threads;
+  if (blocks > pool->num_sms * 8) blocks = pool->num_sms * 8;
+  cudaError_t e = launch_pdl(slot_mapping_kernel, dim3(blocks), dim3(threads), 0, (cudaStream_t)stream, block_tables,
+                             (int)max_blocks_per_seq, context_lens, query_start_loc, (int)num_seqs, (int)num_tokens,
+                             (int)pool->cfg.num_blocks, slot_mapping, pool->dev_error);
+  if (e != cudaSuccess) return cuda_fail(e, "slot_mapping launch");
+  pool->last_launches = 1;
+  return PKV_OK;
+}

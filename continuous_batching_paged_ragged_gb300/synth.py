@@ -73,38 +73,43 @@ def _irwin_hall_fp16(wa, wb):
     return x.astype(np.float16)              # IEEE round-to-nearest-even
 
 
-def token_values(kind: int, seed: int, layer: int, req_ids, positions, heads: int, head_dim: int) -> np.ndarray:
+def token_values(kind: int, seed: int, layer: int, req_ids, positions, heads: int, head_dim: int,
+                 head_range: Optional[tuple] = None) -> np.ndarray:
     """fp16 [T, heads, head_dim] values of one tensor kind for tokens (req_ids[t], positions[t]).
 
     Counter layout: key = (seed low word, kind << 24 | layer); counter = (pair index of the flattened
     (head, dim) element, position, request id, seed high word).  An even element takes output words
-    0-1 of its pair's Philox call, an odd element words 2-3.
+    0-1 of its pair's Philox call, an odd element words 2-3.  ``head_range=(lo, hi)`` returns only heads
+    lo .. hi-1 (same values as the full tensor's slice).
     """
     req = np.asarray(req_ids, dtype=np.int64).reshape(-1)
     pos = np.asarray(positions, dtype=np.int64).reshape(-1)
     assert req.shape == pos.shape
-    n_el = heads * head_dim
-    assert n_el % 2 == 0
-    pairs = np.arange(n_el // 2, dtype=np.uint64)
+    lo_h, hi_h = head_range if head_range is not None else (0, heads)
+    assert 0 <= lo_h < hi_h <= heads and head_dim % 2 == 0
+    n_el = (hi_h - lo_h) * head_dim
+    pairs = np.arange(lo_h * head_dim // 2, hi_h * head_dim // 2, dtype=np.uint64)
     k0 = seed & 0xFFFFFFFF
     k1 = ((kind & 0xFF) << 24) | (layer & 0xFFFFFF)
     c3 = (seed >> 32) & 0xFFFFFFFF
-    w0, w1, w2, w3 = philox4x32_10(pairs[None, :], pos[:, None].astype(np.uint64) & _MASK32,
-                                   req[:, None].astype(np.uint64) & _MASK32, np.uint64(c3), k0, k1)
-    even = _irwin_hall_fp16(w0, w1)
-    odd = _irwin_hall_fp16(w2, w3)
     out = np.empty((req.shape[0], n_el), dtype=np.float16)
-    out[:, 0::2] = even
-    out[:, 1::2] = odd
-    return out.reshape(req.shape[0], heads, head_dim)
+    step = max(1, (1 << 17) // pairs.shape[0])   # bounded temporaries keep numpy in cache
+    for lo in range(0, req.shape[0], step):
+        hi = min(lo + step, req.shape[0])
+        w0, w1, w2, w3 = philox4x32_10(pairs[None, :], pos[lo:hi, None].astype(np.uint64) & _MASK32,
+                                       req[lo:hi, None].astype(np.uint64) & _MASK32, np.uint64(c3), k0, k1)
+        out[lo:hi, 0::2] = _irwin_hall_fp16(w0, w1)
+        out[lo:hi, 1::2] = _irwin_hall_fp16(w2, w3)
+    return out.reshape(req.shape[0], hi_h - lo_h, head_dim)
 
 
-def sequence_kv(seed: int, layer: int, req_id: int, ctx: int, num_kv_heads: int, head_dim: int):
+def sequence_kv(seed: int, layer: int, req_id: int, ctx: int, num_kv_heads: int, head_dim: int,
+                head_range: Optional[tuple] = None):
     """Contiguous logical-order K and V ([ctx, Hkv, d] fp16) of one sequence at one layer."""
     pos = np.arange(ctx, dtype=np.int64)
     req = np.full(ctx, req_id, dtype=np.int64)
-    k = token_values(KIND_K, seed, layer, req, pos, num_kv_heads, head_dim)
-    v = token_values(KIND_V, seed, layer, req, pos, num_kv_heads, head_dim)
+    k = token_values(KIND_K, seed, layer, req, pos, num_kv_heads, head_dim, head_range)
+    v = token_values(KIND_V, seed, layer, req, pos, num_kv_heads, head_dim, head_range)
     return k, v
 
 
@@ -190,16 +195,28 @@ def scatter_block_tables(context_lens: Sequence[int], block_size: int, num_block
     return bt, perm
 
 
-def _make_batch(name, shape, cached, q_lens, seed, pool_factor=1.25, num_blocks=None, req_base=1000):
+def _make_batch(name, shape, cached, q_lens, seed, pool_factor=1.25, num_blocks=None, req_base=1000,
+                block_seed=None, req_ids=None):
     cached = np.asarray(cached, dtype=np.int32)
     q_lens = np.asarray(q_lens, dtype=np.int32)
     ctx = (cached + q_lens).astype(np.int32)
     need = int(sum((int(c) + shape.block_size - 1) // shape.block_size for c in ctx))
     if num_blocks is None:
         num_blocks = int(math.ceil(pool_factor * need))
-    bt, perm = scatter_block_tables(ctx, shape.block_size, num_blocks, seed)
-    req_ids = np.arange(req_base, req_base + len(ctx), dtype=np.int64)
-    return StepBatch(shape, num_blocks, req_ids, q_lens, ctx, bt, perm, seed, name)
+    bt, perm = scatter_block_tables(ctx, shape.block_size, num_blocks, seed if block_seed is None else block_seed)
+    if req_ids is None:
+        req_ids = np.arange(req_base, req_base + len(ctx), dtype=np.int64)
+    return StepBatch(shape, num_blocks, np.asarray(req_ids, dtype=np.int64), q_lens, ctx, bt, perm, seed, name)
+
+
+def custom_batch(shape: Shape, cached, q_lens, seed: int = 0, num_blocks: Optional[int] = None,
+                 block_seed: Optional[int] = None, req_ids=None, pool_factor: float = 1.25) -> StepBatch:
+    """A pass with the given per-row cached lengths and new-token counts; blocks scattered by block_seed.
+
+    Values depend on (seed, request id, position) only, so two batches that place the same rows in
+    different physical blocks (block_seed) or in a different order hold identical logical K/V/Q."""
+    return _make_batch("custom", shape, cached, q_lens, seed, pool_factor, num_blocks, block_seed=block_seed,
+                       req_ids=req_ids)
 
 
 def tiny_decode(seed: int = 0) -> StepBatch:

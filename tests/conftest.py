@@ -10,7 +10,6 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libpkv.so")
-    config.addinivalue_line("markers", "slow: long-running CPU case")
 
 
 @pytest.fixture(scope="session")
@@ -22,6 +21,9 @@ def cuda():
 
 
 @pytest.fixture(scope="session")
-def pkv_lib():
+def built():
+    """Builds libpkv.so / libpkv_synth.so in-tree if they are missing or stale (nvcc cross-compiles)."""
+    from continuous_batching_paged_ragged_gb300 import _build
+    _build.build()
     from continuous_batching_paged_ragged_gb300 import pkv
     return pkv.load()

@@ -1,0 +1,99 @@
+"""The C++ host scheduler (pkv_sched_*) against the oracle's restatement, step by step, bit for bit."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from continuous_batching_paged_ragged_gb300 import synth
+from continuous_batching_paged_ragged_gb300.pkv import PkvError, Scheduler
+
+TRACES = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "sched_traces.json")))["traces"]
+
+
+def _compare_runs(native, ref, max_steps=100000):
+    n = 0
+    while not ref.done():
+        a = native.step()
+        b = ref.step()
+        assert a["req_ids"].tolist() == b.req_ids.tolist()
+        assert np.array_equal(a["q_lens"], b.q_lens)
+        assert np.array_equal(a["context_lens"], b.context_lens)
+        assert np.array_equal(a["block_tables"], b.block_tables)
+        assert np.array_equal(a["slot_mapping"], b.slot_mapping)
+        assert a["query_start_loc"].tolist() == [0] + np.cumsum(b.q_lens).tolist()
+        assert a["preempted"] == b.preempted and a["admitted"] == b.admitted
+        assert sorted(a["finished"]) == sorted(b.finished)
+        n += 1
+        assert n < max_steps
+    assert native.done()
+    st = native.stats()
+    assert st["steps"] == ref.steps and st["preemptions"] == ref.num_preemptions
+    assert st["recomputed_tokens"] == ref.recomputed_tokens
+    assert st["recomputed_prompt_tokens"] == ref.recomputed_prompt_tokens
+    assert st["max_batch"] == ref.max_batch and st["batch_sum"] == ref.batch_sum
+    assert native.free_list() == list(ref.free)
+    return st
+
+
+@pytest.mark.parametrize("trace", TRACES, ids=[t["name"] for t in TRACES])
+def test_hand_worked_traces(built, trace):
+    native = Scheduler(trace["max_num_seqs"], trace["token_budget"], trace["block_size"], len(trace["free_blocks"]),
+                       trace["free_blocks"])
+    ref = oracle.Scheduler(trace["max_num_seqs"], trace["token_budget"], trace["block_size"], trace["free_blocks"])
+    for rid, p, o in trace["requests"]:
+        native.add(rid, p, o)
+        ref.add(rid, p, o)
+    _compare_runs(native, ref)
+
+
+@pytest.mark.parametrize("num_blocks,cap", [(20000, 256), (20000, 64), (5000, 256), (5000, 64), (1500, 512)])
+def test_trace_workload_matches_oracle(built, num_blocks, cap):
+    """The scheduler-driven trace (256 requests, lognormal prompts, U[50,781] outputs, budget 8192)."""
+    reqs = synth.trace_requests(0)
+    perm = synth.block_permutation(num_blocks, 0)
+    native = Scheduler(cap, 8192, 16, num_blocks, perm)
+    ref = oracle.Scheduler(cap, 8192, 16, perm)
+    for r in reqs:
+        native.add(r.req_id, r.prompt_len, r.max_output)
+        ref.add(r.req_id, r.prompt_len, r.max_output)
+    st = _compare_runs(native, ref)
+    if num_blocks == 5000 and cap == 256:
+        assert st["preemptions"] > 0
+
+
+def test_argument_errors(built):
+    with pytest.raises(PkvError):
+        Scheduler(0, 8192, 16, 100)
+    with pytest.raises(PkvError):
+        Scheduler(4, 8192, 16, 3, [0, 0, 1])
+    s = Scheduler(4, 64, 16, 4)
+    with pytest.raises(PkvError):
+        s.add(1, 100, 1)            # can never fit 4 blocks of 16
+    s.add(1, 10, 2)
+    with pytest.raises(PkvError):
+        s.add(1, 10, 2)             # duplicate id
+    with pytest.raises(PkvError):
+        s.abort(99)
+    with pytest.raises(PkvError):
+        s.set_max_num_seqs(0)
+
+
+def test_abort_and_drain(built):
+    reqs = synth.trace_requests(1, n=40)
+    s = Scheduler(32, 8192, 16, 4000, synth.block_permutation(4000, 1))
+    for r in reqs:
+        s.add(r.req_id, r.prompt_len, r.max_output)
+    for _ in range(3):
+        s.step()
+    s.abort(reqs[0].req_id)
+    s.abort(reqs[35].req_id)        # still waiting
+    st = s.stats()
+    assert st["running"] == 31 and st["waiting"] == 40 - 32 - 1
+    s.set_max_num_seqs(4)
+    rows = s.step()
+    assert len(rows["req_ids"]) == 31 and rows["preempted"] == []
+    while not s.done():
+        s.step()
+    assert s.stats()["free_blocks"] == 4000
