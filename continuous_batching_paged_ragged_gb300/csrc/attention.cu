@@ -605,3 +605,125 @@ extern "C" pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q
   }
   return PKV_OK;
 }
+
+// ---------------------------------------------------------------------------------------------------
+// Allocation-free variant of the attention call.
+//
+// Some callers cannot hand the library a workspace: an engine that has already reserved every byte of
+// device memory for its own pools, or a caller that may not issue cudaMalloc (which can synchronise the
+// whole device) while a pass is in flight.  For them the split-K scratch -- the per-token row/context
+// table and the partial (m, l, o) results -- lives in one fixed array compiled into this library.
+// Each device that loads the library holds the array until the process exits.
+// ---------------------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace pkv {
+
+constexpr size_t kNoAllocScratchBytes = PKV_NOALLOC_SCRATCH_BYTES;  // 16 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// The array's device address, looked up once per device with that device current.  In host code the
+// symbol name itself is only a host-side stand-in and must never reach a kernel.
+static void* noalloc_scratch_ptr(int device, cudaError_t* err) {
+  static std::mutex mu;
+  static void* cached[128] = {};
+  *err = cudaSuccess;
+  if (device < 0 || device >= 128) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[device]) {
+    void* ptr = nullptr;
+    *err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    cached[device] = ptr;
+  }
+  return cached[device];
+}
+
+}  // namespace pkv
+
+extern "C" pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
+                                            int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                            const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
+                                            void* out, void* stream) {
+  clear_error();
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  pool->last_launches = 0;
+  const pkv_config& c = pool->cfg;
+  if (layer < 0 || layer >= c.num_layers) return fail(PKV_ERR_OUT_OF_RANGE, "layer out of range");
+  if (num_seqs < 0 || num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "sizes must be >= 0");
+  if (num_tokens > 0 && num_seqs < 1) return fail(PKV_ERR_INVALID_ARG, "tokens without rows");
+  if (num_seqs > num_tokens) return fail(PKV_ERR_INVALID_ARG, "every row needs at least one query token");
+  if (max_blocks_per_seq < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
+  if (num_tokens == 0) return PKV_OK;
+  if (!q || !out || !block_tables || !context_lens || !query_start_loc)
+    return fail(PKV_ERR_INVALID_ARG, "q, out and metadata pointers must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  if (q == out) return fail(PKV_ERR_INVALID_ARG, "out may not alias q");
+  const WsLayout w = ws_layout(c, num_tokens, max_blocks_per_seq);
+  if (w.max_splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits per row; raise split_blocks");
+  if (w.total > kNoAllocScratchBytes)
+    return fail(PKV_ERR_OUT_OF_RANGE, "pass needs " + std::to_string(w.total) + " bytes of scratch; the built-in "
+                "array holds " + std::to_string(kNoAllocScratchBytes) + " (use pkv_attention with a workspace)");
+  int device = -1;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (device != pool->device) return fail(PKV_ERR_INVALID_ARG, "the pool's device must be the current device");
+  void* scratch = noalloc_scratch_ptr(device, &e);
+  if (!scratch) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch array");
+
+  char* ws = static_cast<char*>(scratch);
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* tok_row = reinterpret_cast<int32_t*>(ws + w.tok_row);
+  int32_t* tok_ctx = reinterpret_cast<int32_t*>(ws + w.tok_ctx);
+  // Nothing in the scratch needs to start at zero: the plan rewrites the token table for every token,
+  // and every partial the merge reads is written by the decode kernel of the same call.
+  const int n = num_seqs > num_tokens ? num_seqs : num_tokens;
+  int blocks = (n + 255) / 256;
+  if (blocks > pool->num_sms * 4) blocks = pool->num_sms * 4;
+  e = launch_pdl(plan_kernel, dim3(blocks), dim3(256), 0, s, context_lens, query_start_loc, (int)num_seqs,
+                 (int)num_tokens, (int)(max_blocks_per_seq * kBS), tok_row, tok_ctx, pool->dev_error);
+  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+
+  DecodeParams p;
+  p.q = static_cast<const __half*>(q);
+  p.kpool = static_cast<const __half*>(pkv_pool_layer_ptr(pool, layer, 0));
+  p.vpool = static_cast<const __half*>(pkv_pool_layer_ptr(pool, layer, 1));
+  p.block_tables = block_tables;
+  p.tok_row = tok_row;
+  p.tok_ctx = tok_ctx;
+  p.out = static_cast<__half*>(out);
+  p.part_o = reinterpret_cast<float*>(ws + w.part_o);
+  p.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
+  p.err = pool->dev_error;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_q_heads = c.num_q_heads;
+  p.num_kv_heads = c.num_kv_heads;
+  p.num_blocks = c.num_blocks;
+  p.split_blocks = c.split_blocks;
+  p.max_splits = w.max_splits;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+  const int group = c.num_q_heads / c.num_kv_heads;
+  switch (c.head_dim) {
+    case 64: e = launch_decode_g<64>(group, p, num_tokens, c.num_kv_heads, w.max_splits, s); break;
+    case 128: e = launch_decode_g<128>(group, p, num_tokens, c.num_kv_heads, w.max_splits, s); break;
+    case 256: e = launch_decode_g<256>(group, p, num_tokens, c.num_kv_heads, w.max_splits, s); break;
+    default: return fail(PKV_ERR_UNSUPPORTED, "head_dim");
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  pool->last_launches = 2;
+  if (w.max_splits > 1) {
+    MergeParams m{p.part_o, p.part_ml, p.tok_ctx, p.out, c.num_q_heads, c.split_blocks, w.max_splits};
+    switch (c.head_dim) {
+      case 64: e = launch_pdl(merge_kernel<64>, dim3(num_tokens, c.num_q_heads), dim3(128), 0, s, m); break;
+      case 128: e = launch_pdl(merge_kernel<128>, dim3(num_tokens, c.num_q_heads), dim3(128), 0, s, m); break;
+      default: e = launch_pdl(merge_kernel<256>, dim3(num_tokens, c.num_q_heads), dim3(128), 0, s, m); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    pool->last_launches = 3;
+  }
+  return PKV_OK;
+}

@@ -171,6 +171,28 @@ pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q, const int
                          const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens, void* out,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* Allocation-free attention.  The pages have no counterpart to this call; it exists for callers that
+ * cannot give the library a workspace -- an engine whose device memory is already carved up by its
+ * own allocator, or code that must not call cudaMalloc (a device-wide synchronisation) mid-pass.
+ *
+ * Does what pkv_attention_plan followed by pkv_attention does, with the same arguments minus the
+ * workspace, and gives the same result.  The split-K scratch lives in one array of
+ * PKV_NOALLOC_SCRATCH_BYTES compiled into libpkv, held on every device that loads the library until
+ * the process exits; the library allocates nothing.  A pass whose scratch
+ * (pkv_attention_workspace_bytes for the same sizes) exceeds that limit is refused with
+ * PKV_ERR_OUT_OF_RANGE before anything is launched.
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current -- the pool's device must be the current device -- so make that first call before
+ * any stream capture.  Every call shares the one array and leaves its contents behind; nothing in it
+ * has to start at zero, but two calls whose kernels can overlap on the GPU (different streams with no
+ * ordering between them) race on it. */
+#define PKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                 const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens, void* out,
+                                 void* stream);
+
 /* Number of kernel launches the last successful pkv_append / pkv_attention_plan / pkv_attention /
  * pkv_slot_mapping call on `pool` enqueued (for accounting; host-side counter). */
 int32_t pkv_last_launch_count(const pkv_pool* pool);
