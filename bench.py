@@ -289,6 +289,9 @@ def run_pkv(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     batch = CONFIGS[args.config]()
+    if args.layers:
+        batch.shape = synth.Shape(args.layers, batch.shape.num_q_heads, batch.shape.num_kv_heads,
+                                  batch.shape.head_dim, batch.shape.block_size)
     s = batch.shape
     layers = list(range(s.num_layers))
     pool = workload.make_pool(batch, split_blocks=args.split_blocks)
@@ -434,6 +437,7 @@ def main():
     ap.add_argument("--config", default="qwen_decode", choices=sorted(CONFIGS))
     ap.add_argument("--split-blocks", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -1,4 +1,4 @@
-// Ragged paged GQA attention: per-pass plan, split-K decode partials, cross-split merge.
+// Ragged paged GQA attention: per-pass plan, persistent split-K decode, cross-split merge.
 //
 // What is computed ("Continuous Batching Is Not a Bigger Batch", sections "What the scheduler does on one
 // step" and "Where the batch size actually comes from"): for every query token of every row, causal
@@ -7,21 +7,27 @@
 // follows") is why the keys are read from blocks in place, with no padding to the widest row.
 //
 // How (GB300 design, not from the pages):
-//  * plan_kernel (once per pass): per packed query token, its row and its causal context length.
-//  * decode_kernel: one CTA per (token, KV head, split of `split_blocks` blocks).  The CTA holds all G
-//    query heads of the KV head, so each K/V block is read from HBM exactly once.  A producer warp
-//    streams whole (block, KV head) runs of K and V into a shared-memory ring with 1-D bulk (TMA) copies
-//    completing on mbarriers; four consumer warps each take every fourth block, compute scores with
-//    packed fp32 FMAs, reduce across lanes with warp shuffles, and keep an online softmax (running max
-//    and sum in the log2 domain) plus an fp32 accumulator.  The warps are combined through shared memory.
-//    A token whose context fits one split writes fp16 output directly; otherwise the split writes an
-//    unnormalised partial (m, l, o) to the workspace.
-//  * merge_kernel: for tokens with more than one split, log-sum-exp combine of the partials -> fp16.
-// The split count of a token depends only on its own context length, so results are bit-identical
-// whatever else is in the batch and whatever the row order or physical block placement.
+//  * plan_kernel (once per pass): per packed query token its row and causal context length, and the pass's
+//    task list.  A task is one split of one (token, KV head): `split_blocks` consecutive 16-token blocks.
+//    The split count of a token depends only on its own context, so results are bit-identical whatever
+//    else is in the batch, whatever the row order and wherever the blocks sit physically.
+//  * decode_kernel: persistent; every warp is an independent worker.  A warp takes tasks from a global
+//    counter and streams each block's K and V runs through its own shared-memory ring with 2-D TMA tile
+//    copies (128-byte swizzle) that its lane 0 issues; independent issuers per SM are what keep HBM busy.
+//    The warp owns the whole split and all G <= 8 query heads of its KV head, so each K/V block is read
+//    from HBM exactly once.  Per 16-key block the group contraction runs on the tensor cores with warp
+//    MMAs: S^T[16 keys x 8 heads] = K Q^T and O^T[d x 8 heads] += V^T P^T, operands fetched from the
+//    swizzled ring with ldmatrix; the online softmax (running max and sum in the log2 domain, fp32)
+//    reduces across the lanes that share a head with warp shuffles.
+//  * merge_kernel: a token whose context fits one split gets its fp16 output from the decode directly.
+//    Otherwise each split leaves an unnormalised partial (m, l, o) and merge_kernel, launched right behind
+//    the decode, combines a token's partials with log-sum-exp weights, spread over many CTAs.  (Merging
+//    in the decode's last-finishing warp was measured slower: the row's last splits finish together at
+//    the end of the launch and their merges serialise there.)
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <mutex>
 #include <string>
 
 #include "pkv_internal.cuh"
@@ -29,46 +35,57 @@
 namespace pkv {
 
 constexpr int kBS = 16;
+constexpr int kWideMergeSplits = 32;  // beyond this many splits per token the merge also splits over splits
+constexpr int kMaxSplitBlocks = 32;   // upper bound on split_blocks (a split's block ids fit one warp)
+constexpr int kHeadsTile = 8;         // query heads per KV head handled by one MMA tile (G <= 8)
 
-__host__ __device__ constexpr int next_pow2(int x) { return x <= 1 ? 1 : 2 * next_pow2((x + 1) / 2); }
+// Ring slots per worker warp: runs (a block's K or V for one KV head, or a task's q) in flight.
+#ifndef PKV_DECODE_RING
+#define PKV_DECODE_RING(D) ((D) == 256 ? 3 : ((D) == 128 ? 3 : 6))
+#endif
+
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+struct WsHeader {
+  int32_t n_tasks;
+  int32_t work;   // next task to hand out
+  int32_t done;   // CTAs of the current decode launch that have finished
+  int32_t pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 template <int D, int G>
 struct DecodeTraits {
-  static constexpr int NCW = 4;                  // consumer warps
-  static constexpr int NTHREADS = (NCW + 1) * 32;  // + one producer warp
-  static constexpr int DG = D / 16;              // lanes sharing one key row in the score phase (16 dims each)
-  static constexpr int TPW = 32 / DG;            // key rows per warp step
-  static constexpr int STEPS = kBS / TPW;        // warp steps per block
-  static constexpr int DPL = D / 32;             // output dims per lane in the value phase
-  static constexpr int RUN = kBS * D * 2;        // bytes of one (block, KV head) run of K (or V)
-  static constexpr int NSTAGE = D == 256 ? 6 : 8;
-  static constexpr int GP = next_pow2(G);        // heads padded to a power of two for the reduction
-  static constexpr int R = GP > DG ? GP / DG : 1;    // heads a lane owns after the reduce-scatter
-  static constexpr int REP = DG > GP ? DG / GP : 1;  // lanes holding the same head (replicas)
-  static constexpr int RING = NSTAGE * 2 * RUN;
-  static constexpr int OFF_P = RING;                                   // [NCW][kBS][GP] probabilities
-  static constexpr int OFF_A = OFF_P + NCW * kBS * GP * 4;             // [NCW][GP] rescale factors
-  static constexpr int OFF_M = OFF_A + NCW * GP * 4;                   // [NCW][GP] running max
-  static constexpr int OFF_L = OFF_M + NCW * GP * 4;                   // [NCW][GP] running sum
-  static constexpr int OFF_BAR = align_up(OFF_L + NCW * GP * 4, 8);
-  static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8;
-  static_assert(D % 16 == 0 && DG <= 32 && kBS % TPW == 0, "head_dim");
-  static_assert(NCW * G * D * 4 <= RING, "combine staging must fit in the ring");
-  static_assert(DPL % 2 == 0, "value phase works on float2 pairs");
+  static constexpr int NW = 4;                     // warps per CTA; each warp is an independent worker
+  static constexpr int NTHREADS = NW * 32;
+  static constexpr int RUN = kBS * D * 2;          // one (block, KV head) run of K or V = D/64 TMA boxes
+  static constexpr int BOXES = D / 64;
+  static constexpr int NR = PKV_DECODE_RING(D);    // ring slots (runs in flight) per warp
+  static constexpr int KS = D / 16;                // MMA k-steps over the head dimension (scores)
+  static constexpr int MT = D / 16;                // MMA m-tiles over the head dimension (values)
+  static constexpr int OV = MT * 4;                // fp32 output values per lane
+  static constexpr int MINB = D == 256 ? 2 : 4;    // CTAs per SM the register budget allows
+  static constexpr int OFF_BAR = NW * NR * RUN;    // [NW][NR] run barriers after the rings
+  static constexpr int SMEM = OFF_BAR + NW * NR * 8 + 1024;  // + slack to align the rings to 1024 bytes
+  static_assert(D % 64 == 0 && G >= 1 && G <= kHeadsTile, "shape");
+  static_assert(RUN % 1024 == 0, "swizzled boxes need 1024-byte aligned slots");
+  static_assert(8 * D * 2 <= RUN && KS % 2 == 0, "a task's q (8 rows) fits one slot");
 };
 
 struct DecodeParams {
+  CUtensorMap kv_map;  // the pool as TMA rows of head_dim values (64-byte aligned: first member)
   const __half* q;
-  const __half* kpool;
-  const __half* vpool;
   const int32_t* block_tables;
   const int32_t* tok_row;
   const int32_t* tok_ctx;
+  const int4* tasks;   // {token, kv head | split << 8, row, causal context}
+  WsHeader* hdr;
   __half* out;
-  float* part_o;
-  float2* part_ml;
+  float* part_o;       // [num_tokens * num_kv_heads * max_splits][32 lanes][D / 4]  (MMA fragment order)
+  float2* part_ml;     // [num_tokens * num_kv_heads * max_splits][8 heads]
   int32_t* err;
+  int layer_row0_k;    // TMA row of (layer, K, block 0, head 0, slot 0)
+  int layer_row0_v;    // TMA row of (layer, V, block 0, head 0, slot 0)
   int max_blocks;
   int num_q_heads;
   int num_kv_heads;
@@ -78,365 +95,531 @@ struct DecodeParams {
   float scale_log2;  // log2(e) / sqrt(head_dim)
 };
 
-// Reduce-scatter of GP values over the DG lanes of a key row (lane bits below DG): halving exchanges
-// while more than one head remains per lane, then plain all-reduce.  Afterwards v[0 .. R-1] are the
-// full sums of heads head_base(lane) + r.
-template <int CNT, int M>
-struct ReduceScatter {
-  template <int N>
-  static __device__ __forceinline__ void run(float (&v)[N], int lane) {
-    if constexpr (M >= 1) {
-      if constexpr (CNT > 1) {
-        constexpr int H = CNT / 2;
-        const bool up = (lane & M) != 0;
-#pragma unroll
-        for (int j = 0; j < H; ++j) {
-          const float send = up ? v[j] : v[j + H];
-          const float keep = up ? v[j + H] : v[j];
-          v[j] = keep + __shfl_xor_sync(0xffffffffu, send, M);
-        }
-        ReduceScatter<H, M / 2>::run(v, lane);
-      } else {
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], M);
-        ReduceScatter<1, M / 2>::run(v, lane);
-      }
-    }
-  }
-  static __device__ __forceinline__ int head_base(int lane) {
-    if constexpr (M >= 1 && CNT > 1) {
-      constexpr int H = CNT / 2;
-      return ((lane & M) ? H : 0) + ReduceScatter<H, M / 2>::head_base(lane);
-    } else {
-      return 0;
-    }
-  }
+// Byte offset of 16-byte chunk c (8 dims) of key row r inside a ring slot written by 64-value TMA boxes
+// with the 128-byte swizzle: box c / 8, row r at 128 bytes, chunk slot (c % 8) XOR (r % 8).
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return (uint32_t)((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// ---------------------------------------------------------------------------------------------------
+// Worker warp.  Measured on this access pattern (scattered 4 KB runs): one issuing thread per CTA tops
+// out near 6 GB/s whatever the ring depth, while 12-16 issuing warps per SM reach 5.6-6 TB/s -- so every
+// warp streams its own runs.  The next task's metadata loads overlap the current task's compute, and
+// the next task's first runs enter the ring before the current task ends.
+// ---------------------------------------------------------------------------------------------------
+struct TaskMeta {
+  int t, g, s, row, ctx, nb, nsplit;
+  int ids;  // lane r holds the physical id of block r of the split (r < nb <= 32)
 };
 
-__device__ __forceinline__ void h8_to_f2(const uint4& raw, float2* f) {
-  const __half2* h = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) f[e] = __half22float2(h[e]);
+__device__ __forceinline__ void task_from_record(const DecodeParams& p, int4 rec, TaskMeta& m) {
+  m.t = rec.x;
+  m.g = rec.y & 0xFF;
+  m.s = rec.y >> 8;
+  m.row = rec.z;
+  m.ctx = rec.w;
+  const int nblk = (m.ctx + kBS - 1) / kBS;
+  m.nb = m.t >= 0 ? min(p.split_blocks, nblk - m.s * p.split_blocks) : 0;
+  m.nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
+}
+
+__device__ __forceinline__ int4 load_record(const DecodeParams& p, int idx, int n_tasks) {
+  return idx < n_tasks ? __ldg(p.tasks + idx) : make_int4(-1, 0, 0, 0);
+}
+
+__device__ __forceinline__ int load_ids(const DecodeParams& p, const TaskMeta& m, int lane) {
+  int id = 0;
+  if (lane < m.nb) {
+    id = __ldg(p.block_tables + (int64_t)m.row * p.max_blocks + m.s * p.split_blocks + lane);
+    if (id < 0 || id >= p.num_blocks) {
+      dev::set_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+      id = 0;  // keep the copy in bounds; this token's output is flagged as invalid
+    }
+  }
+  return id;
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(DecodeTraits<D, G>::NTHREADS)
-decode_kernel(const DecodeParams p) {
+struct Worker {
   using T = DecodeTraits<D, G>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
-  uint64_t* empty = full + T::NSTAGE;
+  const DecodeParams& p;
+  unsigned char* ring;   // this warp's NR slots (1024-byte aligned)
+  uint64_t* bars;        // this warp's NR barriers
+  uint64_t pol;
+  int lane;
+  int n_tasks;
+  int issued = 0;        // runs issued into the ring so far
+  int consumed = 0;      // runs taken out of the ring so far
+  int icur = 0;          // 0: the issue cursor is in the current task, 1: in the next one
+  int ir = 0;            // run index of the issue cursor: 0 q, 1 + 2b K of block b, 2 + 2b V of block b
+  int nstage = 0;        // next task's metadata: 0 nothing, 1 index requested, 2 record loaded, 3 ids loaded
+  int nxt_idx = 0;
+  int4 nxt_rec;
+  TaskMeta cur, nxt;
+  bool ok = true;
 
+  __device__ Worker(const DecodeParams& p_, unsigned char* ring_, uint64_t* bars_, int lane_)
+      : p(p_), ring(ring_), bars(bars_), lane(lane_) {
+    pol = dev::l2_policy_evict_first();
+    n_tasks = p.hdr->n_tasks;
+  }
+
+  static __device__ __forceinline__ int runs(const TaskMeta& m) { return m.t >= 0 ? 1 + 2 * m.nb : 0; }
+
+  // Advance the next task's metadata by one dependent load (called between blocks so each load's
+  // latency hides behind compute); full == true finishes it now.
+  __device__ __forceinline__ void prefetch_next(bool full) {
+    if (nstage == 0) {
+      if (lane == 0) nxt_idx = atomicAdd(&p.hdr->work, 1);
+      nstage = 1;
+      if (!full) return;
+    }
+    if (nstage == 1) {
+      nxt_rec = load_record(p, __shfl_sync(0xffffffffu, nxt_idx, 0), n_tasks);
+      nstage = 2;
+      if (!full) return;
+    }
+    if (nstage == 2) {
+      task_from_record(p, nxt_rec, nxt);
+      nxt.ids = load_ids(p, nxt, lane);
+      nstage = 3;
+    }
+  }
+  __device__ __forceinline__ void issue_run(const TaskMeta& m, int r) {
+    const int slot = issued % T::NR;
+    unsigned char* dst = ring + slot * T::RUN;
+    if (r == 0) {
+      if (lane == 0) {
+        dev::mbar_arrive_expect_tx(&bars[slot], G * D * 2);
+        dev::bulk_g2s(dst, p.q + ((size_t)m.t * p.num_q_heads + (size_t)m.g * G) * D, G * D * 2, &bars[slot], pol);
+      }
+    } else {
+      const int id = __shfl_sync(0xffffffffu, m.ids, (r - 1) >> 1);
+      if (lane == 0) {
+        const int row = (((r - 1) & 1) ? p.layer_row0_v : p.layer_row0_k) + (id * p.num_kv_heads + m.g) * kBS;
+        dev::mbar_arrive_expect_tx(&bars[slot], T::RUN);
+#pragma unroll
+        for (int b = 0; b < T::BOXES; ++b) dev::tma_load_2d(dst + b * 2048, &p.kv_map, b * 64, row, &bars[slot], pol);
+      }
+    }
+    ++issued;
+  }
+  // Issue the next run of the stream (current task, then the next task), if there is one.
+  __device__ __forceinline__ void issue_next() {
+    if (icur == 0) {
+      if (ir < runs(cur)) {
+        issue_run(cur, ir++);
+        return;
+      }
+      icur = 1;
+      ir = 0;
+    }
+    prefetch_next(true);
+    if (ir < runs(nxt)) issue_run(nxt, ir++);
+  }
+  // Wait for the oldest run in the ring; returns its slot's shared-memory address.
+  __device__ __forceinline__ uint32_t wait_run() {
+    const int slot = consumed % T::NR;
+    if (!dev::mbar_wait(&bars[slot], (consumed / T::NR) & 1)) {
+      if (lane == 0) dev::set_error(p.err, PKV_DEVERR_WAIT_TIMEOUT);
+      ok = false;
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    return dev::smem_addr(ring + slot * T::RUN);
+  }
+  // The warp is done with the oldest run: recycle its slot for the next run of the stream.
+  __device__ __forceinline__ void release_run() {
+    __syncwarp();
+    ++consumed;
+    issue_next();
+  }
+  // Move to the next task; the issue cursor is already inside it.
+  __device__ __forceinline__ void advance() {
+    prefetch_next(true);
+    cur = nxt;
+    icur = 0;
+    nstage = 0;
+  }
+};
+
+// Output element held by register r of `lane` in the O^T fragment layout: its dim and its head.
+__device__ __forceinline__ void frag_coord(int lane, int r, int& dim, int& head) {
+  dim = 16 * (r >> 2) + (lane >> 2) + ((r & 2) ? 8 : 0);
+  head = ((lane & 3) << 1) + (r & 1);
+}
+
+template <int D, int G>
+__device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char* rings, uint64_t* all_bars,
+                                            int warp, int lane) {
+  using T = DecodeTraits<D, G>;
+  Worker<D, G> w(p, rings + warp * T::NR * T::RUN, all_bars + warp * T::NR, lane);
+  {
+    int idx = 0;
+    if (lane == 0) idx = atomicAdd(&p.hdr->work, 1);
+    task_from_record(p, load_record(p, __shfl_sync(0xffffffffu, idx, 0), w.n_tasks), w.cur);
+    w.cur.ids = load_ids(p, w.cur, lane);
+  }
+  for (int i = 0; i < T::NR; ++i) w.issue_next();
+
+  const int qh = lane >> 2;        // head whose q this lane feeds to the MMA (B operand column); key row too
+  const int h0 = (lane & 3) << 1;  // heads of this lane's score / output columns: h0, h0 + 1
+  while (w.cur.t >= 0 && w.ok) {
+    const TaskMeta d = w.cur;
+    w.prefetch_next(false);
+    // ---- q as the MMA B operand (Q^T: k = dims, n = heads), from the task's first ring run ----
+    // Rows G..7 of the 8-row tile hold stale bytes; they only feed score and output columns of heads
+    // >= G, which are never written out.
+    uint32_t qb[T::KS][2];
+    {
+      const uint32_t qs = w.wait_run();
+      if (!w.ok) break;
+#pragma unroll
+      for (int k2 = 0; k2 < T::KS / 2; ++k2) {
+        uint32_t r4[4];
+        dev::ldsm_x4(qs + (lane & 7) * (D * 2) + (4 * k2 + (lane >> 3)) * 16, r4);
+        qb[2 * k2][0] = r4[0];
+        qb[2 * k2][1] = r4[1];
+        qb[2 * k2 + 1][0] = r4[2];
+        qb[2 * k2 + 1][1] = r4[3];
+      }
+      w.release_run();
+    }
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[T::MT][4];
+#pragma unroll
+    for (int mt = 0; mt < T::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    for (int i = 0; i < d.nb; ++i) {
+      const int ntok = min(kBS, d.ctx - (d.s * p.split_blocks + i) * kBS);
+      // ---- S^T[16 keys x 8 heads] = K Q^T on the tensor cores ----
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const uint32_t ks_base = w.wait_run();
+        if (!w.ok) break;
+        const int kr = (lane & 7) + ((lane >> 3) & 1) * 8;  // key row this lane addresses for ldmatrix
+#pragma unroll
+        for (int ks = 0; ks < T::KS; ++ks) {
+          uint32_t a[4];
+          dev::ldsm_x4(ks_base + swz(kr, 2 * ks + (lane >> 4)), a);
+          dev::mma_16816(sc, a, qb[ks][0], qb[ks][1]);
+        }
+        w.release_run();
+      }
+      w.prefetch_next(false);  // one dependent metadata load of the next task per block, hidden by compute
+      // ---- online softmax (log2 domain); the lane holds keys qh, qh + 8 for heads h0, h0 + 1 ----
+      const bool v0 = qh < ntok, v1 = qh + 8 < ntok;
+      const float s0 = v0 ? sc[0] * p.scale_log2 : -INFINITY;  // key qh,     head h0
+      const float s1 = v0 ? sc[1] * p.scale_log2 : -INFINITY;  // key qh,     head h0 + 1
+      const float s2 = v1 ? sc[2] * p.scale_log2 : -INFINITY;  // key qh + 8, head h0
+      const float s3 = v1 ? sc[3] * p.scale_log2 : -INFINITY;  // key qh + 8, head h0 + 1
+      float b0 = fmaxf(s0, s2), b1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int m = 4; m < 32; m <<= 1) {
+        b0 = fmaxf(b0, __shfl_xor_sync(0xffffffffu, b0, m));
+        b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, m));
+      }
+      const float n0 = fmaxf(m0, b0), n1 = fmaxf(m1, b1);
+      const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+      m0 = n0;
+      m1 = n1;
+      const float p0 = exp2f(s0 - n0), p1 = exp2f(s1 - n1), p2 = exp2f(s2 - n0), p3 = exp2f(s3 - n1);
+      l0 = l0 * a0 + p0 + p2;
+      l1 = l1 * a1 + p1 + p3;
+#pragma unroll
+      for (int mt = 0; mt < T::MT; ++mt) {
+        o[mt][0] *= a0;
+        o[mt][1] *= a1;
+        o[mt][2] *= a0;
+        o[mt][3] *= a1;
+      }
+      // P^T as the B operand (k = keys, n = heads): transpose the [keys x heads] 8x8 fragments
+      const __half2 pk0 = __floats2half2_rn(p0, p1), pk1 = __floats2half2_rn(p2, p3);
+      const uint32_t pb0 = dev::movmatrix_t(*reinterpret_cast<const uint32_t*>(&pk0));
+      const uint32_t pb1 = dev::movmatrix_t(*reinterpret_cast<const uint32_t*>(&pk1));
+      // ---- O^T[d x 8 heads] += V^T P^T on the tensor cores ----
+      {
+        const uint32_t vs_base = w.wait_run();
+        if (!w.ok) break;
+        if (ntok < kBS) {  // rows past the context may hold anything: zero them so 0 * garbage cannot poison O
+          for (int idx = lane; idx < (kBS - ntok) * (D / 8); idx += 32) {
+            const int r = ntok + idx / (D / 8), c = idx % (D / 8);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vs_base + swz(r, c)), "r"(0) : "memory");
+          }
+          __syncwarp();
+        }
+        const int mat = lane >> 3;                      // ldmatrix matrix this lane addresses
+        const int vr = (lane & 7) + ((mat >> 1) << 3);  // its key row
+#pragma unroll
+        for (int mt = 0; mt < T::MT; ++mt) {
+          uint32_t a[4];
+          dev::ldsm_x4_t(vs_base + swz(vr, 2 * mt + (mat & 1)), a);
+          dev::mma_16816(o[mt], a, pb0, pb1);
+        }
+        if (ntok < kBS) dev::fence_proxy_async_smem();  // the zero-fill precedes the slot's next TMA write
+        w.release_run();
+      }
+    }
+    if (!w.ok) break;
+
+    // ---- finish the split ----
+#pragma unroll
+    for (int m = 4; m < 32; m <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, m);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, m);
+    }
+    const int hq0 = d.g * G;
+    if (d.nsplit == 1) {
+      const float i0 = 1.f / l0, i1 = 1.f / l1;
+#pragma unroll
+      for (int r = 0; r < T::OV; ++r) {
+        int dim, head;
+        frag_coord(lane, r, dim, head);
+        if (head < G)
+          p.out[((size_t)d.t * p.num_q_heads + hq0 + head) * D + dim] =
+              __float2half_rn(o[r >> 2][r & 3] * ((r & 1) ? i1 : i0));
+      }
+    } else {
+      const size_t tg = (size_t)d.t * p.num_kv_heads + d.g;
+      const size_t pidx = tg * p.max_splits + d.s;
+      float4* dst = reinterpret_cast<float4*>(p.part_o + (pidx * 32 + lane) * T::OV);
+#pragma unroll
+      for (int mt = 0; mt < T::MT; ++mt) dst[mt] = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
+      if (lane < 4) {
+        p.part_ml[pidx * kHeadsTile + h0] = make_float2(m0, l0);
+        p.part_ml[pidx * kHeadsTile + h0 + 1] = make_float2(m1, l1);
+      }
+    }
+    __syncwarp();
+    w.advance();
+  }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(DecodeTraits<D, G>::NTHREADS, DecodeTraits<D, G>::MINB)
+decode_kernel(const __grid_constant__ DecodeParams p) {
+  using T = DecodeTraits<D, G>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* rings =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rings + T::OFF_BAR);
   dev::griddep_wait();
   dev::griddep_launch_dependents();
-
-  const int t = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
-  const int ctx = __ldg(p.tok_ctx + t);
-  if (ctx <= 0) return;  // token handled elsewhere or its row is invalid
-  const int nblk = (ctx + kBS - 1) / kBS;
-  const int nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
-  if (s >= nsplit) return;
-  const int first = s * p.split_blocks;
-  const int nb = min(p.split_blocks, nblk - first);
-  const int row = __ldg(p.tok_row + t);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int i = 0; i < T::NSTAGE; ++i) {
-      dev::mbar_init(&full[i], 1);
-      dev::mbar_init(&empty[i], 1);
-    }
+  if (lane == 0) {
+    for (int i = 0; i < T::NR; ++i) dev::mbar_init(&bars[warp * T::NR + i], 1);
     dev::fence_mbar_init();
   }
   // one CTA-uniform decision (a racing error-word update must not split the CTA)
-  if (__syncthreads_or(threadIdx.x == 0 && dev::pool_poisoned(p.err))) return;
-
-  if (warp == T::NCW) {
-    // ---------------- producer warp: stream K/V runs of this split into the ring ----------------
-    const int32_t* bt = p.block_tables + (int64_t)row * p.max_blocks + first;
-    const size_t blk_stride = (size_t)p.num_kv_heads * kBS * D;
-    const size_t head_off = (size_t)g * kBS * D;
-    const uint64_t pol = dev::l2_policy_evict_first();
-    bool ok = true;
-    for (int base = 0; base < nb && ok; base += 32) {
-      int blk = 0;
-      if (base + lane < nb) {
-        blk = __ldg(bt + base + lane);
-        if (blk < 0 || blk >= p.num_blocks) {
-          dev::set_error(p.err, PKV_DEVERR_BLOCK_RANGE);
-          blk = 0;  // keep the copy in bounds; the output of this token is flagged as invalid
-        }
-      }
-      const int cnt = min(32, nb - base);
-      for (int k = 0; k < cnt; ++k) {
-        const int b = __shfl_sync(0xffffffffu, blk, k);
-        if (lane == 0 && ok) {
-          const int idx = base + k;
-          const int slot = idx % T::NSTAGE, round = idx / T::NSTAGE;
-          if (round > 0 && !dev::mbar_wait(&empty[slot], (round - 1) & 1)) {
-            dev::set_error(p.err, PKV_DEVERR_WAIT_TIMEOUT);
-            ok = false;
-          } else {
-            unsigned char* dst = smem + slot * 2 * T::RUN;
-            const size_t src = (size_t)b * blk_stride + head_off;
-            dev::mbar_arrive_expect_tx(&full[slot], 2 * T::RUN);
-            dev::bulk_g2s(dst, p.kpool + src, T::RUN, &full[slot], pol);
-            dev::bulk_g2s(dst + T::RUN, p.vpool + src, T::RUN, &full[slot], pol);
-          }
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-    }
-    return;
-  }
-
-  // ---------------- consumer warps ----------------
-  const int tq = lane / T::DG;  // key row within a warp step
-  const int dg = lane % T::DG;  // 16-dim slice: dims [8 dg, 8 dg + 8) and [D/2 + 8 dg, D/2 + 8 dg + 8)
-  using RS = ReduceScatter<T::GP, T::DG / 2>;
-  const int hbase = RS::head_base(lane);
-  const bool primary = (dg % T::REP) == 0;
-
-  float2 qr[G][8];
-  {
-    const __half* qb = p.q + ((size_t)t * p.num_q_heads + (size_t)g * G) * D;
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(qb + j * D + (dg + c * T::DG) * 8);
-        float2 f[4];
-        h8_to_f2(raw, f);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) qr[j][c * 4 + e] = make_float2(f[e].x * p.scale_log2, f[e].y * p.scale_log2);
-      }
-    }
-  }
-
-  float m_run[T::R], l_run[T::R];
-#pragma unroll
-  for (int r = 0; r < T::R; ++r) {
-    m_run[r] = -INFINITY;
-    l_run[r] = 0.f;
-  }
-  float2 o[G][T::DPL / 2];
-#pragma unroll
-  for (int j = 0; j < G; ++j)
-#pragma unroll
-    for (int e = 0; e < T::DPL / 2; ++e) o[j][e] = make_float2(0.f, 0.f);
-
-  float* Pw = reinterpret_cast<float*>(smem + T::OFF_P) + warp * kBS * T::GP;
-  float* Aw = reinterpret_cast<float*>(smem + T::OFF_A) + warp * T::GP;
-  bool timed_out = false;
-
-  for (int i = warp; i < nb; i += T::NCW) {
-    const int slot = i % T::NSTAGE, round = i / T::NSTAGE;
-    if (!dev::mbar_wait(&full[slot], round & 1)) {
-      if (lane == 0) dev::set_error(p.err, PKV_DEVERR_WAIT_TIMEOUT);
-      timed_out = true;
-      break;
-    }
-    const __half* Ks = reinterpret_cast<const __half*>(smem + slot * 2 * T::RUN);
-    const __half* Vs = Ks + kBS * D;
-    const int ntok = min(kBS, ctx - (first + i) * kBS);
-
-    // scores (log2 domain) of this block's keys
-    float sc[T::STEPS][T::R];
-#pragma unroll
-    for (int st = 0; st < T::STEPS; ++st) {
-      const int tok = st * T::TPW + tq;
-      float2 kf[8];
-      h8_to_f2(*reinterpret_cast<const uint4*>(Ks + tok * D + dg * 8), kf);
-      h8_to_f2(*reinterpret_cast<const uint4*>(Ks + tok * D + (dg + T::DG) * 8), kf + 4);
-      float v[T::GP];
-#pragma unroll
-      for (int j = 0; j < T::GP; ++j) {
-        if (j < G) {
-          float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) a = __ffma2_rn(qr[j][e], kf[e], a);
-          v[j] = a.x + a.y;
-        } else {
-          v[j] = 0.f;
-        }
-      }
-      RS::run(v, lane);
-#pragma unroll
-      for (int r = 0; r < T::R; ++r) sc[st][r] = tok < ntok ? v[r] : -INFINITY;
-    }
-
-    // online softmax update per head
-#pragma unroll
-    for (int r = 0; r < T::R; ++r) {
-      float bm = sc[0][r];
-#pragma unroll
-      for (int st = 1; st < T::STEPS; ++st) bm = fmaxf(bm, sc[st][r]);
-#pragma unroll
-      for (int m = T::DG; m < 32; m <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, m));
-      const float mn = fmaxf(m_run[r], bm);
-      const float alpha = exp2f(m_run[r] - mn);
-      float ls = 0.f;
-#pragma unroll
-      for (int st = 0; st < T::STEPS; ++st) {
-        const float pv = exp2f(sc[st][r] - mn);
-        sc[st][r] = pv;
-        ls += pv;
-      }
-      l_run[r] = l_run[r] * alpha + ls;
-      m_run[r] = mn;
-      const int h = hbase + r;
-      if (primary && h < G) {
-#pragma unroll
-        for (int st = 0; st < T::STEPS; ++st) Pw[(st * T::TPW + tq) * T::GP + h] = sc[st][r];
-        if (tq == 0) Aw[h] = alpha;
-      }
-    }
-    __syncwarp();
-
-    // value accumulation: lane owns dims [lane * DPL, lane * DPL + DPL)
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      const float a = Aw[j];
-#pragma unroll
-      for (int e = 0; e < T::DPL / 2; ++e) o[j][e] = __fmul2_rn(o[j][e], make_float2(a, a));
-    }
-#pragma unroll 4
-    for (int tk = 0; tk < ntok; ++tk) {
-      float2 vf[T::DPL / 2];
-      const __half2* vrow = reinterpret_cast<const __half2*>(Vs + tk * D + lane * T::DPL);
-#pragma unroll
-      for (int e = 0; e < T::DPL / 2; ++e) vf[e] = __half22float2(vrow[e]);
-      const float* prow = Pw + tk * T::GP;
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        const float pj = prow[j];
-        const float2 pp = make_float2(pj, pj);
-#pragma unroll
-        for (int e = 0; e < T::DPL / 2; ++e) o[j][e] = __ffma2_rn(pp, vf[e], o[j][e]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) dev::mbar_arrive(&empty[slot]);
-  }
-  (void)timed_out;
-
-  // ---------------- combine the four warps ----------------
-  float* Mw = reinterpret_cast<float*>(smem + T::OFF_M);
-  float* Lw = reinterpret_cast<float*>(smem + T::OFF_L);
-#pragma unroll
-  for (int r = 0; r < T::R; ++r) {
-    float l = l_run[r];
-#pragma unroll
-    for (int m = T::DG; m < 32; m <<= 1) l += __shfl_xor_sync(0xffffffffu, l, m);
-    const int h = hbase + r;
-    if (primary && tq == 0 && h < G) {
-      Mw[warp * T::GP + h] = m_run[r];
-      Lw[warp * T::GP + h] = l;
-    }
-  }
-  dev::named_bar_sync(1, T::NCW * 32);  // every consumer is done with the ring
-  float* Ow = reinterpret_cast<float*>(smem);  // [NCW][G][D], reusing the ring
-#pragma unroll
-  for (int j = 0; j < G; ++j)
-#pragma unroll
-    for (int e = 0; e < T::DPL / 2; ++e)
-      *reinterpret_cast<float2*>(Ow + (warp * G + j) * D + lane * T::DPL + 2 * e) = o[j][e];
-  dev::named_bar_sync(1, T::NCW * 32);
-
-  for (int e = threadIdx.x; e < G * D; e += T::NCW * 32) {
-    const int j = e / D, dim = e - j * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < T::NCW; ++w) M = fmaxf(M, Mw[w * T::GP + j]);
-    float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < T::NCW; ++w) {
-      const float f = exp2f(Mw[w * T::GP + j] - M);
-      L += Lw[w * T::GP + j] * f;
-      O += Ow[(w * G + j) * D + dim] * f;
-    }
-    const int h = g * G + j;
-    if (nsplit == 1) {
-      p.out[((size_t)t * p.num_q_heads + h) * D + dim] = __float2half_rn(O / L);
-    } else {
-      const size_t pi = ((size_t)t * p.max_splits + s) * p.num_q_heads + h;
-      p.part_o[pi * D + dim] = O;
-      if (dim == 0) p.part_ml[pi] = make_float2(M, L);
+  const bool poisoned = __syncthreads_or(threadIdx.x == 0 && dev::pool_poisoned(p.err));
+  if (!poisoned) worker_loop<D, G>(p, rings, bars, warp, lane);
+  // the last CTA out resets the task counter for the next launch on this plan
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&p.hdr->done, 1) == (int)gridDim.x - 1) {
+      p.hdr->work = 0;
+      p.hdr->done = 0;
+      __threadfence();
     }
   }
 }
 
+// ---------------------------------------------------------------------------------------------------
+// Merge of tokens with more than one split.  Grid (token, KV head, chunk of partial elements), 256
+// threads = SG split groups x (256 / SG) element threads; partials are read in the decode's MMA fragment
+// order, element e of a partial being register e % (D/4) of lane e / (D/4).
+// ---------------------------------------------------------------------------------------------------
 struct MergeParams {
   const float* part_o;
   const float2* part_ml;
   const int32_t* tok_ctx;
   __half* out;
   int num_q_heads;
+  int num_kv_heads;
+  int group;
   int split_blocks;
   int max_splits;
 };
 
-// One CTA per (token, query head) of a token with more than one split.
-template <int D>
-__global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
+template <int D, int SG>
+__global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+  constexpr int OV = D / 4;                  // fp32 values per lane of a partial
+  constexpr int TE = 256 / SG;               // threads along the elements
+  constexpr int EPC = SG == 1 ? 32 * OV : TE;  // elements per CTA
+  constexpr int EPT = EPC / TE;              // elements per thread
+  __shared__ float sM[kHeadsTile], sL[kHeadsTile];
+  __shared__ float red[256];
   dev::griddep_wait();
   dev::griddep_launch_dependents();
-  const int t = blockIdx.x, h = blockIdx.y;
+  const int t = blockIdx.x, g = blockIdx.y;
   const int ctx = __ldg(p.tok_ctx + t);
   if (ctx <= 0) return;
   const int nblk = (ctx + kBS - 1) / kBS;
   const int nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
   if (nsplit <= 1) return;
-  const size_t base = (size_t)t * p.max_splits * p.num_q_heads + h;
-  const float2* ml = p.part_ml + base;
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[(size_t)s * p.num_q_heads].x);
-  for (int dim = threadIdx.x; dim < D; dim += 128) {
-    float L = 0.f, O = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float2 v = ml[(size_t)s * p.num_q_heads];
-      const float f = exp2f(v.x - M);
-      L += v.y * f;
-      O += p.part_o[(base + (size_t)s * p.num_q_heads) * D + dim] * f;
+  const size_t sb = ((size_t)t * p.num_kv_heads + g) * p.max_splits;
+  const int tid = threadIdx.x;
+  // per-head max and sum over the splits: thread (head tid % 8, split stride group tid / 8)
+  {
+    const int h = tid & 7;
+    float M = -INFINITY;
+    for (int s = tid >> 3; s < nsplit; s += 32) M = fmaxf(M, p.part_ml[(sb + s) * kHeadsTile + h].x);
+    red[tid] = M;
+    __syncthreads();
+    if (tid < 8) {
+      float x = red[tid];
+      for (int k = 1; k < 32; ++k) x = fmaxf(x, red[tid + 8 * k]);
+      sM[tid] = x;
     }
-    p.out[((size_t)t * p.num_q_heads + h) * D + dim] = __float2half_rn(O / L);
+    __syncthreads();
+    M = sM[h];
+    float L = 0.f;
+    for (int s = tid >> 3; s < nsplit; s += 32) {
+      const float2 ml = p.part_ml[(sb + s) * kHeadsTile + h];
+      L += ml.y * exp2f(ml.x - M);
+    }
+    __syncthreads();
+    red[tid] = L;
+    __syncthreads();
+    if (tid < 8) {
+      float x = 0.f;
+      for (int k = 0; k < 32; ++k) x += red[tid + 8 * k];
+      sL[tid] = x;
+    }
+    __syncthreads();
+  }
+  const int te = tid % TE, sg = tid / TE;
+  float acc[EPT];
+  int heads[EPT];
+#pragma unroll
+  for (int k = 0; k < EPT; ++k) {
+    const int e = blockIdx.z * EPC + te + k * TE;
+    heads[k] = (((e / OV) & 3) << 1) + ((e % OV) & 1);
+    acc[k] = 0.f;
+  }
+  for (int s = sg; s < nsplit; s += SG) {
+    const float* po = p.part_o + (sb + s) * 32 * OV;
+    const float2* pml = p.part_ml + (sb + s) * kHeadsTile;
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      const int e = blockIdx.z * EPC + te + k * TE;
+      acc[k] += po[e] * exp2f(pml[heads[k]].x - sM[heads[k]]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < EPT; ++k) {
+    if constexpr (SG > 1) {
+      __syncthreads();
+      red[tid] = acc[k];
+      __syncthreads();
+      if (sg != 0) continue;
+      for (int j = 1; j < SG; ++j) acc[k] += red[te + j * TE];
+    }
+    const int e = blockIdx.z * EPC + te + k * TE;
+    const int lane = e / OV, r = e % OV;
+    const int dim = 16 * (r >> 2) + (lane >> 2) + ((r & 2) ? 8 : 0);
+    const int head = heads[k];
+    if (head < p.group)
+      p.out[((size_t)t * p.num_q_heads + (size_t)g * p.group + head) * D + dim] = __float2half_rn(acc[k] / sL[head]);
   }
 }
 
-// Per packed token: its row and causal context (keys it sees); 0 marks a token no kernel should touch.
-// Also validates the per-row metadata, recording violations in the device error word.
-__global__ void __launch_bounds__(256) plan_kernel(const int32_t* __restrict__ context_lens,
-                                                   const int32_t* __restrict__ qsl, int num_seqs, int num_tokens,
-                                                   int max_ctx, int32_t* __restrict__ tok_row,
-                                                   int32_t* __restrict__ tok_ctx, int32_t* err) {
+// ---------------------------------------------------------------------------------------------------
+// Plan: token table, task list, counters.  One CTA (block-wide scans over the tokens).
+// ---------------------------------------------------------------------------------------------------
+constexpr int kPlanThreads = 1024;
+
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;  // inclusive prefix over warps
+  }
+  __syncthreads();
+  const int before = warp == 0 ? 0 : warp_sums[warp - 1];
+  *total = warp_sums[(blockDim.x >> 5) - 1];
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ context_lens,
+                                                            const int32_t* __restrict__ qsl, int num_seqs,
+                                                            int num_tokens, int max_ctx, int split_blocks,
+                                                            int num_kv_heads, int32_t* __restrict__ tok_row,
+                                                            int32_t* __restrict__ tok_ctx, int4* __restrict__ tasks,
+                                                            WsHeader* hdr, int32_t* err) {
+  __shared__ int warp_sums[32];
   dev::griddep_wait();
   dev::griddep_launch_dependents();
-  const int n = max(num_seqs, num_tokens);
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    if (i < num_seqs) {
-      const int q0 = __ldg(qsl + i), q1 = __ldg(qsl + i + 1), ctx = __ldg(context_lens + i);
-      if (q1 < q0 || (i == 0 && q0 != 0) || (i == num_seqs - 1 && q1 != num_tokens))
-        dev::set_error(err, PKV_DEVERR_QSL);
-      if (q1 - q0 < 1 || ctx < q1 - q0 || ctx > max_ctx) dev::set_error(err, PKV_DEVERR_ROW_META);
+  for (int i = threadIdx.x; i < num_seqs; i += blockDim.x) {
+    const int q0 = __ldg(qsl + i), q1 = __ldg(qsl + i + 1), ctx = __ldg(context_lens + i);
+    if (q1 < q0 || (i == 0 && q0 != 0) || (i == num_seqs - 1 && q1 != num_tokens))
+      dev::set_error(err, PKV_DEVERR_QSL);
+    if (q1 - q0 < 1 || ctx < q1 - q0 || ctx > max_ctx) dev::set_error(err, PKV_DEVERR_ROW_META);
+  }
+  int carry = 0;
+  for (int pass = 0; pass < 2; ++pass) {  // pass 0: full splits; pass 1: each token's partial last split
+    for (int base = 0; base < num_tokens; base += blockDim.x) {
+      const int t = base + threadIdx.x;
+      int nblk = 0, row = 0, c = 0;
+      if (t < num_tokens) {
+        if (pass == 0) {
+          const int b = dev::row_of_token(qsl, num_seqs, t);
+          const int q0 = __ldg(qsl + b), q1 = __ldg(qsl + b + 1), ctx = __ldg(context_lens + b);
+          const int q_len = q1 - q0;
+          if (t >= q0 && t < q1 && q_len >= 1 && ctx >= q_len && ctx <= max_ctx) c = ctx - q_len + (t - q0) + 1;
+          tok_row[t] = b;
+          tok_ctx[t] = c;
+          row = b;
+        } else {
+          c = tok_ctx[t];
+          row = tok_row[t];
+        }
+        nblk = (c + kBS - 1) / kBS;
+      }
+      const int nfull = nblk / split_blocks;
+      const int ntail = nblk % split_blocks ? 1 : 0;
+      const int cnt = (pass == 0 ? nfull : ntail) * num_kv_heads;
+      int total = 0;
+      const int off = carry + block_exclusive_scan(cnt, warp_sums, &total);
+      if (cnt > 0) {
+        if (pass == 0) {
+          for (int g = 0; g < num_kv_heads; ++g)
+            for (int s = 0; s < nfull; ++s) tasks[off + g * nfull + s] = make_int4(t, g | (s << 8), row, c);
+        } else {
+          for (int g = 0; g < num_kv_heads; ++g) tasks[off + g] = make_int4(t, g | (nfull << 8), row, c);
+        }
+      }
+      carry += total;
+      __syncthreads();  // warp_sums is reused by the next chunk
     }
-    if (i < num_tokens) {
-      const int b = dev::row_of_token(qsl, num_seqs, i);
-      const int q0 = __ldg(qsl + b), q1 = __ldg(qsl + b + 1), ctx = __ldg(context_lens + b);
-      const int q_len = q1 - q0;
-      int c = 0;
-      if (i >= q0 && i < q1 && q_len >= 1 && ctx >= q_len && ctx <= max_ctx) c = ctx - q_len + (i - q0) + 1;
-      tok_row[i] = b;
-      tok_ctx[i] = c;
-    }
+  }
+  if (threadIdx.x == 0) {
+    hdr->n_tasks = carry;
+    hdr->work = 0;
+    hdr->done = 0;
   }
 }
 
 // ---------------------------------------------------------------------------------------------------
-// Workspace layout
+// Workspace layout and launches
 // ---------------------------------------------------------------------------------------------------
 struct WsLayout {
-  size_t tok_row, tok_ctx, part_ml, part_o, total;
+  size_t hdr, tok_row, tok_ctx, tasks, part_ml, part_o, total;
   int max_splits;
+  int64_t max_tasks;
 };
 
 static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
@@ -444,45 +627,121 @@ static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 static WsLayout ws_layout(const pkv_config& c, int num_tokens, int max_blocks) {
   WsLayout w;
   w.max_splits = (max_blocks + c.split_blocks - 1) / c.split_blocks;
+  w.max_tasks = (int64_t)num_tokens * c.num_kv_heads * w.max_splits;
   size_t off = 0;
+  w.hdr = off;
+  off += sizeof(WsHeader);
   w.tok_row = off;
   off += up256((size_t)num_tokens * 4);
   w.tok_ctx = off;
   off += up256((size_t)num_tokens * 4);
-  const size_t parts = w.max_splits > 1 ? (size_t)num_tokens * w.max_splits * c.num_q_heads : 0;
+  w.tasks = off;
+  off += up256((size_t)w.max_tasks * sizeof(int4));
+  const size_t parts = w.max_splits > 1 ? (size_t)w.max_tasks : 0;  // one partial per (token, KV head, split)
   w.part_ml = off;
-  off += up256(parts * sizeof(float2));
+  off += up256(parts * kHeadsTile * sizeof(float2));
   w.part_o = off;
-  off += up256(parts * c.head_dim * sizeof(float));
+  off += up256(parts * 32 * (c.head_dim / 4) * sizeof(float));
   w.total = off;
   return w;
 }
 
 template <int D, int G>
-static cudaError_t launch_decode(const DecodeParams& p, int num_tokens, int num_kv_heads, int max_splits,
-                                 cudaStream_t stream) {
+static cudaError_t launch_decode(const DecodeParams& p, int num_sms, int64_t max_tasks, cudaStream_t stream) {
   using T = DecodeTraits<D, G>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static int per_sm = 0;
+  if (per_sm == 0) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, G>, T::NTHREADS, T::SMEM);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
   }
-  return launch_pdl(decode_kernel<D, G>, dim3(num_tokens, num_kv_heads, max_splits), dim3(T::NTHREADS), T::SMEM,
-                    stream, p);
+  int64_t grid = (int64_t)num_sms * per_sm;
+  const int64_t groups = (max_tasks + T::NW - 1) / T::NW;
+  if (grid > groups) grid = groups;
+  if (grid < 1) grid = 1;
+  return launch_pdl(decode_kernel<D, G>, dim3((unsigned)grid), dim3(T::NTHREADS), T::SMEM, stream, p);
 }
 
 template <int D>
-static cudaError_t launch_decode_g(int group, const DecodeParams& p, int num_tokens, int num_kv_heads,
-                                   int max_splits, cudaStream_t stream) {
+static cudaError_t launch_decode_g(int group, const DecodeParams& p, int num_sms, int64_t max_tasks,
+                                   cudaStream_t stream) {
   switch (group) {
-    case 1: return launch_decode<D, 1>(p, num_tokens, num_kv_heads, max_splits, stream);
-    case 2: return launch_decode<D, 2>(p, num_tokens, num_kv_heads, max_splits, stream);
-    case 4: return launch_decode<D, 4>(p, num_tokens, num_kv_heads, max_splits, stream);
-    case 6: return launch_decode<D, 6>(p, num_tokens, num_kv_heads, max_splits, stream);
-    case 8: return launch_decode<D, 8>(p, num_tokens, num_kv_heads, max_splits, stream);
+    case 1: return launch_decode<D, 1>(p, num_sms, max_tasks, stream);
+    case 2: return launch_decode<D, 2>(p, num_sms, max_tasks, stream);
+    case 4: return launch_decode<D, 4>(p, num_sms, max_tasks, stream);
+    case 6: return launch_decode<D, 6>(p, num_sms, max_tasks, stream);
+    case 8: return launch_decode<D, 8>(p, num_sms, max_tasks, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+static cudaError_t launch_plan(pkv_pool* pool, char* ws, const WsLayout& w, const int32_t* context_lens,
+                               const int32_t* qsl, int num_seqs, int num_tokens, int max_blocks, cudaStream_t s) {
+  const pkv_config& c = pool->cfg;
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, context_lens, qsl, num_seqs, num_tokens,
+                    max_blocks * kBS, (int)c.split_blocks, (int)c.num_kv_heads,
+                    reinterpret_cast<int32_t*>(ws + w.tok_row), reinterpret_cast<int32_t*>(ws + w.tok_ctx),
+                    reinterpret_cast<int4*>(ws + w.tasks), reinterpret_cast<WsHeader*>(ws + w.hdr),
+                    pool->dev_error);
+}
+
+// decode (+ merge of very long tokens) for one layer on a planned workspace
+static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, const int32_t* block_tables,
+                                   int max_blocks, int num_tokens, void* out, char* ws, const WsLayout& w,
+                                   cudaStream_t s, int* launches) {
+  const pkv_config& c = pool->cfg;
+  DecodeParams p;
+  p.kv_map = pool->kv_map;
+  p.q = static_cast<const __half*>(q);
+  p.block_tables = block_tables;
+  p.tok_row = reinterpret_cast<const int32_t*>(ws + w.tok_row);
+  p.tok_ctx = reinterpret_cast<const int32_t*>(ws + w.tok_ctx);
+  p.tasks = reinterpret_cast<const int4*>(ws + w.tasks);
+  p.hdr = reinterpret_cast<WsHeader*>(ws + w.hdr);
+  p.out = static_cast<__half*>(out);
+  p.part_o = reinterpret_cast<float*>(ws + w.part_o);
+  p.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
+  p.err = pool->dev_error;
+  const int rows_per_pool = c.num_blocks * c.num_kv_heads * c.block_size;
+  p.layer_row0_k = (layer * 2) * rows_per_pool;
+  p.layer_row0_v = (layer * 2 + 1) * rows_per_pool;
+  p.max_blocks = max_blocks;
+  p.num_q_heads = c.num_q_heads;
+  p.num_kv_heads = c.num_kv_heads;
+  p.num_blocks = c.num_blocks;
+  p.split_blocks = c.split_blocks;
+  p.max_splits = w.max_splits;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+  const int group = c.num_q_heads / c.num_kv_heads;
+  cudaError_t e;
+  switch (c.head_dim) {
+    case 64: e = launch_decode_g<64>(group, p, pool->num_sms, w.max_tasks, s); break;
+    case 128: e = launch_decode_g<128>(group, p, pool->num_sms, w.max_tasks, s); break;
+    case 256: e = launch_decode_g<256>(group, p, pool->num_sms, w.max_tasks, s); break;
+    default: return fail(PKV_ERR_UNSUPPORTED, "head_dim");
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  *launches += 1;
+  if (w.max_splits > 1) {
+    MergeParams m{p.part_o, p.part_ml, p.tok_ctx, p.out, c.num_q_heads, c.num_kv_heads, group, c.split_blocks,
+                  w.max_splits};
+    const bool wide = w.max_splits > kWideMergeSplits;
+    const dim3 grid(num_tokens, c.num_kv_heads, wide ? (8 * c.head_dim) / 64 : 1);
+    switch (c.head_dim * 2 + (wide ? 1 : 0)) {
+      case 128: e = launch_pdl(merge_kernel<64, 1>, grid, dim3(256), 0, s, m); break;
+      case 129: e = launch_pdl(merge_kernel<64, 4>, grid, dim3(256), 0, s, m); break;
+      case 256: e = launch_pdl(merge_kernel<128, 1>, grid, dim3(256), 0, s, m); break;
+      case 257: e = launch_pdl(merge_kernel<128, 4>, grid, dim3(256), 0, s, m); break;
+      case 512: e = launch_pdl(merge_kernel<256, 1>, grid, dim3(256), 0, s, m); break;
+      default: e = launch_pdl(merge_kernel<256, 4>, grid, dim3(256), 0, s, m); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    *launches += 1;
+  }
+  return PKV_OK;
 }
 
 }  // namespace pkv
@@ -496,20 +755,38 @@ extern "C" size_t pkv_attention_workspace_bytes(const pkv_pool* pool, int32_t nu
 }
 
 static pkv_status check_common(pkv_pool* pool, const int32_t* context_lens, const int32_t* qsl, int32_t num_seqs,
-                               int32_t num_tokens, int32_t max_blocks, void* workspace, size_t ws_bytes) {
+                               int32_t num_tokens, int32_t max_blocks) {
   if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
   if (num_seqs < 0 || num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "sizes must be >= 0");
   if (num_tokens > 0 && num_seqs < 1) return fail(PKV_ERR_INVALID_ARG, "tokens without rows");
   if (num_seqs > num_tokens) return fail(PKV_ERR_INVALID_ARG, "every row needs at least one query token");
   if (max_blocks < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
-  if (num_tokens > 0 && (!context_lens || !qsl || !workspace))
-    return fail(PKV_ERR_INVALID_ARG, "metadata and workspace pointers must be non-NULL");
+  if (num_tokens > 0 && (!context_lens || !qsl)) return fail(PKV_ERR_INVALID_ARG, "metadata pointers must be non-NULL");
+  const pkv_config& c = pool->cfg;
+  if (c.split_blocks > kMaxSplitBlocks)
+    return fail(PKV_ERR_UNSUPPORTED, "split_blocks above " + std::to_string(kMaxSplitBlocks));
+  const int64_t splits = ((int64_t)max_blocks + c.split_blocks - 1) / c.split_blocks;
+  if (splits >= (1 << 23) || (int64_t)num_tokens * c.num_kv_heads * splits >= (1ll << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "too many splits in one pass; raise split_blocks");
+  return PKV_OK;
+}
+
+static pkv_status check_workspace(pkv_pool* pool, void* workspace, size_t ws_bytes, int32_t num_tokens,
+                                  int32_t max_blocks) {
+  if (num_tokens > 0 && !workspace) return fail(PKV_ERR_INVALID_ARG, "workspace must be non-NULL");
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   const WsLayout w = ws_layout(pool->cfg, num_tokens, max_blocks);
-  if (w.max_splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits per row; raise split_blocks");
   if (ws_bytes < w.total)
     return fail(PKV_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(w.total) + " bytes");
+  return PKV_OK;
+}
+
+static pkv_status check_io(const void* q, const void* out, const int32_t* block_tables) {
+  if (!q || !out || !block_tables) return fail(PKV_ERR_INVALID_ARG, "q, out and block_tables must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  if (q == out) return fail(PKV_ERR_INVALID_ARG, "out may not alias q");
   return PKV_OK;
 }
 
@@ -517,21 +794,15 @@ extern "C" pkv_status pkv_attention_plan(pkv_pool* pool, const int32_t* context_
                                          int32_t num_seqs, int32_t num_tokens, int32_t max_blocks_per_seq,
                                          void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
-  pkv_status st = check_common(pool, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq,
-                               workspace, workspace_bytes);
+  pkv_status st = check_common(pool, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq);
+  if (st == PKV_OK) st = check_workspace(pool, workspace, workspace_bytes, num_tokens, max_blocks_per_seq);
   if (st != PKV_OK) return st;
   pool->last_launches = 0;
   pool->plan = PlanKey{workspace, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq};
   if (num_tokens == 0) return PKV_OK;
   const WsLayout w = ws_layout(pool->cfg, num_tokens, max_blocks_per_seq);
-  char* ws = static_cast<char*>(workspace);
-  const int n = num_seqs > num_tokens ? num_seqs : num_tokens;
-  int blocks = (n + 255) / 256;
-  if (blocks > pool->num_sms * 4) blocks = pool->num_sms * 4;
-  cudaError_t e = launch_pdl(plan_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, context_lens,
-                             query_start_loc, (int)num_seqs, (int)num_tokens, (int)(max_blocks_per_seq * kBS),
-                             reinterpret_cast<int32_t*>(ws + w.tok_row), reinterpret_cast<int32_t*>(ws + w.tok_ctx),
-                             pool->dev_error);
+  cudaError_t e = launch_plan(pool, static_cast<char*>(workspace), w, context_lens, query_start_loc, num_seqs,
+                              num_tokens, max_blocks_per_seq, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     pool->plan = PlanKey{};
     return cuda_fail(e, "plan launch");
@@ -545,65 +816,24 @@ extern "C" pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q
                                     const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens, void* out,
                                     void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
-  pkv_status st = check_common(pool, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq,
-                               workspace, workspace_bytes);
+  pkv_status st = check_common(pool, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq);
+  if (st == PKV_OK) st = check_workspace(pool, workspace, workspace_bytes, num_tokens, max_blocks_per_seq);
   if (st != PKV_OK) return st;
   pool->last_launches = 0;
-  const pkv_config& c = pool->cfg;
-  if (layer < 0 || layer >= c.num_layers) return fail(PKV_ERR_OUT_OF_RANGE, "layer out of range");
+  if (layer < 0 || layer >= pool->cfg.num_layers) return fail(PKV_ERR_OUT_OF_RANGE, "layer out of range");
   if (num_tokens == 0) return PKV_OK;
-  if (!q || !out || !block_tables) return fail(PKV_ERR_INVALID_ARG, "q, out and block_tables must be non-NULL");
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
-    return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
-  if (q == out) return fail(PKV_ERR_INVALID_ARG, "out may not alias q");
+  st = check_io(q, out, block_tables);
+  if (st != PKV_OK) return st;
   const PlanKey& k = pool->plan;
   if (k.workspace != workspace || k.context_lens != context_lens || k.query_start_loc != query_start_loc ||
       k.num_seqs != num_seqs || k.num_tokens != num_tokens || k.max_blocks_per_seq != max_blocks_per_seq)
     return fail(PKV_ERR_INVALID_ARG, "no matching plan: call pkv_attention_plan for this workspace and metadata");
-
-  const WsLayout w = ws_layout(c, num_tokens, max_blocks_per_seq);
-  char* ws = static_cast<char*>(workspace);
-  DecodeParams p;
-  p.q = static_cast<const __half*>(q);
-  p.kpool = static_cast<const __half*>(pkv_pool_layer_ptr(pool, layer, 0));
-  p.vpool = static_cast<const __half*>(pkv_pool_layer_ptr(pool, layer, 1));
-  p.block_tables = block_tables;
-  p.tok_row = reinterpret_cast<const int32_t*>(ws + w.tok_row);
-  p.tok_ctx = reinterpret_cast<const int32_t*>(ws + w.tok_ctx);
-  p.out = static_cast<__half*>(out);
-  p.part_o = reinterpret_cast<float*>(ws + w.part_o);
-  p.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
-  p.err = pool->dev_error;
-  p.max_blocks = max_blocks_per_seq;
-  p.num_q_heads = c.num_q_heads;
-  p.num_kv_heads = c.num_kv_heads;
-  p.num_blocks = c.num_blocks;
-  p.split_blocks = c.split_blocks;
-  p.max_splits = w.max_splits;
-  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
-
-  const int group = c.num_q_heads / c.num_kv_heads;
-  cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e;
-  switch (c.head_dim) {
-    case 64: e = launch_decode_g<64>(group, p, num_tokens, c.num_kv_heads, w.max_splits, s); break;
-    case 128: e = launch_decode_g<128>(group, p, num_tokens, c.num_kv_heads, w.max_splits, s); break;
-    case 256: e = launch_decode_g<256>(group, p, num_tokens, c.num_kv_heads, w.max_splits, s); break;
-    default: return fail(PKV_ERR_UNSUPPORTED, "head_dim");
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  pool->last_launches = 1;
-  if (w.max_splits > 1) {
-    MergeParams m{p.part_o, p.part_ml, p.tok_ctx, p.out, c.num_q_heads, c.split_blocks, w.max_splits};
-    switch (c.head_dim) {
-      case 64: e = launch_pdl(merge_kernel<64>, dim3(num_tokens, c.num_q_heads), dim3(128), 0, s, m); break;
-      case 128: e = launch_pdl(merge_kernel<128>, dim3(num_tokens, c.num_q_heads), dim3(128), 0, s, m); break;
-      default: e = launch_pdl(merge_kernel<256>, dim3(num_tokens, c.num_q_heads), dim3(128), 0, s, m); break;
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-    pool->last_launches = 2;
-  }
-  return PKV_OK;
+  const WsLayout w = ws_layout(pool->cfg, num_tokens, max_blocks_per_seq);
+  int launches = 0;
+  st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_tokens, out,
+                        static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches);
+  pool->last_launches = launches;
+  return st;
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -611,12 +841,10 @@ extern "C" pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q
 //
 // Some callers cannot hand the library a workspace: an engine that has already reserved every byte of
 // device memory for its own pools, or a caller that may not issue cudaMalloc (which can synchronise the
-// whole device) while a pass is in flight.  For them the split-K scratch -- the per-token row/context
-// table and the partial (m, l, o) results -- lives in one fixed array compiled into this library.
-// Each device that loads the library holds the array until the process exits.
+// whole device) while a pass is in flight.  For them the split-K scratch -- the per-token table, the
+// task list, the merge counters and the partial (m, l, o) results -- lives in one fixed array compiled
+// into this library.  Each device that loads the library holds the array until the process exits.
 // ---------------------------------------------------------------------------------------------------
-#include <mutex>
-
 namespace pkv {
 
 constexpr size_t kNoAllocScratchBytes = PKV_NOALLOC_SCRATCH_BYTES;  // 16 MiB per device
@@ -649,22 +877,14 @@ extern "C" pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const
                                             const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
                                             void* out, void* stream) {
   clear_error();
-  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  pkv_status st = check_common(pool, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq);
+  if (st != PKV_OK) return st;
   pool->last_launches = 0;
-  const pkv_config& c = pool->cfg;
-  if (layer < 0 || layer >= c.num_layers) return fail(PKV_ERR_OUT_OF_RANGE, "layer out of range");
-  if (num_seqs < 0 || num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "sizes must be >= 0");
-  if (num_tokens > 0 && num_seqs < 1) return fail(PKV_ERR_INVALID_ARG, "tokens without rows");
-  if (num_seqs > num_tokens) return fail(PKV_ERR_INVALID_ARG, "every row needs at least one query token");
-  if (max_blocks_per_seq < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
+  if (layer < 0 || layer >= pool->cfg.num_layers) return fail(PKV_ERR_OUT_OF_RANGE, "layer out of range");
   if (num_tokens == 0) return PKV_OK;
-  if (!q || !out || !block_tables || !context_lens || !query_start_loc)
-    return fail(PKV_ERR_INVALID_ARG, "q, out and metadata pointers must be non-NULL");
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
-    return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
-  if (q == out) return fail(PKV_ERR_INVALID_ARG, "out may not alias q");
-  const WsLayout w = ws_layout(c, num_tokens, max_blocks_per_seq);
-  if (w.max_splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits per row; raise split_blocks");
+  st = check_io(q, out, block_tables);
+  if (st != PKV_OK) return st;
+  const WsLayout w = ws_layout(pool->cfg, num_tokens, max_blocks_per_seq);
   if (w.total > kNoAllocScratchBytes)
     return fail(PKV_ERR_OUT_OF_RANGE, "pass needs " + std::to_string(w.total) + " bytes of scratch; the built-in "
                 "array holds " + std::to_string(kNoAllocScratchBytes) + " (use pkv_attention with a workspace)");
@@ -674,56 +894,14 @@ extern "C" pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const
   if (device != pool->device) return fail(PKV_ERR_INVALID_ARG, "the pool's device must be the current device");
   void* scratch = noalloc_scratch_ptr(device, &e);
   if (!scratch) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch array");
-
+  // What must start at zero -- the task counter -- is cleared by the plan kernel on every call;
+  // everything else is written before it is read.
   char* ws = static_cast<char*>(scratch);
   cudaStream_t s = (cudaStream_t)stream;
-  int32_t* tok_row = reinterpret_cast<int32_t*>(ws + w.tok_row);
-  int32_t* tok_ctx = reinterpret_cast<int32_t*>(ws + w.tok_ctx);
-  // Nothing in the scratch needs to start at zero: the plan rewrites the token table for every token,
-  // and every partial the merge reads is written by the decode kernel of the same call.
-  const int n = num_seqs > num_tokens ? num_seqs : num_tokens;
-  int blocks = (n + 255) / 256;
-  if (blocks > pool->num_sms * 4) blocks = pool->num_sms * 4;
-  e = launch_pdl(plan_kernel, dim3(blocks), dim3(256), 0, s, context_lens, query_start_loc, (int)num_seqs,
-                 (int)num_tokens, (int)(max_blocks_per_seq * kBS), tok_row, tok_ctx, pool->dev_error);
+  e = launch_plan(pool, ws, w, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq, s);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
-
-  DecodeParams p;
-  p.q = static_cast<const __half*>(q);
-  p.kpool = static_cast<const __half*>(pkv_pool_layer_ptr(pool, layer, 0));
-  p.vpool = static_cast<const __half*>(pkv_pool_layer_ptr(pool, layer, 1));
-  p.block_tables = block_tables;
-  p.tok_row = tok_row;
-  p.tok_ctx = tok_ctx;
-  p.out = static_cast<__half*>(out);
-  p.part_o = reinterpret_cast<float*>(ws + w.part_o);
-  p.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
-  p.err = pool->dev_error;
-  p.max_blocks = max_blocks_per_seq;
-  p.num_q_heads = c.num_q_heads;
-  p.num_kv_heads = c.num_kv_heads;
-  p.num_blocks = c.num_blocks;
-  p.split_blocks = c.split_blocks;
-  p.max_splits = w.max_splits;
-  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
-  const int group = c.num_q_heads / c.num_kv_heads;
-  switch (c.head_dim) {
-    case 64: e = launch_decode_g<64>(group, p, num_tokens, c.num_kv_heads, w.max_splits, s); break;
-    case 128: e = launch_decode_g<128>(group, p, num_tokens, c.num_kv_heads, w.max_splits, s); break;
-    case 256: e = launch_decode_g<256>(group, p, num_tokens, c.num_kv_heads, w.max_splits, s); break;
-    default: return fail(PKV_ERR_UNSUPPORTED, "head_dim");
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  pool->last_launches = 2;
-  if (w.max_splits > 1) {
-    MergeParams m{p.part_o, p.part_ml, p.tok_ctx, p.out, c.num_q_heads, c.split_blocks, w.max_splits};
-    switch (c.head_dim) {
-      case 64: e = launch_pdl(merge_kernel<64>, dim3(num_tokens, c.num_q_heads), dim3(128), 0, s, m); break;
-      case 128: e = launch_pdl(merge_kernel<128>, dim3(num_tokens, c.num_q_heads), dim3(128), 0, s, m); break;
-      default: e = launch_pdl(merge_kernel<256>, dim3(num_tokens, c.num_q_heads), dim3(128), 0, s, m); break;
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-    pool->last_launches = 3;
-  }
-  return PKV_OK;
+  int launches = 1;
+  st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_tokens, out, ws, w, s, &launches);
+  pool->last_launches = launches;
+  return st;
 }

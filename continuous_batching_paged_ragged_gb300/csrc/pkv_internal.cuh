@@ -3,6 +3,7 @@
 // bulk (TMA) copy engine on sm_103a.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap and its enums (types only; the encoder is fetched from the driver at run time)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,6 +34,7 @@ struct PlanKey {
 }  // namespace pkv
 
 struct pkv_pool {
+  CUtensorMap kv_map;          // 2-D view [rows = L*2*num_blocks*Hkv*16, head_dim] of the cache, 128B swizzle
   pkv_config cfg;
   char* base = nullptr;        // device: cache, then the status area
   size_t cache_bytes = 0;      // bytes of the fp16 cache region
@@ -116,15 +118,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Bounded wait: polls for at most ~1 s of wall time, then returns false; callers record
-// PKV_DEVERR_WAIT_TIMEOUT and unwind without touching the barrier again.
+// Bounded wait: gives up (returns false) only after more than 2^16 polls AND more than ~1 s of
+// %globaltimer time, measured as a signed difference so that an adjustment of the timer can neither
+// wrap the elapsed time nor end the wait early on its own.  Callers record PKV_DEVERR_WAIT_TIMEOUT
+// and unwind without touching the barrier again.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > 1000000000ull) return false;
+  for (uint32_t polls = 1;; ++polls) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((polls & 255u) == 0 && polls > (1u << 16)) {
+      const int64_t dt = (int64_t)(globaltimer_ns() - t0);
+      if (dt > 1000000000ll) return false;
+    }
   }
 }
 
@@ -143,6 +149,47 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       : "memory");
 }
 
+// 2-D tiled TMA load of a box of `map` at element coordinates (x, y) into shared memory.
+__device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(smem_addr(dst_smem)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)),
+      "l"(policy)
+      : "memory");
+}
+
+// Warp-level matrix helpers (sm_80+ forms, valid on sm_103a).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col)
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -152,6 +199,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+
+// GPU-scope atomic add with release semantics: earlier writes of this thread (and of warp mates ordered
+// before it by a warp barrier) are visible to whoever acquires the counter afterwards.
+__device__ __forceinline__ int atom_add_release_gpu(int32_t* addr, int v) {
+  int old;
+  asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ void set_error(int32_t* err, int32_t bits) {
   if (err) atomicOr(err, bits);

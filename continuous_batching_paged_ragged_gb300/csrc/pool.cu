@@ -42,6 +42,37 @@ static pkv_status check_config(const pkv_config* c) {
   return PKV_OK;
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The cache seen by the TMA engine: rows of head_dim fp16 values, one row per (layer, K/V, block, KV head,
+// slot), boxes of 16 rows x 64 values (128 bytes) with the 128-byte swizzle, so a (block, KV head) run of
+// K or V is head_dim / 64 boxes.
+static pkv_status encode_kv_map(pkv_pool* p) {
+  static EncodeTiledFn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  const pkv_config& c = p->cfg;
+  const uint64_t rows = (uint64_t)c.num_layers * 2 * c.num_blocks * c.num_kv_heads * c.block_size;
+  if (rows >= (1ull << 31)) return fail(PKV_ERR_UNSUPPORTED, "pool too large for 32-bit TMA row coordinates");
+  cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(&p->kv_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->base, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
+  return PKV_OK;
+}
+
 static size_t cache_bytes_of(const pkv_config* c) {
   return (size_t)2 * c->num_layers * (size_t)c->num_blocks * c->num_kv_heads * c->block_size * c->head_dim *
          sizeof(__half);
@@ -84,6 +115,11 @@ extern "C" pkv_status pkv_pool_init(const pkv_config* cfg, void* dev_cache, size
   if (e != cudaSuccess) {
     delete p;
     return cuda_fail(e, "cudaDeviceGetAttribute");
+  }
+  st = encode_kv_map(p);
+  if (st != PKV_OK) {
+    delete p;
+    return st;
   }
   e = cudaMemset(p->dev_error, 0, kStatusBytes);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();

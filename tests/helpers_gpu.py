@@ -45,7 +45,8 @@ def run_batch(batch: synth.StepBatch, layers, num_layers=None, split_blocks=0, p
     outs = [torch.empty_like(q) for q in qs]
     workload.run_pass(pool, ds, layers, qs, ks, vs, outs)
     torch.cuda.synchronize()
-    assert pool.check() == 0, "device error word set"
+    bits = pool.check()
+    assert bits == 0, f"device error word set: {bits:#x}"
     return pool, ds, outs
 
 

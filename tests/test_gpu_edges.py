@@ -36,13 +36,23 @@ def test_context_of_one_returns_v_exactly(cuda, built):
             assert np.array_equal(out[b, h].view(np.uint16), v[h // 6].view(np.uint16))
 
 
-@pytest.mark.parametrize("split_blocks", [1, 3, 16, 64])
+@pytest.mark.parametrize("split_blocks", [1, 3, 16, 32])
 def test_split_size_does_not_change_the_answer(cuda, built, split_blocks):
     shape = synth.Shape(1, 12, 2, 128)
     batch = synth.custom_batch(shape, [1000, 37, 400, 0], [1, 1, 5, 64], seed=2)
     pool, ds, outs = run_batch(batch, [0], split_blocks=split_blocks)
     for b in range(batch.num_seqs):
         assert_close(row_slice(batch, outs[0], b), oracle_row(batch, 0, b), f"split {split_blocks} row {b}")
+
+
+def test_split_size_above_limit_is_refused(cuda, built):
+    batch = synth.tiny_decode(0)
+    pool = workload.make_pool(batch, split_blocks=64)
+    ds = workload.upload(batch, pool)
+    attn = workload.Attention(pool, ds)
+    with pytest.raises(pkv.PkvError) as e:
+        attn.plan()
+    assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
 
 
 def test_invariant_to_physical_block_placement(cuda, built):
