@@ -11,19 +11,22 @@
 //    task list.  A task is one split of one (token, KV head): `split_blocks` consecutive 16-token blocks.
 //    The split count of a token depends only on its own context, so results are bit-identical whatever
 //    else is in the batch, whatever the row order and wherever the blocks sit physically.
-//  * decode_kernel: persistent; every warp is an independent worker.  A warp takes tasks from a global
-//    counter and streams each block's K and V runs through its own shared-memory ring with 2-D TMA tile
-//    copies (128-byte swizzle) that its lane 0 issues; independent issuers per SM are what keep HBM busy.
-//    The warp owns the whole split and all G <= 8 query heads of its KV head, so each K/V block is read
-//    from HBM exactly once.  Per 16-key block the group contraction runs on the tensor cores with warp
-//    MMAs: S^T[16 keys x 8 heads] = K Q^T and O^T[d x 8 heads] += V^T P^T, operands fetched from the
-//    swizzled ring with ldmatrix; the online softmax (running max and sum in the log2 domain, fp32)
-//    reduces across the lanes that share a head with warp shuffles.
-//  * merge_kernel: a token whose context fits one split gets its fp16 output from the decode directly.
-//    Otherwise each split leaves an unnormalised partial (m, l, o) and merge_kernel, launched right behind
-//    the decode, combines a token's partials with log-sum-exp weights, spread over many CTAs.  (Merging
-//    in the decode's last-finishing warp was measured slower: the row's last splits finish together at
-//    the end of the launch and their merges serialise there.)
+//  * decode_kernel: persistent; a CTA of 4 warps takes one task at a time from a global counter, and
+//    the task's blocks are dealt round-robin to its warps (block i to warp i % 4).  Every warp streams its
+//    blocks' K and V runs through its own shared-memory ring with 2-D TMA tile copies (128-byte swizzle)
+//    that its lane 0 issues: independent issuers per SM are what keep HBM busy, and sharing a task four
+//    ways keeps all of them busy even when a pass has few tasks.  The KV head's G <= 8 query heads ride
+//    along, so each K/V block is read from HBM exactly once.  Per 16-key block the group contraction runs
+//    on the tensor cores with warp MMAs: S^T[16 keys x 8 heads] = K Q^T and O^T[d x 8 heads] += V^T P^T,
+//    operands fetched from the swizzled ring with ldmatrix; the online softmax (running max and sum in
+//    the log2 domain, fp32) reduces across the lanes that share a head with warp shuffles.  At the end of
+//    a task the four warps' (m, l, o) are combined with log-sum-exp weights through shared memory.
+//  * Cross-split merge: a token whose context fits one split gets its fp16 output from the decode
+//    directly.  Otherwise each split leaves an unnormalised partial (m, l, o); the CTA that finishes the
+//    token's last split merges them with log-sum-exp weights, inside the same launch (a separate merge
+//    launch cost more than the merge: its CTAs cannot start until the decode's have left the SMs).
+//    Tokens with more than 32 splits are merged by merge_kernel, launched behind the decode, which
+//    spreads one token's merge over many CTAs.
 #include <cuda_fp16.h>
 
 #include <cmath>
@@ -35,28 +38,31 @@
 namespace pkv {
 
 constexpr int kBS = 16;
-constexpr int kWideMergeSplits = 32;  // beyond this many splits per token the merge also splits over splits
+constexpr int kFusedMergeSplits = 32;  // tokens with up to this many splits are merged inside the decode
 constexpr int kMaxSplitBlocks = 32;   // upper bound on split_blocks (a split's block ids fit one warp)
 constexpr int kHeadsTile = 8;         // query heads per KV head handled by one MMA tile (G <= 8)
 
-// Ring slots per worker warp: runs (a block's K or V for one KV head, or a task's q) in flight.
+// Ring slots per warp: runs (a block's K or V for one KV head, or a task's q) in flight.
 #ifndef PKV_DECODE_RING
-#define PKV_DECODE_RING(D) ((D) == 256 ? 3 : ((D) == 128 ? 3 : 6))
+#define PKV_DECODE_RING(D) ((D) == 256 ? 2 : ((D) == 128 ? 3 : 5))
 #endif
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 struct WsHeader {
   int32_t n_tasks;
-  int32_t work;   // next task to hand out
+  int32_t work;   // dynamic tasks handed out so far (each CTA's first two tasks are static)
   int32_t done;   // CTAs of the current decode launch that have finished
   int32_t pad[61];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
+constexpr int kSmemPerSM = 228 * 1024;  // shared memory of one SM
+constexpr int kSmemReservedPerCTA = 1024;
+
 template <int D, int G>
 struct DecodeTraits {
-  static constexpr int NW = 4;                     // warps per CTA; each warp is an independent worker
+  static constexpr int NW = 4;                     // warps per CTA; block i of a task goes to warp i % NW
   static constexpr int NTHREADS = NW * 32;
   static constexpr int RUN = kBS * D * 2;          // one (block, KV head) run of K or V = D/64 TMA boxes
   static constexpr int BOXES = D / 64;
@@ -64,12 +70,18 @@ struct DecodeTraits {
   static constexpr int KS = D / 16;                // MMA k-steps over the head dimension (scores)
   static constexpr int MT = D / 16;                // MMA m-tiles over the head dimension (values)
   static constexpr int OV = MT * 4;                // fp32 output values per lane
-  static constexpr int MINB = D == 256 ? 2 : 4;    // CTAs per SM the register budget allows
   static constexpr int OFF_BAR = NW * NR * RUN;    // [NW][NR] run barriers after the rings
-  static constexpr int SMEM = OFF_BAR + NW * NR * 8 + 1024;  // + slack to align the rings to 1024 bytes
+  static constexpr int OFF_CO = OFF_BAR + NW * NR * 8;         // combine: [NW][OV][32 lanes] fp32 o
+  static constexpr int OFF_CM = OFF_CO + NW * OV * 32 * 4;     // combine: [NW][8 heads] running max
+  static constexpr int OFF_CL = OFF_CM + NW * kHeadsTile * 4;  // combine: [NW][8 heads] running sum
+  static constexpr int OFF_IDX = OFF_CL + NW * kHeadsTile * 4; // [4] task indices, merge target, its splits
+  static constexpr int SMEM = OFF_IDX + 32 + 1024;  // + slack to align the rings to 1024 bytes
+  static constexpr int FIT = kSmemPerSM / (SMEM + kSmemReservedPerCTA);
+  static constexpr int MINB = FIT < 4 ? FIT : 4;   // CTAs per SM (shared memory bound)
   static_assert(D % 64 == 0 && G >= 1 && G <= kHeadsTile, "shape");
   static_assert(RUN % 1024 == 0, "swizzled boxes need 1024-byte aligned slots");
   static_assert(8 * D * 2 <= RUN && KS % 2 == 0, "a task's q (8 rows) fits one slot");
+  static_assert(MINB >= 1, "shared memory");
 };
 
 struct DecodeParams {
@@ -81,8 +93,9 @@ struct DecodeParams {
   const int4* tasks;   // {token, kv head | split << 8, row, causal context}
   WsHeader* hdr;
   __half* out;
-  float* part_o;       // [num_tokens * num_kv_heads * max_splits][32 lanes][D / 4]  (MMA fragment order)
+  float* part_o;       // [num_tokens * num_kv_heads * max_splits][8 heads][D]
   float2* part_ml;     // [num_tokens * num_kv_heads * max_splits][8 heads]
+  int32_t* merge_cnt;  // [num_tokens * num_kv_heads] splits finished; zero between launches
   int32_t* err;
   int layer_row0_k;    // TMA row of (layer, K, block 0, head 0, slot 0)
   int layer_row0_v;    // TMA row of (layer, V, block 0, head 0, slot 0)
@@ -102,24 +115,27 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 }
 
 // ---------------------------------------------------------------------------------------------------
-// Worker warp.  Measured on this access pattern (scattered 4 KB runs): one issuing thread per CTA tops
-// out near 6 GB/s whatever the ring depth, while 12-16 issuing warps per SM reach 5.6-6 TB/s -- so every
-// warp streams its own runs.  The next task's metadata loads overlap the current task's compute, and
-// the next task's first runs enter the ring before the current task ends.
+// Per-warp stream.  Measured on this access pattern (scattered 4 KB runs): one issuing thread per CTA
+// tops out near 6 GB/s whatever the ring depth, while 12-16 issuing warps per SM reach 5.6-6 TB/s -- so
+// every warp streams its own runs.  The next task's metadata loads overlap the current task's compute,
+// and the next task's first runs enter the ring before the current task ends.
 // ---------------------------------------------------------------------------------------------------
 struct TaskMeta {
-  int t, g, s, row, ctx, nb, nsplit;
-  int ids;  // lane r holds the physical id of block r of the split (r < nb <= 32)
+  int t, g, s, row, ctx, nsplit;
+  int nbw;  // blocks of the split dealt to this warp: blocks warp, warp + NW, ...
+  int ids;  // lane j holds the physical id of this warp's block j (j < nbw <= 8)
 };
 
-__device__ __forceinline__ void task_from_record(const DecodeParams& p, int4 rec, TaskMeta& m) {
+template <int NW>
+__device__ __forceinline__ void task_from_record(const DecodeParams& p, int4 rec, int warp, TaskMeta& m) {
   m.t = rec.x;
   m.g = rec.y & 0xFF;
   m.s = rec.y >> 8;
   m.row = rec.z;
   m.ctx = rec.w;
   const int nblk = (m.ctx + kBS - 1) / kBS;
-  m.nb = m.t >= 0 ? min(p.split_blocks, nblk - m.s * p.split_blocks) : 0;
+  const int nb = m.t >= 0 ? min(p.split_blocks, nblk - m.s * p.split_blocks) : 0;
+  m.nbw = nb > warp ? (nb - warp + NW - 1) / NW : 0;
   m.nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
 }
 
@@ -127,10 +143,11 @@ __device__ __forceinline__ int4 load_record(const DecodeParams& p, int idx, int 
   return idx < n_tasks ? __ldg(p.tasks + idx) : make_int4(-1, 0, 0, 0);
 }
 
-__device__ __forceinline__ int load_ids(const DecodeParams& p, const TaskMeta& m, int lane) {
+template <int NW>
+__device__ __forceinline__ int load_ids(const DecodeParams& p, const TaskMeta& m, int warp, int lane) {
   int id = 0;
-  if (lane < m.nb) {
-    id = __ldg(p.block_tables + (int64_t)m.row * p.max_blocks + m.s * p.split_blocks + lane);
+  if (lane < m.nbw) {
+    id = __ldg(p.block_tables + (int64_t)m.row * p.max_blocks + m.s * p.split_blocks + warp + NW * lane);
     if (id < 0 || id >= p.num_blocks) {
       dev::set_error(p.err, PKV_DEVERR_BLOCK_RANGE);
       id = 0;  // keep the copy in bounds; this token's output is flagged as invalid
@@ -145,44 +162,43 @@ struct Worker {
   const DecodeParams& p;
   unsigned char* ring;   // this warp's NR slots (1024-byte aligned)
   uint64_t* bars;        // this warp's NR barriers
+  const volatile int* idx_ring;  // the CTA's task indices: task k at [k % 4]
   uint64_t pol;
-  int lane;
+  int warp, lane;
   int n_tasks;
+  int k = 0;             // the CTA's sequence number of the current task
   int issued = 0;        // runs issued into the ring so far
   int consumed = 0;      // runs taken out of the ring so far
   int icur = 0;          // 0: the issue cursor is in the current task, 1: in the next one
-  int ir = 0;            // run index of the issue cursor: 0 q, 1 + 2b K of block b, 2 + 2b V of block b
-  int nstage = 0;        // next task's metadata: 0 nothing, 1 index requested, 2 record loaded, 3 ids loaded
-  int nxt_idx = 0;
+  int ir = 0;            // run index of the issue cursor: 0 q, 1 + 2j K of block j, 2 + 2j V of block j
+  int nstage = 0;        // next task's metadata: 0 nothing, 1 record loaded, 2 ids loaded
   int4 nxt_rec;
   TaskMeta cur, nxt;
   bool ok = true;
 
-  __device__ Worker(const DecodeParams& p_, unsigned char* ring_, uint64_t* bars_, int lane_)
-      : p(p_), ring(ring_), bars(bars_), lane(lane_) {
+  __device__ Worker(const DecodeParams& p_, unsigned char* ring_, uint64_t* bars_, const int* idx_ring_,
+                    int warp_, int lane_)
+      : p(p_), ring(ring_), bars(bars_), idx_ring(idx_ring_), warp(warp_), lane(lane_) {
     pol = dev::l2_policy_evict_first();
     n_tasks = p.hdr->n_tasks;
+    task_from_record<T::NW>(p, load_record(p, idx_ring[0], n_tasks), warp, cur);
+    cur.ids = load_ids<T::NW>(p, cur, warp, lane);
   }
 
-  static __device__ __forceinline__ int runs(const TaskMeta& m) { return m.t >= 0 ? 1 + 2 * m.nb : 0; }
+  static __device__ __forceinline__ int runs(const TaskMeta& m) { return m.t >= 0 && m.nbw > 0 ? 1 + 2 * m.nbw : 0; }
 
   // Advance the next task's metadata by one dependent load (called between blocks so each load's
   // latency hides behind compute); full == true finishes it now.
   __device__ __forceinline__ void prefetch_next(bool full) {
     if (nstage == 0) {
-      if (lane == 0) nxt_idx = atomicAdd(&p.hdr->work, 1);
+      nxt_rec = load_record(p, idx_ring[(k + 1) & 3], n_tasks);
       nstage = 1;
       if (!full) return;
     }
     if (nstage == 1) {
-      nxt_rec = load_record(p, __shfl_sync(0xffffffffu, nxt_idx, 0), n_tasks);
+      task_from_record<T::NW>(p, nxt_rec, warp, nxt);
+      nxt.ids = load_ids<T::NW>(p, nxt, warp, lane);
       nstage = 2;
-      if (!full) return;
-    }
-    if (nstage == 2) {
-      task_from_record(p, nxt_rec, nxt);
-      nxt.ids = load_ids(p, nxt, lane);
-      nstage = 3;
     }
   }
   __device__ __forceinline__ void issue_run(const TaskMeta& m, int r) {
@@ -205,17 +221,27 @@ struct Worker {
     ++issued;
   }
   // Issue the next run of the stream (current task, then the next task), if there is one.
-  __device__ __forceinline__ void issue_next() {
+  __device__ __forceinline__ bool issue_next() {
     if (icur == 0) {
       if (ir < runs(cur)) {
         issue_run(cur, ir++);
-        return;
+        return true;
       }
       icur = 1;
       ir = 0;
     }
     prefetch_next(true);
-    if (ir < runs(nxt)) issue_run(nxt, ir++);
+    if (ir < runs(nxt)) {
+      issue_run(nxt, ir++);
+      return true;
+    }
+    return false;
+  }
+  // Top the ring up.  It runs dry when the warp had no blocks in the task just finished (a short split
+  // deals nothing to some warps), since only consuming a run issues the next one.
+  __device__ __forceinline__ void fill() {
+    while (issued - consumed < T::NR && issue_next()) {
+    }
   }
   // Wait for the oldest run in the ring; returns its slot's shared-memory address.
   __device__ __forceinline__ uint32_t wait_run() {
@@ -231,14 +257,19 @@ struct Worker {
   __device__ __forceinline__ void release_run() {
     __syncwarp();
     ++consumed;
-    issue_next();
+    if (ok) issue_next();
   }
   // Move to the next task; the issue cursor is already inside it.
   __device__ __forceinline__ void advance() {
     prefetch_next(true);
     cur = nxt;
+    ++k;
     icur = 0;
     nstage = 0;
+  }
+  // Before leaving early (a wait gave up): let the copies still in flight land, each wait bounded.
+  __device__ __forceinline__ void drain() {
+    for (; consumed < issued; ++consumed) dev::mbar_wait(&bars[consumed % T::NR], (consumed / T::NR) & 1);
   }
 };
 
@@ -247,32 +278,123 @@ __device__ __forceinline__ void frag_coord(int lane, int r, int& dim, int& head)
   dim = 16 * (r >> 2) + (lane >> 2) + ((r & 2) ? 8 : 0);
   head = ((lane & 3) << 1) + (r & 1);
 }
+// ... and back: the lane and register holding (dim, head).
+__device__ __forceinline__ void frag_slot(int dim, int head, int& lane, int& r) {
+  lane = ((dim & 7) << 2) | (head >> 1);
+  r = ((dim >> 4) << 2) | (((dim >> 3) & 1) << 1) | (head & 1);
+}
+
+// Merge a token's split partials (all of them final) into its fp16 output, with log-sum-exp weights in
+// split order, so the result does not depend on which CTA merges.  The partials were written by other
+// CTAs during this launch: they are read from L2 (.cg), never from a possibly stale L1 line.
+template <int D, int G, int NT>
+__device__ __forceinline__ void merge_splits(const DecodeParams& p, int tg, int nsplit) {
+  constexpr int NG = G * D / 4;            // groups of 4 consecutive dims of one head
+  constexpr int EG = (NG + NT - 1) / NT;   // groups per thread
+  constexpr int U = EG >= 4 ? 2 : 4;       // splits whose loads are in flight together
+  const int t = tg / p.num_kv_heads, g = tg % p.num_kv_heads;
+  const size_t sb = (size_t)tg * p.max_splits;
+  float M[EG], L[EG];
+  float4 acc[EG];
+#pragma unroll
+  for (int j = 0; j < EG; ++j) {
+    M[j] = -INFINITY;
+    L[j] = 0.f;
+    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int s0 = 0; s0 < nsplit; s0 += U) {
+    float2 ml[EG][U];
+    float4 o[EG][U];
+#pragma unroll
+    for (int j = 0; j < EG; ++j) {
+      const int e4 = threadIdx.x + j * NT;
+      const int h = (4 * e4) / D, dim = (4 * e4) % D;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (e4 < NG && s0 + u < nsplit) {
+          const size_t pi = (sb + s0 + u) * kHeadsTile + h;
+          ml[j][u] = __ldcg(p.part_ml + pi);
+          o[j][u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + pi * D + dim));
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < EG; ++j) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (s0 + u < nsplit) {
+          const float nM = fmaxf(M[j], ml[j][u].x);
+          const float a = exp2f(M[j] - nM), f = exp2f(ml[j][u].x - nM);
+          M[j] = nM;
+          L[j] = L[j] * a + ml[j][u].y * f;
+          acc[j].x = acc[j].x * a + o[j][u].x * f;
+          acc[j].y = acc[j].y * a + o[j][u].y * f;
+          acc[j].z = acc[j].z * a + o[j][u].z * f;
+          acc[j].w = acc[j].w * a + o[j][u].w * f;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < EG; ++j) {
+    const int e4 = threadIdx.x + j * NT;
+    if (e4 >= NG) continue;
+    const int h = (4 * e4) / D, dim = (4 * e4) % D;
+    const float il = 1.f / L[j];
+    const __half2 lo = __floats2half2_rn(acc[j].x * il, acc[j].y * il);
+    const __half2 hi = __floats2half2_rn(acc[j].z * il, acc[j].w * il);
+    uint2 v;
+    v.x = *reinterpret_cast<const uint32_t*>(&lo);
+    v.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.num_q_heads + (size_t)g * G + h) * D + dim) = v;
+  }
+}
 
 template <int D, int G>
-__device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char* rings, uint64_t* all_bars,
-                                            int warp, int lane) {
+__device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char* smem, int warp, int lane) {
   using T = DecodeTraits<D, G>;
-  Worker<D, G> w(p, rings + warp * T::NR * T::RUN, all_bars + warp * T::NR, lane);
-  {
-    int idx = 0;
-    if (lane == 0) idx = atomicAdd(&p.hdr->work, 1);
-    task_from_record(p, load_record(p, __shfl_sync(0xffffffffu, idx, 0), w.n_tasks), w.cur);
-    w.cur.ids = load_ids(p, w.cur, lane);
-  }
-  for (int i = 0; i < T::NR; ++i) w.issue_next();
+  uint64_t* all_bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
+  float* co = reinterpret_cast<float*>(smem + T::OFF_CO);
+  float* cm = reinterpret_cast<float*>(smem + T::OFF_CM);
+  float* cl = reinterpret_cast<float*>(smem + T::OFF_CL);
+  int* idx_ring = reinterpret_cast<int*>(smem + T::OFF_IDX);
+  Worker<D, G> w(p, smem + warp * T::NR * T::RUN, all_bars + warp * T::NR, idx_ring, warp, lane);
+  // Split completion (thread 0 only): after writing a split's partial the CTA counts it on the token's
+  // counter, and the CTA that completes the count merges the token.  The count's result is examined only
+  // at the end of the CTA's next task, so its round trip never stalls the stream.
+  int pend_tg = -1, pend_prev = 0, pend_ns = 0;
+  auto resolve_pending = [&]() {  // thread 0: publish the token this CTA must merge, or -1
+    int tg = -1;
+    if (pend_tg >= 0 && pend_prev == pend_ns - 1) {
+      tg = pend_tg;
+      p.merge_cnt[tg] = 0;       // ready for the next launch on this plan
+      dev::fence_acq_rel_gpu();  // acquire: the other splits' partials, released with their counts
+    }
+    idx_ring[4] = tg;
+    idx_ring[5] = pend_ns;
+    pend_tg = -1;
+  };
 
   const int qh = lane >> 2;        // head whose q this lane feeds to the MMA (B operand column); key row too
   const int h0 = (lane & 3) << 1;  // heads of this lane's score / output columns: h0, h0 + 1
-  while (w.cur.t >= 0 && w.ok) {
+  int pending = 0;                 // thread 0: index of the task two ahead, published at the task's end
+  bool cta_ok = true;              // CTA-uniform: no wait gave up
+  while (w.cur.t >= 0) {           // uniform: every warp reads the same index
+    if (threadIdx.x == 0) pending = 2 * (int)gridDim.x + atomicAdd(&p.hdr->work, 1);
     const TaskMeta d = w.cur;
+    w.fill();
     w.prefetch_next(false);
-    // ---- q as the MMA B operand (Q^T: k = dims, n = heads), from the task's first ring run ----
-    // Rows G..7 of the 8-row tile hold stale bytes; they only feed score and output columns of heads
-    // >= G, which are never written out.
-    uint32_t qb[T::KS][2];
-    {
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[T::MT][4];
+#pragma unroll
+    for (int mt = 0; mt < T::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    if (d.nbw > 0 && w.ok) {
+      // ---- q as the MMA B operand (Q^T: k = dims, n = heads), from the task's first ring run ----
+      // Rows G..7 of the 8-row tile hold stale bytes; they only feed score and output columns of heads
+      // >= G, which are never written out.
+      uint32_t qb[T::KS][2];
       const uint32_t qs = w.wait_run();
-      if (!w.ok) break;
 #pragma unroll
       for (int k2 = 0; k2 < T::KS / 2; ++k2) {
         uint32_t r4[4];
@@ -283,115 +405,138 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
         qb[2 * k2 + 1][1] = r4[3];
       }
       w.release_run();
-    }
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[T::MT][4];
-#pragma unroll
-    for (int mt = 0; mt < T::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    for (int i = 0; i < d.nb; ++i) {
-      const int ntok = min(kBS, d.ctx - (d.s * p.split_blocks + i) * kBS);
-      // ---- S^T[16 keys x 8 heads] = K Q^T on the tensor cores ----
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const uint32_t ks_base = w.wait_run();
-        if (!w.ok) break;
-        const int kr = (lane & 7) + ((lane >> 3) & 1) * 8;  // key row this lane addresses for ldmatrix
+      for (int j = 0; j < d.nbw && w.ok; ++j) {
+        const int ntok = min(kBS, d.ctx - (d.s * p.split_blocks + warp + T::NW * j) * kBS);
+        // ---- S^T[16 keys x 8 heads] = K Q^T on the tensor cores ----
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const uint32_t ks_base = w.wait_run();
+          const int kr = (lane & 7) + ((lane >> 3) & 1) * 8;  // key row this lane addresses for ldmatrix
 #pragma unroll
-        for (int ks = 0; ks < T::KS; ++ks) {
-          uint32_t a[4];
-          dev::ldsm_x4(ks_base + swz(kr, 2 * ks + (lane >> 4)), a);
-          dev::mma_16816(sc, a, qb[ks][0], qb[ks][1]);
-        }
-        w.release_run();
-      }
-      w.prefetch_next(false);  // one dependent metadata load of the next task per block, hidden by compute
-      // ---- online softmax (log2 domain); the lane holds keys qh, qh + 8 for heads h0, h0 + 1 ----
-      const bool v0 = qh < ntok, v1 = qh + 8 < ntok;
-      const float s0 = v0 ? sc[0] * p.scale_log2 : -INFINITY;  // key qh,     head h0
-      const float s1 = v0 ? sc[1] * p.scale_log2 : -INFINITY;  // key qh,     head h0 + 1
-      const float s2 = v1 ? sc[2] * p.scale_log2 : -INFINITY;  // key qh + 8, head h0
-      const float s3 = v1 ? sc[3] * p.scale_log2 : -INFINITY;  // key qh + 8, head h0 + 1
-      float b0 = fmaxf(s0, s2), b1 = fmaxf(s1, s3);
-#pragma unroll
-      for (int m = 4; m < 32; m <<= 1) {
-        b0 = fmaxf(b0, __shfl_xor_sync(0xffffffffu, b0, m));
-        b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, m));
-      }
-      const float n0 = fmaxf(m0, b0), n1 = fmaxf(m1, b1);
-      const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
-      m0 = n0;
-      m1 = n1;
-      const float p0 = exp2f(s0 - n0), p1 = exp2f(s1 - n1), p2 = exp2f(s2 - n0), p3 = exp2f(s3 - n1);
-      l0 = l0 * a0 + p0 + p2;
-      l1 = l1 * a1 + p1 + p3;
-#pragma unroll
-      for (int mt = 0; mt < T::MT; ++mt) {
-        o[mt][0] *= a0;
-        o[mt][1] *= a1;
-        o[mt][2] *= a0;
-        o[mt][3] *= a1;
-      }
-      // P^T as the B operand (k = keys, n = heads): transpose the [keys x heads] 8x8 fragments
-      const __half2 pk0 = __floats2half2_rn(p0, p1), pk1 = __floats2half2_rn(p2, p3);
-      const uint32_t pb0 = dev::movmatrix_t(*reinterpret_cast<const uint32_t*>(&pk0));
-      const uint32_t pb1 = dev::movmatrix_t(*reinterpret_cast<const uint32_t*>(&pk1));
-      // ---- O^T[d x 8 heads] += V^T P^T on the tensor cores ----
-      {
-        const uint32_t vs_base = w.wait_run();
-        if (!w.ok) break;
-        if (ntok < kBS) {  // rows past the context may hold anything: zero them so 0 * garbage cannot poison O
-          for (int idx = lane; idx < (kBS - ntok) * (D / 8); idx += 32) {
-            const int r = ntok + idx / (D / 8), c = idx % (D / 8);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vs_base + swz(r, c)), "r"(0) : "memory");
+          for (int ks = 0; ks < T::KS; ++ks) {
+            uint32_t a[4];
+            dev::ldsm_x4(ks_base + swz(kr, 2 * ks + (lane >> 4)), a);
+            dev::mma_16816(sc, a, qb[ks][0], qb[ks][1]);
           }
-          __syncwarp();
+          w.release_run();
         }
-        const int mat = lane >> 3;                      // ldmatrix matrix this lane addresses
-        const int vr = (lane & 7) + ((mat >> 1) << 3);  // its key row
+        w.prefetch_next(false);  // one dependent metadata load of the next task per block, hidden by compute
+        // ---- online softmax (log2 domain); the lane holds keys qh, qh + 8 for heads h0, h0 + 1 ----
+        const bool v0 = qh < ntok, v1 = qh + 8 < ntok;
+        const float s0 = v0 ? sc[0] * p.scale_log2 : -INFINITY;  // key qh,     head h0
+        const float s1 = v0 ? sc[1] * p.scale_log2 : -INFINITY;  // key qh,     head h0 + 1
+        const float s2 = v1 ? sc[2] * p.scale_log2 : -INFINITY;  // key qh + 8, head h0
+        const float s3 = v1 ? sc[3] * p.scale_log2 : -INFINITY;  // key qh + 8, head h0 + 1
+        float b0 = fmaxf(s0, s2), b1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int m = 4; m < 32; m <<= 1) {
+          b0 = fmaxf(b0, __shfl_xor_sync(0xffffffffu, b0, m));
+          b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, m));
+        }
+        const float n0 = fmaxf(m0, b0), n1 = fmaxf(m1, b1);
+        const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        const float p0 = exp2f(s0 - n0), p1 = exp2f(s1 - n1), p2 = exp2f(s2 - n0), p3 = exp2f(s3 - n1);
+        l0 = l0 * a0 + p0 + p2;
+        l1 = l1 * a1 + p1 + p3;
 #pragma unroll
         for (int mt = 0; mt < T::MT; ++mt) {
-          uint32_t a[4];
-          dev::ldsm_x4_t(vs_base + swz(vr, 2 * mt + (mat & 1)), a);
-          dev::mma_16816(o[mt], a, pb0, pb1);
+          o[mt][0] *= a0;
+          o[mt][1] *= a1;
+          o[mt][2] *= a0;
+          o[mt][3] *= a1;
         }
-        if (ntok < kBS) dev::fence_proxy_async_smem();  // the zero-fill precedes the slot's next TMA write
-        w.release_run();
+        // P^T as the B operand (k = keys, n = heads): transpose the [keys x heads] 8x8 fragments
+        const __half2 pk0 = __floats2half2_rn(p0, p1), pk1 = __floats2half2_rn(p2, p3);
+        const uint32_t pb0 = dev::movmatrix_t(*reinterpret_cast<const uint32_t*>(&pk0));
+        const uint32_t pb1 = dev::movmatrix_t(*reinterpret_cast<const uint32_t*>(&pk1));
+        // ---- O^T[d x 8 heads] += V^T P^T on the tensor cores ----
+        {
+          const uint32_t vs_base = w.wait_run();
+          if (ntok < kBS) {  // rows past the context may hold anything: zero them so 0 * garbage cannot poison O
+            for (int idx = lane; idx < (kBS - ntok) * (D / 8); idx += 32) {
+              const int r = ntok + idx / (D / 8), c = idx % (D / 8);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vs_base + swz(r, c)), "r"(0) : "memory");
+            }
+            __syncwarp();
+          }
+          const int mat = lane >> 3;                      // ldmatrix matrix this lane addresses
+          const int vr = (lane & 7) + ((mat >> 1) << 3);  // its key row
+#pragma unroll
+          for (int mt = 0; mt < T::MT; ++mt) {
+            uint32_t a[4];
+            dev::ldsm_x4_t(vs_base + swz(vr, 2 * mt + (mat & 1)), a);
+            dev::mma_16816(o[mt], a, pb0, pb1);
+          }
+          if (ntok < kBS) dev::fence_proxy_async_smem();  // the zero-fill precedes the slot's next TMA write
+          w.release_run();
+        }
       }
     }
-    if (!w.ok) break;
 
-    // ---- finish the split ----
+    // ---- publish this warp's share of the split; a warp with no blocks publishes (-inf, 0, 0) ----
 #pragma unroll
     for (int m = 4; m < 32; m <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, m);
       l1 += __shfl_xor_sync(0xffffffffu, l1, m);
     }
-    const int hq0 = d.g * G;
-    if (d.nsplit == 1) {
-      const float i0 = 1.f / l0, i1 = 1.f / l1;
 #pragma unroll
-      for (int r = 0; r < T::OV; ++r) {
-        int dim, head;
-        frag_coord(lane, r, dim, head);
-        if (head < G)
-          p.out[((size_t)d.t * p.num_q_heads + hq0 + head) * D + dim] =
-              __float2half_rn(o[r >> 2][r & 3] * ((r & 1) ? i1 : i0));
+    for (int r = 0; r < T::OV; ++r) co[(warp * T::OV + r) * 32 + lane] = o[r >> 2][r & 3];
+    if (lane < 4) {
+      cm[warp * kHeadsTile + h0] = m0;
+      cm[warp * kHeadsTile + h0 + 1] = m1;
+      cl[warp * kHeadsTile + h0] = l0;
+      cl[warp * kHeadsTile + h0 + 1] = l1;
+    }
+    if (threadIdx.x == 0) {
+      idx_ring[(w.k + 2) & 3] = pending;
+      resolve_pending();
+    }
+    if (!__syncthreads_and(w.ok)) {  // a wait gave up somewhere in the CTA: stop together
+      cta_ok = false;
+      break;
+    }
+    if (idx_ring[4] >= 0) merge_splits<D, G, T::NTHREADS>(p, idx_ring[4], idx_ring[5]);
+
+    // ---- combine the warps' shares with log-sum-exp weights; write the output or the split's partial ----
+    const size_t pidx = ((size_t)d.t * p.num_kv_heads + d.g) * p.max_splits + d.s;
+    for (int e = threadIdx.x; e < G * D; e += T::NTHREADS) {
+      const int h = e / D, dim = e % D;
+      int ln, r;
+      frag_slot(dim, h, ln, r);
+      float M = cm[h];
+#pragma unroll
+      for (int v = 1; v < T::NW; ++v) M = fmaxf(M, cm[v * kHeadsTile + h]);
+      float L = 0.f, acc = 0.f;
+#pragma unroll
+      for (int v = 0; v < T::NW; ++v) {
+        const float f = exp2f(cm[v * kHeadsTile + h] - M);
+        L += cl[v * kHeadsTile + h] * f;
+        acc += co[(v * T::OV + r) * 32 + ln] * f;
       }
-    } else {
-      const size_t tg = (size_t)d.t * p.num_kv_heads + d.g;
-      const size_t pidx = tg * p.max_splits + d.s;
-      float4* dst = reinterpret_cast<float4*>(p.part_o + (pidx * 32 + lane) * T::OV);
-#pragma unroll
-      for (int mt = 0; mt < T::MT; ++mt) dst[mt] = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
-      if (lane < 4) {
-        p.part_ml[pidx * kHeadsTile + h0] = make_float2(m0, l0);
-        p.part_ml[pidx * kHeadsTile + h0 + 1] = make_float2(m1, l1);
+      if (d.nsplit == 1) {
+        p.out[((size_t)d.t * p.num_q_heads + (size_t)d.g * G + h) * D + dim] = __float2half_rn(acc / L);
+      } else {
+        p.part_o[(pidx * kHeadsTile + h) * D + dim] = acc;
+        if (dim == 0) p.part_ml[pidx * kHeadsTile + h] = make_float2(M, L);
       }
     }
-    __syncwarp();
+    __syncthreads();  // the combine buffers are free again; the partial is written
+    if (threadIdx.x == 0 && d.nsplit > 1 && d.nsplit <= kFusedMergeSplits) {
+      pend_tg = d.t * p.num_kv_heads + d.g;
+      pend_prev = dev::atom_add_release_gpu(p.merge_cnt + pend_tg, 1);  // releases the CTA's partial
+      pend_ns = d.nsplit;
+    }
     w.advance();
   }
+  if (cta_ok) {  // the CTA's last split may still complete a token
+    if (threadIdx.x == 0) resolve_pending();
+    __syncthreads();
+    if (idx_ring[4] >= 0) merge_splits<D, G, T::NTHREADS>(p, idx_ring[4], idx_ring[5]);
+  }
+  if (!w.ok || w.consumed < w.issued) w.drain();
 }
 
 template <int D, int G>
@@ -399,9 +544,10 @@ __global__ void __launch_bounds__(DecodeTraits<D, G>::NTHREADS, DecodeTraits<D, 
 decode_kernel(const __grid_constant__ DecodeParams p) {
   using T = DecodeTraits<D, G>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* rings =
+  unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rings + T::OFF_BAR);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
+  int* idx_ring = reinterpret_cast<int*>(smem + T::OFF_IDX);
   dev::griddep_wait();
   dev::griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -409,9 +555,13 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     for (int i = 0; i < T::NR; ++i) dev::mbar_init(&bars[warp * T::NR + i], 1);
     dev::fence_mbar_init();
   }
+  if (threadIdx.x == 0) {  // the first two tasks are static: no counter round trip before the first copy
+    idx_ring[0] = blockIdx.x;
+    idx_ring[1] = blockIdx.x + gridDim.x;
+  }
   // one CTA-uniform decision (a racing error-word update must not split the CTA)
   const bool poisoned = __syncthreads_or(threadIdx.x == 0 && dev::pool_poisoned(p.err));
-  if (!poisoned) worker_loop<D, G>(p, rings, bars, warp, lane);
+  if (!poisoned) worker_loop<D, G>(p, smem, warp, lane);
   // the last CTA out resets the task counter for the next launch on this plan
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -425,9 +575,9 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
 }
 
 // ---------------------------------------------------------------------------------------------------
-// Merge of tokens with more than one split.  Grid (token, KV head, chunk of partial elements), 256
-// threads = SG split groups x (256 / SG) element threads; partials are read in the decode's MMA fragment
-// order, element e of a partial being register e % (D/4) of lane e / (D/4).
+// Merge of tokens with more than kFusedMergeSplits splits.  Grid (token, KV head, chunk of partial
+// elements), 256 threads = SG split groups x (256 / SG) element threads; element e of a partial is head
+// e / D, dim e % D.
 // ---------------------------------------------------------------------------------------------------
 struct MergeParams {
   const float* part_o;
@@ -443,9 +593,8 @@ struct MergeParams {
 
 template <int D, int SG>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
-  constexpr int OV = D / 4;                  // fp32 values per lane of a partial
-  constexpr int TE = 256 / SG;               // threads along the elements
-  constexpr int EPC = SG == 1 ? 32 * OV : TE;  // elements per CTA
+  constexpr int TE = 256 / SG;                        // threads along the elements
+  constexpr int EPC = SG == 1 ? kHeadsTile * D : TE;  // elements per CTA
   constexpr int EPT = EPC / TE;              // elements per thread
   __shared__ float sM[kHeadsTile], sL[kHeadsTile];
   __shared__ float red[256];
@@ -456,7 +605,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   if (ctx <= 0) return;
   const int nblk = (ctx + kBS - 1) / kBS;
   const int nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
-  if (nsplit <= 1) return;
+  if (nsplit <= kFusedMergeSplits || (int)blockIdx.z * EPC >= p.group * D) return;
   const size_t sb = ((size_t)t * p.num_kv_heads + g) * p.max_splits;
   const int tid = threadIdx.x;
   // per-head max and sum over the splits: thread (head tid % 8, split stride group tid / 8)
@@ -489,21 +638,22 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
     __syncthreads();
   }
   const int te = tid % TE, sg = tid / TE;
+  const int E = p.group * D;  // elements that belong to real query heads
   float acc[EPT];
   int heads[EPT];
 #pragma unroll
   for (int k = 0; k < EPT; ++k) {
     const int e = blockIdx.z * EPC + te + k * TE;
-    heads[k] = (((e / OV) & 3) << 1) + ((e % OV) & 1);
+    heads[k] = min(e / D, kHeadsTile - 1);
     acc[k] = 0.f;
   }
   for (int s = sg; s < nsplit; s += SG) {
-    const float* po = p.part_o + (sb + s) * 32 * OV;
+    const float* po = p.part_o + (sb + s) * kHeadsTile * D;
     const float2* pml = p.part_ml + (sb + s) * kHeadsTile;
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
       const int e = blockIdx.z * EPC + te + k * TE;
-      acc[k] += po[e] * exp2f(pml[heads[k]].x - sM[heads[k]]);
+      if (e < E) acc[k] += po[e] * exp2f(pml[heads[k]].x - sM[heads[k]]);
     }
   }
 #pragma unroll
@@ -516,11 +666,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
       for (int j = 1; j < SG; ++j) acc[k] += red[te + j * TE];
     }
     const int e = blockIdx.z * EPC + te + k * TE;
-    const int lane = e / OV, r = e % OV;
-    const int dim = 16 * (r >> 2) + (lane >> 2) + ((r & 2) ? 8 : 0);
-    const int head = heads[k];
-    if (head < p.group)
-      p.out[((size_t)t * p.num_q_heads + (size_t)g * p.group + head) * D + dim] = __float2half_rn(acc[k] / sL[head]);
+    if (e < E)
+      p.out[((size_t)t * p.num_q_heads + (size_t)g * p.group + heads[k]) * D + e % D] =
+          __float2half_rn(acc[k] / sL[heads[k]]);
   }
 }
 
@@ -558,8 +706,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                                                             const int32_t* __restrict__ qsl, int num_seqs,
                                                             int num_tokens, int max_ctx, int split_blocks,
                                                             int num_kv_heads, int32_t* __restrict__ tok_row,
-                                                            int32_t* __restrict__ tok_ctx, int4* __restrict__ tasks,
-                                                            WsHeader* hdr, int32_t* err) {
+                                                            int32_t* __restrict__ tok_ctx, int32_t* __restrict__ merge_cnt,
+                                                            int4* __restrict__ tasks, WsHeader* hdr, int32_t* err) {
   __shared__ int warp_sums[32];
   dev::griddep_wait();
   dev::griddep_launch_dependents();
@@ -569,8 +717,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
       dev::set_error(err, PKV_DEVERR_QSL);
     if (q1 - q0 < 1 || ctx < q1 - q0 || ctx > max_ctx) dev::set_error(err, PKV_DEVERR_ROW_META);
   }
+  for (int i = threadIdx.x; i < num_tokens * num_kv_heads; i += blockDim.x) merge_cnt[i] = 0;
   int carry = 0;
-  for (int pass = 0; pass < 2; ++pass) {  // pass 0: full splits; pass 1: each token's partial last split
+  // Pass 0 lists each token's short last split, pass 1 its full splits in token order: tokens then
+  // complete, and get merged, all through the launch rather than together at its end, and the launch
+  // ends on equal-sized tasks.
+  for (int pass = 0; pass < 2; ++pass) {
     for (int base = 0; base < num_tokens; base += blockDim.x) {
       const int t = base + threadIdx.x;
       int nblk = 0, row = 0, c = 0;
@@ -591,15 +743,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
       }
       const int nfull = nblk / split_blocks;
       const int ntail = nblk % split_blocks ? 1 : 0;
-      const int cnt = (pass == 0 ? nfull : ntail) * num_kv_heads;
+      const int cnt = (pass == 0 ? ntail : nfull) * num_kv_heads;
       int total = 0;
       const int off = carry + block_exclusive_scan(cnt, warp_sums, &total);
       if (cnt > 0) {
         if (pass == 0) {
+          for (int g = 0; g < num_kv_heads; ++g) tasks[off + g] = make_int4(t, g | (nfull << 8), row, c);
+        } else {
           for (int g = 0; g < num_kv_heads; ++g)
             for (int s = 0; s < nfull; ++s) tasks[off + g * nfull + s] = make_int4(t, g | (s << 8), row, c);
-        } else {
-          for (int g = 0; g < num_kv_heads; ++g) tasks[off + g] = make_int4(t, g | (nfull << 8), row, c);
         }
       }
       carry += total;
@@ -617,7 +769,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 // Workspace layout and launches
 // ---------------------------------------------------------------------------------------------------
 struct WsLayout {
-  size_t hdr, tok_row, tok_ctx, tasks, part_ml, part_o, total;
+  size_t hdr, tok_row, tok_ctx, merge_cnt, tasks, part_ml, part_o, total;
   int max_splits;
   int64_t max_tasks;
 };
@@ -635,6 +787,8 @@ static WsLayout ws_layout(const pkv_config& c, int num_tokens, int max_blocks) {
   off += up256((size_t)num_tokens * 4);
   w.tok_ctx = off;
   off += up256((size_t)num_tokens * 4);
+  w.merge_cnt = off;
+  off += up256((size_t)num_tokens * c.num_kv_heads * 4);
   w.tasks = off;
   off += up256((size_t)w.max_tasks * sizeof(int4));
   const size_t parts = w.max_splits > 1 ? (size_t)w.max_tasks : 0;  // one partial per (token, KV head, split)
@@ -658,9 +812,8 @@ static cudaError_t launch_decode(const DecodeParams& p, int num_sms, int64_t max
     if (e != cudaSuccess) return e;
     per_sm = n > 0 ? n : 1;
   }
-  int64_t grid = (int64_t)num_sms * per_sm;
-  const int64_t groups = (max_tasks + T::NW - 1) / T::NW;
-  if (grid > groups) grid = groups;
+  int64_t grid = (int64_t)num_sms * per_sm;  // persistent: one CTA per resident slot, one task at a time
+  if (grid > max_tasks) grid = max_tasks;
   if (grid < 1) grid = 1;
   return launch_pdl(decode_kernel<D, G>, dim3((unsigned)grid), dim3(T::NTHREADS), T::SMEM, stream, p);
 }
@@ -684,7 +837,7 @@ static cudaError_t launch_plan(pkv_pool* pool, char* ws, const WsLayout& w, cons
   return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, context_lens, qsl, num_seqs, num_tokens,
                     max_blocks * kBS, (int)c.split_blocks, (int)c.num_kv_heads,
                     reinterpret_cast<int32_t*>(ws + w.tok_row), reinterpret_cast<int32_t*>(ws + w.tok_ctx),
-                    reinterpret_cast<int4*>(ws + w.tasks), reinterpret_cast<WsHeader*>(ws + w.hdr),
+                    reinterpret_cast<int32_t*>(ws + w.merge_cnt), reinterpret_cast<int4*>(ws + w.tasks), reinterpret_cast<WsHeader*>(ws + w.hdr),
                     pool->dev_error);
 }
 
@@ -704,6 +857,7 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
   p.out = static_cast<__half*>(out);
   p.part_o = reinterpret_cast<float*>(ws + w.part_o);
   p.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
+  p.merge_cnt = reinterpret_cast<int32_t*>(ws + w.merge_cnt);
   p.err = pool->dev_error;
   const int rows_per_pool = c.num_blocks * c.num_kv_heads * c.block_size;
   p.layer_row0_k = (layer * 2) * rows_per_pool;
@@ -725,17 +879,13 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   *launches += 1;
-  if (w.max_splits > 1) {
+  if (w.max_splits > kFusedMergeSplits) {
     MergeParams m{p.part_o, p.part_ml, p.tok_ctx, p.out, c.num_q_heads, c.num_kv_heads, group, c.split_blocks,
                   w.max_splits};
-    const bool wide = w.max_splits > kWideMergeSplits;
-    const dim3 grid(num_tokens, c.num_kv_heads, wide ? (8 * c.head_dim) / 64 : 1);
-    switch (c.head_dim * 2 + (wide ? 1 : 0)) {
-      case 128: e = launch_pdl(merge_kernel<64, 1>, grid, dim3(256), 0, s, m); break;
-      case 129: e = launch_pdl(merge_kernel<64, 4>, grid, dim3(256), 0, s, m); break;
-      case 256: e = launch_pdl(merge_kernel<128, 1>, grid, dim3(256), 0, s, m); break;
-      case 257: e = launch_pdl(merge_kernel<128, 4>, grid, dim3(256), 0, s, m); break;
-      case 512: e = launch_pdl(merge_kernel<256, 1>, grid, dim3(256), 0, s, m); break;
+    const dim3 grid(num_tokens, c.num_kv_heads, (kHeadsTile * c.head_dim) / 64);
+    switch (c.head_dim) {
+      case 64: e = launch_pdl(merge_kernel<64, 4>, grid, dim3(256), 0, s, m); break;
+      case 128: e = launch_pdl(merge_kernel<128, 4>, grid, dim3(256), 0, s, m); break;
       default: e = launch_pdl(merge_kernel<256, 4>, grid, dim3(256), 0, s, m); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
@@ -894,7 +1044,7 @@ extern "C" pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const
   if (device != pool->device) return fail(PKV_ERR_INVALID_ARG, "the pool's device must be the current device");
   void* scratch = noalloc_scratch_ptr(device, &e);
   if (!scratch) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch array");
-  // What must start at zero -- the task counter -- is cleared by the plan kernel on every call;
+  // What must start at zero -- the task and split counters -- is cleared by the plan kernel on every call;
   // everything else is written before it is read.
   char* ws = static_cast<char*>(scratch);
   cudaStream_t s = (cudaStream_t)stream;

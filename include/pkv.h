@@ -93,7 +93,9 @@ void pkv_pool_destroy(pkv_pool* pool);
 void* pkv_pool_layer_ptr(const pkv_pool* pool, int32_t layer, int32_t kv);
 
 /* Synchronously read the device error word (PKV_DEVERR_* bits) into *bits, then clear it if `clear`.
- * Waits for all work on the legacy default stream's device. */
+ * Waits for all work on the legacy default stream's device.  While PKV_DEVERR_WAIT_TIMEOUT is set,
+ * attention launches return without work; after clearing it, issue a new pkv_attention_plan before
+ * the next pkv_attention (the interrupted launch may have left split counters mid-count). */
 pkv_status pkv_pool_check(pkv_pool* pool, int32_t* bits, int32_t clear);
 
 /* ------------------------------------------------------------------------------------------------
