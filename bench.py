@@ -5,6 +5,9 @@ Default workload: the Qwen2.5-1.5B-shaped decode batch (28 layers, 12 q / 2 KV h
 256 rows with contexts uniform in [256, 768] plus one new token, blocks of 16 scattered over a pool 1.25x
 the need, fp16 values from the seeded generator).  A step = one attention plan + 28 x (append + attention).
 
+The timed region replays the step as one CUDA graph (captured from the same library calls), so the
+number is the GPU's, not the host's launch rate; `--eager` times the calls issued one by one instead.
+
 Prints one JSON line (rank 0).  `value` is algorithmic HBM bytes per second of the whole step (K/V read
 once per row and layer, q read, output written, block tables, append traffic); `ctx_tokens_per_s` is the
 number of context tokens attended per second.  `--impl reference` times the CPU oracle instead.
@@ -44,7 +47,7 @@ CONFIGS = {
 # DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
 # source they were taken on; reported as null once the source changes.
-TRAFFIC = {}
+TRAFFIC = {"c6583ba3d0c8": 142.62e6}  # profiles/decode_kernel_qwen_decode.md
 
 FALLBACK_HBM_GBS = 6800.0
 
@@ -306,13 +309,36 @@ def run_pkv(args, rank, world, local):
     torch.cuda.synchronize()
     assert pool.check() == 0
 
+    # the step as one CUDA graph: the same calls, captured on a side stream, replayed on `stream`
+    graph = None
+    if not args.eager:
+        cap = torch.cuda.Stream(dev)
+        cstep = RawStep(pool, ds, attn, qs, ks, vs, outs, cap.cuda_stream)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for _ in range(3):
+                cstep(layers)
+        torch.cuda.synchronize()
+        cstep.launches = 0
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            cstep(layers)
+        launches_per_step = cstep.launches
+        torch.cuda.synchronize()
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step(layers)
+
     attn_bytes, append_bytes = algorithmic_bytes(batch)
     step_bytes = (attn_bytes + append_bytes) * len(layers)
     ctx_tokens = int(batch.context_lens.astype(np.int64).sum()) * len(layers)
 
     # ---- device-resident timed region ----
     for _ in range(args.warmup):
-        step(layers)
+        run_step()
     torch.cuda.synchronize()
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
@@ -323,12 +349,12 @@ def run_pkv(args, rank, world, local):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step(layers)
+        run_step()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if sampler else None
-    launches = step.launches
+    launches = step.launches if graph is None else launches_per_step * args.steps
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     assert pool.check() == 0
 
@@ -365,14 +391,15 @@ def run_pkv(args, rank, world, local):
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
                    "rows": batch.num_seqs, "new_tokens": batch.num_tokens,
                    "context_tokens_per_layer": int(batch.context_lens.sum()), "pool_blocks": batch.num_blocks,
-                   "split_blocks": pool.cfg.split_blocks,
+                   "split_blocks": pool.cfg.split_blocks or 16,
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of K/V per step rotating over "
-                         f"{s.num_layers} layer pools", "parallelism": f"replicas x{world}"},
+                         f"{s.num_layers} layer pools", "parallelism": f"replicas x{world}",
+                   "launch": "eager" if graph is None else "cuda_graph"},
         "pct_of_peak": 100.0 * value / world / peak,
         "ctx_tokens_per_s": ctx_tokens * world / (ms * 1e-3),
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": TRAFFIC.get(sh), "kernel": "pkv_attention (decode partials + merge)",
+                     "traffic": TRAFFIC.get(sh), "kernel": "decode_kernel (split-K decode, fused merge)",
                      "per_launch_bytes": attn_bytes, "avg_launch_ms": attn_ms, "peak_source": peak_src,
                      "source": sh},
         "e2e": e2e,
@@ -438,6 +465,7 @@ def main():
     ap.add_argument("--split-blocks", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
+    ap.add_argument("--eager", action="store_true", help="time the calls issued one by one, not a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -548,8 +548,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
   int* idx_ring = reinterpret_cast<int*>(smem + T::OFF_IDX);
-  dev::griddep_wait();
-  dev::griddep_launch_dependents();
+  // set-up that reads nothing written by earlier kernels runs before the dependency wait
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) {
     for (int i = 0; i < T::NR; ++i) dev::mbar_init(&bars[warp * T::NR + i], 1);
@@ -559,6 +558,8 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     idx_ring[0] = blockIdx.x;
     idx_ring[1] = blockIdx.x + gridDim.x;
   }
+  dev::griddep_wait();
+  dev::griddep_launch_dependents();
   // one CTA-uniform decision (a racing error-word update must not split the CTA)
   const bool poisoned = __syncthreads_or(threadIdx.x == 0 && dev::pool_poisoned(p.err));
   if (!poisoned) worker_loop<D, G>(p, smem, warp, lane);
