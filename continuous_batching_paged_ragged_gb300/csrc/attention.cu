@@ -33,29 +33,17 @@
 #include <mutex>
 #include <string>
 
-#include "pkv_internal.cuh"
+#include "attn_common.cuh"
 
 namespace pkv {
 
-constexpr int kBS = 16;
 constexpr int kFusedMergeSplits = 32;  // tokens with up to this many splits are merged inside the decode
 constexpr int kMaxSplitBlocks = 32;   // upper bound on split_blocks (a split's block ids fit one warp)
-constexpr int kHeadsTile = 8;         // query heads per KV head handled by one MMA tile (G <= 8)
 
 // Ring slots per warp: runs (a block's K or V for one KV head, or a task's q) in flight.
 #ifndef PKV_DECODE_RING
 #define PKV_DECODE_RING(D) ((D) == 256 ? 2 : ((D) == 128 ? 3 : 5))
 #endif
-
-__host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
-
-struct WsHeader {
-  int32_t n_tasks;
-  int32_t work;   // dynamic tasks handed out so far (each CTA's first two tasks are static)
-  int32_t done;   // CTAs of the current decode launch that have finished
-  int32_t pad[61];
-};
-static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 constexpr int kSmemPerSM = 228 * 1024;  // shared memory of one SM
 constexpr int kSmemReservedPerCTA = 1024;
@@ -703,84 +691,152 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
   return before + x - v;
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ context_lens,
-                                                            const int32_t* __restrict__ qsl, int num_seqs,
-                                                            int num_tokens, int max_ctx, int split_blocks,
-                                                            int num_kv_heads, int32_t* __restrict__ tok_row,
-                                                            int32_t* __restrict__ tok_ctx, int32_t* __restrict__ merge_cnt,
-                                                            int4* __restrict__ tasks, WsHeader* hdr, int32_t* err) {
-  __shared__ int warp_sums[32];
-  dev::griddep_wait();
-  dev::griddep_launch_dependents();
-  for (int i = threadIdx.x; i < num_seqs; i += blockDim.x) {
-    const int q0 = __ldg(qsl + i), q1 = __ldg(qsl + i + 1), ctx = __ldg(context_lens + i);
-    if (q1 < q0 || (i == 0 && q0 != 0) || (i == num_seqs - 1 && q1 != num_tokens))
-      dev::set_error(err, PKV_DEVERR_QSL);
-    if (q1 - q0 < 1 || ctx < q1 - q0 || ctx > max_ctx) dev::set_error(err, PKV_DEVERR_ROW_META);
+struct PlanParams {
+  const int32_t* context_lens;
+  const int32_t* qsl;
+  int num_seqs, num_tokens, max_ctx, split_blocks, num_kv_heads;
+  int prefill_min_qlen;  // rows with at least this many new tokens become prefill items (0: none)
+  int prefill_pos;       // query positions per prefill item
+  int32_t* tok_row;
+  int32_t* tok_ctx;
+  int32_t* merge_cnt;
+  int4* tasks;
+  int4* items;
+  WsHeader* hdr;
+  int32_t* err;
+};
+
+__device__ __forceinline__ bool row_meta_ok(int q_len, int ctx, int max_ctx) {
+  return q_len >= 1 && ctx >= q_len && ctx <= max_ctx;
+}
+
+// Prefill items of row b in plan order: (position block qb, KV head g); `fn(qb, cost, rec)` per qb.
+template <typename F>
+__device__ __forceinline__ void for_row_items(const PlanParams& p, int b, F fn) {
+  const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1), ctx = __ldg(p.context_lens + b);
+  const int q_len = q1 - q0;
+  if (p.prefill_min_qlen <= 0 || q_len < p.prefill_min_qlen || !row_meta_ok(q_len, ctx, p.max_ctx)) return;
+  for (int qb = 0; qb * p.prefill_pos < q_len; ++qb) {
+    const int npos = min(p.prefill_pos, q_len - qb * p.prefill_pos);
+    const int w = ctx - q_len + qb * p.prefill_pos;  // keys visible to the block's first position, minus one
+    const int cost = (w + npos + kPrefillKeys - 1) / kPrefillKeys;
+    fn(cost, make_int4(b, npos << 16, q0 + qb * p.prefill_pos, w));
   }
-  for (int i = threadIdx.x; i < num_tokens * num_kv_heads; i += blockDim.x) merge_cnt[i] = 0;
-  int carry = 0;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) {
+  __shared__ int warp_sums[32];
+  __shared__ int hist[kPrefillBuckets];
+  dev::griddep_wait();
+  for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
+    const int q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1), ctx = __ldg(p.context_lens + i);
+    if (q1 < q0 || (i == 0 && q0 != 0) || (i == p.num_seqs - 1 && q1 != p.num_tokens))
+      dev::set_error(p.err, PKV_DEVERR_QSL);
+    if (!row_meta_ok(q1 - q0, ctx, p.max_ctx)) dev::set_error(p.err, PKV_DEVERR_ROW_META);
+  }
+  for (int i = threadIdx.x; i < p.num_tokens * p.num_kv_heads; i += blockDim.x) p.merge_cnt[i] = 0;
+  for (int i = threadIdx.x; i < kPrefillBuckets; i += blockDim.x) hist[i] = 0;
+
+  // ---- decode tasks: tokens of rows that are not prefill items ----
   // Pass 0 lists each token's short last split, pass 1 its full splits in token order: tokens then
   // complete, and get merged, all through the launch rather than together at its end, and the launch
   // ends on equal-sized tasks.
+  int carry = 0;
   for (int pass = 0; pass < 2; ++pass) {
-    for (int base = 0; base < num_tokens; base += blockDim.x) {
+    for (int base = 0; base < p.num_tokens; base += blockDim.x) {
       const int t = base + threadIdx.x;
       int nblk = 0, row = 0, c = 0;
-      if (t < num_tokens) {
+      if (t < p.num_tokens) {
         if (pass == 0) {
-          const int b = dev::row_of_token(qsl, num_seqs, t);
-          const int q0 = __ldg(qsl + b), q1 = __ldg(qsl + b + 1), ctx = __ldg(context_lens + b);
+          const int b = dev::row_of_token(p.qsl, p.num_seqs, t);
+          const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1), ctx = __ldg(p.context_lens + b);
           const int q_len = q1 - q0;
-          if (t >= q0 && t < q1 && q_len >= 1 && ctx >= q_len && ctx <= max_ctx) c = ctx - q_len + (t - q0) + 1;
-          tok_row[t] = b;
-          tok_ctx[t] = c;
+          const bool prefill = p.prefill_min_qlen > 0 && q_len >= p.prefill_min_qlen;
+          if (t >= q0 && t < q1 && row_meta_ok(q_len, ctx, p.max_ctx) && !prefill) c = ctx - q_len + (t - q0) + 1;
+          p.tok_row[t] = b;
+          p.tok_ctx[t] = c;  // 0: no decode work (prefill row or invalid metadata)
           row = b;
         } else {
-          c = tok_ctx[t];
-          row = tok_row[t];
+          c = p.tok_ctx[t];
+          row = p.tok_row[t];
         }
         nblk = (c + kBS - 1) / kBS;
       }
-      const int nfull = nblk / split_blocks;
-      const int ntail = nblk % split_blocks ? 1 : 0;
-      const int cnt = (pass == 0 ? ntail : nfull) * num_kv_heads;
+      const int nfull = nblk / p.split_blocks;
+      const int ntail = nblk % p.split_blocks ? 1 : 0;
+      const int cnt = (pass == 0 ? ntail : nfull) * p.num_kv_heads;
       int total = 0;
       const int off = carry + block_exclusive_scan(cnt, warp_sums, &total);
       if (cnt > 0) {
         if (pass == 0) {
-          for (int g = 0; g < num_kv_heads; ++g) tasks[off + g] = make_int4(t, g | (nfull << 8), row, c);
+          for (int g = 0; g < p.num_kv_heads; ++g) p.tasks[off + g] = make_int4(t, g | (nfull << 8), row, c);
         } else {
-          for (int g = 0; g < num_kv_heads; ++g)
-            for (int s = 0; s < nfull; ++s) tasks[off + g * nfull + s] = make_int4(t, g | (s << 8), row, c);
+          for (int g = 0; g < p.num_kv_heads; ++g)
+            for (int s = 0; s < nfull; ++s) p.tasks[off + g * nfull + s] = make_int4(t, g | (s << 8), row, c);
         }
       }
       carry += total;
       __syncthreads();  // warp_sums is reused by the next chunk
     }
   }
-  if (threadIdx.x == 0) {
-    hdr->n_tasks = carry;
-    hdr->work = 0;
-    hdr->done = 0;
+
+  // ---- prefill items, bucketed by K/V tile count, longest first ----
+  auto bucket_of = [](int cost) { return kPrefillBuckets - 1 - min(cost, kPrefillBuckets - 1); };
+  for (int b = threadIdx.x; b < p.num_seqs; b += blockDim.x)
+    for_row_items(p, b, [&](int cost, int4) { atomicAdd(&hist[bucket_of(cost)], p.num_kv_heads); });
+  __syncthreads();
+  int n_items = 0;
+  for (int base = 0; base < kPrefillBuckets; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const int v = i < kPrefillBuckets ? hist[i] : 0;
+    int total = 0;
+    const int off = n_items + block_exclusive_scan(v, warp_sums, &total);
+    __syncthreads();
+    if (i < kPrefillBuckets) hist[i] = off;  // first slot of the bucket
+    n_items += total;
+    __syncthreads();
   }
+  for (int b = threadIdx.x; b < p.num_seqs; b += blockDim.x)
+    for_row_items(p, b, [&](int cost, int4 rec) {
+      const int at = atomicAdd(&hist[bucket_of(cost)], p.num_kv_heads);
+      for (int g = 0; g < p.num_kv_heads; ++g) p.items[at + g] = make_int4(rec.x, g | rec.y, rec.z, rec.w);
+    });
+
+  if (threadIdx.x == 0) {
+    p.hdr->n_tasks = carry;
+    p.hdr->work = 0;
+    p.hdr->done = 0;
+    p.hdr->n_items = n_items;
+    p.hdr->pwork = 0;
+    p.hdr->pdone = 0;
+  }
+  __threadfence();
+  dev::griddep_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------------------------------
 // Workspace layout and launches
 // ---------------------------------------------------------------------------------------------------
 struct WsLayout {
-  size_t hdr, tok_row, tok_ctx, merge_cnt, tasks, part_ml, part_o, total;
+  size_t hdr, tok_row, tok_ctx, merge_cnt, tasks, items, part_ml, part_o, total;
   int max_splits;
   int64_t max_tasks;
+  int prefill_min_qlen;  // 0: every row takes the decode path
+  int prefill_pos;
+  int64_t max_items;
 };
 
 static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
-static WsLayout ws_layout(const pkv_config& c, int num_tokens, int max_blocks) {
+static WsLayout ws_layout(const pkv_config& c, int num_seqs, int num_tokens, int max_blocks) {
   WsLayout w;
   w.max_splits = (max_blocks + c.split_blocks - 1) / c.split_blocks;
   w.max_tasks = (int64_t)num_tokens * c.num_kv_heads * w.max_splits;
+  const int group = c.num_q_heads / c.num_kv_heads;
+  const bool prefill = prefill_supported(c.head_dim, group);
+  w.prefill_min_qlen = prefill ? kPrefillMinQlen : 0;
+  w.prefill_pos = prefill_positions(group);
+  w.max_items = prefill ? (int64_t)c.num_kv_heads * ((num_tokens + w.prefill_pos - 1) / w.prefill_pos + num_seqs) : 0;
   size_t off = 0;
   w.hdr = off;
   off += sizeof(WsHeader);
@@ -792,6 +848,8 @@ static WsLayout ws_layout(const pkv_config& c, int num_tokens, int max_blocks) {
   off += up256((size_t)num_tokens * c.num_kv_heads * 4);
   w.tasks = off;
   off += up256((size_t)w.max_tasks * sizeof(int4));
+  w.items = off;
+  off += up256((size_t)w.max_items * sizeof(int4));
   const size_t parts = w.max_splits > 1 ? (size_t)w.max_tasks : 0;  // one partial per (token, KV head, split)
   w.part_ml = off;
   off += up256(parts * kHeadsTile * sizeof(float2));
@@ -835,17 +893,30 @@ static cudaError_t launch_decode_g(int group, const DecodeParams& p, int num_sms
 static cudaError_t launch_plan(pkv_pool* pool, char* ws, const WsLayout& w, const int32_t* context_lens,
                                const int32_t* qsl, int num_seqs, int num_tokens, int max_blocks, cudaStream_t s) {
   const pkv_config& c = pool->cfg;
-  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, context_lens, qsl, num_seqs, num_tokens,
-                    max_blocks * kBS, (int)c.split_blocks, (int)c.num_kv_heads,
-                    reinterpret_cast<int32_t*>(ws + w.tok_row), reinterpret_cast<int32_t*>(ws + w.tok_ctx),
-                    reinterpret_cast<int32_t*>(ws + w.merge_cnt), reinterpret_cast<int4*>(ws + w.tasks), reinterpret_cast<WsHeader*>(ws + w.hdr),
-                    pool->dev_error);
+  PlanParams p;
+  p.context_lens = context_lens;
+  p.qsl = qsl;
+  p.num_seqs = num_seqs;
+  p.num_tokens = num_tokens;
+  p.max_ctx = max_blocks * kBS;
+  p.split_blocks = c.split_blocks;
+  p.num_kv_heads = c.num_kv_heads;
+  p.prefill_min_qlen = w.prefill_min_qlen;
+  p.prefill_pos = w.prefill_pos;
+  p.tok_row = reinterpret_cast<int32_t*>(ws + w.tok_row);
+  p.tok_ctx = reinterpret_cast<int32_t*>(ws + w.tok_ctx);
+  p.merge_cnt = reinterpret_cast<int32_t*>(ws + w.merge_cnt);
+  p.tasks = reinterpret_cast<int4*>(ws + w.tasks);
+  p.items = reinterpret_cast<int4*>(ws + w.items);
+  p.hdr = reinterpret_cast<WsHeader*>(ws + w.hdr);
+  p.err = pool->dev_error;
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p);
 }
 
-// decode (+ merge of very long tokens) for one layer on a planned workspace
+// decode (+ merge of very long tokens) and prefill tiles for one layer on a planned workspace
 static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, const int32_t* block_tables,
-                                   int max_blocks, int num_tokens, void* out, char* ws, const WsLayout& w,
-                                   cudaStream_t s, int* launches) {
+                                   int max_blocks, int num_seqs, int num_tokens, void* out, char* ws,
+                                   const WsLayout& w, cudaStream_t s, int* launches) {
   const pkv_config& c = pool->cfg;
   DecodeParams p;
   p.kv_map = pool->kv_map;
@@ -892,6 +963,29 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
     *launches += 1;
   }
+  // prefill rows exist only if some row has at least prefill_min_qlen new tokens
+  if (w.prefill_min_qlen > 0 && num_tokens - num_seqs >= w.prefill_min_qlen - 1) {
+    PrefillArgs a;
+    a.kv_map = &pool->kv_map;
+    a.q = q;
+    a.out = out;
+    a.block_tables = block_tables;
+    a.items = reinterpret_cast<const int4*>(ws + w.items);
+    a.hdr = p.hdr;
+    a.err = p.err;
+    a.layer_row0_k = p.layer_row0_k;
+    a.layer_row0_v = p.layer_row0_v;
+    a.max_blocks = max_blocks;
+    a.num_q_heads = c.num_q_heads;
+    a.num_kv_heads = c.num_kv_heads;
+    a.num_blocks = c.num_blocks;
+    a.head_dim = c.head_dim;
+    a.num_sms = pool->num_sms;
+    a.max_items = w.max_items;
+    e = launch_prefill(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    *launches += 1;
+  }
   return PKV_OK;
 }
 
@@ -902,7 +996,7 @@ using namespace pkv;
 extern "C" size_t pkv_attention_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t num_tokens,
                                                 int32_t max_blocks_per_seq) {
   if (!pool || num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq < 1) return 0;
-  return ws_layout(pool->cfg, num_tokens, max_blocks_per_seq).total;
+  return ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks_per_seq).total;
 }
 
 static pkv_status check_common(pkv_pool* pool, const int32_t* context_lens, const int32_t* qsl, int32_t num_seqs,
@@ -922,12 +1016,12 @@ static pkv_status check_common(pkv_pool* pool, const int32_t* context_lens, cons
   return PKV_OK;
 }
 
-static pkv_status check_workspace(pkv_pool* pool, void* workspace, size_t ws_bytes, int32_t num_tokens,
+static pkv_status check_workspace(pkv_pool* pool, void* workspace, size_t ws_bytes, int32_t num_seqs, int32_t num_tokens,
                                   int32_t max_blocks) {
   if (num_tokens > 0 && !workspace) return fail(PKV_ERR_INVALID_ARG, "workspace must be non-NULL");
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  const WsLayout w = ws_layout(pool->cfg, num_tokens, max_blocks);
+  const WsLayout w = ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks);
   if (ws_bytes < w.total)
     return fail(PKV_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(w.total) + " bytes");
   return PKV_OK;
@@ -946,12 +1040,12 @@ extern "C" pkv_status pkv_attention_plan(pkv_pool* pool, const int32_t* context_
                                          void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
   pkv_status st = check_common(pool, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq);
-  if (st == PKV_OK) st = check_workspace(pool, workspace, workspace_bytes, num_tokens, max_blocks_per_seq);
+  if (st == PKV_OK) st = check_workspace(pool, workspace, workspace_bytes, num_seqs, num_tokens, max_blocks_per_seq);
   if (st != PKV_OK) return st;
   pool->last_launches = 0;
   pool->plan = PlanKey{workspace, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq};
   if (num_tokens == 0) return PKV_OK;
-  const WsLayout w = ws_layout(pool->cfg, num_tokens, max_blocks_per_seq);
+  const WsLayout w = ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks_per_seq);
   cudaError_t e = launch_plan(pool, static_cast<char*>(workspace), w, context_lens, query_start_loc, num_seqs,
                               num_tokens, max_blocks_per_seq, (cudaStream_t)stream);
   if (e != cudaSuccess) {
@@ -968,7 +1062,7 @@ extern "C" pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q
                                     void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
   pkv_status st = check_common(pool, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq);
-  if (st == PKV_OK) st = check_workspace(pool, workspace, workspace_bytes, num_tokens, max_blocks_per_seq);
+  if (st == PKV_OK) st = check_workspace(pool, workspace, workspace_bytes, num_seqs, num_tokens, max_blocks_per_seq);
   if (st != PKV_OK) return st;
   pool->last_launches = 0;
   if (layer < 0 || layer >= pool->cfg.num_layers) return fail(PKV_ERR_OUT_OF_RANGE, "layer out of range");
@@ -979,9 +1073,9 @@ extern "C" pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q
   if (k.workspace != workspace || k.context_lens != context_lens || k.query_start_loc != query_start_loc ||
       k.num_seqs != num_seqs || k.num_tokens != num_tokens || k.max_blocks_per_seq != max_blocks_per_seq)
     return fail(PKV_ERR_INVALID_ARG, "no matching plan: call pkv_attention_plan for this workspace and metadata");
-  const WsLayout w = ws_layout(pool->cfg, num_tokens, max_blocks_per_seq);
+  const WsLayout w = ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks_per_seq);
   int launches = 0;
-  st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_tokens, out,
+  st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_seqs, num_tokens, out,
                         static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches);
   pool->last_launches = launches;
   return st;
@@ -1035,7 +1129,7 @@ extern "C" pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const
   if (num_tokens == 0) return PKV_OK;
   st = check_io(q, out, block_tables);
   if (st != PKV_OK) return st;
-  const WsLayout w = ws_layout(pool->cfg, num_tokens, max_blocks_per_seq);
+  const WsLayout w = ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks_per_seq);
   if (w.total > kNoAllocScratchBytes)
     return fail(PKV_ERR_OUT_OF_RANGE, "pass needs " + std::to_string(w.total) + " bytes of scratch; the built-in "
                 "array holds " + std::to_string(kNoAllocScratchBytes) + " (use pkv_attention with a workspace)");
@@ -1052,7 +1146,8 @@ extern "C" pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const
   e = launch_plan(pool, ws, w, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq, s);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   int launches = 1;
-  st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_tokens, out, ws, w, s, &launches);
+  st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_seqs, num_tokens, out, ws, w, s,
+                        &launches);
   pool->last_launches = launches;
   return st;
 }

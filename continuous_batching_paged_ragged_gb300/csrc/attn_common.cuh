@@ -1,0 +1,61 @@
+// Definitions shared by the attention translation units: the per-pass workspace header, the prefill
+// work-item record and the prefill launch entry.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+constexpr int kBS = 16;          // tokens per cache block
+constexpr int kHeadsTile = 8;    // query heads per KV head handled by one decode MMA tile (G <= 8)
+
+// Rows with at least this many new tokens (a prefill chunk) go to the tensor-core tile kernel; shorter
+// rows (decode, short chunks) to the split-K decode kernel.  The choice depends on the row alone, so a
+// row's result does not depend on the rest of the batch.
+constexpr int kPrefillMinQlen = 16;
+constexpr int kPrefillRows = 128;  // MMA rows of a prefill tile: (query position, query head) pairs
+constexpr int kPrefillKeys = 128;  // keys per K/V tile
+constexpr int kPrefillBuckets = 1024;
+
+// Query positions per prefill item: the G query heads of a KV head are packed into the MMA rows.
+__host__ __device__ constexpr int prefill_positions(int group) { return kPrefillRows / group; }
+
+struct WsHeader {
+  int32_t n_tasks;   // decode tasks of the pass
+  int32_t work;      // dynamic decode tasks handed out so far (each CTA's first two are static)
+  int32_t done;      // decode CTAs of the current launch that have finished
+  int32_t n_items;   // prefill items of the pass
+  int32_t pwork;     // dynamic prefill items handed out so far (each CTA's first is static)
+  int32_t pdone;     // prefill CTAs of the current launch that have finished
+  int32_t pad[58];
+};
+static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
+
+// A prefill item: one KV head, up to prefill_positions(G) consecutive query positions of one row.
+//   x: row (block-table row)          y: KV head | (positions << 16)
+//   z: first query token (packed)     w: keys visible to the item's first position, minus one
+// Position i of the item attends causally to keys 0 .. w + i.
+
+struct PrefillArgs {
+  const CUtensorMap* kv_map;  // device copy is passed by value below; this one is host-side
+  const void* q;
+  void* out;
+  const int32_t* block_tables;
+  const int4* items;
+  WsHeader* hdr;
+  int32_t* err;
+  int layer_row0_k, layer_row0_v;
+  int max_blocks, num_q_heads, num_kv_heads, num_blocks, head_dim;
+  int num_sms;
+  int64_t max_items;
+};
+
+// Launch the prefill tile kernel for one layer (programmatic dependent launch on `stream`).
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+// Whether the tile kernel serves this head shape (otherwise every row takes the decode path).
+bool prefill_supported(int head_dim, int group);
+
+}  // namespace pkv

@@ -1,0 +1,72 @@
+"""GPU parity of the chunked-prefill tile path (rows with >= 16 new tokens, head_dim 64 or 128) against the
+fp64 oracle: chunks over zero, short and long cached prefixes, chunk lengths around the tile sizes
+(positions per tile = 128 / G, 128 keys per K/V tile, 16-token blocks), every supported head grouping,
+and the same rows mixed with decode rows in one pass."""
+import numpy as np
+import pytest
+import torch
+
+from continuous_batching_paged_ragged_gb300 import synth
+from helpers_gpu import assert_close, oracle_row, row_slice, run_batch
+
+pytestmark = pytest.mark.gpu
+
+# (cached, q_len): chunk boundaries against P = 128 / G positions per tile and 128-key K/V tiles
+PREFILL_ROWS = [(0, 16), (0, 21), (0, 22), (0, 127), (0, 128), (0, 129), (0, 300), (5, 43), (127, 16),
+                (128, 17), (1000, 64), (2047, 200), (16, 250)]
+SHAPES = [(12, 2, 128), (8, 8, 64), (8, 1, 128), (16, 4, 128), (4, 2, 64), (8, 8, 128), (16, 16, 64)]
+
+
+@pytest.mark.parametrize("hq,hkv,d", SHAPES)
+def test_prefill_rows_all_shapes(cuda, built, hq, hkv, d):
+    shape = synth.Shape(1, hq, hkv, d)
+    cached, qls = zip(*PREFILL_ROWS)
+    batch = synth.custom_batch(shape, cached, qls, seed=21)
+    pool, ds, outs = run_batch(batch, [0])
+    for b in range(batch.num_seqs):
+        assert_close(row_slice(batch, outs[0], b), oracle_row(batch, 0, b), f"{(hq, hkv, d)} row {b} {PREFILL_ROWS[b]}")
+
+
+def test_prefill_mixed_with_decode_rows(cuda, built):
+    """Decode rows, short chunks (decode path) and long chunks (tile path) in one pass, two layers."""
+    shape = synth.Shape(2, 12, 2, 128)
+    rows = [(300, 1), (0, 40), (17, 1), (700, 15), (64, 16), (3000, 1), (250, 333), (1, 1)]
+    cached, qls = zip(*rows)
+    batch = synth.custom_batch(shape, cached, qls, seed=8)
+    pool, ds, outs = run_batch(batch, [0, 1])
+    for layer in (0, 1):
+        for b in range(batch.num_seqs):
+            assert_close(row_slice(batch, outs[layer], b), oracle_row(batch, layer, b), f"layer {layer} row {b}")
+
+
+def test_prefill_row_alone_equals_batched(cuda, built):
+    """A prefill row's output is bit-identical alone and inside a batch."""
+    shape = synth.Shape(1, 12, 2, 128)
+    rows = [(100, 1), (0, 180), (900, 1), (40, 77)]
+    cached, qls = zip(*rows)
+    full = synth.custom_batch(shape, cached, qls, seed=12)
+    _, _, of = run_batch(full, [0])
+    for b in (1, 3):
+        alone = synth.custom_batch(shape, [cached[b]], [qls[b]], seed=12, req_ids=[full.req_ids[b]])
+        _, _, oa = run_batch(alone, [0])
+        assert np.array_equal(oa[0].cpu().numpy().view(np.uint16), row_slice(full, of[0], b).view(np.uint16))
+
+
+def test_prefill_output_rows_untouched_outside_the_pass(cuda, built):
+    """The tile path writes exactly the pass's tokens: a sentinel past the last token survives."""
+    shape = synth.Shape(1, 8, 2, 128)
+    batch = synth.custom_batch(shape, [0, 33], [50, 20], seed=3)
+    from continuous_batching_paged_ragged_gb300 import workload
+    pool = workload.make_pool(batch)
+    workload.prefill_cache(pool, batch, [0])
+    ds = workload.upload(batch, pool)
+    qs, ks, vs = workload.step_inputs(ds, [0])
+    T = batch.num_tokens
+    big = torch.full((T + 4, 8, 128), 7.0, dtype=torch.float16, device=cuda)
+    out = big[:T]
+    workload.run_pass(pool, ds, [0], qs, ks, vs, [out])
+    torch.cuda.synchronize()
+    assert pool.check() == 0
+    assert torch.all(big[T:] == 7.0)
+    for b in range(batch.num_seqs):
+        assert_close(row_slice(batch, out, b), oracle_row(batch, 0, b), f"row {b}")
