@@ -835,7 +835,7 @@ static WsLayout ws_layout(const pkv_config& c, int num_seqs, int num_tokens, int
   const int group = c.num_q_heads / c.num_kv_heads;
   const bool prefill = prefill_supported(c.head_dim, group);
   w.prefill_min_qlen = prefill ? kPrefillMinQlen : 0;
-  w.prefill_pos = prefill_positions(group);
+  w.prefill_pos = prefill_item_positions(group);
   w.max_items = prefill ? (int64_t)c.num_kv_heads * ((num_tokens + w.prefill_pos - 1) / w.prefill_pos + num_seqs) : 0;
   size_t off = 0;
   w.hdr = off;

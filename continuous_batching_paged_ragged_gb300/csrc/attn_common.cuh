@@ -16,11 +16,11 @@ constexpr int kHeadsTile = 8;    // query heads per KV head handled by one decod
 // rows (decode, short chunks) to the split-K decode kernel.  The choice depends on the row alone, so a
 // row's result does not depend on the rest of the batch.
 constexpr int kPrefillMinQlen = 16;
-constexpr int kPrefillRows = 128;  // MMA rows of a prefill tile: (query position, query head) pairs
-constexpr int kPrefillKeys = 128;  // keys per K/V tile
+constexpr int kPrefillRows = 128;  // MMA rows of a prefill Q tile: (query position, query head) pairs
+constexpr int kPrefillKeys = 64;   // keys per K/V tile
 constexpr int kPrefillBuckets = 1024;
 
-// Query positions per prefill item: the G query heads of a KV head are packed into the MMA rows.
+// Query positions per prefill Q tile: the G query heads of a KV head are packed into the MMA rows.
 __host__ __device__ constexpr int prefill_positions(int group) { return kPrefillRows / group; }
 
 struct WsHeader {
@@ -34,7 +34,7 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
-// A prefill item: one KV head, up to prefill_positions(G) consecutive query positions of one row.
+// A prefill item: one KV head, up to prefill_item_positions(G) consecutive query positions of one row.
 //   x: row (block-table row)          y: KV head | (positions << 16)
 //   z: first query token (packed)     w: keys visible to the item's first position, minus one
 // Position i of the item attends causally to keys 0 .. w + i.
@@ -57,5 +57,7 @@ struct PrefillArgs {
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 // Whether the tile kernel serves this head shape (otherwise every row takes the decode path).
 bool prefill_supported(int head_dim, int group);
+// Query positions per prefill item (the Q tiles of one item share their K/V tiles).
+int prefill_item_positions(int group);
 
 }  // namespace pkv

@@ -7,17 +7,20 @@
 // head h reading KV head h / G, scores scaled by 1/sqrt(d), fp32 softmax, fp16 output.
 //
 // How (GB300 design):
-//  * Work item = one KV head and P = 128 / G consecutive query positions of one row.  Its G query heads
-//    are packed into the 128 MMA rows (row r = position r / G, head r % G), so every K/V tile is read
-//    once for all heads of the group and the causal diagonal wastes at most P keys per tile.
-//  * Persistent CTAs of 5 warps.  Warp 4 (control) streams K/V tiles of 128 keys from the paged pool
-//    with 2-D TMA copies (128-byte swizzle) into a 2-stage ring and issues, from one thread, the MMAs
-//    S = Q K^T (M 128, N 128, K d) and O += P V (M 128, N d, K 128) with fp32 accumulators in tensor
-//    memory.  Warps 0-3 (softmax) own one S row each (TMEM lane = thread): they load S with tcgen05.ld,
-//    apply the causal mask and an online softmax in the log2 domain, and write P as fp16 into a swizzled
-//    shared-memory tile that the next MMA reads.  The running max is lazy: O (in TMEM) and the running
-//    sum are rescaled only when a row's max grows by more than 8 (a factor 256), which keeps P <= 256
-//    and the arithmetic exact up to rounding.
+//  * A Q tile is 128 MMA rows = P = 128 / G consecutive query positions x the G query heads of one KV
+//    head (row r = position r / G, head r % G): every K/V tile is read once for the whole group, and
+//    the causal diagonal wastes at most P keys per tile.  A work item is two adjacent Q tiles of one row
+//    and KV head; they share every K/V tile.
+//  * Persistent CTAs of 10 warps.  Warp 9 streams 64-key K/V tiles from the paged pool with 2-D TMA
+//    copies (128-byte swizzle) into a 3-stage ring, block ids fetched a tile ahead.  Warp 8 issues, from
+//    one thread, the MMAs S = Q K^T (M 128, N 64, K d) and O += P V (M 128, N d, K 64) of both Q tiles,
+//    fp32 accumulators in tensor memory (per Q tile: two S buffers and O; 512 columns in all).  Warpgroups 0 and 1 (softmax)
+//    each own one Q tile, one S/O row per thread (TMEM lane = thread): they load S with tcgen05.ld,
+//    apply the causal mask and an online softmax in the log2 domain, and write P as fp16 into one of two
+//    swizzled shared-memory operand tiles.  With S and P double-buffered the tensor core computes the
+//    next tile's scores and the other group's products while a group runs its softmax.
+//  * The running max is lazy: O (in TMEM) and the running sum are rescaled only when a row's max grows
+//    by more than 8 (a factor 256), which keeps P <= 256 and the arithmetic exact up to rounding.
 //  * Items are taken longest first (the plan sorts them by K/V tile count) from a global counter.
 #include <cuda_fp16.h>
 
@@ -29,27 +32,34 @@ namespace pkv {
 
 namespace {
 
-constexpr int kStages = 2;
-constexpr int kThreads = 160;          // 4 softmax warps + 1 control warp
-constexpr int kBarItem = 1, kBarQ = 2, kBarP = 3;  // named barriers (0 is __syncthreads)
+constexpr int kStages = 3;             // K/V ring depth
+constexpr int kWG = 2;                 // softmax warpgroups = Q tiles per item
+constexpr int kMmaWarp = 4 * kWG;      // issues the MMAs and hands out items
+constexpr int kTmaWarp = 4 * kWG + 1;  // streams K/V tiles
+constexpr int kThreads = (4 * kWG + 2) * 32;
+constexpr int kBarItem = 1, kBarQ = 2; // named barriers (0 is __syncthreads)
+constexpr int kBarQThreads = (4 * kWG + 1) * 32;  // softmax groups + the MMA warp
 constexpr float kRescaleLog2 = 8.f;    // lazy rescale threshold (log2 units)
+constexpr int kKeys = kPrefillKeys;    // keys per K/V tile
+static_assert(kKeys == 64, "one 128-byte swizzle atom of P per row");
 
 template <int D, int G>
 struct PfTraits {
-  static constexpr int DH = D / 64;                 // 64-wide column halves of a row (128-byte swizzle atoms)
-  static constexpr int P = prefill_positions(G);    // query positions per item
-  static constexpr int TILE = DH * 128 * 128;       // bytes of a 128-row x D fp16 tile (Q, K or V)
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + TILE;       // stage s: K at OFF_KV + 2 s TILE, V after it
-  static constexpr int OFF_P = OFF_KV + kStages * 2 * TILE;  // P: 128 rows x 128 keys fp16 (32 KB)
-  static constexpr int OFF_BAR = OFF_P + 2 * 128 * 128;      // kfull[2], vfull[2], s_done, pv_done
-  static constexpr int OFF_MISC = OFF_BAR + 64;              // TMEM base, item record, abort flag
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;          // + slack to align to 1024 bytes
-  static constexpr uint32_t TMEM_COLS = 256;                 // S: columns 0..127, O: 128..128+D-1
-  static constexpr uint32_t IDESC_S = dev::umma_idesc_f16(128, 128, false, false);
+  static constexpr int DH = D / 64;                   // 64-column halves of a row (128-byte swizzle atoms)
+  static constexpr int P = prefill_positions(G);      // query positions per Q tile
+  static constexpr int QTILE = DH * 128 * 128;        // 128 rows x D fp16
+  static constexpr int KVTILE = DH * kKeys * 128;     // 64 keys x D fp16
+  static constexpr int PTILE = 128 * kKeys * 2;       // 128 rows x 64 keys fp16
+  static constexpr int OFF_Q = 0;                                  // [kWG]
+  static constexpr int OFF_KV = OFF_Q + kWG * QTILE;               // [kStages] {K, V}
+  static constexpr int OFF_P = OFF_KV + kStages * 2 * KVTILE;      // [kWG][2]
+  static constexpr int OFF_BAR = OFF_P + kWG * 2 * PTILE;          // mbarriers
+  static constexpr int OFF_MISC = OFF_BAR + 256;                   // TMEM base, item record, abort flag
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;                // + slack to align to 1024 bytes
+  static constexpr uint32_t TMEM_COLS = 512;  // group w: S buffers at 256 w + {0, 64}, O at 256 w + 128
+  static constexpr uint32_t IDESC_S = dev::umma_idesc_f16(128, kKeys, false, false);
   static constexpr uint32_t IDESC_PV = dev::umma_idesc_f16(128, D, false, true);
   static_assert(D == 64 || D == 128, "head_dim");
-  static_assert(128 + D <= (int)TMEM_COLS, "TMEM columns");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -66,19 +76,22 @@ struct PfParams {
   float scale_log2;
 };
 
-struct Shared {
-  uint64_t* kfull;
-  uint64_t* vfull;
-  uint64_t* s_done;
-  uint64_t* pv_done;
+struct Bars {
+  uint64_t* kfull;    // [kStages]  K tile landed (TMA bytes)
+  uint64_t* vfull;    // [kStages]  V tile landed
+  uint64_t* kfree;    // [kStages]  the scores that read the stage's K tile have completed (tcgen05.commit)
+  uint64_t* vfree;    // [kStages]  the products that read the stage's V tile have completed
+  uint64_t* s_done;   // [kWG][2]   S buffer written (tcgen05.commit)
+  uint64_t* p_ready;  // [kWG][2]   P buffer written, O rescaled (128 arrivals)
+  uint64_t* pv_done;  // [kWG][2]   O += P V of that P buffer completed (tcgen05.commit)
   uint32_t* tmem_base;
   int4* item;
   volatile int* abort;
 };
 
 // Bounded wait that, once any wait of the CTA has given up, no longer waits at all: every thread then
-// runs through the remaining (bounded) loop with garbage and the CTA stays in step at its barriers.
-__device__ __forceinline__ void pf_wait(const Shared& sh, uint64_t* bar, uint32_t parity, int32_t* err) {
+// runs through the remaining (bounded) loops with garbage and the CTA stays in step at its barriers.
+__device__ __forceinline__ void pf_wait(const Bars& sh, uint64_t* bar, uint32_t parity, int32_t* err) {
   if (*sh.abort) return;
   if (!dev::mbar_wait(bar, parity)) {
     *sh.abort = 1;
@@ -86,20 +99,113 @@ __device__ __forceinline__ void pf_wait(const Shared& sh, uint64_t* bar, uint32_
   }
 }
 
-// Byte offset of 16-byte chunk c (8 fp16) of row r in a 128-row tile stored as 64-column halves with the
-// 128-byte swizzle.
-__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+// Byte offset of 16-byte chunk c (8 fp16) of row r in a 128-row tile stored as 64-column halves of
+// 16 KB with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t qtile_off(int r, int c) {
   return (uint32_t)((c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// ---- control warp: TMA producer and MMA issuer ----------------------------------------------------
+// The item's geometry as seen by Q tile w.
+struct ItemGeo {
+  int row, g, t0, w0;   // row, KV head, first token, keys visible to the first position minus one
+  int npos[kWG];        // positions of each Q tile (0: the tile is empty)
+  int n[kWG];           // K/V tiles each Q tile needs
+  int n_all;            // K/V tiles of the item
+  int kend_all;         // keys of the item
+  int zfill_wg;         // the group that zeroes V rows past the item's keys in the last tile
+};
+
+template <int P>
+__device__ __forceinline__ ItemGeo item_geo(const int4 rec) {
+  ItemGeo it;
+  it.row = rec.x;
+  it.g = rec.y & 0xFFFF;
+  const int npos = rec.y >> 16;
+  it.t0 = rec.z;
+  it.w0 = rec.w;
+  it.n_all = 0;
+  it.kend_all = 0;
+  it.zfill_wg = 0;
+#pragma unroll
+  for (int w = 0; w < kWG; ++w) {
+    it.npos[w] = max(0, min(P, npos - w * P));
+    const int kend = it.w0 + w * P + it.npos[w];
+    it.n[w] = it.npos[w] > 0 ? (kend + kKeys - 1) / kKeys : 0;
+    if (it.npos[w] > 0) {
+      it.n_all = it.n[w];
+      it.kend_all = kend;
+      it.zfill_wg = w;
+    }
+  }
+  return it;
+}
+
+// ---- TMA warp: K/V tiles of the item into the ring, block ids fetched one tile ahead ----------------
 template <int D, int G>
-__device__ void control_warp(const PfParams& p, unsigned char* smem, const Shared& sh, int lane, int n_items) {
+__device__ void tma_warp(const PfParams& p, unsigned char* smem, const Bars& sh, int lane) {
+  using T = PfTraits<D, G>;
+  constexpr int BPT = kKeys / kBS;  // blocks per K/V tile
+  const uint64_t pol = dev::l2_policy_evict_last();
+  int gt = 0;  // CTA-wide index of the next K/V tile: stage gt % kStages
+  while (true) {
+    dev::named_bar_sync(kBarItem, kThreads);
+    const volatile int* vi = reinterpret_cast<volatile int*>(sh.item);
+    const int4 rec = make_int4(vi[0], vi[1], vi[2], vi[3]);
+    if (rec.x < 0) break;
+    const ItemGeo it = item_geo<T::P>(rec);
+    const int n = it.n_all;
+    const int nblk = (it.kend_all + kBS - 1) / kBS;
+    const int32_t* bt = p.block_tables + (int64_t)it.row * p.max_blocks;
+    auto load_ids = [&](int j) {  // lane i < blocks of tile j: physical id of the tile's block i
+      int id = 0;
+      if (lane < min(BPT, nblk - j * BPT)) {
+        id = __ldg(bt + j * BPT + lane);
+        if (id < 0 || id >= p.num_blocks) {
+          dev::set_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+          id = 0;
+        }
+      }
+      return id;
+    };
+    // TMA of tile j's K (v = false) or V (v = true) into stage (gt + j) % kStages, once the MMAs that read
+    // the tile kStages earlier from that stage have completed.  One 2 KB box (16 keys x 64 columns) per
+    // lane: a single issuing thread would be the bottleneck.
+    auto issue = [&](int j, bool v, int id) {
+      const int gi = gt + j, stage = gi % kStages;
+      if (gi >= kStages) pf_wait(sh, v ? &sh.vfree[stage] : &sh.kfree[stage], ((gi - kStages) / kStages) & 1, p.err);
+      const int nb = min(BPT, nblk - j * BPT);
+      unsigned char* dst = smem + T::OFF_KV + stage * 2 * T::KVTILE + (v ? T::KVTILE : 0);
+      uint64_t* full = v ? &sh.vfull[stage] : &sh.kfull[stage];
+      const int row0 = v ? p.layer_row0_v : p.layer_row0_k;
+      if (lane == 0) dev::mbar_arrive_expect_tx(full, (uint32_t)(nb * T::DH * 2048));
+      __syncwarp();
+      const int blk = lane / T::DH, h = lane % T::DH;
+      const int bid = __shfl_sync(0xffffffffu, id, blk & 31);
+      if (lane < nb * T::DH)
+        dev::tma_load_2d(dst + h * (kKeys * 128) + blk * 2048, &p.kv_map, h * 64,
+                         row0 + (bid * p.num_kv_heads + it.g) * kBS, full, pol);
+    };
+    // K runs one tile ahead of V: a K stage is released by the scores, earlier than a V stage by the products
+    int id_next = n > 0 ? load_ids(0) : 0, id_prev = 0;
+    for (int t = 0; t <= n; ++t) {
+      const int id_cur = id_next;
+      if (t + 1 < n) id_next = load_ids(t + 1);
+      if (t < n) issue(t, false, id_cur);
+      if (t >= 1) issue(t - 1, true, id_prev);
+      id_prev = id_cur;
+    }
+    gt += n;
+  }
+}
+
+// ---- MMA warp: hands out items, issues every MMA from one thread ----------------------------------
+template <int D, int G>
+__device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh, int lane, int n_items) {
   using T = PfTraits<D, G>;
   const uint32_t sbase = dev::smem_addr(smem);
-  const uint32_t tS = *sh.tmem_base, tO = tS + 128;
-  const uint64_t pol = dev::l2_policy_evict_last();
-  int gidx = 0;  // CTA-wide index of the next K/V tile (ring stage gidx % 2, barrier phases)
+  const uint32_t tmem = *sh.tmem_base;
+  int gt = 0;             // CTA-wide index of the next K/V tile: stage gt % kStages
+  int cw[kWG] = {0, 0};   // per Q-tile group: tiles processed so far (S/P/PV buffer cw % 2)
   bool first = true;
   while (true) {
     int4 rec = make_int4(-1, 0, 0, 0);
@@ -111,253 +217,258 @@ __device__ void control_warp(const PfParams& p, unsigned char* smem, const Share
     first = false;
     rec.x = __shfl_sync(0xffffffffu, rec.x, 0);
     rec.y = __shfl_sync(0xffffffffu, rec.y, 0);
+    rec.z = __shfl_sync(0xffffffffu, rec.z, 0);
     rec.w = __shfl_sync(0xffffffffu, rec.w, 0);
     __syncwarp();
     dev::named_bar_arrive(kBarItem, kThreads);
     if (rec.x < 0) break;
-    const int row = rec.x, g = rec.y & 0xFFFF, npos = rec.y >> 16;
-    const int kend = rec.w + npos;                    // keys the item's last position sees
-    const int n = (kend + kPrefillKeys - 1) / kPrefillKeys;
-    const int nblk = (kend + kBS - 1) / kBS;
-    const int32_t* bt = p.block_tables + (int64_t)row * p.max_blocks;
+    const ItemGeo it = item_geo<T::P>(rec);
+    const int n = it.n_all;
 
-    auto issue_tile = [&](int j, int gi) {
-      const int stage = gi % kStages;
-      const int nb = min(8, nblk - j * 8);
-      int id = 0;
-      if (lane < nb) {
-        id = __ldg(bt + j * 8 + lane);
-        if (id < 0 || id >= p.num_blocks) {
-          dev::set_error(p.err, PKV_DEVERR_BLOCK_RANGE);
-          id = 0;
-        }
-      }
-      unsigned char* sk = smem + T::OFF_KV + stage * 2 * T::TILE;
-      unsigned char* sv = sk + T::TILE;
-      if (lane == 0) {
-        dev::mbar_arrive_expect_tx(&sh.kfull[stage], (uint32_t)(nb * T::DH * 2048));
-        dev::mbar_arrive_expect_tx(&sh.vfull[stage], (uint32_t)(nb * T::DH * 2048));
-      }
-      for (int i = 0; i < nb; ++i) {
-        const int bid = __shfl_sync(0xffffffffu, id, i);
-        if (lane == 0) {
-          const int rk = p.layer_row0_k + (bid * p.num_kv_heads + g) * kBS;
-          const int rv = p.layer_row0_v + (bid * p.num_kv_heads + g) * kBS;
-#pragma unroll
-          for (int h = 0; h < T::DH; ++h) {
-            dev::tma_load_2d(sk + h * 16384 + i * 2048, &p.kv_map, h * 64, rk, &sh.kfull[stage], pol);
-            dev::tma_load_2d(sv + h * 16384 + i * 2048, &p.kv_map, h * 64, rv, &sh.vfull[stage], pol);
-          }
-        }
-      }
-    };
-    auto issue_s = [&](int gi) {  // S = Q K^T into TMEM columns 0..127
-      const int stage = gi % kStages;
-      const uint32_t sq = sbase + T::OFF_Q, sk = sbase + T::OFF_KV + stage * 2 * T::TILE;
+    auto issue_s = [&](int w, int j) {  // S_w(j) = Q_w K(j)^T into group w's S buffer (cw + j) % 2
+      const int stage = (gt + j) % kStages, b = (cw[w] + j) & 1;
+      const uint32_t sq = sbase + T::OFF_Q + w * T::QTILE, sk = sbase + T::OFF_KV + stage * 2 * T::KVTILE;
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          dev::umma_f16_ss(tS, dev::umma_desc_sw128(sq + off, 16, 1024), dev::umma_desc_sw128(sk + off, 16, 1024),
+          dev::umma_f16_ss(tmem + 256 * w + 64 * b,
+                           dev::umma_desc_sw128(sq + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                           dev::umma_desc_sw128(sk + (kk >> 2) * (kKeys * 128) + (kk & 3) * 32, 16, 1024),
                            T::IDESC_S, kk > 0);
         }
-        dev::umma_commit(sh.s_done);
+        dev::umma_commit(&sh.s_done[2 * w + b]);
       }
       __syncwarp();
     };
-    auto issue_pv = [&](int gi, bool acc) {  // O (+)= P V into TMEM columns 128..128+D-1
-      const int stage = gi % kStages;
-      const uint32_t sp = sbase + T::OFF_P, sv = sbase + T::OFF_KV + stage * 2 * T::TILE + T::TILE;
+    auto issue_pv = [&](int w, int j) {  // O_w (+)= P_w(j) V(j)
+      const int stage = (gt + j) % kStages, b = (cw[w] + j) & 1;
+      const uint32_t sp = sbase + T::OFF_P + (2 * w + b) * T::PTILE;
+      const uint32_t sv = sbase + T::OFF_KV + stage * 2 * T::KVTILE + T::KVTILE;
       if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < kPrefillKeys / 16; ++kk) {
-          const uint32_t offp = (kk >> 2) * 16384 + (kk & 3) * 32;
-          dev::umma_f16_ss(tO, dev::umma_desc_sw128(sp + offp, 16, 1024),
-                           dev::umma_desc_sw128(sv + kk * 2048, 16384, 1024), T::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          dev::umma_f16_ss(tmem + 256 * w + 128, dev::umma_desc_sw128(sp + kk * 32, 16, 1024),
+                           dev::umma_desc_sw128(sv + kk * 2048, kKeys * 128, 1024), T::IDESC_PV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
         }
-        dev::umma_commit(sh.pv_done);
+        dev::umma_commit(&sh.pv_done[2 * w + b]);
       }
       __syncwarp();
     };
 
-    // the ring's stages are free once the previous item's last P V has completed
-    if (gidx > 0) pf_wait(sh, sh.pv_done, (gidx - 1) & 1, p.err);
-    issue_tile(0, gidx);
-    if (n > 1) issue_tile(1, gidx + 1);
-    dev::named_bar_sync(kBarQ, kThreads);  // Q is in shared memory
+    dev::named_bar_sync(kBarQ, kBarQThreads);  // both Q tiles are in shared memory
     dev::tc_fence_after();
-    pf_wait(sh, &sh.kfull[gidx % kStages], (gidx / kStages) & 1, p.err);
-    issue_s(gidx);
+    pf_wait(sh, &sh.kfull[gt % kStages], (gt / kStages) & 1, p.err);
+#pragma unroll
+    for (int w = 0; w < kWG; ++w)
+      if (it.n[w] > 0) issue_s(w, 0);
+    if (lane == 0) dev::umma_commit(&sh.kfree[gt % kStages]);
+    __syncwarp();
     for (int j = 0; j < n; ++j) {
-      const int gi = gidx + j;
-      dev::named_bar_sync(kBarP, kThreads);  // P(j) written, O rescaled, S(j) read
-      dev::tc_fence_after();
-      pf_wait(sh, &sh.vfull[gi % kStages], (gi / kStages) & 1, p.err);
-      issue_pv(gi, j > 0);
+      const int gi = gt + j;
+      // the next tile's scores, into the other S buffers, while the groups run this tile's softmax
       if (j + 1 < n) {
         pf_wait(sh, &sh.kfull[(gi + 1) % kStages], ((gi + 1) / kStages) & 1, p.err);
-        issue_s(gi + 1);
+#pragma unroll
+        for (int w = 0; w < kWG; ++w)
+          if (j + 1 < it.n[w]) issue_s(w, j + 1);
+        if (lane == 0) dev::umma_commit(&sh.kfree[(gi + 1) % kStages]);
+        __syncwarp();
       }
-      if (j + 2 < n) {  // tile j's stage is free once P(j) V(j) has completed
-        pf_wait(sh, sh.pv_done, gi & 1, p.err);
-        issue_tile(j + 2, gi + 2);
+      // this tile's products; the last tile's V rows are zero-filled by one group: wait for all
+      const bool last = j == n - 1;
+      pf_wait(sh, &sh.vfull[gi % kStages], (gi / kStages) & 1, p.err);
+#pragma unroll
+      for (int w = 0; w < kWG; ++w) {
+        if (j >= it.n[w]) continue;
+        const int c = cw[w] + j;
+        pf_wait(sh, &sh.p_ready[2 * w + (c & 1)], (c >> 1) & 1, p.err);
+        if (!last) {
+          dev::tc_fence_after();
+          issue_pv(w, j);
+        }
       }
+      if (last) {
+        dev::tc_fence_after();
+#pragma unroll
+        for (int w = 0; w < kWG; ++w)
+          if (j < it.n[w]) issue_pv(w, j);
+      }
+      if (lane == 0) dev::umma_commit(&sh.vfree[gi % kStages]);
+      __syncwarp();
     }
-    gidx += n;
+    gt += n;
+#pragma unroll
+    for (int w = 0; w < kWG; ++w) cw[w] += it.n[w];
   }
-  // leave no copy in flight: every issued tile was consumed by an MMA the softmax warps waited for
 }
 
-// ---- softmax warps: one S / O row per thread ------------------------------------------------------
+// ---- softmax warpgroups: one S / O row per thread ---------------------------------------------------
 template <int D, int G>
-__device__ void softmax_warps(const PfParams& p, unsigned char* smem, const Shared& sh, int warp, int lane) {
+__device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars& sh, int wg, int warp, int lane) {
   using T = PfTraits<D, G>;
-  const int r = warp * 32 + lane;  // this thread's tile row and TMEM lane
-  const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-  const uint32_t tS = *sh.tmem_base + lane_addr, tO = tS + 128;
-  unsigned char* sQ = smem + T::OFF_Q;
-  unsigned char* sP = smem + T::OFF_P;
-  const uint32_t sQa = dev::smem_addr(sQ), sPa = dev::smem_addr(sP);
-  int gidx = 0;
+  const int r = (warp & 3) * 32 + lane;  // this thread's tile row and TMEM lane
+  const uint32_t tl = *sh.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + 256 * wg;  // lane, group columns
+  const uint32_t sQa = dev::smem_addr(smem + T::OFF_Q + wg * T::QTILE);
+  const uint32_t sPa = dev::smem_addr(smem + T::OFF_P + 2 * wg * T::PTILE);
+  int cw = 0;  // tiles processed by this group so far
+  int gt = 0;  // K/V tiles of the CTA so far (ring stage / phase of the zero-fill wait)
   while (true) {
     dev::named_bar_sync(kBarItem, kThreads);
     const volatile int* vi = reinterpret_cast<volatile int*>(sh.item);
     const int4 rec = make_int4(vi[0], vi[1], vi[2], vi[3]);
     if (rec.x < 0) break;
-    const int g = rec.y & 0xFFFF, npos = rec.y >> 16, t0 = rec.z, w = rec.w;
-    const int kend = w + npos;
-    const int n = (kend + kPrefillKeys - 1) / kPrefillKeys;
+    const ItemGeo it = item_geo<T::P>(rec);
+    const int n = wg ? it.n[1] : it.n[0];
     const int pos = r / G, hq = r % G;
+    const int npos = wg ? it.npos[1] : it.npos[0];
     const bool valid = r < T::P * G && pos < npos;
-    const int lim = valid ? w + pos : 0;  // last key this row sees (a padding row sees key 0 only)
+    const int first_pos = wg * T::P;
+    const int lim = valid ? it.w0 + first_pos + pos : 0;  // last key this row sees (padding rows: key 0)
+    const size_t tok = (size_t)(it.t0 + first_pos + pos);
 
     // ---- Q tile: row r = (position, head), 128-byte swizzle ----
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(t0 + pos) * p.num_q_heads + (size_t)g * G + hq) * D);
+    if (n > 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (tok * p.num_q_heads + (size_t)it.g * G + hq) * D);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sQa + tile_off(r, c)), "r"(v.x), "r"(v.y),
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sQa + qtile_off(r, c)), "r"(v.x), "r"(v.y),
                      "r"(v.z), "r"(v.w)
                      : "memory");
       }
       dev::fence_proxy_async_smem();
-      dev::named_bar_arrive(kBarQ, kThreads);
     }
+    dev::named_bar_arrive(kBarQ, kBarQThreads);
 
     float m_ref = -INFINITY, l = 0.f;
     for (int j = 0; j < n; ++j) {
-      const int gi = gidx + j;
-      pf_wait(sh, sh.s_done, gi & 1, p.err);
+      const int c = cw + j, b = c & 1;
+      pf_wait(sh, &sh.s_done[2 * wg + b], (c >> 1) & 1, p.err);
       dev::tc_fence_after();
-      uint32_t s[4][32];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) dev::tmem_ld32(tS + 32 * k, s[k]);
+      uint32_t s[2][32];
+      dev::tmem_ld32(tl + 64 * b, s[0]);
+      dev::tmem_ld32(tl + 64 * b + 32, s[1]);
       dev::tmem_wait_ld();
-      // ---- scale to the log2 domain, causal mask, row max ----
-      const int kb = j * kPrefillKeys;
-      const bool full = kb + kPrefillKeys - 1 <= lim;
-      float mx = -INFINITY;
+      // ---- causal mask, row max of the raw scores (four independent chains; the scale is positive) ----
+      const int kb = j * kKeys;
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (kb + kKeys - 1 <= lim) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 2; ++k)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float x = __uint_as_float(s[k][c]) * p.scale_log2;
-          if (!full && kb + 32 * k + c > lim) x = -INFINITY;
-          s[k][c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          for (int e = 0; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(s[k][e]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float x = __uint_as_float(s[k][e]);
+            if (kb + 32 * k + e > lim) x = -INFINITY;
+            s[k][e] = __float_as_uint(x);
+            mx4[e & 3] = fmaxf(mx4[e & 3], x);
+          }
         }
       }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
       // ---- lazy rescale of the running state ----
-      float alpha = 1.f;
       if (j == 0) {
         m_ref = mx;
       } else {
-        pf_wait(sh, sh.pv_done, (gi - 1) & 1, p.err);  // P(j-1) V(j-1) done: P tile free, O settled
-        dev::tc_fence_after();
         const bool need = mx > m_ref + kRescaleLog2;
-        if (need) alpha = exp2f(m_ref - mx);
         if (__any_sync(0xffffffffu, need)) {
+          const int cp = c - 1;  // O += P V of the previous tile must have landed before O is rescaled
+          pf_wait(sh, &sh.pv_done[2 * wg + (cp & 1)], (cp >> 1) & 1, p.err);
+          dev::tc_fence_after();
+          const float alpha = need ? exp2f(m_ref - mx) : 1.f;
 #pragma unroll
           for (int k = 0; k < D / 32; ++k) {
             uint32_t o[32];
-            dev::tmem_ld32(tO + 32 * k, o);
+            dev::tmem_ld32(tl + 128 + 32 * k, o);
             dev::tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            dev::tmem_st32(tO + 32 * k, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            dev::tmem_st32(tl + 128 + 32 * k, o);
           }
           dev::tmem_wait_st();
-        }
-        if (need) {
-          l *= alpha;
-          m_ref = mx;
+          if (need) {
+            l *= alpha;
+            m_ref = mx;
+          }
         }
       }
-      // ---- P = exp2(s - m_ref) as fp16 into the swizzled P tile (row r, keys contiguous) ----
-      float sum = 0.f;
+      // ---- P buffer b is free once the product that read it two tiles ago has completed ----
+      if (j >= 2) pf_wait(sh, &sh.pv_done[2 * wg + b], ((c - 2) >> 1) & 1, p.err);
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t pbuf = sPa + b * T::PTILE;
+      const float nm = -m_ref;  // p = 2^(s * scale_log2 - m_ref): one FFMA and one MUFU per score
 #pragma unroll
-      for (int c8 = 0; c8 < kPrefillKeys / 8; ++c8) {
+      for (int c8 = 0; c8 < kKeys / 8; ++c8) {
         uint32_t h2[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int c = c8 * 8 + 2 * e;
-          const float p0 = exp2f(__uint_as_float(s[c >> 5][c & 31]) - m_ref);
-          const float p1 = exp2f(__uint_as_float(s[(c + 1) >> 5][(c + 1) & 31]) - m_ref);
-          sum += p0 + p1;
+          const int k = c8 * 8 + 2 * e;
+          const float p0 = dev::ex2_approx(fmaf(__uint_as_float(s[k >> 5][k & 31]), p.scale_log2, nm));
+          const float p1 = dev::ex2_approx(fmaf(__uint_as_float(s[(k + 1) >> 5][(k + 1) & 31]), p.scale_log2, nm));
+          sum4[e] += p0 + p1;
           const __half2 hh = __floats2half2_rn(p0, p1);
           h2[e] = *reinterpret_cast<const uint32_t*>(&hh);
         }
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sPa + tile_off(r, c8)), "r"(h2[0]), "r"(h2[1]),
-                     "r"(h2[2]), "r"(h2[3])
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(pbuf + r * 128 + (((c8 ^ (r & 7))) << 4)),
+                     "r"(h2[0]), "r"(h2[1]), "r"(h2[2]), "r"(h2[3])
                      : "memory");
       }
-      l += sum;
-      // ---- last tile: V rows past the item's keys hold stale bytes; zero them (0 * NaN would poison O) ----
-      const int kl = kend - kb;
-      if (j == n - 1 && kl < kPrefillKeys) {
-        const int stage = gi % kStages;
-        pf_wait(sh, &sh.vfull[stage], (gi / kStages) & 1, p.err);
-        const uint32_t sv = dev::smem_addr(smem + T::OFF_KV + stage * 2 * T::TILE + T::TILE);
-        for (int idx = r; idx < (kPrefillKeys - kl) * T::DH * 8; idx += 128) {
-          const int kr = kl + idx / (T::DH * 8), rest = idx % (T::DH * 8);
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sv + (rest >> 3) * 16384 + kr * 128 +
-                                                                          (rest & 7) * 16),
-                       "r"(0)
-                       : "memory");
+      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      // ---- the item's last tile: V rows past its keys hold stale bytes; zero them (0 * NaN = NaN) ----
+      if (wg == it.zfill_wg && j == n - 1) {
+        const int kl = it.kend_all - kb;
+        if (kl < kKeys) {
+          const int gi = gt + j, stage = gi % kStages;
+          pf_wait(sh, &sh.vfull[stage], (gi / kStages) & 1, p.err);
+          const uint32_t sv = dev::smem_addr(smem + T::OFF_KV + stage * 2 * T::KVTILE + T::KVTILE);
+          for (int idx = r; idx < (kKeys - kl) * T::DH * 8; idx += 128) {
+            const int kr = kl + idx / (T::DH * 8), rest = idx % (T::DH * 8);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sv + (rest >> 3) * (kKeys * 128) + kr * 128 +
+                                                                            (rest & 7) * 16),
+                         "r"(0)
+                         : "memory");
+          }
         }
       }
       dev::fence_proxy_async_smem();
       dev::tc_fence_before();
-      dev::named_bar_arrive(kBarP, kThreads);
+      dev::mbar_arrive(&sh.p_ready[2 * wg + b]);
     }
     // ---- epilogue: O / l -> fp16 ----
-    const int gl = gidx + n - 1;
-    pf_wait(sh, sh.pv_done, gl & 1, p.err);
-    dev::tc_fence_after();
-    const float il = 1.f / l;
-    __half* dst = p.out + ((size_t)(t0 + pos) * p.num_q_heads + (size_t)g * G + hq) * D;
+    if (n > 0) {
+      const int cl = cw + n - 1;
+      pf_wait(sh, &sh.pv_done[2 * wg + (cl & 1)], (cl >> 1) & 1, p.err);
+      dev::tc_fence_after();
+      const float il = 1.f / l;
+      __half* dst = p.out + (tok * p.num_q_heads + (size_t)it.g * G + hq) * D;
 #pragma unroll
-    for (int k = 0; k < D / 32; ++k) {
-      uint32_t o[32];
-      dev::tmem_ld32(tO + 32 * k, o);
-      dev::tmem_wait_ld();
-      if (valid) {
+      for (int k = 0; k < D / 32; ++k) {
+        uint32_t o[32];
+        dev::tmem_ld32(tl + 128 + 32 * k, o);
+        dev::tmem_wait_ld();
+        if (valid) {
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint32_t h2[4];
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint32_t h2[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __half2 hh = __floats2half2_rn(__uint_as_float(o[c8 * 8 + 2 * e]) * il,
-                                                 __uint_as_float(o[c8 * 8 + 2 * e + 1]) * il);
-            h2[e] = *reinterpret_cast<const uint32_t*>(&hh);
+            for (int e = 0; e < 4; ++e) {
+              const __half2 hh = __floats2half2_rn(__uint_as_float(o[c8 * 8 + 2 * e]) * il,
+                                                   __uint_as_float(o[c8 * 8 + 2 * e + 1]) * il);
+              h2[e] = *reinterpret_cast<const uint32_t*>(&hh);
+            }
+            *reinterpret_cast<uint4*>(dst + 32 * k + 8 * c8) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
           }
-          *reinterpret_cast<uint4*>(dst + 32 * k + 8 * c8) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
         }
       }
+      dev::tc_fence_before();
     }
-    dev::tc_fence_before();
-    gidx += n;
+    cw += n;
+    gt += it.n_all;
   }
 }
 
@@ -367,18 +478,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Shared sh;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
+  Bars sh;
   sh.kfull = bars;
-  sh.vfull = bars + 2;
-  sh.s_done = bars + 4;
-  sh.pv_done = bars + 5;
+  sh.vfull = bars + kStages;
+  sh.kfree = bars + 2 * kStages;
+  sh.vfree = bars + 3 * kStages;
+  sh.s_done = bars + 4 * kStages;
+  sh.p_ready = sh.s_done + 2 * kWG;
+  sh.pv_done = sh.p_ready + 2 * kWG;
   sh.tmem_base = reinterpret_cast<uint32_t*>(smem + T::OFF_MISC);
   sh.item = reinterpret_cast<int4*>(smem + T::OFF_MISC + 16);
   sh.abort = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 32);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 6; ++i) dev::mbar_init(&bars[i], 1);
+    for (int i = 0; i < 4 * kStages; ++i) dev::mbar_init(&bars[i], 1);
+    for (int i = 0; i < 2 * kWG; ++i) {
+      dev::mbar_init(&sh.s_done[i], 1);
+      dev::mbar_init(&sh.p_ready[i], 128);
+      dev::mbar_init(&sh.pv_done[i], 1);
+    }
     dev::fence_mbar_init();
     *sh.abort = 0;
   }
@@ -392,8 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const bool poisoned = __syncthreads_or(threadIdx.x == 0 && dev::pool_poisoned(p.err));
   dev::tc_fence_after();
   const int n_items = poisoned ? 0 : p.hdr->n_items;
-  if (warp == 4) control_warp<D, G>(p, smem, sh, lane, n_items);
-  else softmax_warps<D, G>(p, smem, sh, warp, lane);
+  if (warp == kMmaWarp) mma_warp<D, G>(p, smem, sh, lane, n_items);
+  else if (warp == kTmaWarp) tma_warp<D, G>(p, smem, sh, lane);
+  else softmax_group<D, G>(p, smem, sh, warp >> 2, warp, lane);
   dev::tc_fence_before();
   __syncthreads();
   dev::tc_fence_after();
@@ -441,6 +561,8 @@ cudaError_t launch_d(int group, const PfParams& p, int num_sms, int64_t max_item
 bool prefill_supported(int head_dim, int group) {
   return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4 || group == 6 || group == 8);
 }
+
+int prefill_item_positions(int group) { return kWG * prefill_positions(group); }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   PfParams p;
