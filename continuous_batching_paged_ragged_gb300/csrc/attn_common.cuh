@@ -17,7 +17,7 @@ constexpr int kHeadsTile = 8;    // query heads per KV head handled by one decod
 // row's result does not depend on the rest of the batch.
 constexpr int kPrefillMinQlen = 16;
 constexpr int kPrefillRows = 128;  // MMA rows of a prefill Q tile: (query position, query head) pairs
-constexpr int kPrefillKeys = 64;   // keys per K/V tile
+constexpr int kPrefillKeys = 128;  // keys per K/V tile
 constexpr int kPrefillBuckets = 1024;
 
 // Query positions per prefill Q tile: the G query heads of a KV head are packed into the MMA rows.

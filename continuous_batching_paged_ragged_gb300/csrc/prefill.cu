@@ -10,15 +10,18 @@
 //  * A Q tile is 128 MMA rows = P = 128 / G consecutive query positions x the G query heads of one KV
 //    head (row r = position r / G, head r % G): every K/V tile is read once for the whole group, and
 //    the causal diagonal wastes at most P keys per tile.  A work item is two adjacent Q tiles of one row
-//    and KV head; they share every K/V tile.
-//  * Persistent CTAs of 10 warps.  Warp 9 streams 64-key K/V tiles from the paged pool with 2-D TMA
-//    copies (128-byte swizzle) into a 3-stage ring, block ids fetched a tile ahead.  Warp 8 issues, from
-//    one thread, the MMAs S = Q K^T (M 128, N 64, K d) and O += P V (M 128, N d, K 64) of both Q tiles,
-//    fp32 accumulators in tensor memory (per Q tile: two S buffers and O; 512 columns in all).  Warpgroups 0 and 1 (softmax)
-//    each own one Q tile, one S/O row per thread (TMEM lane = thread): they load S with tcgen05.ld,
-//    apply the causal mask and an online softmax in the log2 domain, and write P as fp16 into one of two
-//    swizzled shared-memory operand tiles.  With S and P double-buffered the tensor core computes the
-//    next tile's scores and the other group's products while a group runs its softmax.
+//    and KV head; they share every 128-key K/V tile.
+//  * Persistent CTAs of 10 warps.  Warp 9 streams K and V tiles from the paged pool with 2-D TMA copies
+//    (128-byte swizzle) into rings of 3 K and 2 V slots, block ids fetched a tile ahead.  Warp 8 issues,
+//    from one thread, the MMAs S = Q K^T (M 128, N 128, K d) and O += P V (M 128, N d, K 128) of both
+//    Q tiles, fp32 accumulators in tensor memory (per Q tile: S and O, 256 columns; 512 in all).
+//    Warpgroups 0 and 1 (softmax) each own one Q tile, one S/O row per thread (TMEM lane = thread):
+//    they load S with tcgen05.ld, apply the causal mask and an online softmax in the log2 domain, and
+//    store P as fp16 over the S they just read (tcgen05.st); the product takes P straight from tensor
+//    memory.  The MMA order S_0(j), S_1(j), P_0(j)V, S_0(j+1), P_1(j)V, S_1(j+1), ... keeps the tensor
+//    core on one group's products and scores while the other group runs its softmax.
+//  * Measured on GB300: one thread issues a tcgen05.mma about every 96 cycles whatever N up to 128, so
+//    128-wide score tiles (not 64) are what lets the tensor core, not the issue, set the pace.
 //  * The running max is lazy: O (in TMEM) and the running sum are rescaled only when a row's max grows
 //    by more than 8 (a factor 256), which keeps P <= 256 and the arithmetic exact up to rounding.
 //  * Items are taken longest first (the plan sorts them by K/V tile count) from a global counter.
@@ -32,7 +35,8 @@ namespace pkv {
 
 namespace {
 
-constexpr int kStages = 3;             // K/V ring depth
+constexpr int kKSlots = 3;             // K ring depth
+constexpr int kVSlots = 2;             // V ring depth
 constexpr int kWG = 2;                 // softmax warpgroups = Q tiles per item
 constexpr int kMmaWarp = 4 * kWG;      // issues the MMAs and hands out items
 constexpr int kTmaWarp = 4 * kWG + 1;  // streams K/V tiles
@@ -41,22 +45,22 @@ constexpr int kBarItem = 1, kBarQ = 2; // named barriers (0 is __syncthreads)
 constexpr int kBarQThreads = (4 * kWG + 1) * 32;  // softmax groups + the MMA warp
 constexpr float kRescaleLog2 = 8.f;    // lazy rescale threshold (log2 units)
 constexpr int kKeys = kPrefillKeys;    // keys per K/V tile
-static_assert(kKeys == 64, "one 128-byte swizzle atom of P per row");
+static_assert(kKeys == 128, "S of a tile fills 128 TMEM columns; its P (fp16) the first 64");
 
 template <int D, int G>
 struct PfTraits {
   static constexpr int DH = D / 64;                   // 64-column halves of a row (128-byte swizzle atoms)
   static constexpr int P = prefill_positions(G);      // query positions per Q tile
   static constexpr int QTILE = DH * 128 * 128;        // 128 rows x D fp16
-  static constexpr int KVTILE = DH * kKeys * 128;     // 64 keys x D fp16
-  static constexpr int PTILE = 128 * kKeys * 2;       // 128 rows x 64 keys fp16
-  static constexpr int OFF_Q = 0;                                  // [kWG]
-  static constexpr int OFF_KV = OFF_Q + kWG * QTILE;               // [kStages] {K, V}
-  static constexpr int OFF_P = OFF_KV + kStages * 2 * KVTILE;      // [kWG][2]
-  static constexpr int OFF_BAR = OFF_P + kWG * 2 * PTILE;          // mbarriers
-  static constexpr int OFF_MISC = OFF_BAR + 256;                   // TMEM base, item record, abort flag
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;                // + slack to align to 1024 bytes
-  static constexpr uint32_t TMEM_COLS = 512;  // group w: S buffers at 256 w + {0, 64}, O at 256 w + 128
+  static constexpr int KVTILE = DH * kKeys * 128;     // 128 keys x D fp16
+  static constexpr int OFF_Q = 0;                     // [kWG]
+  static constexpr int OFF_K = OFF_Q + kWG * QTILE;   // [kKSlots]
+  static constexpr int OFF_V = OFF_K + kKSlots * KVTILE;  // [kVSlots]
+  static constexpr int OFF_BAR = OFF_V + kVSlots * KVTILE;
+  static constexpr int OFF_MISC = OFF_BAR + 256;      // TMEM base, item record, abort flag
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;   // + slack to align to 1024 bytes
+  // group w: S at 256 w (128 columns; P, as fp16, overwrites its first 64), O at 256 w + 128
+  static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = dev::umma_idesc_f16(128, kKeys, false, false);
   static constexpr uint32_t IDESC_PV = dev::umma_idesc_f16(128, D, false, true);
   static_assert(D == 64 || D == 128, "head_dim");
@@ -77,13 +81,13 @@ struct PfParams {
 };
 
 struct Bars {
-  uint64_t* kfull;    // [kStages]  K tile landed (TMA bytes)
-  uint64_t* vfull;    // [kStages]  V tile landed
-  uint64_t* kfree;    // [kStages]  the scores that read the stage's K tile have completed (tcgen05.commit)
-  uint64_t* vfree;    // [kStages]  the products that read the stage's V tile have completed
-  uint64_t* s_done;   // [kWG][2]   S buffer written (tcgen05.commit)
-  uint64_t* p_ready;  // [kWG][2]   P buffer written, O rescaled (128 arrivals)
-  uint64_t* pv_done;  // [kWG][2]   O += P V of that P buffer completed (tcgen05.commit)
+  uint64_t* kfull;    // [kKSlots]  K tile landed (TMA bytes)
+  uint64_t* kfree;    // [kKSlots]  the scores that read the slot's K tile have completed (tcgen05.commit)
+  uint64_t* vfull;    // [kVSlots]  V tile landed
+  uint64_t* vfree;    // [kVSlots]  the products that read the slot's V tile have completed
+  uint64_t* s_done;   // [kWG]      S of the group's current tile written (and every earlier MMA done)
+  uint64_t* p_ready;  // [kWG]      P written over S, O rescaled (128 arrivals)
+  uint64_t* pv_done;  // [kWG]      the group's product of its current tile completed
   uint32_t* tmem_base;
   int4* item;
   volatile int* abort;
@@ -105,7 +109,7 @@ __device__ __forceinline__ uint32_t qtile_off(int r, int c) {
   return (uint32_t)((c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// The item's geometry as seen by Q tile w.
+// The item's geometry as seen by each of its Q tiles.
 struct ItemGeo {
   int row, g, t0, w0;   // row, KV head, first token, keys visible to the first position minus one
   int npos[kWG];        // positions of each Q tile (0: the tile is empty)
@@ -140,13 +144,14 @@ __device__ __forceinline__ ItemGeo item_geo(const int4 rec) {
   return it;
 }
 
-// ---- TMA warp: K/V tiles of the item into the ring, block ids fetched one tile ahead ----------------
+// ---- TMA warp: K/V tiles of the item into the rings, block ids fetched one tile ahead ---------------
 template <int D, int G>
 __device__ void tma_warp(const PfParams& p, unsigned char* smem, const Bars& sh, int lane) {
   using T = PfTraits<D, G>;
   constexpr int BPT = kKeys / kBS;  // blocks per K/V tile
+  static_assert(BPT * T::DH <= 32, "one box per lane");
   const uint64_t pol = dev::l2_policy_evict_last();
-  int gt = 0;  // CTA-wide index of the next K/V tile: stage gt % kStages
+  int gt = 0;  // CTA-wide index of the next K/V tile
   while (true) {
     dev::named_bar_sync(kBarItem, kThreads);
     const volatile int* vi = reinterpret_cast<volatile int*>(sh.item);
@@ -167,15 +172,17 @@ __device__ void tma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
       }
       return id;
     };
-    // TMA of tile j's K (v = false) or V (v = true) into stage (gt + j) % kStages, once the MMAs that read
-    // the tile kStages earlier from that stage have completed.  One 2 KB box (16 keys x 64 columns) per
-    // lane: a single issuing thread would be the bottleneck.
+    // TMA of tile j's K (v = false) or V (v = true) into its ring slot, once the MMAs that read the tile
+    // a ring-length earlier from that slot have completed.  One 2 KB box (16 keys x 64 columns) per lane:
+    // a single issuing thread would be the bottleneck.
     auto issue = [&](int j, bool v, int id) {
-      const int gi = gt + j, stage = gi % kStages;
-      if (gi >= kStages) pf_wait(sh, v ? &sh.vfree[stage] : &sh.kfree[stage], ((gi - kStages) / kStages) & 1, p.err);
+      const int gi = gt + j;
+      const int slots = v ? kVSlots : kKSlots;
+      const int slot = gi % slots;
+      if (gi >= slots) pf_wait(sh, v ? &sh.vfree[slot] : &sh.kfree[slot], ((gi - slots) / slots) & 1, p.err);
       const int nb = min(BPT, nblk - j * BPT);
-      unsigned char* dst = smem + T::OFF_KV + stage * 2 * T::KVTILE + (v ? T::KVTILE : 0);
-      uint64_t* full = v ? &sh.vfull[stage] : &sh.kfull[stage];
+      unsigned char* dst = smem + (v ? T::OFF_V : T::OFF_K) + slot * T::KVTILE;
+      uint64_t* full = v ? &sh.vfull[slot] : &sh.kfull[slot];
       const int row0 = v ? p.layer_row0_v : p.layer_row0_k;
       if (lane == 0) dev::mbar_arrive_expect_tx(full, (uint32_t)(nb * T::DH * 2048));
       __syncwarp();
@@ -185,7 +192,7 @@ __device__ void tma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
         dev::tma_load_2d(dst + h * (kKeys * 128) + blk * 2048, &p.kv_map, h * 64,
                          row0 + (bid * p.num_kv_heads + it.g) * kBS, full, pol);
     };
-    // K runs one tile ahead of V: a K stage is released by the scores, earlier than a V stage by the products
+    // K runs one tile ahead of V: a K slot is released by the scores, earlier than a V slot by the products
     int id_next = n > 0 ? load_ids(0) : 0, id_prev = 0;
     for (int t = 0; t <= n; ++t) {
       const int id_cur = id_next;
@@ -204,8 +211,12 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
   using T = PfTraits<D, G>;
   const uint32_t sbase = dev::smem_addr(smem);
   const uint32_t tmem = *sh.tmem_base;
-  int gt = 0;             // CTA-wide index of the next K/V tile: stage gt % kStages
-  int cw[kWG] = {0, 0};   // per Q-tile group: tiles processed so far (S/P/PV buffer cw % 2)
+  // base descriptors (Q tile 0, K slot 0, V slot 0): the others differ only in the start-address field
+  const uint64_t dq0 = dev::umma_desc_sw128(sbase + T::OFF_Q, 16, 1024);
+  const uint64_t dk0 = dev::umma_desc_sw128(sbase + T::OFF_K, 16, 1024);
+  const uint64_t dv0 = dev::umma_desc_sw128(sbase + T::OFF_V, kKeys * 128, 1024);
+  int gt = 0;            // CTA-wide index of the next K/V tile
+  int cw[kWG] = {0, 0};  // per Q-tile group: tiles processed so far (barrier phases)
   bool first = true;
   while (true) {
     int4 rec = make_int4(-1, 0, 0, 0);
@@ -225,77 +236,62 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
     const ItemGeo it = item_geo<T::P>(rec);
     const int n = it.n_all;
 
-    auto issue_s = [&](int w, int j) {  // S_w(j) = Q_w K(j)^T into group w's S buffer (cw + j) % 2
-      const int stage = (gt + j) % kStages, b = (cw[w] + j) & 1;
-      const uint32_t sq = sbase + T::OFF_Q + w * T::QTILE, sk = sbase + T::OFF_KV + stage * 2 * T::KVTILE;
+    auto issue_s = [&](int w, int j) {  // S_w(j) = Q_w K(j)^T; commits every earlier MMA too
+      const uint64_t dq = dq0 + (uint64_t)((w * T::QTILE) >> 4);
+      const uint64_t dk = dk0 + (uint64_t)((((gt + j) % kKSlots) * T::KVTILE) >> 4);
       if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          dev::umma_f16_ss(tmem + 256 * w + 64 * b,
-                           dev::umma_desc_sw128(sq + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                           dev::umma_desc_sw128(sk + (kk >> 2) * (kKeys * 128) + (kk & 3) * 32, 16, 1024),
-                           T::IDESC_S, kk > 0);
-        }
-        dev::umma_commit(&sh.s_done[2 * w + b]);
+        for (int kk = 0; kk < D / 16; ++kk)
+          dev::umma_f16_ss(tmem + 256 * w, dq + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+                           dk + (uint64_t)(((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4), T::IDESC_S, kk > 0);
+        dev::umma_commit(&sh.s_done[w]);
       }
       __syncwarp();
     };
-    auto issue_pv = [&](int w, int j) {  // O_w (+)= P_w(j) V(j)
-      const int stage = (gt + j) % kStages, b = (cw[w] + j) & 1;
-      const uint32_t sp = sbase + T::OFF_P + (2 * w + b) * T::PTILE;
-      const uint32_t sv = sbase + T::OFF_KV + stage * 2 * T::KVTILE + T::KVTILE;
+    auto issue_pv = [&](int w, int j) {  // O_w (+)= P_w(j) V(j), P from tensor memory
+      const uint64_t dv = dv0 + (uint64_t)((((gt + j) % kVSlots) * T::KVTILE) >> 4);
       if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          dev::umma_f16_ss(tmem + 256 * w + 128, dev::umma_desc_sw128(sp + kk * 32, 16, 1024),
-                           dev::umma_desc_sw128(sv + kk * 2048, kKeys * 128, 1024), T::IDESC_PV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        dev::umma_commit(&sh.pv_done[2 * w + b]);
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          dev::umma_f16_ts(tmem + 256 * w + 128, tmem + 256 * w + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4),
+                           T::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        dev::umma_commit(&sh.pv_done[w]);
       }
+      __syncwarp();
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (lane == 0) dev::umma_commit(bar);
       __syncwarp();
     };
 
     dev::named_bar_sync(kBarQ, kBarQThreads);  // both Q tiles are in shared memory
     dev::tc_fence_after();
-    pf_wait(sh, &sh.kfull[gt % kStages], (gt / kStages) & 1, p.err);
+    pf_wait(sh, &sh.kfull[gt % kKSlots], (gt / kKSlots) & 1, p.err);
 #pragma unroll
     for (int w = 0; w < kWG; ++w)
       if (it.n[w] > 0) issue_s(w, 0);
-    if (lane == 0) dev::umma_commit(&sh.kfree[gt % kStages]);
-    __syncwarp();
+    commit(&sh.kfree[gt % kKSlots]);
     for (int j = 0; j < n; ++j) {
       const int gi = gt + j;
-      // the next tile's scores, into the other S buffers, while the groups run this tile's softmax
-      if (j + 1 < n) {
-        pf_wait(sh, &sh.kfull[(gi + 1) % kStages], ((gi + 1) / kStages) & 1, p.err);
+      const bool last = j == n - 1;
+      pf_wait(sh, &sh.vfull[gi % kVSlots], (gi / kVSlots) & 1, p.err);
+      if (!last) pf_wait(sh, &sh.kfull[(gi + 1) % kKSlots], ((gi + 1) / kKSlots) & 1, p.err);
+      if (last) {  // one group zero-fills the last tile's V rows past the item's keys: wait for all
 #pragma unroll
         for (int w = 0; w < kWG; ++w)
-          if (j + 1 < it.n[w]) issue_s(w, j + 1);
-        if (lane == 0) dev::umma_commit(&sh.kfree[(gi + 1) % kStages]);
-        __syncwarp();
+          if (j < it.n[w]) pf_wait(sh, &sh.p_ready[w], (cw[w] + j) & 1, p.err);
       }
-      // this tile's products; the last tile's V rows are zero-filled by one group: wait for all
-      const bool last = j == n - 1;
-      pf_wait(sh, &sh.vfull[gi % kStages], (gi / kStages) & 1, p.err);
+      // per group: its product of tile j, then (P has been read) its scores of tile j + 1 over the same S
 #pragma unroll
       for (int w = 0; w < kWG; ++w) {
         if (j >= it.n[w]) continue;
-        const int c = cw[w] + j;
-        pf_wait(sh, &sh.p_ready[2 * w + (c & 1)], (c >> 1) & 1, p.err);
-        if (!last) {
-          dev::tc_fence_after();
-          issue_pv(w, j);
-        }
-      }
-      if (last) {
+        if (!last) pf_wait(sh, &sh.p_ready[w], (cw[w] + j) & 1, p.err);
         dev::tc_fence_after();
-#pragma unroll
-        for (int w = 0; w < kWG; ++w)
-          if (j < it.n[w]) issue_pv(w, j);
+        issue_pv(w, j);
+        if (j + 1 < it.n[w]) issue_s(w, j + 1);
       }
-      if (lane == 0) dev::umma_commit(&sh.vfree[gi % kStages]);
-      __syncwarp();
+      if (!last) commit(&sh.kfree[(gi + 1) % kKSlots]);
+      commit(&sh.vfree[gi % kVSlots]);
     }
     gt += n;
 #pragma unroll
@@ -310,9 +306,8 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
   const int r = (warp & 3) * 32 + lane;  // this thread's tile row and TMEM lane
   const uint32_t tl = *sh.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + 256 * wg;  // lane, group columns
   const uint32_t sQa = dev::smem_addr(smem + T::OFF_Q + wg * T::QTILE);
-  const uint32_t sPa = dev::smem_addr(smem + T::OFF_P + 2 * wg * T::PTILE);
-  int cw = 0;  // tiles processed by this group so far
-  int gt = 0;  // K/V tiles of the CTA so far (ring stage / phase of the zero-fill wait)
+  int cw = 0;  // tiles processed by this group so far (barrier phases)
+  int gt = 0;  // K/V tiles of the CTA so far (V slot / phase of the zero-fill wait)
   while (true) {
     dev::named_bar_sync(kBarItem, kThreads);
     const volatile int* vi = reinterpret_cast<volatile int*>(sh.item);
@@ -343,32 +338,28 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
 
     float m_ref = -INFINITY, l = 0.f;
     for (int j = 0; j < n; ++j) {
-      const int c = cw + j, b = c & 1;
-      pf_wait(sh, &sh.s_done[2 * wg + b], (c >> 1) & 1, p.err);
+      const int c = cw + j;
+      // S(j) written; its commit also covers the product of tile j - 1, so O is settled
+      pf_wait(sh, &sh.s_done[wg], c & 1, p.err);
       dev::tc_fence_after();
-      uint32_t s[2][32];
-      dev::tmem_ld32(tl + 64 * b, s[0]);
-      dev::tmem_ld32(tl + 64 * b + 32, s[1]);
-      dev::tmem_wait_ld();
-      // ---- causal mask, row max of the raw scores (four independent chains; the scale is positive) ----
+      // ---- causal mask, row max of the raw scores (the scale is positive); S read in two 64-column
+      //      halves so a thread never holds more than 64 scores ----
       const int kb = j * kKeys;
+      const bool full = kb + kKeys - 1 <= lim;
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (kb + kKeys - 1 <= lim) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t s[2][32];
+        dev::tmem_ld32(tl + 64 * h, s[0]);
+        dev::tmem_ld32(tl + 64 * h + 32, s[1]);
+        dev::tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < 2; ++k)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(s[k][e]));
-      } else {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-#pragma unroll
           for (int e = 0; e < 32; ++e) {
-            float x = __uint_as_float(s[k][e]);
-            if (kb + 32 * k + e > lim) x = -INFINITY;
-            s[k][e] = __float_as_uint(x);
-            mx4[e & 3] = fmaxf(mx4[e & 3], x);
+            const float x = __uint_as_float(s[k][e]);
+            mx4[e & 3] = fmaxf(mx4[e & 3], (full || kb + 64 * h + 32 * k + e <= lim) ? x : -INFINITY);
           }
-        }
       }
       const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
       // ---- lazy rescale of the running state ----
@@ -377,9 +368,6 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
       } else {
         const bool need = mx > m_ref + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
-          const int cp = c - 1;  // O += P V of the previous tile must have landed before O is rescaled
-          pf_wait(sh, &sh.pv_done[2 * wg + (cp & 1)], (cp >> 1) & 1, p.err);
-          dev::tc_fence_after();
           const float alpha = need ? exp2f(m_ref - mx) : 1.f;
 #pragma unroll
           for (int k = 0; k < D / 32; ++k) {
@@ -390,42 +378,47 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
             dev::tmem_st32(tl + 128 + 32 * k, o);
           }
-          dev::tmem_wait_st();
           if (need) {
             l *= alpha;
             m_ref = mx;
           }
         }
       }
-      // ---- P buffer b is free once the product that read it two tiles ago has completed ----
-      if (j >= 2) pf_wait(sh, &sh.pv_done[2 * wg + b], ((c - 2) >> 1) & 1, p.err);
+      // ---- P = 2^(s * scale_log2 - m_ref) as fp16, over the first 64 columns of S (the columns of the
+      //      first half, already read when the second half is loaded) ----
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t pbuf = sPa + b * T::PTILE;
-      const float nm = -m_ref;  // p = 2^(s * scale_log2 - m_ref): one FFMA and one MUFU per score
+      const float nm = -m_ref;  // one FFMA and one MUFU per score
 #pragma unroll
-      for (int c8 = 0; c8 < kKeys / 8; ++c8) {
-        uint32_t h2[4];
+      for (int h = 0; h < 2; ++h) {
+        uint32_t s[2][32];
+        dev::tmem_ld32(tl + 64 * h, s[0]);
+        dev::tmem_ld32(tl + 64 * h + 32, s[1]);
+        dev::tmem_wait_ld();
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = c8 * 8 + 2 * e;
-          const float p0 = dev::ex2_approx(fmaf(__uint_as_float(s[k >> 5][k & 31]), p.scale_log2, nm));
-          const float p1 = dev::ex2_approx(fmaf(__uint_as_float(s[(k + 1) >> 5][(k + 1) & 31]), p.scale_log2, nm));
-          sum4[e] += p0 + p1;
+        for (int e = 0; e < 32; ++e) {
+          const int k = 2 * e;  // key 64 h + k of the tile
+          float x0 = __uint_as_float(s[k >> 5][k & 31]), x1 = __uint_as_float(s[(k + 1) >> 5][(k + 1) & 31]);
+          if (!full) {
+            if (kb + 64 * h + k > lim) x0 = -INFINITY;
+            if (kb + 64 * h + k + 1 > lim) x1 = -INFINITY;
+          }
+          const float p0 = dev::ex2_approx(fmaf(x0, p.scale_log2, nm));
+          const float p1 = dev::ex2_approx(fmaf(x1, p.scale_log2, nm));
+          sum4[e & 3] += p0 + p1;
           const __half2 hh = __floats2half2_rn(p0, p1);
-          h2[e] = *reinterpret_cast<const uint32_t*>(&hh);
+          pk[e] = *reinterpret_cast<const uint32_t*>(&hh);
         }
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(pbuf + r * 128 + (((c8 ^ (r & 7))) << 4)),
-                     "r"(h2[0]), "r"(h2[1]), "r"(h2[2]), "r"(h2[3])
-                     : "memory");
+        dev::tmem_st32(tl + 32 * h, pk);
       }
       l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       // ---- the item's last tile: V rows past its keys hold stale bytes; zero them (0 * NaN = NaN) ----
       if (wg == it.zfill_wg && j == n - 1) {
         const int kl = it.kend_all - kb;
         if (kl < kKeys) {
-          const int gi = gt + j, stage = gi % kStages;
-          pf_wait(sh, &sh.vfull[stage], (gi / kStages) & 1, p.err);
-          const uint32_t sv = dev::smem_addr(smem + T::OFF_KV + stage * 2 * T::KVTILE + T::KVTILE);
+          const int gi = gt + j, slot = gi % kVSlots;
+          pf_wait(sh, &sh.vfull[slot], (gi / kVSlots) & 1, p.err);
+          const uint32_t sv = dev::smem_addr(smem + T::OFF_V + slot * T::KVTILE);
           for (int idx = r; idx < (kKeys - kl) * T::DH * 8; idx += 128) {
             const int kr = kl + idx / (T::DH * 8), rest = idx % (T::DH * 8);
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sv + (rest >> 3) * (kKeys * 128) + kr * 128 +
@@ -436,13 +429,13 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
         }
       }
       dev::fence_proxy_async_smem();
+      dev::tmem_wait_st();
       dev::tc_fence_before();
-      dev::mbar_arrive(&sh.p_ready[2 * wg + b]);
+      dev::mbar_arrive(&sh.p_ready[wg]);
     }
     // ---- epilogue: O / l -> fp16 ----
     if (n > 0) {
-      const int cl = cw + n - 1;
-      pf_wait(sh, &sh.pv_done[2 * wg + (cl & 1)], (cl >> 1) & 1, p.err);
+      pf_wait(sh, &sh.pv_done[wg], (cw + n - 1) & 1, p.err);
       dev::tc_fence_after();
       const float il = 1.f / l;
       __half* dst = p.out + (tok * p.num_q_heads + (size_t)it.g * G + hq) * D;
@@ -481,22 +474,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
   Bars sh;
   sh.kfull = bars;
-  sh.vfull = bars + kStages;
-  sh.kfree = bars + 2 * kStages;
-  sh.vfree = bars + 3 * kStages;
-  sh.s_done = bars + 4 * kStages;
-  sh.p_ready = sh.s_done + 2 * kWG;
-  sh.pv_done = sh.p_ready + 2 * kWG;
+  sh.kfree = sh.kfull + kKSlots;
+  sh.vfull = sh.kfree + kKSlots;
+  sh.vfree = sh.vfull + kVSlots;
+  sh.s_done = sh.vfree + kVSlots;
+  sh.p_ready = sh.s_done + kWG;
+  sh.pv_done = sh.p_ready + kWG;
   sh.tmem_base = reinterpret_cast<uint32_t*>(smem + T::OFF_MISC);
   sh.item = reinterpret_cast<int4*>(smem + T::OFF_MISC + 16);
   sh.abort = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 32);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 4 * kStages; ++i) dev::mbar_init(&bars[i], 1);
-    for (int i = 0; i < 2 * kWG; ++i) {
-      dev::mbar_init(&sh.s_done[i], 1);
-      dev::mbar_init(&sh.p_ready[i], 128);
-      dev::mbar_init(&sh.pv_done[i], 1);
+    for (int i = 0; i < 2 * (kKSlots + kVSlots); ++i) dev::mbar_init(&bars[i], 1);
+    for (int w = 0; w < kWG; ++w) {
+      dev::mbar_init(&sh.s_done[w], 1);
+      dev::mbar_init(&sh.p_ready[w], 128);
+      dev::mbar_init(&sh.pv_done[w], 1);
     }
     dev::fence_mbar_init();
     *sh.abort = 0;
