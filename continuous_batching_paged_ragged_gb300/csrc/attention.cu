@@ -29,6 +29,7 @@
 //    spreads one token's merge over many CTAs.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 #include <string>
@@ -702,6 +703,9 @@ struct PlanParams {
   int32_t* merge_cnt;
   int4* tasks;
   int4* items;
+  int32_t* items_slot;
+  int2* pf_sync;
+  int max_slots;
   WsHeader* hdr;
   int32_t* err;
 };
@@ -710,7 +714,8 @@ __device__ __forceinline__ bool row_meta_ok(int q_len, int ctx, int max_ctx) {
   return q_len >= 1 && ctx >= q_len && ctx <= max_ctx;
 }
 
-// Prefill items of row b in plan order: (position block qb, KV head g); `fn(qb, cost, rec)` per qb.
+// Prefill items of row b in plan order, one per position block: `fn(n, npos, first token, w)` with n the
+// item's K/V tiles and w the keys visible to its first position minus one.
 template <typename F>
 __device__ __forceinline__ void for_row_items(const PlanParams& p, int b, F fn) {
   const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1), ctx = __ldg(p.context_lens + b);
@@ -718,15 +723,18 @@ __device__ __forceinline__ void for_row_items(const PlanParams& p, int b, F fn) 
   if (p.prefill_min_qlen <= 0 || q_len < p.prefill_min_qlen || !row_meta_ok(q_len, ctx, p.max_ctx)) return;
   for (int qb = 0; qb * p.prefill_pos < q_len; ++qb) {
     const int npos = min(p.prefill_pos, q_len - qb * p.prefill_pos);
-    const int w = ctx - q_len + qb * p.prefill_pos;  // keys visible to the block's first position, minus one
-    const int cost = (w + npos + kPrefillKeys - 1) / kPrefillKeys;
-    fn(cost, make_int4(b, npos << 16, q0 + qb * p.prefill_pos, w));
+    const int w = ctx - q_len + qb * p.prefill_pos;
+    fn((w + npos + kPrefillKeys - 1) / kPrefillKeys, npos, q0 + qb * p.prefill_pos, w);
   }
 }
+
+// K/V tiles of the two chunks of an item of n tiles (the first chunk takes the extra tile).
+__device__ __forceinline__ int split_first(int n) { return (n + 1) / 2; }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) {
   __shared__ int warp_sums[32];
   __shared__ int hist[kPrefillBuckets];
+  __shared__ int n_slots;
   dev::griddep_wait();
   for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
     const int q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1), ctx = __ldg(p.context_lens + i);
@@ -736,6 +744,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   }
   for (int i = threadIdx.x; i < p.num_tokens * p.num_kv_heads; i += blockDim.x) p.merge_cnt[i] = 0;
   for (int i = threadIdx.x; i < kPrefillBuckets; i += blockDim.x) hist[i] = 0;
+  for (int i = threadIdx.x; i < p.max_slots; i += blockDim.x) p.pf_sync[i] = make_int2(0, 0);
+  if (threadIdx.x == 0) n_slots = 0;
 
   // ---- decode tasks: tokens of rows that are not prefill items ----
   // Pass 0 lists each token's short last split, pass 1 its full splits in token order: tokens then
@@ -780,10 +790,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     }
   }
 
-  // ---- prefill items, bucketed by K/V tile count, longest first ----
+  // ---- prefill work entries, bucketed by K/V tile count, longest first; long items in two chunks ----
   auto bucket_of = [](int cost) { return kPrefillBuckets - 1 - min(cost, kPrefillBuckets - 1); };
   for (int b = threadIdx.x; b < p.num_seqs; b += blockDim.x)
-    for_row_items(p, b, [&](int cost, int4) { atomicAdd(&hist[bucket_of(cost)], p.num_kv_heads); });
+    for_row_items(p, b, [&](int n, int, int, int) {
+      if (n > kPrefillSplitTiles) {
+        atomicAdd(&hist[bucket_of(split_first(n))], p.num_kv_heads);
+        atomicAdd(&hist[bucket_of(n - split_first(n))], p.num_kv_heads);
+      } else {
+        atomicAdd(&hist[bucket_of(n)], p.num_kv_heads);
+      }
+    });
   __syncthreads();
   int n_items = 0;
   for (int base = 0; base < kPrefillBuckets; base += blockDim.x) {
@@ -797,9 +814,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     __syncthreads();
   }
   for (int b = threadIdx.x; b < p.num_seqs; b += blockDim.x)
-    for_row_items(p, b, [&](int cost, int4 rec) {
-      const int at = atomicAdd(&hist[bucket_of(cost)], p.num_kv_heads);
-      for (int g = 0; g < p.num_kv_heads; ++g) p.items[at + g] = make_int4(rec.x, g | rec.y, rec.z, rec.w);
+    for_row_items(p, b, [&](int n, int npos, int t0, int w) {
+      const bool split = n > kPrefillSplitTiles;
+      const int slot = split ? atomicAdd(&n_slots, p.num_kv_heads) : -1;
+      for (int chunk = 0; chunk < (split ? 2 : 1); ++chunk) {
+        const int cost = split ? (chunk == 0 ? split_first(n) : n - split_first(n)) : n;
+        const int at = atomicAdd(&hist[bucket_of(cost)], p.num_kv_heads);
+        for (int g = 0; g < p.num_kv_heads; ++g) {
+          p.items[at + g] = make_int4(b, prefill_rec_y(g, npos, chunk, split ? 1 : 0), t0, w);
+          p.items_slot[at + g] = split ? slot + g : -1;
+        }
+      }
     });
 
   if (threadIdx.x == 0) {
@@ -818,7 +843,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
 // Workspace layout and launches
 // ---------------------------------------------------------------------------------------------------
 struct WsLayout {
-  size_t hdr, tok_row, tok_ctx, merge_cnt, tasks, items, part_ml, part_o, total;
+  size_t hdr, tok_row, tok_ctx, merge_cnt, tasks, items, items_slot, pf_sync, pf_ml, pf_o, part_ml, part_o, total;
   int max_splits;
   int64_t max_tasks;
   int prefill_min_qlen;  // 0: every row takes the decode path
@@ -833,10 +858,17 @@ static WsLayout ws_layout(const pkv_config& c, int num_seqs, int num_tokens, int
   w.max_splits = (max_blocks + c.split_blocks - 1) / c.split_blocks;
   w.max_tasks = (int64_t)num_tokens * c.num_kv_heads * w.max_splits;
   const int group = c.num_q_heads / c.num_kv_heads;
-  const bool prefill = prefill_supported(c.head_dim, group);
+  const bool prefill = prefill_supported(c.head_dim, group) && c.num_kv_heads < 256;
   w.prefill_min_qlen = prefill ? kPrefillMinQlen : 0;
   w.prefill_pos = prefill_item_positions(group);
-  w.max_items = prefill ? (int64_t)c.num_kv_heads * ((num_tokens + w.prefill_pos - 1) / w.prefill_pos + num_seqs) : 0;
+  // a prefill row has >= prefill_min_qlen tokens, every other row >= 1: at most R such rows, holding at most
+  // num_tokens - (num_seqs - R) tokens
+  int64_t rows = 0, toks = 0;
+  if (prefill && num_seqs > 0) {
+    rows = std::min<int64_t>(num_seqs, (int64_t)(num_tokens - num_seqs) / (kPrefillMinQlen - 1));
+    toks = num_tokens - (num_seqs - rows);
+  }
+  w.max_items = rows > 0 ? (int64_t)c.num_kv_heads * ((toks + w.prefill_pos - 1) / w.prefill_pos + rows) : 0;
   size_t off = 0;
   w.hdr = off;
   off += sizeof(WsHeader);
@@ -848,8 +880,17 @@ static WsLayout ws_layout(const pkv_config& c, int num_seqs, int num_tokens, int
   off += up256((size_t)num_tokens * c.num_kv_heads * 4);
   w.tasks = off;
   off += up256((size_t)w.max_tasks * sizeof(int4));
+  // prefill: up to two work entries per item (split-KV), one partial slot per item
   w.items = off;
-  off += up256((size_t)w.max_items * sizeof(int4));
+  off += up256((size_t)w.max_items * 2 * sizeof(int4));
+  w.items_slot = off;
+  off += up256((size_t)w.max_items * 2 * sizeof(int32_t));
+  w.pf_sync = off;
+  off += up256((size_t)w.max_items * sizeof(int2));
+  w.pf_ml = off;
+  off += up256((size_t)w.max_items * kPrefillRows * 2 * sizeof(float2));
+  w.pf_o = off;
+  off += up256((size_t)w.max_items * kPrefillRows * 2 * c.head_dim * sizeof(float));
   const size_t parts = w.max_splits > 1 ? (size_t)w.max_tasks : 0;  // one partial per (token, KV head, split)
   w.part_ml = off;
   off += up256(parts * kHeadsTile * sizeof(float2));
@@ -908,6 +949,9 @@ static cudaError_t launch_plan(pkv_pool* pool, char* ws, const WsLayout& w, cons
   p.merge_cnt = reinterpret_cast<int32_t*>(ws + w.merge_cnt);
   p.tasks = reinterpret_cast<int4*>(ws + w.tasks);
   p.items = reinterpret_cast<int4*>(ws + w.items);
+  p.items_slot = reinterpret_cast<int32_t*>(ws + w.items_slot);
+  p.pf_sync = reinterpret_cast<int2*>(ws + w.pf_sync);
+  p.max_slots = (int)w.max_items;
   p.hdr = reinterpret_cast<WsHeader*>(ws + w.hdr);
   p.err = pool->dev_error;
   return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p);
@@ -971,6 +1015,10 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
     a.out = out;
     a.block_tables = block_tables;
     a.items = reinterpret_cast<const int4*>(ws + w.items);
+    a.items_slot = reinterpret_cast<const int32_t*>(ws + w.items_slot);
+    a.pf_sync = reinterpret_cast<int2*>(ws + w.pf_sync);
+    a.pf_ml = reinterpret_cast<float2*>(ws + w.pf_ml);
+    a.pf_o = reinterpret_cast<float*>(ws + w.pf_o);
     a.hdr = p.hdr;
     a.err = p.err;
     a.layer_row0_k = p.layer_row0_k;
@@ -981,7 +1029,7 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
     a.num_blocks = c.num_blocks;
     a.head_dim = c.head_dim;
     a.num_sms = pool->num_sms;
-    a.max_items = w.max_items;
+    a.max_items = 2 * w.max_items;
     e = launch_prefill(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     *launches += 1;

@@ -19,6 +19,9 @@ constexpr int kPrefillMinQlen = 16;
 constexpr int kPrefillRows = 128;  // MMA rows of a prefill Q tile: (query position, query head) pairs
 constexpr int kPrefillKeys = 128;  // keys per K/V tile
 constexpr int kPrefillBuckets = 1024;
+// An item whose keys span more K/V tiles than this runs as two chunks of keys (split-KV) that the
+// second chunk to finish merges; the split depends on the row alone.
+constexpr int kPrefillSplitTiles = 24;
 
 // Query positions per prefill Q tile: the G query heads of a KV head are packed into the MMA rows.
 __host__ __device__ constexpr int prefill_positions(int group) { return kPrefillRows / group; }
@@ -34,10 +37,16 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
-// A prefill item: one KV head, up to prefill_item_positions(G) consecutive query positions of one row.
-//   x: row (block-table row)          y: KV head | (positions << 16)
+// A prefill work entry: one KV head, up to prefill_item_positions(G) consecutive query positions of one
+// row, all of its keys or one of two chunks of them.
+//   x: row (block-table row)
+//   y: KV head | positions << 8 | chunk << 20 | split << 21
 //   z: first query token (packed)     w: keys visible to the item's first position, minus one
-// Position i of the item attends causally to keys 0 .. w + i.
+// Position i of the item attends causally to keys 0 .. w + i.  A split item's two entries share a slot
+// (the partial results and the merge handshake).
+__host__ __device__ constexpr int prefill_rec_y(int g, int npos, int chunk, int split) {
+  return g | (npos << 8) | (chunk << 20) | (split << 21);
+}
 
 struct PrefillArgs {
   const CUtensorMap* kv_map;  // device copy is passed by value below; this one is host-side
@@ -45,6 +54,10 @@ struct PrefillArgs {
   void* out;
   const int32_t* block_tables;
   const int4* items;
+  const int32_t* items_slot;  // per work entry: the split item's slot, or -1
+  int2* pf_sync;              // per slot: {chunks finished, first chunk's partial published}
+  float2* pf_ml;              // per slot: [256 rows] (running max, running sum) of the first chunk
+  float* pf_o;                // per slot: [256 rows][head_dim] unnormalised output of the first chunk
   WsHeader* hdr;
   int32_t* err;
   int layer_row0_k, layer_row0_v;

@@ -41,8 +41,9 @@ constexpr int kWG = 2;                 // softmax warpgroups = Q tiles per item
 constexpr int kMmaWarp = 4 * kWG;      // issues the MMAs and hands out items
 constexpr int kTmaWarp = 4 * kWG + 1;  // streams K/V tiles
 constexpr int kThreads = (4 * kWG + 2) * 32;
-constexpr int kBarItem = 1, kBarQ = 2; // named barriers (0 is __syncthreads)
+constexpr int kBarItem = 1, kBarQ = 2, kBarEpi = 3;  // named barriers (0 is __syncthreads)
 constexpr int kBarQThreads = (4 * kWG + 1) * 32;  // softmax groups + the MMA warp
+constexpr int kSoftmaxThreads = 4 * kWG * 32;
 constexpr float kRescaleLog2 = 8.f;    // lazy rescale threshold (log2 units)
 constexpr int kKeys = kPrefillKeys;    // keys per K/V tile
 static_assert(kKeys == 128, "S of a tile fills 128 TMEM columns; its P (fp16) the first 64");
@@ -57,7 +58,7 @@ struct PfTraits {
   static constexpr int OFF_K = OFF_Q + kWG * QTILE;   // [kKSlots]
   static constexpr int OFF_V = OFF_K + kKSlots * KVTILE;  // [kVSlots]
   static constexpr int OFF_BAR = OFF_V + kVSlots * KVTILE;
-  static constexpr int OFF_MISC = OFF_BAR + 256;      // TMEM base, item record, abort flag
+  static constexpr int OFF_MISC = OFF_BAR + 256;      // TMEM base, item record, abort flag, slot, merge order
   static constexpr int SMEM = OFF_MISC + 64 + 1024;   // + slack to align to 1024 bytes
   // group w: S at 256 w (128 columns; P, as fp16, overwrites its first 64), O at 256 w + 128
   static constexpr uint32_t TMEM_COLS = 512;
@@ -73,6 +74,10 @@ struct PfParams {
   __half* out;
   const int32_t* block_tables;
   const int4* items;
+  const int32_t* items_slot;
+  int2* pf_sync;
+  float2* pf_ml;
+  float* pf_o;
   WsHeader* hdr;
   int32_t* err;
   int layer_row0_k, layer_row0_v;
@@ -91,6 +96,8 @@ struct Bars {
   uint32_t* tmem_base;
   int4* item;
   volatile int* abort;
+  volatile int* slot;   // the current entry's split slot (-1: not split)
+  volatile int* order;  // split entries: 0 if this chunk finished first, 1 if it merges
 };
 
 // Bounded wait that, once any wait of the CTA has given up, no longer waits at all: every thread then
@@ -109,7 +116,7 @@ __device__ __forceinline__ uint32_t qtile_off(int r, int c) {
   return (uint32_t)((c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// The item's geometry as seen by each of its Q tiles.
+// The work entry's geometry as seen by each of the item's Q tiles.
 struct ItemGeo {
   int row, g, t0, w0;   // row, KV head, first token, keys visible to the first position minus one
   int npos[kWG];        // positions of each Q tile (0: the tile is empty)
@@ -117,14 +124,18 @@ struct ItemGeo {
   int n_all;            // K/V tiles of the item
   int kend_all;         // keys of the item
   int zfill_wg;         // the group that zeroes V rows past the item's keys in the last tile
+  int split, chunk;     // split-KV: this entry is chunk `chunk` of 2
+  int tb, te;           // K/V tiles [tb, te) of the item that this entry processes
 };
 
 template <int P>
 __device__ __forceinline__ ItemGeo item_geo(const int4 rec) {
   ItemGeo it;
   it.row = rec.x;
-  it.g = rec.y & 0xFFFF;
-  const int npos = rec.y >> 16;
+  it.g = rec.y & 0xFF;
+  const int npos = (rec.y >> 8) & 0x1FF;
+  it.chunk = (rec.y >> 20) & 1;
+  it.split = (rec.y >> 21) & 1;
   it.t0 = rec.z;
   it.w0 = rec.w;
   it.n_all = 0;
@@ -141,6 +152,9 @@ __device__ __forceinline__ ItemGeo item_geo(const int4 rec) {
       it.zfill_wg = w;
     }
   }
+  const int h = (it.n_all + 1) / 2;  // the first chunk takes the extra tile
+  it.tb = it.split && it.chunk ? h : 0;
+  it.te = it.split && !it.chunk ? h : it.n_all;
   return it;
 }
 
@@ -158,10 +172,11 @@ __device__ void tma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
     const int4 rec = make_int4(vi[0], vi[1], vi[2], vi[3]);
     if (rec.x < 0) break;
     const ItemGeo it = item_geo<T::P>(rec);
-    const int n = it.n_all;
+    const int n = it.te - it.tb;  // tiles of this entry: item tiles tb .. te - 1
     const int nblk = (it.kend_all + kBS - 1) / kBS;
     const int32_t* bt = p.block_tables + (int64_t)it.row * p.max_blocks;
-    auto load_ids = [&](int j) {  // lane i < blocks of tile j: physical id of the tile's block i
+    auto load_ids = [&](int u) {
+      const int j = it.tb + u;  // lane i < blocks of tile j: physical id of the tile's block i
       int id = 0;
       if (lane < min(BPT, nblk - j * BPT)) {
         id = __ldg(bt + j * BPT + lane);
@@ -175,8 +190,8 @@ __device__ void tma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
     // TMA of tile j's K (v = false) or V (v = true) into its ring slot, once the MMAs that read the tile
     // a ring-length earlier from that slot have completed.  One 2 KB box (16 keys x 64 columns) per lane:
     // a single issuing thread would be the bottleneck.
-    auto issue = [&](int j, bool v, int id) {
-      const int gi = gt + j;
+    auto issue = [&](int u, bool v, int id) {
+      const int j = it.tb + u, gi = gt + u;
       const int slots = v ? kVSlots : kKSlots;
       const int slot = gi % slots;
       if (gi >= slots) pf_wait(sh, v ? &sh.vfree[slot] : &sh.kfree[slot], ((gi - slots) / slots) & 1, p.err);
@@ -222,8 +237,13 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
     int4 rec = make_int4(-1, 0, 0, 0);
     if (lane == 0) {
       const int idx = first ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&p.hdr->pwork, 1);
-      if (idx < n_items) rec = __ldg(p.items + idx);
+      int slot = -1;
+      if (idx < n_items) {
+        rec = __ldg(p.items + idx);
+        slot = __ldg(p.items_slot + idx);
+      }
       *sh.item = rec;
+      *sh.slot = slot;
     }
     first = false;
     rec.x = __shfl_sync(0xffffffffu, rec.x, 0);
@@ -234,9 +254,12 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
     dev::named_bar_arrive(kBarItem, kThreads);
     if (rec.x < 0) break;
     const ItemGeo it = item_geo<T::P>(rec);
-    const int n = it.n_all;
+    const int n = it.te - it.tb;  // tiles of this entry; u below is the entry's tile, tb + u the item's
+    int ne[kWG];                  // tiles of this entry per group
+#pragma unroll
+    for (int w = 0; w < kWG; ++w) ne[w] = max(0, min(it.te, it.n[w]) - it.tb);
 
-    auto issue_s = [&](int w, int j) {  // S_w(j) = Q_w K(j)^T; commits every earlier MMA too
+    auto issue_s = [&](int w, int j) {  // S_w(u = j) = Q_w K^T; commits every earlier MMA too
       const uint64_t dq = dq0 + (uint64_t)((w * T::QTILE) >> 4);
       const uint64_t dk = dk0 + (uint64_t)((((gt + j) % kKSlots) * T::KVTILE) >> 4);
       if (lane == 0) {
@@ -269,7 +292,7 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
     pf_wait(sh, &sh.kfull[gt % kKSlots], (gt / kKSlots) & 1, p.err);
 #pragma unroll
     for (int w = 0; w < kWG; ++w)
-      if (it.n[w] > 0) issue_s(w, 0);
+      if (ne[w] > 0) issue_s(w, 0);
     commit(&sh.kfree[gt % kKSlots]);
     for (int j = 0; j < n; ++j) {
       const int gi = gt + j;
@@ -279,23 +302,23 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
       if (last) {  // one group zero-fills the last tile's V rows past the item's keys: wait for all
 #pragma unroll
         for (int w = 0; w < kWG; ++w)
-          if (j < it.n[w]) pf_wait(sh, &sh.p_ready[w], (cw[w] + j) & 1, p.err);
+          if (j < ne[w]) pf_wait(sh, &sh.p_ready[w], (cw[w] + j) & 1, p.err);
       }
       // per group: its product of tile j, then (P has been read) its scores of tile j + 1 over the same S
 #pragma unroll
       for (int w = 0; w < kWG; ++w) {
-        if (j >= it.n[w]) continue;
+        if (j >= ne[w]) continue;
         if (!last) pf_wait(sh, &sh.p_ready[w], (cw[w] + j) & 1, p.err);
         dev::tc_fence_after();
         issue_pv(w, j);
-        if (j + 1 < it.n[w]) issue_s(w, j + 1);
+        if (j + 1 < ne[w]) issue_s(w, j + 1);
       }
       if (!last) commit(&sh.kfree[(gi + 1) % kKSlots]);
       commit(&sh.vfree[gi % kVSlots]);
     }
     gt += n;
 #pragma unroll
-    for (int w = 0; w < kWG; ++w) cw[w] += it.n[w];
+    for (int w = 0; w < kWG; ++w) cw[w] += ne[w];
   }
 }
 
@@ -314,7 +337,8 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
     const int4 rec = make_int4(vi[0], vi[1], vi[2], vi[3]);
     if (rec.x < 0) break;
     const ItemGeo it = item_geo<T::P>(rec);
-    const int n = wg ? it.n[1] : it.n[0];
+    const int slot = *sh.slot;
+    const int n = max(0, min(it.te, wg ? it.n[1] : it.n[0]) - it.tb);  // this group's tiles of the entry
     const int pos = r / G, hq = r % G;
     const int npos = wg ? it.npos[1] : it.npos[0];
     const bool valid = r < T::P * G && pos < npos;
@@ -337,8 +361,8 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
     dev::named_bar_arrive(kBarQ, kBarQThreads);
 
     float m_ref = -INFINITY, l = 0.f;
-    for (int j = 0; j < n; ++j) {
-      const int c = cw + j;
+    for (int u = 0; u < n; ++u) {
+      const int c = cw + u, j = it.tb + u;  // j: the item's tile
       // S(j) written; its commit also covers the product of tile j - 1, so O is settled
       pf_wait(sh, &sh.s_done[wg], c & 1, p.err);
       dev::tc_fence_after();
@@ -363,7 +387,7 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
       }
       const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
       // ---- lazy rescale of the running state ----
-      if (j == 0) {
+      if (u == 0) {
         m_ref = mx;
       } else {
         const bool need = mx > m_ref + kRescaleLog2;
@@ -413,12 +437,12 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
       }
       l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       // ---- the item's last tile: V rows past its keys hold stale bytes; zero them (0 * NaN = NaN) ----
-      if (wg == it.zfill_wg && j == n - 1) {
+      if (wg == it.zfill_wg && j == it.n_all - 1) {
         const int kl = it.kend_all - kb;
         if (kl < kKeys) {
-          const int gi = gt + j, slot = gi % kVSlots;
-          pf_wait(sh, &sh.vfull[slot], (gi / kVSlots) & 1, p.err);
-          const uint32_t sv = dev::smem_addr(smem + T::OFF_V + slot * T::KVTILE);
+          const int gi = gt + u, vs = gi % kVSlots;
+          pf_wait(sh, &sh.vfull[vs], (gi / kVSlots) & 1, p.err);
+          const uint32_t sv = dev::smem_addr(smem + T::OFF_V + vs * T::KVTILE);
           for (int idx = r; idx < (kKeys - kl) * T::DH * 8; idx += 128) {
             const int kr = kl + idx / (T::DH * 8), rest = idx % (T::DH * 8);
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sv + (rest >> 3) * (kKeys * 128) + kr * 128 +
@@ -433,35 +457,121 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
       dev::tc_fence_before();
       dev::mbar_arrive(&sh.p_ready[wg]);
     }
-    // ---- epilogue: O / l -> fp16 ----
+    // ---- epilogue: O / l -> fp16, or for a split item the chunk handshake ----
+    __half* dst = p.out + (tok * p.num_q_heads + (size_t)it.g * G + hq) * D;
     if (n > 0) {
       pf_wait(sh, &sh.pv_done[wg], (cw + n - 1) & 1, p.err);
       dev::tc_fence_after();
-      const float il = 1.f / l;
-      __half* dst = p.out + (tok * p.num_q_heads + (size_t)it.g * G + hq) * D;
+    }
+    auto store_row = [&](int k, const float (&v)[32]) {  // 32 output columns of this row, fp16
 #pragma unroll
-      for (int k = 0; k < D / 32; ++k) {
-        uint32_t o[32];
-        dev::tmem_ld32(tl + 128 + 32 * k, o);
-        dev::tmem_wait_ld();
-        if (valid) {
+      for (int c8 = 0; c8 < 4; ++c8) {
+        uint32_t h2[4];
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            uint32_t h2[4];
+        for (int e = 0; e < 4; ++e) {
+          const __half2 hh = __floats2half2_rn(v[c8 * 8 + 2 * e], v[c8 * 8 + 2 * e + 1]);
+          h2[e] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+        *reinterpret_cast<uint4*>(dst + 32 * k + 8 * c8) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+      }
+    };
+    if (!it.split) {
+      if (n > 0) {
+        const float il = 1.f / l;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __half2 hh = __floats2half2_rn(__uint_as_float(o[c8 * 8 + 2 * e]) * il,
-                                                   __uint_as_float(o[c8 * 8 + 2 * e + 1]) * il);
-              h2[e] = *reinterpret_cast<const uint32_t*>(&hh);
-            }
-            *reinterpret_cast<uint4*>(dst + 32 * k + 8 * c8) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-          }
+        for (int k = 0; k < D / 32; ++k) {
+          uint32_t o[32];
+          dev::tmem_ld32(tl + 128 + 32 * k, o);
+          dev::tmem_wait_ld();
+          float v[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * il;
+          if (valid) store_row(k, v);
         }
       }
-      dev::tc_fence_before();
+    } else {
+      // The chunk that finishes first publishes its unnormalised (m, l, O); the other merges them in
+      // chunk order (the result does not depend on which chunk finished first) and writes fp16.
+      const size_t prow = (size_t)slot * (2 * kPrefillRows) + wg * kPrefillRows + r;
+      const int2* sync = p.pf_sync + slot;
+      if (threadIdx.x == 0) *sh.order = atomicAdd(const_cast<int*>(&sync->x), 1);
+      dev::named_bar_sync(kBarEpi, kSoftmaxThreads);
+      const int order = *sh.order;
+      const float m_own = n > 0 ? m_ref : -INFINITY, l_own = n > 0 ? l : 0.f;
+      if (order == 0) {
+        p.pf_ml[prow] = make_float2(m_own, l_own);
+        if (n > 0) {
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) {
+            uint32_t o[32];
+            dev::tmem_ld32(tl + 128 + 32 * k, o);
+            dev::tmem_wait_ld();
+            float4* po = reinterpret_cast<float4*>(p.pf_o + prow * D + 32 * k);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              po[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]), __uint_as_float(o[4 * e + 2]),
+                                  __uint_as_float(o[4 * e + 3]));
+          }
+        }
+        dev::named_bar_sync(kBarEpi, kSoftmaxThreads);  // every row published
+        if (threadIdx.x == 0) {
+          __threadfence();
+          atomicExch(const_cast<int*>(&sync->y), 1);
+        }
+      } else {
+        if (threadIdx.x == 0) {  // bounded wait for the other chunk's partial
+          const uint64_t t0 = dev::globaltimer_ns();
+          uint32_t polls = 0;
+          while (atomicAdd(const_cast<int*>(&sync->y), 0) == 0) {
+            if ((++polls & 255u) == 0 && polls > (1u << 16) && (int64_t)(dev::globaltimer_ns() - t0) > 1000000000ll) {
+              *sh.abort = 1;
+              dev::set_error(p.err, PKV_DEVERR_WAIT_TIMEOUT);
+              break;
+            }
+          }
+          __threadfence();
+        }
+        dev::named_bar_sync(kBarEpi, kSoftmaxThreads);
+        const float2 mlo = __ldcg(p.pf_ml + prow);
+        // chunk 0 first, whichever of the two this is
+        const float m0 = it.chunk ? mlo.x : m_own, l0 = it.chunk ? mlo.y : l_own;
+        const float m1 = it.chunk ? m_own : mlo.x, l1 = it.chunk ? l_own : mlo.y;
+        const float M = fmaxf(m0, m1);
+        const float f0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M), f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+        const float il = 1.f / (l0 * f0 + l1 * f1);
+        const bool other_has = mlo.x != -INFINITY;
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) {
+          uint32_t o[32];
+          if (n > 0) {
+            dev::tmem_ld32(tl + 128 + 32 * k, o);
+            dev::tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+          float v[32];
+          const float4* po = reinterpret_cast<const float4*>(p.pf_o + prow * D + 32 * k);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 q4 = other_has && valid ? __ldcg(po + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float ot[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float own = __uint_as_float(o[4 * e + i]);
+              const float a0 = it.chunk ? ot[i] : own, a1 = it.chunk ? own : ot[i];
+              v[4 * e + i] = (a0 * f0 + a1 * f1) * il;
+            }
+          }
+          if (valid) store_row(k, v);
+        }
+        dev::named_bar_sync(kBarEpi, kSoftmaxThreads);
+        if (threadIdx.x == 0) *const_cast<int2*>(sync) = make_int2(0, 0);  // ready for the next launch
+      }
     }
+    if (n > 0) dev::tc_fence_before();
     cw += n;
-    gt += it.n_all;
+    gt += it.te - it.tb;  // K/V tiles of this entry (ring position shared with the TMA and MMA warps)
   }
 }
 
@@ -483,6 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   sh.tmem_base = reinterpret_cast<uint32_t*>(smem + T::OFF_MISC);
   sh.item = reinterpret_cast<int4*>(smem + T::OFF_MISC + 16);
   sh.abort = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 32);
+  sh.slot = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 36);
+  sh.order = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 40);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2 * (kKSlots + kVSlots); ++i) dev::mbar_init(&bars[i], 1);
@@ -564,6 +676,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.out = static_cast<__half*>(a.out);
   p.block_tables = a.block_tables;
   p.items = a.items;
+  p.items_slot = a.items_slot;
+  p.pf_sync = a.pf_sync;
+  p.pf_ml = a.pf_ml;
+  p.pf_o = a.pf_o;
   p.hdr = a.hdr;
   p.err = a.err;
   p.layer_row0_k = a.layer_row0_k;

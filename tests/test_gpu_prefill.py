@@ -70,3 +70,16 @@ def test_prefill_output_rows_untouched_outside_the_pass(cuda, built):
     assert torch.all(big[T:] == 7.0)
     for b in range(batch.num_seqs):
         assert_close(row_slice(batch, out, b), oracle_row(batch, 0, b), f"row {b}")
+
+
+def test_prefill_split_items_many_entries_per_cta(cuda, built):
+    """Chunks on long cached prefixes (more than 24 K/V tiles: split in two key ranges and merged) with more
+    work entries than SMs, so CTAs run several entries back to back; two layers reuse the merge slots."""
+    shape = synth.Shape(2, 12, 2, 128)
+    rows = [(3000, 512), (2500, 300), (4000, 256), (2200, 700), (17, 1), (5000, 40)]
+    cached, qls = zip(*rows)
+    batch = synth.custom_batch(shape, cached, qls, seed=31)
+    pool, ds, outs = run_batch(batch, [0, 1])
+    for layer in (0, 1):
+        for b in range(batch.num_seqs):
+            assert_close(row_slice(batch, outs[layer], b), oracle_row(batch, layer, b), f"layer {layer} row {b}")
