@@ -64,13 +64,60 @@ def algorithmic_bytes(batch: synth.StepBatch):
     return attn, append
 
 
-def measured_peak():
+FALLBACK_TENSOR_TFLOPS = 1900.0
+PREFILL_MIN_QLEN = 16  # rows with this many new tokens run on the tensor-core tile kernel
+
+
+def measured_peak(key: str = "hbm_gbs", fallback: float = FALLBACK_HBM_GBS):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
-            return float(json.load(f)["hbm_gbs"]), "measured"
+            return float(json.load(f)[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return fallback, "fallback"
+
+
+def prefill_flops(batch: synth.StepBatch) -> int:
+    """Per layer: 4 d Hq (causal query-key pairs) over the rows that take the tile kernel."""
+    s = batch.shape
+    pairs = 0
+    for c, q in zip(batch.context_lens.astype(np.int64), batch.q_lens.astype(np.int64)):
+        if q >= PREFILL_MIN_QLEN:
+            pairs += int(q * (c - q) + q * (q + 1) // 2)
+    return 4 * s.head_dim * s.num_q_heads * pairs
+
+
+def time_prefill_rows(batch: synth.StepBatch, reps: int = 20):
+    """Mean CUDA-event time of one attention call over only the batch's prefill rows (the tile kernel,
+    plus an empty decode launch), rotating over the layers; None if the batch has no such rows."""
+    rows = [b for b in range(batch.num_seqs) if batch.q_lens[b] >= PREFILL_MIN_QLEN]
+    if not rows:
+        return None
+    s = batch.shape
+    sub = synth.custom_batch(s, batch.cached_lens[rows], batch.q_lens[rows], seed=batch.seed,
+                             req_ids=batch.req_ids[rows])
+    layers = list(range(s.num_layers))
+    pool = workload.make_pool(sub)
+    workload.prefill_cache(pool, sub, layers)
+    ds = workload.upload(sub, pool)
+    qs, _, _ = workload.step_inputs(ds, layers)
+    outs = [torch.empty_like(q) for q in qs]
+    attn = workload.Attention(pool, ds)
+    attn.plan()
+    for i, layer in enumerate(layers):
+        attn.run(layer, qs[i], outs[i])
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(reps):
+        for i, layer in enumerate(layers):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            attn.run(layer, qs[i], outs[i])
+            b.record()
+            ev.append((a, b))
+    torch.cuda.synchronize()
+    assert pool.check() == 0
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
 def source_hash() -> str:
@@ -376,6 +423,8 @@ def run_pkv(args, rank, world, local):
     # ---- end to end through the public calls with host buffers ----
     e2e = run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_bytes)
 
+    pf_ms = time_prefill_rows(batch) if rank == 0 else None
+
     if rank != 0:
         return
     peak, peak_src = measured_peak()
@@ -405,6 +454,21 @@ def run_pkv(args, rank, world, local):
         "e2e": e2e,
         "clocks": clocks,
     }
+    if pf_ms is not None:
+        # a mixed pass: the prefill rows are tensor-bound, the decode rows HBM-bound (report both)
+        tpeak, tsrc = measured_peak("bf16_tflops", FALLBACK_TENSOR_TFLOPS)
+        flops = prefill_flops(batch)
+        decode = line["roofline"]
+        decode["kernel"] = "decode_kernel + prefill_kernel (whole attention call)"
+        line["roofline"] = {"bound": "tensor", "achieved": flops / (pf_ms * 1e-3) / 1e12, "peak": tpeak,
+                            "unit": "TFLOP/s", "frac": flops / (pf_ms * 1e-3) / 1e12 / tpeak, "traffic": None,
+                            "kernel": "prefill_kernel (tcgen05, prefill rows alone)", "flops_per_launch": flops,
+                            "avg_launch_ms": pf_ms, "peak_source": f"{tsrc} bf16 dense (fp16 runs at the same rate)"}
+        line["attention_call_roofline"] = decode
+        hbm_ms = step_bytes / (peak * 1e9) * 1e3
+        tensor_ms = flops * len(layers) / (tpeak * 1e12) * 1e3
+        line["lower_bounds_ms_per_step"] = {"hbm": hbm_ms, "tensor": tensor_ms, "sum": hbm_ms + tensor_ms,
+                                            "max": max(hbm_ms, tensor_ms), "measured": ms}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(batch)
     print(json.dumps(line), flush=True)
