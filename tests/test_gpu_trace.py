@@ -1,0 +1,66 @@
+"""Scheduler-driven passes on the GPU: the C++ scheduler's batches (256 lognormal-prompt requests, token
+budget 8,192) run through slot mapping, kv_append and attention on a persistent paged pool, as the pages'
+engine does one pass after another ("Continuous Batching Is Not a Bigger Batch", sections "What the
+scheduler does on one step" and "The allocator is the other half").  The 5,000-block pool preempts and
+recomputes; a re-prefilled request rewrites identical key/value bits, so its later rows still match the
+oracle.  Checked every pass: the device slot mapping against the scheduler's, the device error word, and
+sampled rows (decode rows and one bounded prefill row) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from continuous_batching_paged_ragged_gb300 import pkv, synth, workload
+from helpers_gpu import assert_close, oracle_row, row_slice
+
+pytestmark = pytest.mark.gpu
+
+SEED = 0
+LAYERS = [0, 1]
+
+
+def _step_batch(shape, num_blocks, st):
+    return synth.StepBatch(shape, num_blocks, st["req_ids"], st["q_lens"], st["context_lens"],
+                           np.ascontiguousarray(st["block_tables"]), np.zeros(0, dtype=np.int32), SEED, "trace")
+
+
+@pytest.mark.parametrize("num_blocks,cap,steps", [(20000, 256, 24), (5000, 256, 84), (20000, 64, 16)])
+def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps):
+    shape = synth.Shape(len(LAYERS), 12, 2, 128)
+    sched = pkv.Scheduler(cap, 8192, 16, num_blocks, free_order=synth.block_permutation(num_blocks, SEED))
+    for r in synth.trace_requests(SEED):
+        sched.add(r.req_id, r.prompt_len, r.max_output)
+    probe = synth.custom_batch(shape, [1], [1], seed=SEED, num_blocks=num_blocks)
+    pool = workload.make_pool(probe)
+    pool.cache_view().view(torch.int16).fill_(0x7E00)  # fp16 NaN wherever nothing was appended
+    rng = np.random.default_rng(7)
+    preempted, rechecked = set(), 0
+    for step in range(steps):
+        st = sched.step()
+        preempted.update(st["preempted"])
+        if len(st["req_ids"]) == 0:
+            break
+        batch = _step_batch(shape, num_blocks, st)
+        ds = workload.upload(batch, pool)
+        assert np.array_equal(ds.slot_mapping.cpu().numpy(), st["slot_mapping"]), f"step {step}: slot mapping"
+        qs, ks, vs = workload.step_inputs(ds, LAYERS)
+        outs = [torch.empty_like(q) for q in qs]
+        workload.run_pass(pool, ds, LAYERS, qs, ks, vs, outs)
+        torch.cuda.synchronize()
+        assert pool.check() == 0, f"step {step}: device error word"
+        ql, ctx = batch.q_lens, batch.context_lens
+        decode = np.nonzero(ql == 1)[0]
+        sample = list(rng.choice(decode, size=min(2, decode.size), replace=False)) if decode.size else []
+        chunk = [b for b in np.nonzero(ql > 1)[0] if int(ql[b]) * int(ctx[b]) <= 600_000]
+        if chunk:
+            sample.append(chunk[0])
+        back = [b for b in range(batch.num_seqs) if int(batch.req_ids[b]) in preempted]
+        if back:
+            sample.append(back[0])  # a request readmitted after preemption (its cache was recomputed)
+            rechecked += 1
+        for b in sample:
+            assert_close(row_slice(batch, outs[1], b), oracle_row(batch, 1, int(b)),
+                         f"step {step} row {b} (req {batch.req_ids[b]}, q_len {ql[b]}, ctx {ctx[b]})")
+    stats = sched.stats()
+    if num_blocks == 5000:
+        assert stats["preemptions"] > 0 and rechecked > 0, stats
+    sched.close()
