@@ -129,14 +129,14 @@ __device__ __forceinline__ void task_from_record(const DecodeParams& p, int4 rec
 }
 
 __device__ __forceinline__ int4 load_record(const DecodeParams& p, int idx, int n_tasks) {
-  return idx < n_tasks ? __ldg(p.tasks + idx) : make_int4(-1, 0, 0, 0);
+  return idx < n_tasks ? __ldcg(p.tasks + idx) : make_int4(-1, 0, 0, 0);
 }
 
 template <int NW>
 __device__ __forceinline__ int load_ids(const DecodeParams& p, const TaskMeta& m, int warp, int lane) {
   int id = 0;
   if (lane < m.nbw) {
-    id = __ldg(p.block_tables + (int64_t)m.row * p.max_blocks + m.s * p.split_blocks + warp + NW * lane);
+    id = __ldcg(p.block_tables + (int64_t)m.row * p.max_blocks + m.s * p.split_blocks + warp + NW * lane);
     if (id < 0 || id >= p.num_blocks) {
       dev::set_error(p.err, PKV_DEVERR_BLOCK_RANGE);
       id = 0;  // keep the copy in bounds; this token's output is flagged as invalid
@@ -169,7 +169,7 @@ struct Worker {
                     int warp_, int lane_)
       : p(p_), ring(ring_), bars(bars_), idx_ring(idx_ring_), warp(warp_), lane(lane_) {
     pol = dev::l2_policy_evict_first();
-    n_tasks = p.hdr->n_tasks;
+    n_tasks = __ldcg(&p.hdr->n_tasks);
     task_from_record<T::NW>(p, load_record(p, idx_ring[0], n_tasks), warp, cur);
     cur.ids = load_ids<T::NW>(p, cur, warp, lane);
   }
@@ -347,7 +347,15 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
   float* cm = reinterpret_cast<float*>(smem + T::OFF_CM);
   float* cl = reinterpret_cast<float*>(smem + T::OFF_CL);
   int* idx_ring = reinterpret_cast<int*>(smem + T::OFF_IDX);
+  // The first task's record and block ids are loaded before the dependency wait: the plan kernel that
+  // wrote the task list released its dependents only after its writes (and a fence), and block tables
+  // are final before the plan; they are read through L2, never a possibly stale L1 line.  The task
+  // counters, q and the cache (written by the append just before) are touched only after the wait.
   Worker<D, G> w(p, smem + warp * T::NR * T::RUN, all_bars + warp * T::NR, idx_ring, warp, lane);
+  dev::griddep_wait();
+  dev::griddep_launch_dependents();
+  // one CTA-uniform decision (a racing error-word update must not split the CTA)
+  if (__syncthreads_or(threadIdx.x == 0 && dev::pool_poisoned(p.err))) return;
   // Split completion (thread 0 only): after writing a split's partial the CTA counts it on the token's
   // counter, and the CTA that completes the count merges the token.  The count's result is examined only
   // at the end of the CTA's next task, so its round trip never stalls the stream.
@@ -547,11 +555,8 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     idx_ring[0] = blockIdx.x;
     idx_ring[1] = blockIdx.x + gridDim.x;
   }
-  dev::griddep_wait();
-  dev::griddep_launch_dependents();
-  // one CTA-uniform decision (a racing error-word update must not split the CTA)
-  const bool poisoned = __syncthreads_or(threadIdx.x == 0 && dev::pool_poisoned(p.err));
-  if (!poisoned) worker_loop<D, G>(p, smem, warp, lane);
+  __syncthreads();
+  worker_loop<D, G>(p, smem, warp, lane);  // waits for the previous kernel itself, after its first loads
   // the last CTA out resets the task counter for the next launch on this plan
   __syncthreads();
   if (threadIdx.x == 0) {
