@@ -287,9 +287,11 @@ def run_reference(args, rank, world):
 # ----------------------------------------------------------------------------------------------------
 
 class RawStep:
-    """The timed step with every pointer resolved up front: plan + per layer (append, attention)."""
+    """The timed step with every pointer resolved up front: plan + per layer append and attention, as one
+    pkv_attention_append call (fused=True) or pkv_append then pkv_attention."""
 
-    def __init__(self, pool, ds, attn, qs, ks, vs, outs, stream):
+    def __init__(self, pool, ds, attn, qs, ks, vs, outs, stream, fused=True):
+        self.fused = fused
         self.lib = pkv.load()
         self.pool = pool.handle
         self.ds = ds
@@ -328,11 +330,23 @@ class RawStep:
             raise pkv.PkvError(st, "pkv_attention", pkv.pkv_last_error())
         self.launches += self.lib.pkv_last_launch_count(self.pool)
 
+    def attention_append(self, i, layer):
+        d = self.ds
+        st = self.lib.pkv_attention_append(self.pool, layer, self.q[i], self.k[i], self.v[i], self.slots, self.bt,
+                                           d.max_blocks, self.ctx, self.qsl, d.num_seqs, d.num_tokens, self.o[i],
+                                           self.ws, self.ws_bytes, self.stream)
+        if st:
+            raise pkv.PkvError(st, "pkv_attention_append", pkv.pkv_last_error())
+        self.launches += self.lib.pkv_last_launch_count(self.pool)
+
     def __call__(self, layers):
         self.plan()
         for i, layer in enumerate(layers):
-            self.append(i, layer)
-            self.attention(i, layer)
+            if self.fused:
+                self.attention_append(i, layer)
+            else:
+                self.append(i, layer)
+                self.attention(i, layer)
 
 
 def run_pkv(args, rank, world, local):
@@ -352,7 +366,7 @@ def run_pkv(args, rank, world, local):
     attn = workload.Attention(pool, ds)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
-    step = RawStep(pool, ds, attn, qs, ks, vs, outs, sp)
+    step = RawStep(pool, ds, attn, qs, ks, vs, outs, sp, fused=not args.unfused)
     torch.cuda.synchronize()
     assert pool.check() == 0
 
@@ -360,7 +374,7 @@ def run_pkv(args, rank, world, local):
     graph = None
     if not args.eager:
         cap = torch.cuda.Stream(dev)
-        cstep = RawStep(pool, ds, attn, qs, ks, vs, outs, cap.cuda_stream)
+        cstep = RawStep(pool, ds, attn, qs, ks, vs, outs, cap.cuda_stream, fused=not args.unfused)
         cap.wait_stream(stream)
         with torch.cuda.stream(cap):
             for _ in range(3):
@@ -411,10 +425,14 @@ def run_pkv(args, rank, world, local):
     for _ in range(n_kernel_steps):
         step.plan()
         for i, layer in enumerate(layers):
-            step.append(i, layer)
+            if not step.fused:
+                step.append(i, layer)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            step.attention(i, layer)
+            if step.fused:
+                step.attention_append(i, layer)  # the decode kernel does the append too
+            else:
+                step.attention(i, layer)
             b.record(stream)
             kev.append((a, b))
     torch.cuda.synchronize()
@@ -428,7 +446,8 @@ def run_pkv(args, rank, world, local):
     if rank != 0:
         return
     peak, peak_src = measured_peak()
-    achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+    kernel_bytes = attn_bytes + (append_bytes if step.fused else 0)
+    achieved = kernel_bytes / (attn_ms * 1e-3) / 1e9
     sh = source_hash()
     value = step_bytes * world / (ms * 1e-3) / 1e9
     line = {
@@ -443,13 +462,15 @@ def run_pkv(args, rank, world, local):
                    "split_blocks": pool.cfg.split_blocks or 16,
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of K/V per step rotating over "
                          f"{s.num_layers} layer pools", "parallelism": f"replicas x{world}",
-                   "launch": "eager" if graph is None else "cuda_graph"},
+                   "launch": "eager" if graph is None else "cuda_graph",
+                   "layer_call": "pkv_append + pkv_attention" if args.unfused else "pkv_attention_append"},
         "pct_of_peak": 100.0 * value / world / peak,
         "ctx_tokens_per_s": ctx_tokens * world / (ms * 1e-3),
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": TRAFFIC.get(sh), "kernel": "decode_kernel (split-K decode, fused merge)",
-                     "per_launch_bytes": attn_bytes, "avg_launch_ms": attn_ms, "peak_source": peak_src,
+                     "traffic": TRAFFIC.get(sh),
+                     "kernel": "decode_kernel (split-K decode, fused merge" + (", fused append)" if step.fused else ")"),
+                     "per_launch_bytes": kernel_bytes, "avg_launch_ms": attn_ms, "peak_source": peak_src,
                      "source": sh},
         "e2e": e2e,
         "clocks": clocks,
@@ -489,7 +510,8 @@ def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_
     d_k = torch.stack(ks)
     d_v = torch.stack(vs)
     d_out = torch.stack(outs)
-    step = RawStep(pool, ds, attn, list(d_q), list(d_k), list(d_v), list(d_out), stream.cuda_stream)
+    step = RawStep(pool, ds, attn, list(d_q), list(d_k), list(d_v), list(d_out), stream.cuda_stream,
+                   fused=not args.unfused)
     h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_bt, h_ctx, h_qsl, h_slots))
     d2h = h_out.numel() * h_out.element_size()
 
@@ -530,6 +552,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     ap.add_argument("--eager", action="store_true", help="time the calls issued one by one, not a CUDA graph")
+    ap.add_argument("--unfused", action="store_true", help="pkv_append then pkv_attention per layer, not the "
+                    "fused pkv_attention_append")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

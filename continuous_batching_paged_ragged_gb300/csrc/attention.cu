@@ -86,6 +86,16 @@ struct DecodeParams {
   float2* part_ml;     // [num_tokens * num_kv_heads * max_splits][8 heads]
   int32_t* merge_cnt;  // [num_tokens * num_kv_heads] splits finished; zero between launches
   int32_t* err;
+  // Append fused into the attention (k_in != nullptr): keys and values of this pass's tokens are taken
+  // from k_in / v_in [T][Hkv][D] wherever a tile holds them, and the warp holding a token's own
+  // position writes that token into the cache at slots[t].
+  const __half* k_in;
+  const __half* v_in;
+  const int64_t* slots;
+  const int32_t* qsl;
+  __half* cache_k;     // this layer's K pool [num_blocks][Hkv][16][D]
+  __half* cache_v;
+  int64_t num_slots;
   int layer_row0_k;    // TMA row of (layer, K, block 0, head 0, slot 0)
   int layer_row0_v;    // TMA row of (layer, V, block 0, head 0, slot 0)
   int max_blocks;
@@ -113,6 +123,7 @@ struct TaskMeta {
   int t, g, s, row, ctx, nsplit;
   int nbw;  // blocks of the split dealt to this warp: blocks warp, warp + NW, ...
   int ids;  // lane j holds the physical id of this warp's block j (j < nbw <= 8)
+  int nst;  // fused append: the row's first position appended this pass (its token is t - (ctx-1 - nst))
 };
 
 template <int NW>
@@ -130,6 +141,13 @@ __device__ __forceinline__ void task_from_record(const DecodeParams& p, int4 rec
 
 __device__ __forceinline__ int4 load_record(const DecodeParams& p, int idx, int n_tasks) {
   return idx < n_tasks ? __ldcg(p.tasks + idx) : make_int4(-1, 0, 0, 0);
+}
+
+// First position of the row that this pass appends (fused append only): the row's first token sits at
+// position ctx - 1 - (t - query_start_loc[row]).
+__device__ __forceinline__ int load_nst(const DecodeParams& p, const TaskMeta& m) {
+  if (p.k_in == nullptr || m.t < 0) return 1 << 30;
+  return m.ctx - 1 - (m.t - __ldcg(p.qsl + m.row));
 }
 
 template <int NW>
@@ -172,6 +190,7 @@ struct Worker {
     n_tasks = __ldcg(&p.hdr->n_tasks);
     task_from_record<T::NW>(p, load_record(p, idx_ring[0], n_tasks), warp, cur);
     cur.ids = load_ids<T::NW>(p, cur, warp, lane);
+    cur.nst = load_nst(p, cur);
   }
 
   static __device__ __forceinline__ int runs(const TaskMeta& m) { return m.t >= 0 && m.nbw > 0 ? 1 + 2 * m.nbw : 0; }
@@ -187,6 +206,7 @@ struct Worker {
     if (nstage == 1) {
       task_from_record<T::NW>(p, nxt_rec, warp, nxt);
       nxt.ids = load_ids<T::NW>(p, nxt, warp, lane);
+      nxt.nst = load_nst(p, nxt);
       nstage = 2;
     }
   }
@@ -404,11 +424,43 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
       w.release_run();
 
       for (int j = 0; j < d.nbw && w.ok; ++j) {
-        const int ntok = min(kBS, d.ctx - (d.s * p.split_blocks + warp + T::NW * j) * kBS);
+        const int bpos = (d.s * p.split_blocks + warp + T::NW * j) * kBS;  // the block's first position
+        const int ntok = min(kBS, d.ctx - bpos);
+        // fused append: positions ov0 .. bpos + ntok - 1 of the block are this pass's tokens; their rows
+        // come from the inputs (the cache may not hold them yet), and the block holding the token's own
+        // position writes it into the cache
+        const int ov0 = max(bpos, d.nst), nov = bpos + ntok - ov0;
+        auto override_rows = [&](uint32_t base, const __half* src) {
+          for (int idx = lane; idx < nov * (D / 8); idx += 32) {
+            const int rr = ov0 - bpos + idx / (D / 8), cc = idx % (D / 8);
+            const int tk = d.t - (d.ctx - 1 - (bpos + rr));
+            const uint4 v = __ldcg(reinterpret_cast<const uint4*>(src + ((size_t)tk * p.num_kv_heads + d.g) * D) + cc);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(rr, cc)), "r"(v.x), "r"(v.y),
+                         "r"(v.z), "r"(v.w)
+                         : "memory");
+          }
+          __syncwarp();
+        };
+        if (nov > 0 && d.ctx - 1 < bpos + kBS) {
+          const int64_t slot = __ldcg(p.slots + d.t);
+          if (slot != -1) {
+            if (slot < 0 || slot >= p.num_slots) {
+              if (lane == 0) dev::set_error(p.err, PKV_DEVERR_SLOT_RANGE);
+            } else {
+              const size_t src = ((size_t)d.t * p.num_kv_heads + d.g) * D;
+              const size_t dst = (((size_t)(slot >> 4) * p.num_kv_heads + d.g) * kBS + (slot & 15)) * D;
+              for (int cc = lane; cc < D / 8; cc += 32) {
+                reinterpret_cast<uint4*>(p.cache_k + dst)[cc] = __ldcg(reinterpret_cast<const uint4*>(p.k_in + src) + cc);
+                reinterpret_cast<uint4*>(p.cache_v + dst)[cc] = __ldcg(reinterpret_cast<const uint4*>(p.v_in + src) + cc);
+              }
+            }
+          }
+        }
         // ---- S^T[16 keys x 8 heads] = K Q^T on the tensor cores ----
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
         {
           const uint32_t ks_base = w.wait_run();
+          if (nov > 0) override_rows(ks_base, p.k_in);
           const int kr = (lane & 7) + ((lane >> 3) & 1) * 8;  // key row this lane addresses for ldmatrix
 #pragma unroll
           for (int ks = 0; ks < T::KS; ++ks) {
@@ -416,6 +468,7 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
             dev::ldsm_x4(ks_base + swz(kr, 2 * ks + (lane >> 4)), a);
             dev::mma_16816(sc, a, qb[ks][0], qb[ks][1]);
           }
+          if (nov > 0) dev::fence_proxy_async_smem();  // the override precedes the slot's next TMA write
           w.release_run();
         }
         w.prefetch_next(false);  // one dependent metadata load of the next task per block, hidden by compute
@@ -459,6 +512,7 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
             }
             __syncwarp();
           }
+          if (nov > 0) override_rows(vs_base, p.v_in);
           const int mat = lane >> 3;                      // ldmatrix matrix this lane addresses
           const int vr = (lane & 7) + ((mat >> 1) << 3);  // its key row
 #pragma unroll
@@ -467,7 +521,7 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
             dev::ldsm_x4_t(vs_base + swz(vr, 2 * mt + (mat & 1)), a);
             dev::mma_16816(o[mt], a, pb0, pb1);
           }
-          if (ntok < kBS) dev::fence_proxy_async_smem();  // the zero-fill precedes the slot's next TMA write
+          if (ntok < kBS || nov > 0) dev::fence_proxy_async_smem();  // generic writes precede the next TMA write
           w.release_run();
         }
       }
@@ -962,10 +1016,19 @@ static cudaError_t launch_plan(pkv_pool* pool, char* ws, const WsLayout& w, cons
   return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p);
 }
 
+// Inputs of an append fused into the decode launch (k == nullptr: not fused).
+struct FusedAppend {
+  const void* k = nullptr;
+  const void* v = nullptr;
+  const int64_t* slots = nullptr;
+  const int32_t* qsl = nullptr;
+};
+
 // decode (+ merge of very long tokens) and prefill tiles for one layer on a planned workspace
 static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, const int32_t* block_tables,
                                    int max_blocks, int num_seqs, int num_tokens, void* out, char* ws,
-                                   const WsLayout& w, cudaStream_t s, int* launches) {
+                                   const WsLayout& w, cudaStream_t s, int* launches,
+                                   const FusedAppend& fa = FusedAppend()) {
   const pkv_config& c = pool->cfg;
   DecodeParams p;
   p.kv_map = pool->kv_map;
@@ -980,6 +1043,13 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
   p.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
   p.merge_cnt = reinterpret_cast<int32_t*>(ws + w.merge_cnt);
   p.err = pool->dev_error;
+  p.k_in = static_cast<const __half*>(fa.k);
+  p.v_in = static_cast<const __half*>(fa.v);
+  p.slots = fa.slots;
+  p.qsl = fa.qsl;
+  p.cache_k = static_cast<__half*>(pkv_pool_layer_ptr(pool, layer, 0));
+  p.cache_v = static_cast<__half*>(pkv_pool_layer_ptr(pool, layer, 1));
+  p.num_slots = (int64_t)c.num_blocks * c.block_size;
   const int rows_per_pool = c.num_blocks * c.num_kv_heads * c.block_size;
   p.layer_row0_k = (layer * 2) * rows_per_pool;
   p.layer_row0_v = (layer * 2 + 1) * rows_per_pool;
@@ -1130,6 +1200,55 @@ extern "C" pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q
   int launches = 0;
   st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_seqs, num_tokens, out,
                         static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches);
+  pool->last_launches = launches;
+  return st;
+}
+
+// ---------------------------------------------------------------------------------------------------
+// kv_append + attention of one layer as one call.  When no row of the pass can take the prefill path
+// (every row has fewer than kPrefillMinQlen new tokens), the append runs inside the decode launch: tiles
+// take this pass's keys and values from the inputs and each token is written to the cache by the warp
+// whose block holds its position, so the attention waits for no separate append.  Otherwise it is the
+// append kernel followed by the attention.
+// ---------------------------------------------------------------------------------------------------
+extern "C" pkv_status pkv_attention_append(pkv_pool* pool, int32_t layer, const void* q, const void* k,
+                                           const void* v, const int64_t* slot_mapping, const int32_t* block_tables,
+                                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                           const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
+                                           void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  pkv_status st = check_common(pool, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq);
+  if (st == PKV_OK) st = check_workspace(pool, workspace, workspace_bytes, num_seqs, num_tokens, max_blocks_per_seq);
+  if (st != PKV_OK) return st;
+  pool->last_launches = 0;
+  if (layer < 0 || layer >= pool->cfg.num_layers) return fail(PKV_ERR_OUT_OF_RANGE, "layer out of range");
+  if (num_tokens == 0) return PKV_OK;
+  st = check_io(q, out, block_tables);
+  if (st != PKV_OK) return st;
+  if (!k || !v || !slot_mapping) return fail(PKV_ERR_INVALID_ARG, "k, v and slot_mapping must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  const PlanKey& pk = pool->plan;
+  if (pk.workspace != workspace || pk.context_lens != context_lens || pk.query_start_loc != query_start_loc ||
+      pk.num_seqs != num_seqs || pk.num_tokens != num_tokens || pk.max_blocks_per_seq != max_blocks_per_seq)
+    return fail(PKV_ERR_INVALID_ARG, "no matching plan: call pkv_attention_plan for this workspace and metadata");
+  const WsLayout w = ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks_per_seq);
+  int launches = 0;
+  if (w.max_items > 0) {  // prefill rows possible: they read the cache, so append first
+    st = pkv_append(pool, layer, k, v, slot_mapping, num_tokens, stream);
+    if (st != PKV_OK) return st;
+    launches = pool->last_launches;
+    st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_seqs, num_tokens, out,
+                          static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches);
+  } else {
+    FusedAppend fa;
+    fa.k = k;
+    fa.v = v;
+    fa.slots = slot_mapping;
+    fa.qsl = query_start_loc;
+    st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_seqs, num_tokens, out,
+                          static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches, fa);
+  }
   pool->last_launches = launches;
   return st;
 }

@@ -72,6 +72,8 @@ SIGNATURES = {
     "pkv_attention_plan": (ctypes.c_int, [_p, _p, _p, _i32, _i32, _i32, _p, _sz, _p]),
     "pkv_attention": (ctypes.c_int, [_p, _i32, _p, _p, _i32, _p, _p, _i32, _i32, _p, _p, _sz, _p]),
     "pkv_attention_noalloc": (ctypes.c_int, [_p, _i32, _p, _p, _i32, _p, _p, _i32, _i32, _p, _p]),
+    "pkv_attention_append": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _p, _p, _sz,
+                                            _p]),
     "pkv_last_launch_count": (_i32, [_p]),
     "pkv_last_error": (ctypes.c_char_p, []),
     "pkv_sched_create": (ctypes.c_int, [ctypes.POINTER(pkv_sched_config), _p, ctypes.POINTER(_p)]),
@@ -183,6 +185,15 @@ def pkv_attention(pool: int, layer: int, q, block_tables, max_blocks_per_seq: in
     _check(load().pkv_attention(pool, layer, _ptr(q), _ptr(block_tables), max_blocks_per_seq, _ptr(context_lens),
                                 _ptr(query_start_loc), num_seqs, num_tokens, _ptr(out), _ptr(workspace),
                                 workspace_bytes, _stream(stream)), "pkv_attention")
+
+
+def pkv_attention_append(pool: int, layer: int, q, k, v, slot_mapping, block_tables, max_blocks_per_seq: int,
+                         context_lens, query_start_loc, num_seqs: int, num_tokens: int, out, workspace,
+                         workspace_bytes: int, stream=None) -> None:
+    _check(load().pkv_attention_append(pool, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(block_tables),
+                                       max_blocks_per_seq, _ptr(context_lens), _ptr(query_start_loc), num_seqs,
+                                       num_tokens, _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "pkv_attention_append")
 
 
 def pkv_attention_noalloc(pool: int, layer: int, q, block_tables, max_blocks_per_seq: int, context_lens,

@@ -125,13 +125,24 @@ class Attention:
         pkv.pkv_attention(self.pool.handle, layer, q, d.block_tables, d.max_blocks, d.context_lens,
                           d.query_start_loc, d.num_seqs, d.num_tokens, out, self.workspace, self.ws_bytes, stream)
 
+    def run_append(self, layer: int, q, k, v, out, stream=None):
+        d = self.ds
+        pkv.pkv_attention_append(self.pool.handle, layer, q, k, v, d.slot_mapping, d.block_tables, d.max_blocks,
+                                 d.context_lens, d.query_start_loc, d.num_seqs, d.num_tokens, out, self.workspace,
+                                 self.ws_bytes, stream)
 
-def run_pass(pool: pkv.Pool, ds: DeviceStep, layers: List[int], qs, ks, vs, outs, attn: Optional[Attention] = None):
-    """One forward pass's hot path: per layer, append this pass's K/V, then attention."""
+
+def run_pass(pool: pkv.Pool, ds: DeviceStep, layers: List[int], qs, ks, vs, outs, attn: Optional[Attention] = None,
+             fused: bool = False):
+    """One forward pass's hot path: per layer, append this pass's K/V, then attention (fused: one
+    pkv_attention_append call per layer)."""
     if attn is None:
         attn = Attention(pool, ds)
     attn.plan()
     for i, layer in enumerate(layers):
-        pkv.pkv_append(pool.handle, layer, ks[i], vs[i], ds.slot_mapping, ds.num_tokens)
-        attn.run(layer, qs[i], outs[i])
+        if fused:
+            attn.run_append(layer, qs[i], ks[i], vs[i], outs[i])
+        else:
+            pkv.pkv_append(pool.handle, layer, ks[i], vs[i], ds.slot_mapping, ds.num_tokens)
+            attn.run(layer, qs[i], outs[i])
     return attn

@@ -173,6 +173,24 @@ pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q, const int
                          const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens, void* out,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* kv_append and attention of one layer in one call: the same result -- cache contents and output --
+ * as pkv_append(pool, layer, k, v, slot_mapping, num_tokens) followed by pkv_attention(...) with the
+ * other arguments, under the same plan.  When no row of the pass can take the prefill path (every row
+ * has fewer than 16 new tokens; the host checks num_tokens - num_seqs < 15), the append runs inside
+ * the decode launch: tiles take this pass's keys and values from k / v directly, and each token is
+ * written to the cache by the warp whose block holds its position, so no separate append precedes the
+ * attention.  Otherwise this is the append launch followed by the attention launches.  Tokens of rows
+ * whose metadata is rejected (PKV_DEVERR_ROW_META) are not appended on the fused path.
+ *
+ * k, v             fp16 [num_tokens][num_kv_heads][head_dim]   device, 16-byte aligned
+ * slot_mapping     int64 [num_tokens]                          device (-1: skip the token)
+ * (everything else as pkv_attention) */
+pkv_status pkv_attention_append(pkv_pool* pool, int32_t layer, const void* q, const void* k, const void* v,
+                                const int64_t* slot_mapping, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, const int32_t* query_start_loc, int32_t num_seqs,
+                                int32_t num_tokens, void* out, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
 /* Allocation-free attention.  The pages have no counterpart to this call; it exists for callers that
  * cannot give the library a workspace -- an engine whose device memory is already carved up by its
  * own allocator, or code that must not call cudaMalloc (a device-wide synchronisation) mid-pass.
