@@ -96,6 +96,10 @@ struct DecodeParams {
   __half* cache_k;     // this layer's K pool [num_blocks][Hkv][16][D]
   __half* cache_v;
   int64_t num_slots;
+  // Launched right behind the prefill kernel of the same pass: its inputs were final once that kernel
+  // passed its own dependency wait, so the decode runs in the prefill's tail (on SMs the prefill has left)
+  // and waits for it only at its end, so that whatever follows sees both complete.
+  int late_wait;
   int layer_row0_k;    // TMA row of (layer, K, block 0, head 0, slot 0)
   int layer_row0_v;    // TMA row of (layer, V, block 0, head 0, slot 0)
   int max_blocks;
@@ -372,7 +376,7 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
   // are final before the plan; they are read through L2, never a possibly stale L1 line.  The task
   // counters, q and the cache (written by the append just before) are touched only after the wait.
   Worker<D, G> w(p, smem + warp * T::NR * T::RUN, all_bars + warp * T::NR, idx_ring, warp, lane);
-  dev::griddep_wait();
+  if (!p.late_wait) dev::griddep_wait();
   dev::griddep_launch_dependents();
   // one CTA-uniform decision (a racing error-word update must not split the CTA)
   if (__syncthreads_or(threadIdx.x == 0 && dev::pool_poisoned(p.err))) return;
@@ -621,6 +625,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
       __threadfence();
     }
   }
+  if (p.late_wait) dev::griddep_wait();  // complete only after the prefill kernel ahead of it
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -1061,28 +1066,10 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
   p.max_splits = w.max_splits;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
   const int group = c.num_q_heads / c.num_kv_heads;
+  // Prefill rows exist only if some row has at least prefill_min_qlen new tokens.  Their tile kernel goes
+  // first; the decode kernel follows in its tail (late_wait).
+  p.late_wait = 0;
   cudaError_t e;
-  switch (c.head_dim) {
-    case 64: e = launch_decode_g<64>(group, p, pool->num_sms, w.max_tasks, s); break;
-    case 128: e = launch_decode_g<128>(group, p, pool->num_sms, w.max_tasks, s); break;
-    case 256: e = launch_decode_g<256>(group, p, pool->num_sms, w.max_tasks, s); break;
-    default: return fail(PKV_ERR_UNSUPPORTED, "head_dim");
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  *launches += 1;
-  if (w.max_splits > kFusedMergeSplits) {
-    MergeParams m{p.part_o, p.part_ml, p.tok_ctx, p.out, c.num_q_heads, c.num_kv_heads, group, c.split_blocks,
-                  w.max_splits};
-    const dim3 grid(num_tokens, c.num_kv_heads, (kHeadsTile * c.head_dim) / 64);
-    switch (c.head_dim) {
-      case 64: e = launch_pdl(merge_kernel<64, 4>, grid, dim3(256), 0, s, m); break;
-      case 128: e = launch_pdl(merge_kernel<128, 4>, grid, dim3(256), 0, s, m); break;
-      default: e = launch_pdl(merge_kernel<256, 4>, grid, dim3(256), 0, s, m); break;
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-    *launches += 1;
-  }
-  // prefill rows exist only if some row has at least prefill_min_qlen new tokens
   if (w.prefill_min_qlen > 0 && num_tokens - num_seqs >= w.prefill_min_qlen - 1) {
     PrefillArgs a;
     a.kv_map = &pool->kv_map;
@@ -1107,6 +1094,27 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
     a.max_items = 2 * w.max_items;
     e = launch_prefill(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    *launches += 1;
+    p.late_wait = 1;
+  }
+  switch (c.head_dim) {
+    case 64: e = launch_decode_g<64>(group, p, pool->num_sms, w.max_tasks, s); break;
+    case 128: e = launch_decode_g<128>(group, p, pool->num_sms, w.max_tasks, s); break;
+    case 256: e = launch_decode_g<256>(group, p, pool->num_sms, w.max_tasks, s); break;
+    default: return fail(PKV_ERR_UNSUPPORTED, "head_dim");
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  *launches += 1;
+  if (w.max_splits > kFusedMergeSplits) {
+    MergeParams m{p.part_o, p.part_ml, p.tok_ctx, p.out, c.num_q_heads, c.num_kv_heads, group, c.split_blocks,
+                  w.max_splits};
+    const dim3 grid(num_tokens, c.num_kv_heads, (kHeadsTile * c.head_dim) / 64);
+    switch (c.head_dim) {
+      case 64: e = launch_pdl(merge_kernel<64, 4>, grid, dim3(256), 0, s, m); break;
+      case 128: e = launch_pdl(merge_kernel<128, 4>, grid, dim3(256), 0, s, m); break;
+      default: e = launch_pdl(merge_kernel<256, 4>, grid, dim3(256), 0, s, m); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
     *launches += 1;
   }
   return PKV_OK;
