@@ -64,3 +64,39 @@ def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps):
     if num_blocks == 5000:
         assert stats["preemptions"] > 0 and rechecked > 0, stats
     sched.close()
+
+
+@pytest.mark.parametrize("num_blocks,cap", [(20000, 256), (20000, 64), (5000, 256)])
+def test_scheduler_trace_to_exhaustion(cuda, built, num_blocks, cap):
+    """Every pass of the trace until the scheduler is done, one layer: slot mapping and device error word
+    checked every pass, one row against the oracle every 25th pass and on the last."""
+    shape = synth.Shape(1, 12, 2, 128)
+    sched = pkv.Scheduler(cap, 8192, 16, num_blocks, free_order=synth.block_permutation(num_blocks, SEED))
+    for r in synth.trace_requests(SEED):
+        sched.add(r.req_id, r.prompt_len, r.max_output)
+    probe = synth.custom_batch(shape, [1], [1], seed=SEED, num_blocks=num_blocks)
+    pool = workload.make_pool(probe)
+    pool.cache_view().view(torch.int16).fill_(0x7E00)
+    step, tokens = 0, 0
+    while not sched.done():
+        st = sched.step()
+        assert len(st["req_ids"]) > 0, f"step {step}: the scheduler made no progress"
+        batch = _step_batch(shape, num_blocks, st)
+        ds = workload.upload(batch, pool)
+        assert np.array_equal(ds.slot_mapping.cpu().numpy(), st["slot_mapping"]), f"step {step}: slot mapping"
+        qs, ks, vs = workload.step_inputs(ds, [0])
+        outs = [torch.empty_like(qs[0])]
+        workload.run_pass(pool, ds, [0], qs, ks, vs, outs, fused=True)
+        tokens += batch.num_tokens
+        if step % 25 == 0 or sched.done():
+            torch.cuda.synchronize()
+            assert pool.check() == 0, f"step {step}: device error word"
+            b = int(np.argmin(batch.q_lens.astype(np.int64) * batch.context_lens))  # the cheapest row to check
+            assert_close(row_slice(batch, outs[0], b), oracle_row(batch, 0, b), f"step {step} row {b}")
+        step += 1
+    torch.cuda.synchronize()
+    assert pool.check() == 0
+    stats = sched.stats()
+    assert stats["steps"] == step and stats["running"] == 0 and stats["waiting"] == 0
+    assert tokens == stats["tokens_scheduled"]
+    sched.close()
