@@ -41,35 +41,63 @@ namespace pkv {
 constexpr int kFusedMergeSplits = 32;  // tokens with up to this many splits are merged inside the decode
 constexpr int kMaxSplitBlocks = 32;   // upper bound on split_blocks (a split's block ids fit one warp)
 
-// Ring slots per warp: runs (a block's K or V for one KV head, or a task's q) in flight.
+// Ring slots per streaming warp: runs (a block's K or V for one KV head, or a task's q) in flight; fewer
+// where the shared memory of two CTAs per SM does not hold them.
 #ifndef PKV_DECODE_RING
-#define PKV_DECODE_RING(D) ((D) == 256 ? 2 : ((D) == 128 ? 3 : 5))
+#define PKV_DECODE_RING(D) ((D) == 256 ? 2 : ((D) == 128 ? 5 : 8))
 #endif
 
 constexpr int kSmemPerSM = 228 * 1024;  // shared memory of one SM
 constexpr int kSmemReservedPerCTA = 1024;
+constexpr int kStaticTasks = 2;         // tasks blockIdx.x + j * gridDim.x (j < 2) are a CTA's without a counter
+
+// One task as the scheduler warp hands it to the streaming warps and the combiner warp (shared memory).
+struct TaskEntry {
+  int4 rec;  // {token (-1: no more tasks), kv head | split << 8, row, causal context}
+  int nst;   // the row's first position appended this pass
+  int nb;    // blocks in the split
+  int rot;   // block i of the split goes to streaming warp (i + rot) % 4 (a function of the row alone)
+  int pad;
+  int ids[kMaxSplitBlocks];  // the split's physical block ids
+};
 
 template <int D, int G>
 struct DecodeTraits {
-  static constexpr int NW = 4;                     // warps per CTA; block i of a task goes to warp i % NW
-  static constexpr int NTHREADS = NW * 32;
+  static constexpr int NW = 4;                     // streaming warps; then the combiner and the scheduler
+  static constexpr int NTHREADS = (NW + 2) * 32;
   static constexpr int RUN = kBS * D * 2;          // one (block, KV head) run of K or V = D/64 TMA boxes
   static constexpr int BOXES = D / 64;
-  static constexpr int NR = PKV_DECODE_RING(D);    // ring slots (runs in flight) per warp
   static constexpr int KS = D / 16;                // MMA k-steps over the head dimension (scores)
   static constexpr int MT = D / 16;                // MMA m-tiles over the head dimension (values)
-  static constexpr int OV = MT * 4;                // fp32 output values per lane
-  static constexpr int OFF_BAR = NW * NR * RUN;    // [NW][NR] run barriers after the rings
-  static constexpr int OFF_CO = OFF_BAR + NW * NR * 8;         // combine: [NW][OV][32 lanes] fp32 o
-  static constexpr int OFF_CM = OFF_CO + NW * OV * 32 * 4;     // combine: [NW][8 heads] running max
-  static constexpr int OFF_CL = OFF_CM + NW * kHeadsTile * 4;  // combine: [NW][8 heads] running sum
-  static constexpr int OFF_IDX = OFF_CL + NW * kHeadsTile * 4; // [4] task indices, merge target, its splits
-  static constexpr int SMEM = OFF_IDX + 32 + 1024;  // + slack to align the rings to 1024 bytes
+  static constexpr int OV = MT * 4;                // fp32 output values per lane (8-head fragment)
+  static constexpr int LG = (G + 1) / 2;           // lanes l with (l & 3) < LG hold real heads
+  static constexpr int SHL = 8 * LG;               // such lanes
+  static constexpr int QD = 3;                     // task queue depth
+  static constexpr int MS = D >= 256 ? 2 : 4;      // split partials a merge stages per round
+  // everything but the rings: shares, staging, merge staging, queue, barriers, flag, alignment slack
+  static constexpr int REST = NW * OV * SHL * 4 + NW * kHeadsTile * 8 + G * D * 4 + MS * (G * D * 4 + 64) +
+                              QD * (int)sizeof(TaskEntry) + (12 * NW + 2 * QD + 1) * 8 + 16 + 1024;
+  static constexpr int NR_FIT = (kSmemPerSM / 2 - kSmemReservedPerCTA - REST) / (NW * RUN);
+  static constexpr int NR = PKV_DECODE_RING(D) < NR_FIT ? PKV_DECODE_RING(D) : (NR_FIT < 2 ? 2 : NR_FIT);
+  static constexpr int OFF_SHARE = NW * NR * RUN;                    // [NW][OV][SHL] fp32 o shares
+  static constexpr int OFF_SML = OFF_SHARE + NW * OV * SHL * 4;      // [NW][8] float2 (m, l) shares
+  static constexpr int OFF_STG = OFF_SML + NW * kHeadsTile * 8;      // combiner staging [G][D] fp32
+  static constexpr int OFF_MO = OFF_STG + G * D * 4;                 // merge staging: [MS][G][D] fp32 o
+  static constexpr int OFF_MML = OFF_MO + MS * G * D * 4;            // merge staging: [MS][8] float2 (m, l)
+  static constexpr int OFF_Q = OFF_MML + MS * 64;                    // [QD] TaskEntry
+  static constexpr int OFF_BAR = OFF_Q + QD * (int)sizeof(TaskEntry);
+  // barriers: ring [NW][NR], share_full [NW], share_empty [NW], queue full [QD], queue empty [QD], merge
+  static constexpr int NBARS = NW * NR + 2 * NW + 2 * QD + 1;
+  static constexpr int OFF_FLAG = OFF_BAR + NBARS * 8;               // the CTA's abort flag
+  static constexpr int SMEM = OFF_FLAG + 16 + 1024;                  // + slack to align the rings to 1024 bytes
   static constexpr int FIT = kSmemPerSM / (SMEM + kSmemReservedPerCTA);
-  static constexpr int MINB = FIT < 4 ? FIT : 4;   // CTAs per SM (shared memory bound)
+  static constexpr int MINB = FIT < 3 ? FIT : 3;   // CTAs per SM (shared memory bound)
   static_assert(D % 64 == 0 && G >= 1 && G <= kHeadsTile, "shape");
   static_assert(RUN % 1024 == 0, "swizzled boxes need 1024-byte aligned slots");
   static_assert(8 * D * 2 <= RUN && KS % 2 == 0, "a task's q (8 rows) fits one slot");
+  static_assert(OFF_Q % 16 == 0 && OFF_BAR % 8 == 0 && OFF_STG % 16 == 0 && OFF_MO % 16 == 0 && OFF_MML % 16 == 0,
+                "alignment");
+  static_assert(NR <= PKV_DECODE_RING(D) && SMEM <= OFF_SHARE + REST + 16 * NW + 64, "shared-memory budget");
   static_assert(MINB >= 1, "shared memory");
 };
 
@@ -77,8 +105,7 @@ struct DecodeParams {
   CUtensorMap kv_map;  // the pool as TMA rows of head_dim values (64-byte aligned: first member)
   const __half* q;
   const int32_t* block_tables;
-  const int32_t* tok_row;
-  const int32_t* tok_ctx;
+  const int32_t* qsl;  // query_start_loc
   const int4* tasks;   // {token, kv head | split << 8, row, causal context}
   WsHeader* hdr;
   __half* out;
@@ -92,7 +119,6 @@ struct DecodeParams {
   const __half* k_in;
   const __half* v_in;
   const int64_t* slots;
-  const int32_t* qsl;
   __half* cache_k;     // this layer's K pool [num_blocks][Hkv][16][D]
   __half* cache_v;
   int64_t num_slots;
@@ -108,6 +134,7 @@ struct DecodeParams {
   int num_blocks;
   int split_blocks;
   int max_splits;
+  int max_tasks;     // entries of the task list (loads stay below it; n_tasks of them are this pass's)
   float scale_log2;  // log2(e) / sqrt(head_dim)
 };
 
@@ -117,123 +144,152 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// ---------------------------------------------------------------------------------------------------
-// Per-warp stream.  Measured on this access pattern (scattered 4 KB runs): one issuing thread per CTA
-// tops out near 6 GB/s whatever the ring depth, while 12-16 issuing warps per SM reach 5.6-6 TB/s -- so
-// every warp streams its own runs.  The next task's metadata loads overlap the current task's compute,
-// and the next task's first runs enter the ring before the current task ends.
-// ---------------------------------------------------------------------------------------------------
-struct TaskMeta {
-  int t, g, s, row, ctx, nsplit;
-  int nbw;  // blocks of the split dealt to this warp: blocks warp, warp + NW, ...
-  int ids;  // lane j holds the physical id of this warp's block j (j < nbw <= 8)
-  int nst;  // fused append: the row's first position appended this pass (its token is t - (ctx-1 - nst))
-};
-
-template <int NW>
-__device__ __forceinline__ void task_from_record(const DecodeParams& p, int4 rec, int warp, TaskMeta& m) {
-  m.t = rec.x;
-  m.g = rec.y & 0xFF;
-  m.s = rec.y >> 8;
-  m.row = rec.z;
-  m.ctx = rec.w;
-  const int nblk = (m.ctx + kBS - 1) / kBS;
-  const int nb = m.t >= 0 ? min(p.split_blocks, nblk - m.s * p.split_blocks) : 0;
-  m.nbw = nb > warp ? (nb - warp + NW - 1) / NW : 0;
-  m.nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
-}
-
-__device__ __forceinline__ int4 load_record(const DecodeParams& p, int idx, int n_tasks) {
-  return idx < n_tasks ? __ldcg(p.tasks + idx) : make_int4(-1, 0, 0, 0);
-}
-
-// First position of the row that this pass appends (fused append only): the row's first token sits at
-// position ctx - 1 - (t - query_start_loc[row]).
-__device__ __forceinline__ int load_nst(const DecodeParams& p, const TaskMeta& m) {
-  if (p.k_in == nullptr || m.t < 0) return 1 << 30;
-  return m.ctx - 1 - (m.t - __ldcg(p.qsl + m.row));
-}
-
-template <int NW>
-__device__ __forceinline__ int load_ids(const DecodeParams& p, const TaskMeta& m, int warp, int lane) {
-  int id = 0;
-  if (lane < m.nbw) {
-    id = __ldcg(p.block_tables + (int64_t)m.row * p.max_blocks + m.s * p.split_blocks + warp + NW * lane);
-    if (id < 0 || id >= p.num_blocks) {
-      dev::set_error(p.err, PKV_DEVERR_BLOCK_RANGE);
-      id = 0;  // keep the copy in bounds; this token's output is flagged as invalid
+// Wait for phase `parity` of `bar`.  Gives up (false) as soon as another warp of the CTA has given up (the
+// abort flag), or after more than 2^16 polls and ~1 s of %globaltimer time; then it records
+// PKV_DEVERR_WAIT_TIMEOUT and raises the abort flag, so that every warp of the CTA unwinds.
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* err) {
+  if (dev::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = dev::globaltimer_ns();
+  for (uint32_t polls = 1;; ++polls) {
+    if (dev::mbar_try_wait(bar, parity)) return true;
+    if ((polls & 31u) == 0) {
+      if (*abort) return false;
+      if (polls > (1u << 16) && (int64_t)(dev::globaltimer_ns() - t0) > 1000000000ll) {
+        dev::set_error(err, PKV_DEVERR_WAIT_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
     }
   }
-  return id;
 }
 
+// Shared-memory map of one decode CTA.
 template <int D, int G>
-struct Worker {
+struct DecodeSmem {
+  using T = DecodeTraits<D, G>;
+  unsigned char* ring;  // [NW][NR] slots of RUN bytes
+  float* sh_o;          // [NW][OV][SHL]
+  float2* sh_ml;        // [NW][8]
+  float* stg;           // [G][D] fp32 (or [G][D] fp16 for a final output)
+  float* mo;            // [MS][G][D] merge staging
+  float2* mml;          // [MS][8]
+  TaskEntry* queue;     // [QD]
+  uint64_t* ring_bar;   // [NW][NR]
+  uint64_t* share_full;
+  uint64_t* share_empty;
+  uint64_t* qfull;
+  uint64_t* qempty;
+  uint64_t* merge_bar;
+  volatile int* abort;
+  __device__ explicit DecodeSmem(unsigned char* s) {
+    ring = s;
+    sh_o = reinterpret_cast<float*>(s + T::OFF_SHARE);
+    sh_ml = reinterpret_cast<float2*>(s + T::OFF_SML);
+    stg = reinterpret_cast<float*>(s + T::OFF_STG);
+    mo = reinterpret_cast<float*>(s + T::OFF_MO);
+    mml = reinterpret_cast<float2*>(s + T::OFF_MML);
+    queue = reinterpret_cast<TaskEntry*>(s + T::OFF_Q);
+    ring_bar = reinterpret_cast<uint64_t*>(s + T::OFF_BAR);
+    share_full = ring_bar + T::NW * T::NR;
+    share_empty = share_full + T::NW;
+    qfull = share_empty + T::NW;
+    qempty = qfull + T::QD;
+    merge_bar = qempty + T::QD;
+    abort = reinterpret_cast<volatile int*>(s + T::OFF_FLAG);
+  }
+};
+
+// A task as a streaming warp sees it.
+struct TaskView {
+  int t, g, s, row, ctx, nsplit, nst;
+  int nbw;          // blocks of the split dealt to this warp: task-local blocks bw, bw + 4, ...
+  int bw;
+  const int* ids;   // shared memory: the split's block ids
+};
+
+__device__ __forceinline__ int warp_blocks(int nb, int bw) { return nb > bw ? (nb - bw + 3) / 4 : 0; }
+
+// ---------------------------------------------------------------------------------------------------
+// Streaming warp: takes the CTA's tasks in queue order, streams the K and V runs of its share of each
+// task's blocks through its own ring with TMA, and computes the group contraction on the tensor cores.
+// At the end of a task it leaves its unnormalised (m, l, o) in its share slot for the combiner warp and
+// goes straight on: the next task's first runs are already in its ring.  Measured on this access pattern
+// (scattered 4 KB runs): one issuing thread per CTA cannot keep HBM busy, many independent issuers per
+// SM can -- hence every streaming warp issues its own copies.
+// ---------------------------------------------------------------------------------------------------
+template <int D, int G>
+struct Streamer {
   using T = DecodeTraits<D, G>;
   const DecodeParams& p;
+  const DecodeSmem<D, G>& sm;
   unsigned char* ring;   // this warp's NR slots (1024-byte aligned)
   uint64_t* bars;        // this warp's NR barriers
-  const volatile int* idx_ring;  // the CTA's task indices: task k at [k % 4]
   uint64_t pol;
   int warp, lane;
-  int n_tasks;
   int k = 0;             // the CTA's sequence number of the current task
   int issued = 0;        // runs issued into the ring so far
   int consumed = 0;      // runs taken out of the ring so far
   int icur = 0;          // 0: the issue cursor is in the current task, 1: in the next one
   int ir = 0;            // run index of the issue cursor: 0 q, 1 + 2j K of block j, 2 + 2j V of block j
-  int nstage = 0;        // next task's metadata: 0 nothing, 1 record loaded, 2 ids loaded
-  int4 nxt_rec;
-  TaskMeta cur, nxt;
+  bool has_nxt = false;
+  int pre = 0;           // runs of the first task issued before the dependency wait (slots 1 .. pre-1)
+  TaskView cur, nxt;
   bool ok = true;
 
-  __device__ Worker(const DecodeParams& p_, unsigned char* ring_, uint64_t* bars_, const int* idx_ring_,
-                    int warp_, int lane_)
-      : p(p_), ring(ring_), bars(bars_), idx_ring(idx_ring_), warp(warp_), lane(lane_) {
+  __device__ Streamer(const DecodeParams& p_, const DecodeSmem<D, G>& sm_, int warp_, int lane_)
+      : p(p_), sm(sm_), warp(warp_), lane(lane_) {
+    ring = sm.ring + warp * T::NR * T::RUN;
+    bars = sm.ring_bar + warp * T::NR;
     pol = dev::l2_policy_evict_first();
-    n_tasks = __ldcg(&p.hdr->n_tasks);
-    task_from_record<T::NW>(p, load_record(p, idx_ring[0], n_tasks), warp, cur);
-    cur.ids = load_ids<T::NW>(p, cur, warp, lane);
-    cur.nst = load_nst(p, cur);
   }
 
-  static __device__ __forceinline__ int runs(const TaskMeta& m) { return m.t >= 0 && m.nbw > 0 ? 1 + 2 * m.nbw : 0; }
-
-  // Advance the next task's metadata by one dependent load (called between blocks so each load's
-  // latency hides behind compute); full == true finishes it now.
-  __device__ __forceinline__ void prefetch_next(bool full) {
-    if (nstage == 0) {
-      nxt_rec = load_record(p, idx_ring[(k + 1) & 3], n_tasks);
-      nstage = 1;
-      if (!full) return;
+  // Task kk of the queue (waits until the scheduler warp has published it).
+  __device__ void take(int kk, TaskView& v) {
+    const bool got = cta_wait(&sm.qfull[kk % T::QD], (kk / T::QD) & 1, sm.abort, p.err);
+    ok = __all_sync(0xffffffffu, got) && ok;
+    if (!ok) {
+      v.t = -1;
+      v.nbw = 0;
+      return;
     }
-    if (nstage == 1) {
-      task_from_record<T::NW>(p, nxt_rec, warp, nxt);
-      nxt.ids = load_ids<T::NW>(p, nxt, warp, lane);
-      nxt.nst = load_nst(p, nxt);
-      nstage = 2;
-    }
+    const TaskEntry* e = &sm.queue[kk % T::QD];
+    const int4 rec = e->rec;
+    v.t = rec.x;
+    v.g = rec.y & 0xFF;
+    v.s = rec.y >> 8;
+    v.row = rec.z;
+    v.ctx = rec.w;
+    v.nst = e->nst;
+    const int nblk = (v.ctx + kBS - 1) / kBS;
+    v.nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
+    v.bw = (warp - e->rot) & 3;
+    v.nbw = v.t >= 0 ? warp_blocks(e->nb, v.bw) : 0;
+    v.ids = e->ids;
   }
-  __device__ __forceinline__ void issue_run(const TaskMeta& m, int r) {
-    const int slot = issued % T::NR;
+  static __device__ __forceinline__ int runs(const TaskView& v) { return v.t >= 0 && v.nbw > 0 ? 1 + 2 * v.nbw : 0; }
+  __device__ __forceinline__ int block_pos(const TaskView& v, int j) const {
+    return (v.s * p.split_blocks + v.bw + 4 * j) * kBS;
+  }
+
+  __device__ __forceinline__ void issue_slot(const TaskView& v, int r, int slot) {
     unsigned char* dst = ring + slot * T::RUN;
+    if (lane != 0) return;
     if (r == 0) {
-      if (lane == 0) {
-        dev::mbar_arrive_expect_tx(&bars[slot], G * D * 2);
-        dev::bulk_g2s(dst, p.q + ((size_t)m.t * p.num_q_heads + (size_t)m.g * G) * D, G * D * 2, &bars[slot], pol);
-      }
+      dev::mbar_arrive_expect_tx(&bars[slot], G * D * 2);
+      dev::bulk_g2s(dst, p.q + ((size_t)v.t * p.num_q_heads + (size_t)v.g * G) * D, G * D * 2, &bars[slot], pol);
     } else {
-      const int id = __shfl_sync(0xffffffffu, m.ids, (r - 1) >> 1);
-      if (lane == 0) {
-        const int row = (((r - 1) & 1) ? p.layer_row0_v : p.layer_row0_k) + (id * p.num_kv_heads + m.g) * kBS;
-        dev::mbar_arrive_expect_tx(&bars[slot], T::RUN);
+      const int id = v.ids[v.bw + 4 * ((r - 1) >> 1)];
+      const int row = (((r - 1) & 1) ? p.layer_row0_v : p.layer_row0_k) + (id * p.num_kv_heads + v.g) * kBS;
+      dev::mbar_arrive_expect_tx(&bars[slot], T::RUN);
 #pragma unroll
-        for (int b = 0; b < T::BOXES; ++b) dev::tma_load_2d(dst + b * 2048, &p.kv_map, b * 64, row, &bars[slot], pol);
-      }
+      for (int b = 0; b < T::BOXES; ++b) dev::tma_load_2d(dst + b * 2048, &p.kv_map, b * 64, row, &bars[slot], pol);
     }
+  }
+  __device__ __forceinline__ void issue_run(const TaskView& v, int r) {
+    issue_slot(v, r, issued % T::NR);
     ++issued;
   }
-  // Issue the next run of the stream (current task, then the next task), if there is one.
+  // Issue the next run of the stream (current task, then the next one), if there is one.
   __device__ __forceinline__ bool issue_next() {
     if (icur == 0) {
       if (ir < runs(cur)) {
@@ -243,27 +299,28 @@ struct Worker {
       icur = 1;
       ir = 0;
     }
-    prefetch_next(true);
-    if (ir < runs(nxt)) {
+    if (!has_nxt) {
+      if (cur.t < 0) return false;
+      take(k + 1, nxt);
+      has_nxt = true;
+    }
+    if (ok && ir < runs(nxt)) {
       issue_run(nxt, ir++);
       return true;
     }
     return false;
   }
-  // Top the ring up.  It runs dry when the warp had no blocks in the task just finished (a short split
-  // deals nothing to some warps), since only consuming a run issues the next one.
+  // Top the ring up.  It runs dry when the warp had no blocks in the task just finished, since only
+  // consuming a run issues the next one.
   __device__ __forceinline__ void fill() {
-    while (issued - consumed < T::NR && issue_next()) {
+    while (ok && issued - consumed < T::NR && issue_next()) {
     }
   }
   // Wait for the oldest run in the ring; returns its slot's shared-memory address.
   __device__ __forceinline__ uint32_t wait_run() {
     const int slot = consumed % T::NR;
-    if (!dev::mbar_wait(&bars[slot], (consumed / T::NR) & 1)) {
-      if (lane == 0) dev::set_error(p.err, PKV_DEVERR_WAIT_TIMEOUT);
-      ok = false;
-    }
-    ok = __all_sync(0xffffffffu, ok);
+    const bool got = cta_wait(&bars[slot], (consumed / T::NR) & 1, sm.abort, p.err);
+    ok = __all_sync(0xffffffffu, got) && ok;
     return dev::smem_addr(ring + slot * T::RUN);
   }
   // The warp is done with the oldest run: recycle its slot for the next run of the stream.
@@ -272,139 +329,52 @@ struct Worker {
     ++consumed;
     if (ok) issue_next();
   }
-  // Move to the next task; the issue cursor is already inside it.
-  __device__ __forceinline__ void advance() {
-    prefetch_next(true);
-    cur = nxt;
-    ++k;
-    icur = 0;
-    nstage = 0;
+  // Before the dependency wait: the first task, and its first K/V runs wherever nothing that the previous
+  // kernel writes can be in them (positions the appended tokens never reach, or rows that are replaced
+  // from the appended inputs anyway).  q comes after the wait.
+  __device__ void prologue() {
+    take(0, cur);
+    if (!ok || runs(cur) == 0) return;
+    pre = 1;
+    while (pre < T::NR && pre < runs(cur)) {
+      const int bpos = block_pos(cur, (pre - 1) >> 1);
+      if (!(p.k_in != nullptr || p.late_wait || bpos + kBS <= cur.nst)) break;
+      issue_slot(cur, pre, pre);
+      ++pre;
+    }
   }
-  // Before leaving early (a wait gave up): let the copies still in flight land, each wait bounded.
-  __device__ __forceinline__ void drain() {
+  __device__ void after_wait() {
+    if (!ok || runs(cur) == 0) return;
+    issue_slot(cur, 0, 0);
+    issued = pre;
+    ir = pre;
+  }
+  // The copies issued but not consumed must land before the CTA leaves (each wait bounded).
+  __device__ void drain() {
     for (; consumed < issued; ++consumed) dev::mbar_wait(&bars[consumed % T::NR], (consumed / T::NR) & 1);
+  }
+  __device__ __forceinline__ void advance() {
+    if (!has_nxt) take(k + 1, nxt);
+    if (icur == 0) ir = 0;
+    cur = nxt;
+    has_nxt = false;
+    icur = 0;
+    ++k;
   }
 };
 
-// Output element held by register r of `lane` in the O^T fragment layout: its dim and its head.
-__device__ __forceinline__ void frag_coord(int lane, int r, int& dim, int& head) {
-  dim = 16 * (r >> 2) + (lane >> 2) + ((r & 2) ? 8 : 0);
-  head = ((lane & 3) << 1) + (r & 1);
-}
-// ... and back: the lane and register holding (dim, head).
-__device__ __forceinline__ void frag_slot(int dim, int head, int& lane, int& r) {
-  lane = ((dim & 7) << 2) | (head >> 1);
-  r = ((dim >> 4) << 2) | (((dim >> 3) & 1) << 1) | (head & 1);
-}
-
-// Merge a token's split partials (all of them final) into its fp16 output, with log-sum-exp weights in
-// split order, so the result does not depend on which CTA merges.  The partials were written by other
-// CTAs during this launch: they are read from L2 (.cg), never from a possibly stale L1 line.
-template <int D, int G, int NT>
-__device__ __forceinline__ void merge_splits(const DecodeParams& p, int tg, int nsplit) {
-  constexpr int NG = G * D / 4;            // groups of 4 consecutive dims of one head
-  constexpr int EG = (NG + NT - 1) / NT;   // groups per thread
-  constexpr int U = EG >= 4 ? 2 : 4;       // splits whose loads are in flight together
-  const int t = tg / p.num_kv_heads, g = tg % p.num_kv_heads;
-  const size_t sb = (size_t)tg * p.max_splits;
-  float M[EG], L[EG];
-  float4 acc[EG];
-#pragma unroll
-  for (int j = 0; j < EG; ++j) {
-    M[j] = -INFINITY;
-    L[j] = 0.f;
-    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  for (int s0 = 0; s0 < nsplit; s0 += U) {
-    float2 ml[EG][U];
-    float4 o[EG][U];
-#pragma unroll
-    for (int j = 0; j < EG; ++j) {
-      const int e4 = threadIdx.x + j * NT;
-      const int h = (4 * e4) / D, dim = (4 * e4) % D;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (e4 < NG && s0 + u < nsplit) {
-          const size_t pi = (sb + s0 + u) * kHeadsTile + h;
-          ml[j][u] = __ldcg(p.part_ml + pi);
-          o[j][u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + pi * D + dim));
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < EG; ++j) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (s0 + u < nsplit) {
-          const float nM = fmaxf(M[j], ml[j][u].x);
-          const float a = exp2f(M[j] - nM), f = exp2f(ml[j][u].x - nM);
-          M[j] = nM;
-          L[j] = L[j] * a + ml[j][u].y * f;
-          acc[j].x = acc[j].x * a + o[j][u].x * f;
-          acc[j].y = acc[j].y * a + o[j][u].y * f;
-          acc[j].z = acc[j].z * a + o[j][u].z * f;
-          acc[j].w = acc[j].w * a + o[j][u].w * f;
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < EG; ++j) {
-    const int e4 = threadIdx.x + j * NT;
-    if (e4 >= NG) continue;
-    const int h = (4 * e4) / D, dim = (4 * e4) % D;
-    const float il = 1.f / L[j];
-    const __half2 lo = __floats2half2_rn(acc[j].x * il, acc[j].y * il);
-    const __half2 hi = __floats2half2_rn(acc[j].z * il, acc[j].w * il);
-    uint2 v;
-    v.x = *reinterpret_cast<const uint32_t*>(&lo);
-    v.y = *reinterpret_cast<const uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.num_q_heads + (size_t)g * G + h) * D + dim) = v;
-  }
-}
-
 template <int D, int G>
-__device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char* smem, int warp, int lane) {
+__device__ __forceinline__ void stream_loop(const DecodeParams& p, const DecodeSmem<D, G>& sm, Streamer<D, G>& w) {
   using T = DecodeTraits<D, G>;
-  uint64_t* all_bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
-  float* co = reinterpret_cast<float*>(smem + T::OFF_CO);
-  float* cm = reinterpret_cast<float*>(smem + T::OFF_CM);
-  float* cl = reinterpret_cast<float*>(smem + T::OFF_CL);
-  int* idx_ring = reinterpret_cast<int*>(smem + T::OFF_IDX);
-  // The first task's record and block ids are loaded before the dependency wait: the plan kernel that
-  // wrote the task list released its dependents only after its writes (and a fence), and block tables
-  // are final before the plan; they are read through L2, never a possibly stale L1 line.  The task
-  // counters, q and the cache (written by the append just before) are touched only after the wait.
-  Worker<D, G> w(p, smem + warp * T::NR * T::RUN, all_bars + warp * T::NR, idx_ring, warp, lane);
-  if (!p.late_wait) dev::griddep_wait();
-  dev::griddep_launch_dependents();
-  // one CTA-uniform decision (a racing error-word update must not split the CTA)
-  if (__syncthreads_or(threadIdx.x == 0 && dev::pool_poisoned(p.err))) return;
-  // Split completion (thread 0 only): after writing a split's partial the CTA counts it on the token's
-  // counter, and the CTA that completes the count merges the token.  The count's result is examined only
-  // at the end of the CTA's next task, so its round trip never stalls the stream.
-  int pend_tg = -1, pend_prev = 0, pend_ns = 0;
-  auto resolve_pending = [&]() {  // thread 0: publish the token this CTA must merge, or -1
-    int tg = -1;
-    if (pend_tg >= 0 && pend_prev == pend_ns - 1) {
-      tg = pend_tg;
-      p.merge_cnt[tg] = 0;       // ready for the next launch on this plan
-      dev::fence_acq_rel_gpu();  // acquire: the other splits' partials, released with their counts
-    }
-    idx_ring[4] = tg;
-    idx_ring[5] = pend_ns;
-    pend_tg = -1;
-  };
-
+  const int lane = w.lane, warp = w.warp;
   const int qh = lane >> 2;        // head whose q this lane feeds to the MMA (B operand column); key row too
   const int h0 = (lane & 3) << 1;  // heads of this lane's score / output columns: h0, h0 + 1
-  int pending = 0;                 // thread 0: index of the task two ahead, published at the task's end
-  bool cta_ok = true;              // CTA-uniform: no wait gave up
-  while (w.cur.t >= 0) {           // uniform: every warp reads the same index
-    if (threadIdx.x == 0) pending = 2 * (int)gridDim.x + atomicAdd(&p.hdr->work, 1);
-    const TaskMeta d = w.cur;
+  int shares = 0;                  // shares this warp has handed to the combiner warp
+  float* my_o = sm.sh_o + warp * T::OV * T::SHL;
+  float2* my_ml = sm.sh_ml + warp * kHeadsTile;
+  while (w.ok && w.cur.t >= 0) {
+    const TaskView d = w.cur;
     w.fill();
-    w.prefetch_next(false);
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o[T::MT][4];
 #pragma unroll
@@ -428,13 +398,34 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
       w.release_run();
 
       for (int j = 0; j < d.nbw && w.ok; ++j) {
-        const int bpos = (d.s * p.split_blocks + warp + T::NW * j) * kBS;  // the block's first position
+        const int bpos = w.block_pos(d, j);  // the block's first position
         const int ntok = min(kBS, d.ctx - bpos);
         // fused append: positions ov0 .. bpos + ntok - 1 of the block are this pass's tokens; their rows
         // come from the inputs (the cache may not hold them yet), and the block holding the token's own
         // position writes it into the cache
-        const int ov0 = max(bpos, d.nst), nov = bpos + ntok - ov0;
-        auto override_rows = [&](uint32_t base, const __half* src) {
+        const int ov0 = max(bpos, d.nst), nov = p.k_in != nullptr ? bpos + ntok - ov0 : 0;
+        const bool own = nov > 0 && d.ctx - 1 < bpos + kBS;  // the block holds the token's own position
+        // Up to 32 16-byte chunks of new rows (one decode token's row at d <= 256): every lane loads its
+        // chunk now, while the block's K and V tiles are in flight, so no dependent global load sits between
+        // a tile's arrival and its use; more rows (a short chunk) are read after the tile lands.
+        const bool pf = nov > 0 && nov * (D / 8) <= 32;
+        const int prr = ov0 - bpos + lane / (D / 8), pcc = lane % (D / 8);  // this lane's row and chunk
+        uint4 pk = make_uint4(0, 0, 0, 0), pv = pk;
+        if (pf && lane < nov * (D / 8)) {
+          const size_t src = ((size_t)(d.t - (d.ctx - 1 - (bpos + prr))) * p.num_kv_heads + d.g) * D;
+          pk = __ldcg(reinterpret_cast<const uint4*>(p.k_in + src) + pcc);
+          pv = __ldcg(reinterpret_cast<const uint4*>(p.v_in + src) + pcc);
+        }
+        const int64_t slot = own ? __ldcg(p.slots + d.t) : -1;
+        auto override_rows = [&](uint32_t base, const __half* src, const uint4& pre) {
+          if (pf) {
+            if (lane < nov * (D / 8))
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(prr, pcc)), "r"(pre.x),
+                           "r"(pre.y), "r"(pre.z), "r"(pre.w)
+                           : "memory");
+            __syncwarp();
+            return;
+          }
           for (int idx = lane; idx < nov * (D / 8); idx += 32) {
             const int rr = ov0 - bpos + idx / (D / 8), cc = idx % (D / 8);
             const int tk = d.t - (d.ctx - 1 - (bpos + rr));
@@ -445,26 +436,12 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
           }
           __syncwarp();
         };
-        if (nov > 0 && d.ctx - 1 < bpos + kBS) {
-          const int64_t slot = __ldcg(p.slots + d.t);
-          if (slot != -1) {
-            if (slot < 0 || slot >= p.num_slots) {
-              if (lane == 0) dev::set_error(p.err, PKV_DEVERR_SLOT_RANGE);
-            } else {
-              const size_t src = ((size_t)d.t * p.num_kv_heads + d.g) * D;
-              const size_t dst = (((size_t)(slot >> 4) * p.num_kv_heads + d.g) * kBS + (slot & 15)) * D;
-              for (int cc = lane; cc < D / 8; cc += 32) {
-                reinterpret_cast<uint4*>(p.cache_k + dst)[cc] = __ldcg(reinterpret_cast<const uint4*>(p.k_in + src) + cc);
-                reinterpret_cast<uint4*>(p.cache_v + dst)[cc] = __ldcg(reinterpret_cast<const uint4*>(p.v_in + src) + cc);
-              }
-            }
-          }
-        }
         // ---- S^T[16 keys x 8 heads] = K Q^T on the tensor cores ----
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
         {
           const uint32_t ks_base = w.wait_run();
-          if (nov > 0) override_rows(ks_base, p.k_in);
+          if (!w.ok) break;
+          if (nov > 0) override_rows(ks_base, p.k_in, pk);
           const int kr = (lane & 7) + ((lane >> 3) & 1) * 8;  // key row this lane addresses for ldmatrix
 #pragma unroll
           for (int ks = 0; ks < T::KS; ++ks) {
@@ -475,7 +452,6 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
           if (nov > 0) dev::fence_proxy_async_smem();  // the override precedes the slot's next TMA write
           w.release_run();
         }
-        w.prefetch_next(false);  // one dependent metadata load of the next task per block, hidden by compute
         // ---- online softmax (log2 domain); the lane holds keys qh, qh + 8 for heads h0, h0 + 1 ----
         const bool v0 = qh < ntok, v1 = qh + 8 < ntok;
         const float s0 = v0 ? sc[0] * p.scale_log2 : -INFINITY;  // key qh,     head h0
@@ -509,6 +485,7 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
         // ---- O^T[d x 8 heads] += V^T P^T on the tensor cores ----
         {
           const uint32_t vs_base = w.wait_run();
+          if (!w.ok) break;
           if (ntok < kBS) {  // rows past the context may hold anything: zero them so 0 * garbage cannot poison O
             for (int idx = lane; idx < (kBS - ntok) * (D / 8); idx += 32) {
               const int r = ntok + idx / (D / 8), c = idx % (D / 8);
@@ -516,7 +493,7 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
             }
             __syncwarp();
           }
-          if (nov > 0) override_rows(vs_base, p.v_in);
+          if (nov > 0) override_rows(vs_base, p.v_in, pv);
           const int mat = lane >> 3;                      // ldmatrix matrix this lane addresses
           const int vr = (lane & 7) + ((mat >> 1) << 3);  // its key row
 #pragma unroll
@@ -528,71 +505,443 @@ __device__ __forceinline__ void worker_loop(const DecodeParams& p, unsigned char
           if (ntok < kBS || nov > 0) dev::fence_proxy_async_smem();  // generic writes precede the next TMA write
           w.release_run();
         }
+        // ---- fused append: the token's own key and value into the cache ----
+        if (own && slot != -1) {
+          if (slot < 0 || slot >= p.num_slots) {
+            if (lane == 0) dev::set_error(p.err, PKV_DEVERR_SLOT_RANGE);
+          } else {
+            const size_t dst = (((size_t)(slot >> 4) * p.num_kv_heads + d.g) * kBS + (slot & 15)) * D;
+            if (pf) {  // the lanes holding the last new row hold the token's own row
+              if (lane < nov * (D / 8) && prr == d.ctx - 1 - bpos) {
+                reinterpret_cast<uint4*>(p.cache_k + dst)[pcc] = pk;
+                reinterpret_cast<uint4*>(p.cache_v + dst)[pcc] = pv;
+              }
+            } else {
+              const size_t src = ((size_t)d.t * p.num_kv_heads + d.g) * D;
+              for (int cc = lane; cc < D / 8; cc += 32) {
+                reinterpret_cast<uint4*>(p.cache_k + dst)[cc] = __ldcg(reinterpret_cast<const uint4*>(p.k_in + src) + cc);
+                reinterpret_cast<uint4*>(p.cache_v + dst)[cc] = __ldcg(reinterpret_cast<const uint4*>(p.v_in + src) + cc);
+              }
+            }
+          }
+        }
       }
     }
+    if (!w.ok) break;
 
-    // ---- publish this warp's share of the split; a warp with no blocks publishes (-inf, 0, 0) ----
+    // ---- hand this warp's share of the split to the combiner warp ----
+    if (d.nbw > 0) {
 #pragma unroll
-    for (int m = 4; m < 32; m <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, m);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, m);
-    }
-#pragma unroll
-    for (int r = 0; r < T::OV; ++r) co[(warp * T::OV + r) * 32 + lane] = o[r >> 2][r & 3];
-    if (lane < 4) {
-      cm[warp * kHeadsTile + h0] = m0;
-      cm[warp * kHeadsTile + h0 + 1] = m1;
-      cl[warp * kHeadsTile + h0] = l0;
-      cl[warp * kHeadsTile + h0 + 1] = l1;
-    }
-    if (threadIdx.x == 0) {
-      idx_ring[(w.k + 2) & 3] = pending;
-      resolve_pending();
-    }
-    if (!__syncthreads_and(w.ok)) {  // a wait gave up somewhere in the CTA: stop together
-      cta_ok = false;
-      break;
-    }
-    if (idx_ring[4] >= 0) merge_splits<D, G, T::NTHREADS>(p, idx_ring[4], idx_ring[5]);
-
-    // ---- combine the warps' shares with log-sum-exp weights; write the output or the split's partial ----
-    const size_t pidx = ((size_t)d.t * p.num_kv_heads + d.g) * p.max_splits + d.s;
-    for (int e = threadIdx.x; e < G * D; e += T::NTHREADS) {
-      const int h = e / D, dim = e % D;
-      int ln, r;
-      frag_slot(dim, h, ln, r);
-      float M = cm[h];
-#pragma unroll
-      for (int v = 1; v < T::NW; ++v) M = fmaxf(M, cm[v * kHeadsTile + h]);
-      float L = 0.f, acc = 0.f;
-#pragma unroll
-      for (int v = 0; v < T::NW; ++v) {
-        const float f = exp2f(cm[v * kHeadsTile + h] - M);
-        L += cl[v * kHeadsTile + h] * f;
-        acc += co[(v * T::OV + r) * 32 + ln] * f;
+      for (int m = 4; m < 32; m <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, m);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, m);
       }
-      if (d.nsplit == 1) {
-        p.out[((size_t)d.t * p.num_q_heads + (size_t)d.g * G + h) * D + dim] = __float2half_rn(acc / L);
-      } else {
-        p.part_o[(pidx * kHeadsTile + h) * D + dim] = acc;
-        if (dim == 0) p.part_ml[pidx * kHeadsTile + h] = make_float2(M, L);
+      if (shares > 0) {  // the slot is free once the combiner warp has taken the previous share
+        const bool got = cta_wait(&sm.share_empty[warp], (shares - 1) & 1, sm.abort, p.err);
+        if (!__all_sync(0xffffffffu, got)) {
+          w.ok = false;
+          break;
+        }
       }
+      const int hg = lane & 3;
+      if (hg < T::LG) {
+        const int ci = (lane >> 2) * T::LG + hg;
+#pragma unroll
+        for (int r = 0; r < T::OV; ++r) my_o[r * T::SHL + ci] = o[r >> 2][r & 3];
+        if (lane < T::LG) {
+          my_ml[h0] = make_float2(m0, l0);
+          my_ml[h0 + 1] = make_float2(m1, l1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&sm.share_full[warp]);
+      ++shares;
     }
-    __syncthreads();  // the combine buffers are free again; the partial is written
-    if (threadIdx.x == 0 && d.nsplit > 1 && d.nsplit <= kFusedMergeSplits) {
-      pend_tg = d.t * p.num_kv_heads + d.g;
-      pend_prev = dev::atom_add_release_gpu(p.merge_cnt + pend_tg, 1);  // releases the CTA's partial
-      pend_ns = d.nsplit;
-    }
+    __syncwarp();
+    if (lane == 0) dev::mbar_arrive(&sm.qempty[w.k % T::QD]);  // done with the task's queue entry
     w.advance();
   }
-  if (cta_ok) {  // the CTA's last split may still complete a token
-    if (threadIdx.x == 0) resolve_pending();
-    __syncthreads();
-    if (idx_ring[4] >= 0) merge_splits<D, G, T::NTHREADS>(p, idx_ring[4], idx_ring[5]);
-  }
-  if (!w.ok || w.consumed < w.issued) w.drain();
 }
+
+// Merge a token's split partials (all of them final) into its fp16 output, with log-sum-exp weights in
+// split order, so the result does not depend on which CTA merges.  The partials were written by other
+// CTAs during this launch: they are read from L2 (.cg), never from a possibly stale L1 line.  Executed by
+// NT threads with indices tid = 0 .. NT-1.
+template <int D, int G, int NT>
+__device__ __forceinline__ void merge_splits(const DecodeParams& p, int tg, int nsplit, int tid) {
+  constexpr int NG = G * D / 4;            // groups of 4 consecutive dims of one head
+  constexpr int EG = (NG + NT - 1) / NT;   // groups per thread
+  constexpr int U = EG >= 8 ? 1 : (EG >= 4 ? 2 : 4);  // splits whose loads are in flight together
+  const int t = tg / p.num_kv_heads, g = tg % p.num_kv_heads;
+  const size_t sb = (size_t)tg * p.max_splits;
+  float M[EG], L[EG];
+  float4 acc[EG];
+#pragma unroll
+  for (int j = 0; j < EG; ++j) {
+    M[j] = -INFINITY;
+    L[j] = 0.f;
+    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int s0 = 0; s0 < nsplit; s0 += U) {
+    float2 ml[EG][U];
+    float4 o[EG][U];
+#pragma unroll
+    for (int j = 0; j < EG; ++j) {
+      const int e4 = tid + j * NT;
+      const int h = (4 * e4) / D, dim = (4 * e4) % D;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (e4 < NG && s0 + u < nsplit) {
+          const size_t pi = (sb + s0 + u) * kHeadsTile + h;
+          ml[j][u] = __ldcg(p.part_ml + pi);
+          o[j][u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + pi * D + dim));
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < EG; ++j) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (s0 + u < nsplit) {
+          const float nM = fmaxf(M[j], ml[j][u].x);
+          const float a = exp2f(M[j] - nM), f = exp2f(ml[j][u].x - nM);
+          M[j] = nM;
+          L[j] = L[j] * a + ml[j][u].y * f;
+          acc[j].x = acc[j].x * a + o[j][u].x * f;
+          acc[j].y = acc[j].y * a + o[j][u].y * f;
+          acc[j].z = acc[j].z * a + o[j][u].z * f;
+          acc[j].w = acc[j].w * a + o[j][u].w * f;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < EG; ++j) {
+    const int e4 = tid + j * NT;
+    if (e4 >= NG) continue;
+    const int h = (4 * e4) / D, dim = (4 * e4) % D;
+    const float il = 1.f / L[j];
+    const __half2 lo = __floats2half2_rn(acc[j].x * il, acc[j].y * il);
+    const __half2 hi = __floats2half2_rn(acc[j].z * il, acc[j].w * il);
+    uint2 v;
+    v.x = *reinterpret_cast<const uint32_t*>(&lo);
+    v.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.num_q_heads + (size_t)g * G + h) * D + dim) = v;
+  }
+}
+
+// Output element held by register r of `lane` in the O^T fragment layout: its dim and its head.
+__device__ __forceinline__ void frag_coord(int lane, int r, int& dim, int& head) {
+  dim = 16 * (r >> 2) + (lane >> 2) + ((r & 2) ? 8 : 0);
+  head = ((lane & 3) << 1) + (r & 1);
+}
+
+// ---------------------------------------------------------------------------------------------------
+// Scheduler warp: publishes the CTA's tasks into the queue.  The first two are static (blockIdx.x and
+// blockIdx.x + gridDim.x, published before the dependency wait); every later one is claimed from a global
+// counter only when the streaming warps have moved on from the task whose queue slot it takes, so a CTA
+// holds at most two tasks it has not started and the launch ends balanced (the task list is ordered
+// largest first).
+// ---------------------------------------------------------------------------------------------------
+template <int D, int G>
+struct Scheduler {
+  using T = DecodeTraits<D, G>;
+  const DecodeParams& p;
+  const DecodeSmem<D, G>& sm;
+  int lane;
+  int n_tasks = 0;
+  int filled = 0;        // queue entries published so far (task sequence numbers 0 .. filled-1)
+  bool ended = false;    // an end-of-work entry has been published
+  int next_dyn = 0;      // lane 0: result of the counter increment for the next dynamic entry
+
+  __device__ Scheduler(const DecodeParams& p_, const DecodeSmem<D, G>& sm_, int lane_) : p(p_), sm(sm_), lane(lane_) {}
+
+  // Publish task indices idx[0 .. n-1] as the next n queue entries, the loads of all of them in flight
+  // together; an index past the task list ends the work (nothing after it is published).
+  template <int N>
+  __device__ void publish(const int (&idx)[N]) {
+    int4 rec[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) rec[j] = idx[j] < p.max_tasks ? __ldcg(p.tasks + idx[j]) : make_int4(-1, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < N; ++j)  // the count arrives alongside the records: no load waits for it
+      if (idx[j] >= n_tasks) rec[j] = make_int4(-1, 0, 0, 0);
+    int id[N], q0[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      id[j] = 0;
+      q0[j] = 0;
+      if (rec[j].x >= 0) {
+        const int s = rec[j].y >> 8, nblk = (rec[j].w + kBS - 1) / kBS;
+        if (lane < min(p.split_blocks, nblk - s * p.split_blocks))
+          id[j] = __ldcg(p.block_tables + (int64_t)rec[j].z * p.max_blocks + s * p.split_blocks + lane);
+        q0[j] = __ldcg(p.qsl + rec[j].z);
+      }
+    }
+    const int first = filled;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      if (ended) break;
+      TaskEntry* e = &sm.queue[filled % T::QD];
+      int nb = 0, nst = 0, rot = 0;
+      if (rec[j].x >= 0) {
+        const int g = rec[j].y & 0xFF, s = rec[j].y >> 8, ctx = rec[j].w;
+        nb = min(p.split_blocks, (ctx + kBS - 1) / kBS - s * p.split_blocks);
+        if (lane < nb) {
+          int v = id[j];
+          if (v < 0 || v >= p.num_blocks) {
+            dev::set_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+            v = 0;  // keep the copy in bounds; this token's output is flagged as invalid
+          }
+          e->ids[lane] = v;
+        }
+        const int qi = rec[j].x - q0[j];  // the token's index among its row's new tokens
+        nst = ctx - 1 - qi;
+        rot = (qi + g + s) & 3;  // row-local, so the dealing (and the result) does not depend on the batch
+      }
+      if (lane == 0) {
+        e->rec = rec[j];
+        e->nst = nst;
+        e->nb = nb;
+        e->rot = rot;
+      }
+      ++filled;
+      ended = rec[j].x < 0;
+    }
+    __syncwarp();
+    if (lane == 0)
+      for (int f = first; f < filled; ++f) dev::mbar_arrive(&sm.qfull[f % T::QD]);
+  }
+  // Before the dependency wait: the static entries (they touch no counter).
+  __device__ void prologue() {
+    n_tasks = __ldcg(&p.hdr->n_tasks);
+    int idx[kStaticTasks];
+#pragma unroll
+    for (int j = 0; j < kStaticTasks; ++j) idx[j] = blockIdx.x + j * gridDim.x;
+    publish(idx);
+  }
+  __device__ void run() {
+    static_assert(kStaticTasks < T::QD, "queue");
+    if (ended) return;
+    if (lane == 0) next_dyn = atomicAdd(&p.hdr->work, 1);
+    while (!ended) {
+      // the slot's previous task must be left by every streaming warp and read by the combiner
+      if (filled >= T::QD &&
+          !cta_wait(&sm.qempty[filled % T::QD], ((filled - T::QD) / T::QD) & 1, sm.abort, p.err))
+        return;
+      const int idx[1] = {kStaticTasks * (int)gridDim.x + __shfl_sync(0xffffffffu, next_dyn, 0)};
+      publish(idx);
+      if (!ended && lane == 0) next_dyn = atomicAdd(&p.hdr->work, 1);  // used at the next publish
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------------------------------
+// Combiner warp: combines the streaming warps' shares of every task with log-sum-exp weights, writes a
+// one-split token's fp16 output or a split's unnormalised partial, counts finished splits on the token's
+// counter, and merges a token whose count it completed.  Nothing here stalls the streaming warps.
+// A split's count is issued one task after its partial was written and examined one task later still,
+// so neither the release (which waits for earlier stores) nor the atomic's round trip stalls the warp.
+// ---------------------------------------------------------------------------------------------------
+template <int D, int G>
+struct Combiner {
+  using T = DecodeTraits<D, G>;
+  const DecodeParams& p;
+  const DecodeSmem<D, G>& sm;
+  int lane;
+  uint32_t merges = 0;   // merge rounds staged so far (parity of merge_bar)
+
+  __device__ Combiner(const DecodeParams& p_, const DecodeSmem<D, G>& sm_, int lane_) : p(p_), sm(sm_), lane(lane_) {}
+
+  // A count issued earlier: lane 0 holds the counter's old value.  The warp that completes a token's
+  // count merges it.
+  __device__ bool finish_count(int tg, int nsplit, int prev_lane0) {
+    const int prev = __shfl_sync(0xffffffffu, prev_lane0, 0);
+    if (prev != nsplit - 1) return true;
+    if (lane == 0) {
+      p.merge_cnt[tg] = 0;       // ready for the next launch on this plan
+      dev::fence_acq_rel_gpu();  // acquire: the other splits' partials, released with their counts
+    }
+    __syncwarp();
+    return merge_staged(tg, nsplit);
+  }
+  // Merge a token's split partials (all final) into its fp16 output: rounds of MS partials staged in
+  // shared memory by bulk copies whose loads are all in flight together, combined with log-sum-exp
+  // weights in split order, so the result does not depend on which CTA merges.
+  __device__ bool merge_staged(int tg, int nsplit) {
+    constexpr int NG = G * D / 4;         // groups of 4 consecutive dims of one head
+    constexpr int EG = (NG + 31) / 32;    // groups per lane
+    const size_t sb = (size_t)tg * p.max_splits;
+    float M[EG], L[EG];
+    float4 acc[EG];
+#pragma unroll
+    for (int j = 0; j < EG; ++j) {
+      M[j] = -INFINITY;
+      L[j] = 0.f;
+      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // the partials were written through the generic proxy (other CTAs, and this warp): order them before
+    // the bulk copies' reads
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    for (int s0 = 0; s0 < nsplit; s0 += T::MS) {
+      const int ms = min(T::MS, nsplit - s0);
+      __syncwarp();
+      if (lane == 0) {
+        dev::fence_proxy_async_smem();  // this warp's reads of the previous round precede the new copies
+        dev::mbar_arrive_expect_tx(sm.merge_bar, ms * (G * D * 4 + kHeadsTile * 8));
+        for (int u = 0; u < ms; ++u) {
+          const size_t pi = (sb + s0 + u) * kHeadsTile;
+          dev::bulk_g2s_plain(sm.mo + u * G * D, p.part_o + pi * D, G * D * 4, sm.merge_bar);
+          dev::bulk_g2s_plain(sm.mml + u * kHeadsTile, p.part_ml + pi, kHeadsTile * 8, sm.merge_bar);
+        }
+      }
+      if (!cta_wait(sm.merge_bar, merges & 1, sm.abort, p.err)) return false;
+      ++merges;
+      for (int u = 0; u < ms; ++u) {
+#pragma unroll
+        for (int j = 0; j < EG; ++j) {
+          const int e4 = lane + 32 * j;
+          if (e4 >= NG) continue;
+          const int h = (4 * e4) / D;
+          const float2 ml = sm.mml[u * kHeadsTile + h];
+          const float4 o = reinterpret_cast<const float4*>(sm.mo + u * G * D)[e4];
+          const float nM = fmaxf(M[j], ml.x);
+          const float a = exp2f(M[j] - nM), f = exp2f(ml.x - nM);
+          M[j] = nM;
+          L[j] = L[j] * a + ml.y * f;
+          acc[j].x = acc[j].x * a + o.x * f;
+          acc[j].y = acc[j].y * a + o.y * f;
+          acc[j].z = acc[j].z * a + o.z * f;
+          acc[j].w = acc[j].w * a + o.w * f;
+        }
+      }
+    }
+    const int t = tg / p.num_kv_heads, g = tg % p.num_kv_heads;
+#pragma unroll
+    for (int j = 0; j < EG; ++j) {
+      const int e4 = lane + 32 * j;
+      if (e4 >= NG) continue;
+      const float il = 1.f / L[j];
+      const __half2 lo = __floats2half2_rn(acc[j].x * il, acc[j].y * il);
+      const __half2 hi = __floats2half2_rn(acc[j].z * il, acc[j].w * il);
+      uint2 v;
+      v.x = *reinterpret_cast<const uint32_t*>(&lo);
+      v.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.num_q_heads + (size_t)g * G) * D + 4 * e4) = v;
+    }
+    return true;
+  }
+
+  __device__ void run() {
+    uint32_t taken = 0;               // bit w: parity of the shares taken from streaming warp w so far
+    int wr_tg = -1, wr_ns = 0;        // partial written, count not issued yet
+    int ct_tg = -1, ct_ns = 0, ct_prev = 0;  // count issued, result not examined yet
+    const int hg = lane & 3;
+    const bool real = hg < T::LG;     // this lane's fragment columns hold real heads
+    const int ci = (lane >> 2) * T::LG + hg;
+    for (int k = 0;; ++k) {
+      // ---- the task's description; then its queue slot may be refilled ----
+      if (!cta_wait(&sm.qfull[k % T::QD], (k / T::QD) & 1, sm.abort, p.err)) return;
+      const TaskEntry* e = &sm.queue[k % T::QD];
+      const int4 rec = e->rec;
+      const int nb = e->nb, rot = e->rot;
+      __syncwarp();
+      if (rec.x < 0) break;
+      if (lane == 0) dev::mbar_arrive(&sm.qempty[k % T::QD]);
+      const int t = rec.x, g = rec.y & 0xFF, s = rec.y >> 8, ctx = rec.w;
+      const int nblk = (ctx + kBS - 1) / kBS;
+      const int nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
+      // ---- combine the shares in warp order (a fixed order: the result does not depend on timing) ----
+      float acc[T::OV];
+#pragma unroll
+      for (int r = 0; r < T::OV; ++r) acc[r] = 0.f;
+      float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+      for (int w = 0; w < T::NW; ++w) {
+        if (warp_blocks(nb, (w - rot) & 3) == 0) continue;
+        if (!cta_wait(&sm.share_full[w], (taken >> w) & 1, sm.abort, p.err)) return;
+        taken ^= 1u << w;
+        if (real) {
+          const float2 ma = sm.sh_ml[w * kHeadsTile + 2 * hg], mb = sm.sh_ml[w * kHeadsTile + 2 * hg + 1];
+          float a0 = 1.f, f0 = 0.f, a1 = 1.f, f1 = 0.f;
+          if (ma.x != -INFINITY) {
+            const float nM = fmaxf(M0, ma.x);
+            a0 = exp2f(M0 - nM);
+            f0 = exp2f(ma.x - nM);
+            M0 = nM;
+            L0 = L0 * a0 + ma.y * f0;
+          }
+          if (mb.x != -INFINITY) {
+            const float nM = fmaxf(M1, mb.x);
+            a1 = exp2f(M1 - nM);
+            f1 = exp2f(mb.x - nM);
+            M1 = nM;
+            L1 = L1 * a1 + mb.y * f1;
+          }
+          const float* so = sm.sh_o + w * T::OV * T::SHL;
+#pragma unroll
+          for (int r = 0; r < T::OV; ++r) acc[r] = acc[r] * ((r & 1) ? a1 : a0) + so[r * T::SHL + ci] * ((r & 1) ? f1 : f0);
+        }
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(&sm.share_empty[w]);
+      }
+      // ---- stage the result in shared memory (the fragment layout is not the output layout) ----
+      if (real) {
+        if (nsplit == 1) {
+          __half* sh = reinterpret_cast<__half*>(sm.stg);
+          const float i0 = 1.f / L0, i1 = 1.f / L1;
+#pragma unroll
+          for (int r = 0; r < T::OV; ++r) {
+            int dim, head;
+            frag_coord(lane, r, dim, head);
+            if (head < G) sh[head * D + dim] = __float2half_rn(acc[r] * ((r & 1) ? i1 : i0));
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < T::OV; ++r) {
+            int dim, head;
+            frag_coord(lane, r, dim, head);
+            if (head < G) sm.stg[head * D + dim] = acc[r];
+          }
+        }
+      }
+      // ---- the count of the partial written one task ago: its stores are long complete, so the release
+      // does not wait; then the count issued one task ago, whose result has arrived: maybe a merge ----
+      int new_prev = 0;
+      if (wr_tg >= 0 && lane == 0) new_prev = dev::atom_add_release_gpu(p.merge_cnt + wr_tg, 1);
+      if (ct_tg >= 0 && !finish_count(ct_tg, ct_ns, ct_prev)) return;
+      ct_tg = wr_tg;
+      ct_ns = wr_ns;
+      ct_prev = new_prev;
+      wr_tg = -1;
+      // ---- write the output, or the split's partial ----
+      __syncwarp();
+      if (nsplit == 1) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)t * p.num_q_heads + (size_t)g * G) * D);
+        for (int c = lane; c < G * D / 8; c += 32) dst[c] = reinterpret_cast<const uint4*>(sm.stg)[c];
+      } else {
+        const size_t tg = (size_t)t * p.num_kv_heads + g;
+        const size_t pidx = tg * p.max_splits + s;
+        float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * kHeadsTile * D);
+        for (int c = lane; c < G * D / 4; c += 32) dst[c] = reinterpret_cast<const float4*>(sm.stg)[c];
+        if (real && lane < T::LG) {
+          if (2 * lane < G) p.part_ml[pidx * kHeadsTile + 2 * lane] = make_float2(M0, L0);
+          if (2 * lane + 1 < G) p.part_ml[pidx * kHeadsTile + 2 * lane + 1] = make_float2(M1, L1);
+        }
+        if (nsplit <= kFusedMergeSplits) {
+          wr_tg = (int)tg;
+          wr_ns = nsplit;
+        }
+      }
+      __syncwarp();  // the staging buffer is free again
+    }
+    // ---- flush: the last partial's count, then the two outstanding results ----
+    int new_prev = 0;
+    __syncwarp();
+    if (wr_tg >= 0 && lane == 0) new_prev = dev::atom_add_release_gpu(p.merge_cnt + wr_tg, 1);
+    if (ct_tg >= 0 && !finish_count(ct_tg, ct_ns, ct_prev)) return;
+    if (wr_tg >= 0) finish_count(wr_tg, wr_ns, new_prev);
+  }
+};
 
 template <int D, int G>
 __global__ void __launch_bounds__(DecodeTraits<D, G>::NTHREADS, DecodeTraits<D, G>::MINB)
@@ -601,21 +950,51 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
-  int* idx_ring = reinterpret_cast<int*>(smem + T::OFF_IDX);
-  // set-up that reads nothing written by earlier kernels runs before the dependency wait
+  const DecodeSmem<D, G> sm(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    for (int i = 0; i < T::NR; ++i) dev::mbar_init(&bars[warp * T::NR + i], 1);
+  // set-up that reads nothing written by earlier kernels runs before the dependency wait
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < T::NW * T::NR; ++i) dev::mbar_init(&sm.ring_bar[i], 1);
+    for (int i = 0; i < T::NW; ++i) {
+      dev::mbar_init(&sm.share_full[i], 1);
+      dev::mbar_init(&sm.share_empty[i], 1);
+    }
+    for (int i = 0; i < T::QD; ++i) {
+      dev::mbar_init(&sm.qfull[i], 1);
+      dev::mbar_init(&sm.qempty[i], T::NW + 1);  // the streaming warps and the combiner
+    }
+    dev::mbar_init(sm.merge_bar, 1);
+    *sm.abort = 0;
     dev::fence_mbar_init();
   }
-  if (threadIdx.x == 0) {  // the first two tasks are static: no counter round trip before the first copy
-    idx_ring[0] = blockIdx.x;
-    idx_ring[1] = blockIdx.x + gridDim.x;
-  }
+  __syncwarp();
   __syncthreads();
-  worker_loop<D, G>(p, smem, warp, lane);  // waits for the previous kernel itself, after its first loads
+  // The static tasks' records and block ids are read before the dependency wait: the plan kernel that
+  // wrote the task list released its dependents only after its writes (and a fence), and block tables are
+  // final before the plan; they are read through L2, never a possibly stale L1 line.  So are the first K/V
+  // runs wherever no appended token can be in them.  q, the task counter and the partials are touched only
+  // after the wait.
+  Streamer<D, G> w(p, sm, warp, lane);
+  Scheduler<D, G> sch(p, sm, lane);
+  if (warp < T::NW) w.prologue(); else if (warp == T::NW + 1) sch.prologue();
+  if (!p.late_wait) dev::griddep_wait();
+  dev::griddep_launch_dependents();
+  if (warp < T::NW) w.after_wait();  // the first task's q (in bounds even if the pool turns out poisoned)
+  // one CTA-uniform decision (a racing error-word update must not split the CTA); every warp arrives
+  // converged at each CTA barrier (its predicate is computed first)
+  int pz = 0;
+  if (threadIdx.x == 0) pz = dev::pool_poisoned(p.err) ? 1 : 0;
+  __syncwarp();
+  const bool poisoned = __syncthreads_or(pz);
+  if (warp < T::NW) {
+    if (!poisoned) stream_loop<D, G>(p, sm, w);
+    w.drain();
+  } else if (!poisoned) {
+    if (warp == T::NW) Combiner<D, G>(p, sm, lane).run();
+    else sch.run();
+  }
   // the last CTA out resets the task counter for the next launch on this plan
+  __syncwarp();
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -799,6 +1178,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   __shared__ int warp_sums[32];
   __shared__ int hist[kPrefillBuckets];
   __shared__ int n_slots;
+  __shared__ int tail_at[kMaxSplitBlocks + 1];  // per last-split size: its task count, then its next slot
+  __shared__ int n_dec;
   dev::griddep_wait();
   for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
     const int q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1), ctx = __ldg(p.context_lens + i);
@@ -808,49 +1189,56 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   }
   for (int i = threadIdx.x; i < p.num_tokens * p.num_kv_heads; i += blockDim.x) p.merge_cnt[i] = 0;
   for (int i = threadIdx.x; i < kPrefillBuckets; i += blockDim.x) hist[i] = 0;
+  for (int i = threadIdx.x; i <= kMaxSplitBlocks; i += blockDim.x) tail_at[i] = 0;
   for (int i = threadIdx.x; i < p.max_slots; i += blockDim.x) p.pf_sync[i] = make_int2(0, 0);
   if (threadIdx.x == 0) n_slots = 0;
+  __syncthreads();
 
   // ---- decode tasks: tokens of rows that are not prefill items ----
-  // Pass 0 lists each token's short last split, pass 1 its full splits in token order: tokens then
-  // complete, and get merged, all through the launch rather than together at its end, and the launch
-  // ends on equal-sized tasks.
+  // Largest first: every token's full splits in token order, then the short last splits by decreasing
+  // size.  The CTAs that take the last tasks of a launch then hold little work each, so the launch ends
+  // nearly together on every SM.  (The order decides which CTA computes a split, never the result.)
   int carry = 0;
-  for (int pass = 0; pass < 2; ++pass) {
-    for (int base = 0; base < p.num_tokens; base += blockDim.x) {
-      const int t = base + threadIdx.x;
-      int nblk = 0, row = 0, c = 0;
-      if (t < p.num_tokens) {
-        if (pass == 0) {
-          const int b = dev::row_of_token(p.qsl, p.num_seqs, t);
-          const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1), ctx = __ldg(p.context_lens + b);
-          const int q_len = q1 - q0;
-          const bool prefill = p.prefill_min_qlen > 0 && q_len >= p.prefill_min_qlen;
-          if (t >= q0 && t < q1 && row_meta_ok(q_len, ctx, p.max_ctx) && !prefill) c = ctx - q_len + (t - q0) + 1;
-          p.tok_row[t] = b;
-          p.tok_ctx[t] = c;  // 0: no decode work (prefill row or invalid metadata)
-          row = b;
-        } else {
-          c = p.tok_ctx[t];
-          row = p.tok_row[t];
-        }
-        nblk = (c + kBS - 1) / kBS;
-      }
-      const int nfull = nblk / p.split_blocks;
-      const int ntail = nblk % p.split_blocks ? 1 : 0;
-      const int cnt = (pass == 0 ? ntail : nfull) * p.num_kv_heads;
-      int total = 0;
-      const int off = carry + block_exclusive_scan(cnt, warp_sums, &total);
-      if (cnt > 0) {
-        if (pass == 0) {
-          for (int g = 0; g < p.num_kv_heads; ++g) p.tasks[off + g] = make_int4(t, g | (nfull << 8), row, c);
-        } else {
-          for (int g = 0; g < p.num_kv_heads; ++g)
-            for (int s = 0; s < nfull; ++s) p.tasks[off + g * nfull + s] = make_int4(t, g | (s << 8), row, c);
-        }
-      }
-      carry += total;
-      __syncthreads();  // warp_sums is reused by the next chunk
+  for (int base = 0; base < p.num_tokens; base += blockDim.x) {
+    const int t = base + threadIdx.x;
+    int nblk = 0, row = 0, c = 0;
+    if (t < p.num_tokens) {
+      const int b = dev::row_of_token(p.qsl, p.num_seqs, t);
+      const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1), ctx = __ldg(p.context_lens + b);
+      const int q_len = q1 - q0;
+      const bool prefill = p.prefill_min_qlen > 0 && q_len >= p.prefill_min_qlen;
+      if (t >= q0 && t < q1 && row_meta_ok(q_len, ctx, p.max_ctx) && !prefill) c = ctx - q_len + (t - q0) + 1;
+      p.tok_row[t] = b;
+      p.tok_ctx[t] = c;  // 0: no decode work (prefill row or invalid metadata)
+      row = b;
+      nblk = (c + kBS - 1) / kBS;
+    }
+    const int nfull = nblk / p.split_blocks, tail = nblk % p.split_blocks;
+    if (tail > 0) atomicAdd(&tail_at[tail], p.num_kv_heads);
+    const int cnt = nfull * p.num_kv_heads;
+    int total = 0;
+    const int off = carry + block_exclusive_scan(cnt, warp_sums, &total);
+    for (int g = 0; g < p.num_kv_heads && cnt > 0; ++g)
+      for (int s = 0; s < nfull; ++s) p.tasks[off + g * nfull + s] = make_int4(t, g | (s << 8), row, c);
+    carry += total;
+    __syncthreads();  // warp_sums is reused by the next chunk
+  }
+  if (threadIdx.x == 0) {  // each last-split size's first slot, largest size first
+    int at = carry;
+    for (int sz = kMaxSplitBlocks; sz >= 1; --sz) {
+      const int n = tail_at[sz];
+      tail_at[sz] = at;
+      at += n;
+    }
+    n_dec = at;
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < p.num_tokens; t += blockDim.x) {
+    const int c = p.tok_ctx[t];  // written by this thread above
+    const int nblk = (c + kBS - 1) / kBS, nfull = nblk / p.split_blocks, tail = nblk % p.split_blocks;
+    if (tail > 0) {
+      const int at = atomicAdd(&tail_at[tail], p.num_kv_heads), row = p.tok_row[t];
+      for (int g = 0; g < p.num_kv_heads; ++g) p.tasks[at + g] = make_int4(t, g | (nfull << 8), row, c);
     }
   }
 
@@ -892,7 +1280,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     });
 
   if (threadIdx.x == 0) {
-    p.hdr->n_tasks = carry;
+    p.hdr->n_tasks = n_dec;
     p.hdr->work = 0;
     p.hdr->done = 0;
     p.hdr->n_items = n_items;
@@ -1026,12 +1414,11 @@ struct FusedAppend {
   const void* k = nullptr;
   const void* v = nullptr;
   const int64_t* slots = nullptr;
-  const int32_t* qsl = nullptr;
 };
 
 // decode (+ merge of very long tokens) and prefill tiles for one layer on a planned workspace
 static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, const int32_t* block_tables,
-                                   int max_blocks, int num_seqs, int num_tokens, void* out, char* ws,
+                                   const int32_t* qsl, int max_blocks, int num_seqs, int num_tokens, void* out, char* ws,
                                    const WsLayout& w, cudaStream_t s, int* launches,
                                    const FusedAppend& fa = FusedAppend()) {
   const pkv_config& c = pool->cfg;
@@ -1039,8 +1426,7 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
   p.kv_map = pool->kv_map;
   p.q = static_cast<const __half*>(q);
   p.block_tables = block_tables;
-  p.tok_row = reinterpret_cast<const int32_t*>(ws + w.tok_row);
-  p.tok_ctx = reinterpret_cast<const int32_t*>(ws + w.tok_ctx);
+  p.qsl = qsl;
   p.tasks = reinterpret_cast<const int4*>(ws + w.tasks);
   p.hdr = reinterpret_cast<WsHeader*>(ws + w.hdr);
   p.out = static_cast<__half*>(out);
@@ -1051,7 +1437,6 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
   p.k_in = static_cast<const __half*>(fa.k);
   p.v_in = static_cast<const __half*>(fa.v);
   p.slots = fa.slots;
-  p.qsl = fa.qsl;
   p.cache_k = static_cast<__half*>(pkv_pool_layer_ptr(pool, layer, 0));
   p.cache_v = static_cast<__half*>(pkv_pool_layer_ptr(pool, layer, 1));
   p.num_slots = (int64_t)c.num_blocks * c.block_size;
@@ -1064,6 +1449,7 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
   p.num_blocks = c.num_blocks;
   p.split_blocks = c.split_blocks;
   p.max_splits = w.max_splits;
+  p.max_tasks = (int)w.max_tasks;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
   const int group = c.num_q_heads / c.num_kv_heads;
   // Prefill rows exist only if some row has at least prefill_min_qlen new tokens.  Their tile kernel goes
@@ -1106,7 +1492,7 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   *launches += 1;
   if (w.max_splits > kFusedMergeSplits) {
-    MergeParams m{p.part_o, p.part_ml, p.tok_ctx, p.out, c.num_q_heads, c.num_kv_heads, group, c.split_blocks,
+    MergeParams m{p.part_o, p.part_ml, reinterpret_cast<const int32_t*>(ws + w.tok_ctx), p.out, c.num_q_heads, c.num_kv_heads, group, c.split_blocks,
                   w.max_splits};
     const dim3 grid(num_tokens, c.num_kv_heads, (kHeadsTile * c.head_dim) / 64);
     switch (c.head_dim) {
@@ -1206,7 +1592,7 @@ extern "C" pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q
     return fail(PKV_ERR_INVALID_ARG, "no matching plan: call pkv_attention_plan for this workspace and metadata");
   const WsLayout w = ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks_per_seq);
   int launches = 0;
-  st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_seqs, num_tokens, out,
+  st = launch_attention(pool, layer, q, block_tables, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens, out,
                         static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches);
   pool->last_launches = launches;
   return st;
@@ -1246,16 +1632,15 @@ extern "C" pkv_status pkv_attention_append(pkv_pool* pool, int32_t layer, const 
     st = pkv_append(pool, layer, k, v, slot_mapping, num_tokens, stream);
     if (st != PKV_OK) return st;
     launches = pool->last_launches;
-    st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_seqs, num_tokens, out,
-                          static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches);
+    st = launch_attention(pool, layer, q, block_tables, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens,
+                          out, static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches);
   } else {
     FusedAppend fa;
     fa.k = k;
     fa.v = v;
     fa.slots = slot_mapping;
-    fa.qsl = query_start_loc;
-    st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_seqs, num_tokens, out,
-                          static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches, fa);
+    st = launch_attention(pool, layer, q, block_tables, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens,
+                          out, static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches, fa);
   }
   pool->last_launches = launches;
   return st;
@@ -1326,8 +1711,8 @@ extern "C" pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const
   e = launch_plan(pool, ws, w, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq, s);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   int launches = 1;
-  st = launch_attention(pool, layer, q, block_tables, max_blocks_per_seq, num_seqs, num_tokens, out, ws, w, s,
-                        &launches);
+  st = launch_attention(pool, layer, q, block_tables, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens, out,
+                        ws, w, s, &launches);
   pool->last_launches = launches;
   return st;
 }
