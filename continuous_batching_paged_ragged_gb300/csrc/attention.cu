@@ -49,7 +49,7 @@ constexpr int kMaxSplitBlocks = 32;   // upper bound on split_blocks (a split's 
 
 constexpr int kSmemPerSM = 228 * 1024;  // shared memory of one SM
 constexpr int kSmemReservedPerCTA = 1024;
-constexpr int kStaticTasks = 2;         // tasks blockIdx.x + j * gridDim.x (j < 2) are a CTA's without a counter
+constexpr int kStaticTasks = 2;         // each CTA's first two tasks come without a counter (see Scheduler)
 
 // One task as the scheduler warp hands it to the streaming warps and the combiner warp (shared memory).
 struct TaskEntry {
@@ -73,21 +73,21 @@ struct DecodeTraits {
   static constexpr int LG = (G + 1) / 2;           // lanes l with (l & 3) < LG hold real heads
   static constexpr int SHL = 8 * LG;               // such lanes
   static constexpr int QD = 3;                     // task queue depth
-  static constexpr int MS = D >= 256 ? 2 : 4;      // split partials a merge stages per round
-  // everything but the rings: shares, staging, merge staging, queue, barriers, flag, alignment slack
-  static constexpr int REST = NW * OV * SHL * 4 + NW * kHeadsTile * 8 + G * D * 4 + MS * (G * D * 4 + 64) +
-                              QD * (int)sizeof(TaskEntry) + (12 * NW + 2 * QD + 1) * 8 + 16 + 1024;
+  static constexpr int QB = kHeadsTile * D * 2;    // a streaming warp's q buffer (8 rows; rows >= G unused)
+  // everything but the rings: q buffers, shares, staging, queue, barriers, flag, alignment slack
+  static constexpr int REST = NW * QB + NW * OV * SHL * 4 + NW * kHeadsTile * 8 + G * D * 4 + 64 +
+                              QD * (int)sizeof(TaskEntry) + (13 * NW + 2 * QD) * 8 + 16 + 1024;
   static constexpr int NR_FIT = (kSmemPerSM / 2 - kSmemReservedPerCTA - REST) / (NW * RUN);
   static constexpr int NR = PKV_DECODE_RING(D) < NR_FIT ? PKV_DECODE_RING(D) : (NR_FIT < 2 ? 2 : NR_FIT);
-  static constexpr int OFF_SHARE = NW * NR * RUN;                    // [NW][OV][SHL] fp32 o shares
+  static constexpr int OFF_QB = NW * NR * RUN;                       // [NW] q buffers
+  static constexpr int OFF_SHARE = OFF_QB + NW * QB;                 // [NW][OV][SHL] fp32 o shares
   static constexpr int OFF_SML = OFF_SHARE + NW * OV * SHL * 4;      // [NW][8] float2 (m, l) shares
   static constexpr int OFF_STG = OFF_SML + NW * kHeadsTile * 8;      // combiner staging [G][D] fp32
-  static constexpr int OFF_MO = OFF_STG + G * D * 4;                 // merge staging: [MS][G][D] fp32 o
-  static constexpr int OFF_MML = OFF_MO + MS * G * D * 4;            // merge staging: [MS][8] float2 (m, l)
-  static constexpr int OFF_Q = OFF_MML + MS * 64;                    // [QD] TaskEntry
+  static constexpr int OFF_MML = OFF_STG + G * D * 4;                // staged split's (m, l): [8] float2
+  static constexpr int OFF_Q = OFF_MML + 64;                         // [QD] TaskEntry
   static constexpr int OFF_BAR = OFF_Q + QD * (int)sizeof(TaskEntry);
-  // barriers: ring [NW][NR], share_full [NW], share_empty [NW], queue full [QD], queue empty [QD], merge
-  static constexpr int NBARS = NW * NR + 2 * NW + 2 * QD + 1;
+  // barriers: ring [NW][NR], share_full [NW], share_empty [NW], queue full [QD], queue empty [QD], q [NW]
+  static constexpr int NBARS = NW * NR + 3 * NW + 2 * QD;
   static constexpr int OFF_FLAG = OFF_BAR + NBARS * 8;               // the CTA's abort flag
   static constexpr int SMEM = OFF_FLAG + 16 + 1024;                  // + slack to align the rings to 1024 bytes
   static constexpr int FIT = kSmemPerSM / (SMEM + kSmemReservedPerCTA);
@@ -95,8 +95,7 @@ struct DecodeTraits {
   static_assert(D % 64 == 0 && G >= 1 && G <= kHeadsTile, "shape");
   static_assert(RUN % 1024 == 0, "swizzled boxes need 1024-byte aligned slots");
   static_assert(8 * D * 2 <= RUN && KS % 2 == 0, "a task's q (8 rows) fits one slot");
-  static_assert(OFF_Q % 16 == 0 && OFF_BAR % 8 == 0 && OFF_STG % 16 == 0 && OFF_MO % 16 == 0 && OFF_MML % 16 == 0,
-                "alignment");
+  static_assert(OFF_Q % 16 == 0 && OFF_BAR % 8 == 0 && OFF_STG % 16 == 0 && OFF_MML % 16 == 0, "alignment");
   static_assert(NR <= PKV_DECODE_RING(D) && SMEM <= OFF_SHARE + REST + 16 * NW + 64, "shared-memory budget");
   static_assert(MINB >= 1, "shared memory");
 };
@@ -168,25 +167,25 @@ template <int D, int G>
 struct DecodeSmem {
   using T = DecodeTraits<D, G>;
   unsigned char* ring;  // [NW][NR] slots of RUN bytes
+  unsigned char* qbuf;  // [NW][QB]
   float* sh_o;          // [NW][OV][SHL]
   float2* sh_ml;        // [NW][8]
   float* stg;           // [G][D] fp32 (or [G][D] fp16 for a final output)
-  float* mo;            // [MS][G][D] merge staging
-  float2* mml;          // [MS][8]
+  float2* mml;          // [8] (m, l) of the staged split
   TaskEntry* queue;     // [QD]
   uint64_t* ring_bar;   // [NW][NR]
   uint64_t* share_full;
   uint64_t* share_empty;
   uint64_t* qfull;
   uint64_t* qempty;
-  uint64_t* merge_bar;
+  uint64_t* qbar;       // [NW] the q buffers' barriers
   volatile int* abort;
   __device__ explicit DecodeSmem(unsigned char* s) {
     ring = s;
+    qbuf = s + T::OFF_QB;
     sh_o = reinterpret_cast<float*>(s + T::OFF_SHARE);
     sh_ml = reinterpret_cast<float2*>(s + T::OFF_SML);
     stg = reinterpret_cast<float*>(s + T::OFF_STG);
-    mo = reinterpret_cast<float*>(s + T::OFF_MO);
     mml = reinterpret_cast<float2*>(s + T::OFF_MML);
     queue = reinterpret_cast<TaskEntry*>(s + T::OFF_Q);
     ring_bar = reinterpret_cast<uint64_t*>(s + T::OFF_BAR);
@@ -194,7 +193,7 @@ struct DecodeSmem {
     share_empty = share_full + T::NW;
     qfull = share_empty + T::NW;
     qempty = qfull + T::QD;
-    merge_bar = qempty + T::QD;
+    qbar = qempty + T::QD;
     abort = reinterpret_cast<volatile int*>(s + T::OFF_FLAG);
   }
 };
@@ -230,16 +229,24 @@ struct Streamer {
   int issued = 0;        // runs issued into the ring so far
   int consumed = 0;      // runs taken out of the ring so far
   int icur = 0;          // 0: the issue cursor is in the current task, 1: in the next one
-  int ir = 0;            // run index of the issue cursor: 0 q, 1 + 2j K of block j, 2 + 2j V of block j
+  int ir = 0;            // run index of the issue cursor: 2j K of block j, 2j + 1 V of block j
   bool has_nxt = false;
-  int pre = 0;           // runs of the first task issued before the dependency wait (slots 1 .. pre-1)
   TaskView cur, nxt;
   bool ok = true;
+  // The task's q does not travel through the ring: it has its own buffer, filled with the next task's q
+  // as soon as that task is published, so no task starts by waiting for it.
+  unsigned char* qbuf;
+  uint64_t* qbar;
+  int q_seq = -1;        // task whose q was last issued into the buffer
+  int q_used = 0;        // q loads taken out of the buffer so far
+  bool q_busy = false;   // the buffer holds (or awaits) a q not yet taken
 
   __device__ Streamer(const DecodeParams& p_, const DecodeSmem<D, G>& sm_, int warp_, int lane_)
       : p(p_), sm(sm_), warp(warp_), lane(lane_) {
     ring = sm.ring + warp * T::NR * T::RUN;
     bars = sm.ring_bar + warp * T::NR;
+    qbuf = sm.qbuf + warp * T::QB;
+    qbar = sm.qbar + warp;
     pol = dev::l2_policy_evict_first();
   }
 
@@ -266,7 +273,7 @@ struct Streamer {
     v.nbw = v.t >= 0 ? warp_blocks(e->nb, v.bw) : 0;
     v.ids = e->ids;
   }
-  static __device__ __forceinline__ int runs(const TaskView& v) { return v.t >= 0 && v.nbw > 0 ? 1 + 2 * v.nbw : 0; }
+  static __device__ __forceinline__ int runs(const TaskView& v) { return v.t >= 0 ? 2 * v.nbw : 0; }
   __device__ __forceinline__ int block_pos(const TaskView& v, int j) const {
     return (v.s * p.split_blocks + v.bw + 4 * j) * kBS;
   }
@@ -274,16 +281,55 @@ struct Streamer {
   __device__ __forceinline__ void issue_slot(const TaskView& v, int r, int slot) {
     unsigned char* dst = ring + slot * T::RUN;
     if (lane != 0) return;
-    if (r == 0) {
-      dev::mbar_arrive_expect_tx(&bars[slot], G * D * 2);
-      dev::bulk_g2s(dst, p.q + ((size_t)v.t * p.num_q_heads + (size_t)v.g * G) * D, G * D * 2, &bars[slot], pol);
-    } else {
-      const int id = v.ids[v.bw + 4 * ((r - 1) >> 1)];
-      const int row = (((r - 1) & 1) ? p.layer_row0_v : p.layer_row0_k) + (id * p.num_kv_heads + v.g) * kBS;
-      dev::mbar_arrive_expect_tx(&bars[slot], T::RUN);
+    const int id = v.ids[v.bw + 4 * (r >> 1)];
+    const int row = ((r & 1) ? p.layer_row0_v : p.layer_row0_k) + (id * p.num_kv_heads + v.g) * kBS;
+    dev::mbar_arrive_expect_tx(&bars[slot], T::RUN);
 #pragma unroll
-      for (int b = 0; b < T::BOXES; ++b) dev::tma_load_2d(dst + b * 2048, &p.kv_map, b * 64, row, &bars[slot], pol);
+    for (int b = 0; b < T::BOXES; ++b) dev::tma_load_2d(dst + b * 2048, &p.kv_map, b * 64, row, &bars[slot], pol);
+  }
+  // Task kk's q into the warp's q buffer (which must be free).
+  __device__ __forceinline__ void issue_q(const TaskView& v, int kk) {
+    if (lane == 0) {
+      dev::fence_proxy_async_smem();  // the warp's reads of the previous q precede this copy
+      dev::mbar_arrive_expect_tx(qbar, G * D * 2);
+      dev::bulk_g2s(qbuf, p.q + ((size_t)v.t * p.num_q_heads + (size_t)v.g * G) * D, G * D * 2, qbar, pol);
     }
+    q_seq = kk;
+    q_busy = true;
+  }
+  // The next task's q as soon as its entry is published; never waits for the entry.
+  __device__ __forceinline__ void prefetch_q() {
+    if (q_busy || q_seq == k + 1 || cur.t < 0 || !ok) return;
+    if (!has_nxt) {
+      const bool ready = __all_sync(0xffffffffu, dev::mbar_test_wait(&sm.qfull[(k + 1) % T::QD], ((k + 1) / T::QD) & 1));
+      if (!ready) return;
+      take(k + 1, nxt);
+      has_nxt = true;
+    }
+    if (ok && nxt.t >= 0 && nxt.nbw > 0) issue_q(nxt, k + 1);
+  }
+  // The current task's q as MMA B fragments (Q^T: k = dims, n = heads); rows G..7 of the buffer hold stale
+  // bytes, which only feed score and output columns of heads >= G, never written out.  Then the buffer is
+  // free for the next task's q.
+  __device__ __forceinline__ void load_q(uint32_t (&qb)[T::KS][2]) {
+    if (q_seq != k) issue_q(cur, k);  // not prefetched
+    const bool got = cta_wait(qbar, q_used & 1, sm.abort, p.err);
+    ok = __all_sync(0xffffffffu, got) && ok;
+    if (!ok) return;
+    const uint32_t qs = dev::smem_addr(qbuf);
+#pragma unroll
+    for (int k2 = 0; k2 < T::KS / 2; ++k2) {
+      uint32_t r4[4];
+      dev::ldsm_x4(qs + (lane & 7) * (D * 2) + (4 * k2 + (lane >> 3)) * 16, r4);
+      qb[2 * k2][0] = r4[0];
+      qb[2 * k2][1] = r4[1];
+      qb[2 * k2 + 1][0] = r4[2];
+      qb[2 * k2 + 1][1] = r4[3];
+    }
+    ++q_used;
+    q_busy = false;
+    __syncwarp();  // every lane's reads precede the next copy into the buffer
+    prefetch_q();
   }
   __device__ __forceinline__ void issue_run(const TaskView& v, int r) {
     issue_slot(v, r, issued % T::NR);
@@ -303,6 +349,7 @@ struct Streamer {
       if (cur.t < 0) return false;
       take(k + 1, nxt);
       has_nxt = true;
+      prefetch_q();
     }
     if (ok && ir < runs(nxt)) {
       issue_run(nxt, ir++);
@@ -334,24 +381,22 @@ struct Streamer {
   // from the appended inputs anyway).  q comes after the wait.
   __device__ void prologue() {
     take(0, cur);
-    if (!ok || runs(cur) == 0) return;
-    pre = 1;
-    while (pre < T::NR && pre < runs(cur)) {
-      const int bpos = block_pos(cur, (pre - 1) >> 1);
+    if (!ok) return;
+    while (issued < T::NR && issued < runs(cur)) {
+      const int bpos = block_pos(cur, issued >> 1);
       if (!(p.k_in != nullptr || p.late_wait || bpos + kBS <= cur.nst)) break;
-      issue_slot(cur, pre, pre);
-      ++pre;
+      issue_slot(cur, issued, issued);
+      ++issued;
     }
+    ir = issued;
   }
   __device__ void after_wait() {
-    if (!ok || runs(cur) == 0) return;
-    issue_slot(cur, 0, 0);
-    issued = pre;
-    ir = pre;
+    if (ok && runs(cur) > 0) issue_q(cur, 0);
   }
   // The copies issued but not consumed must land before the CTA leaves (each wait bounded).
   __device__ void drain() {
     for (; consumed < issued; ++consumed) dev::mbar_wait(&bars[consumed % T::NR], (consumed / T::NR) & 1);
+    if (q_busy) dev::mbar_wait(qbar, q_used & 1);
   }
   __device__ __forceinline__ void advance() {
     if (!has_nxt) take(k + 1, nxt);
@@ -381,21 +426,9 @@ __device__ __forceinline__ void stream_loop(const DecodeParams& p, const DecodeS
     for (int mt = 0; mt < T::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
     if (d.nbw > 0 && w.ok) {
-      // ---- q as the MMA B operand (Q^T: k = dims, n = heads), from the task's first ring run ----
-      // Rows G..7 of the 8-row tile hold stale bytes; they only feed score and output columns of heads
-      // >= G, which are never written out.
+      // ---- q as the MMA B operand (Q^T: k = dims, n = heads) ----
       uint32_t qb[T::KS][2];
-      const uint32_t qs = w.wait_run();
-#pragma unroll
-      for (int k2 = 0; k2 < T::KS / 2; ++k2) {
-        uint32_t r4[4];
-        dev::ldsm_x4(qs + (lane & 7) * (D * 2) + (4 * k2 + (lane >> 3)) * 16, r4);
-        qb[2 * k2][0] = r4[0];
-        qb[2 * k2][1] = r4[1];
-        qb[2 * k2 + 1][0] = r4[2];
-        qb[2 * k2 + 1][1] = r4[3];
-      }
-      w.release_run();
+      w.load_q(qb);
 
       for (int j = 0; j < d.nbw && w.ok; ++j) {
         const int bpos = w.block_pos(d, j);  // the block's first position
@@ -505,6 +538,7 @@ __device__ __forceinline__ void stream_loop(const DecodeParams& p, const DecodeS
           if (ntok < kBS || nov > 0) dev::fence_proxy_async_smem();  // generic writes precede the next TMA write
           w.release_run();
         }
+        w.prefetch_q();  // the next task's q, once the scheduler has published it
         // ---- fused append: the token's own key and value into the cache ----
         if (own && slot != -1) {
           if (slot < 0 || slot >= p.num_slots) {
@@ -637,11 +671,11 @@ __device__ __forceinline__ void frag_coord(int lane, int r, int& dim, int& head)
 }
 
 // ---------------------------------------------------------------------------------------------------
-// Scheduler warp: publishes the CTA's tasks into the queue.  The first two are static (blockIdx.x and
-// blockIdx.x + gridDim.x, published before the dependency wait); every later one is claimed from a global
-// counter only when the streaming warps have moved on from the task whose queue slot it takes, so a CTA
-// holds at most two tasks it has not started and the launch ends balanced (the task list is ordered
-// largest first).
+// Scheduler warp: publishes the CTA's tasks into the queue.  The first two are static and published before
+// the dependency wait: task blockIdx.x and task 2 * gridDim.x - 1 - blockIdx.x, so that over a task list
+// ordered largest first every CTA starts with a pair of about the same total size.  Every later task is
+// claimed from a global counter once the streaming warps have finished the task two entries back: a CTA
+// then holds one task it has not started, and the launch ends balanced.
 // ---------------------------------------------------------------------------------------------------
 template <int D, int G>
 struct Scheduler {
@@ -715,19 +749,20 @@ struct Scheduler {
   // Before the dependency wait: the static entries (they touch no counter).
   __device__ void prologue() {
     n_tasks = __ldcg(&p.hdr->n_tasks);
-    int idx[kStaticTasks];
-#pragma unroll
-    for (int j = 0; j < kStaticTasks; ++j) idx[j] = blockIdx.x + j * gridDim.x;
+    static_assert(kStaticTasks == 2, "static pairing");
+    const int idx[kStaticTasks] = {(int)blockIdx.x, 2 * (int)gridDim.x - 1 - (int)blockIdx.x};
     publish(idx);
   }
   __device__ void run() {
     static_assert(kStaticTasks < T::QD, "queue");
     if (ended) return;
     if (lane == 0) next_dyn = atomicAdd(&p.hdr->work, 1);
+    static_assert(T::QD == 3, "entry m is claimed after task m - 2, whose slot is (m - 2) % 3");
     while (!ended) {
-      // the slot's previous task must be left by every streaming warp and read by the combiner
-      if (filled >= T::QD &&
-          !cta_wait(&sm.qempty[filled % T::QD], ((filled - T::QD) / T::QD) & 1, sm.abort, p.err))
+      // claim entry m once every streaming warp has finished task m - 2 and the combiner has read it (which
+      // also frees entry m's slot, last used by task m - 3)
+      if (filled >= 2 &&
+          !cta_wait(&sm.qempty[(filled - 2) % T::QD], ((filled - 2) / T::QD) & 1, sm.abort, p.err))
         return;
       const int idx[1] = {kStaticTasks * (int)gridDim.x + __shfl_sync(0xffffffffu, next_dyn, 0)};
       publish(idx);
@@ -737,40 +772,34 @@ struct Scheduler {
 };
 
 // ---------------------------------------------------------------------------------------------------
-// Combiner warp: combines the streaming warps' shares of every task with log-sum-exp weights, writes a
-// one-split token's fp16 output or a split's unnormalised partial, counts finished splits on the token's
-// counter, and merges a token whose count it completed.  Nothing here stalls the streaming warps.
-// A split's count is issued one task after its partial was written and examined one task later still,
-// so neither the release (which waits for earlier stores) nor the atomic's round trip stalls the warp.
+// Combiner warp: combines the streaming warps' shares of every task with log-sum-exp weights and writes a
+// one-split token's fp16 output.  A split of a multi-split token is finished one of two ways:
+//  * every other split of the token was already counted when the combiner took the task (an acquire load
+//    of the token's counter, issued as the task starts): it merges the token at once -- the other splits'
+//    partials from L2, its own from shared memory -- and resets the counter.  Under the largest-first task
+//    order this is the usual case for a token's last, small split.
+//  * otherwise it writes its unnormalised partial and counts it on the token's counter; the count is
+//    issued one task later (its release then waits for no fresh store) and examined one task later still
+//    (its round trip hidden), and the warp that completes the count merges the token.
+// Nothing here stalls the streaming warps.
 // ---------------------------------------------------------------------------------------------------
 template <int D, int G>
 struct Combiner {
   using T = DecodeTraits<D, G>;
+  static constexpr int NG = G * D / 4;         // groups of 4 consecutive dims of one head (the G heads)
+  static constexpr int EG = (NG + 31) / 32;    // groups per lane
+  static constexpr int R = EG <= 6 ? 2 : 1;    // other splits whose loads are in flight together
   const DecodeParams& p;
   const DecodeSmem<D, G>& sm;
   int lane;
-  uint32_t merges = 0;   // merge rounds staged so far (parity of merge_bar)
 
   __device__ Combiner(const DecodeParams& p_, const DecodeSmem<D, G>& sm_, int lane_) : p(p_), sm(sm_), lane(lane_) {}
 
-  // A count issued earlier: lane 0 holds the counter's old value.  The warp that completes a token's
-  // count merges it.
-  __device__ bool finish_count(int tg, int nsplit, int prev_lane0) {
-    const int prev = __shfl_sync(0xffffffffu, prev_lane0, 0);
-    if (prev != nsplit - 1) return true;
-    if (lane == 0) {
-      p.merge_cnt[tg] = 0;       // ready for the next launch on this plan
-      dev::fence_acq_rel_gpu();  // acquire: the other splits' partials, released with their counts
-    }
-    __syncwarp();
-    return merge_staged(tg, nsplit);
-  }
-  // Merge a token's split partials (all final) into its fp16 output: rounds of MS partials staged in
-  // shared memory by bulk copies whose loads are all in flight together, combined with log-sum-exp
-  // weights in split order, so the result does not depend on which CTA merges.
-  __device__ bool merge_staged(int tg, int nsplit) {
-    constexpr int NG = G * D / 4;         // groups of 4 consecutive dims of one head
-    constexpr int EG = (NG + 31) / 32;    // groups per lane
+  // Merge the nsplit partials of token-head tg (all final) into its fp16 output with log-sum-exp weights in
+  // split order, so the result does not depend on which CTA merges or how.  Split `own` (-1: none) is this
+  // warp's and was never written out: its o is in the staging buffer ([G][D] fp32), its (m, l) in own_ml.
+  // The others are read from L2 (.cg): they were written by other CTAs during this launch.
+  __device__ void merge(int tg, int nsplit, int own) {
     const size_t sb = (size_t)tg * p.max_splits;
     float M[EG], L[EG];
     float4 acc[EG];
@@ -780,41 +809,62 @@ struct Combiner {
       L[j] = 0.f;
       acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    // the partials were written through the generic proxy (other CTAs, and this warp): order them before
-    // the bulk copies' reads
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    for (int s0 = 0; s0 < nsplit; s0 += T::MS) {
-      const int ms = min(T::MS, nsplit - s0);
-      __syncwarp();
-      if (lane == 0) {
-        dev::fence_proxy_async_smem();  // this warp's reads of the previous round precede the new copies
-        dev::mbar_arrive_expect_tx(sm.merge_bar, ms * (G * D * 4 + kHeadsTile * 8));
-        for (int u = 0; u < ms; ++u) {
-          const size_t pi = (sb + s0 + u) * kHeadsTile;
-          dev::bulk_g2s_plain(sm.mo + u * G * D, p.part_o + pi * D, G * D * 4, sm.merge_bar);
-          dev::bulk_g2s_plain(sm.mml + u * kHeadsTile, p.part_ml + pi, kHeadsTile * 8, sm.merge_bar);
+    const int nrem = nsplit - (own >= 0 ? 1 : 0);  // splits read from L2
+    for (int s0 = 0, r0 = 0; s0 < nsplit;) {
+      // this round: the next n splits read from L2 (and the own split, if it falls among them), in order
+      const int n = min(R, nrem - r0);
+      const bool own_in = own >= s0 && own <= s0 + n;
+      const int s1 = min(nsplit, s0 + n + (own_in ? 1 : 0));
+      float4 o[R][EG];
+      float2 ml[R][EG];
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        if (u >= n) break;
+        const int su = s0 + u + (own_in && own <= s0 + u ? 1 : 0);
+#pragma unroll
+        for (int j = 0; j < EG; ++j) {
+          const int e4 = lane + 32 * j;
+          if (e4 < NG) {
+            ml[u][j] = __ldcg(p.part_ml + (sb + su) * kHeadsTile + (4 * e4) / D);
+            o[u][j] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (sb + su) * kHeadsTile * D) + e4);
+          }
         }
       }
-      if (!cta_wait(sm.merge_bar, merges & 1, sm.abort, p.err)) return false;
-      ++merges;
-      for (int u = 0; u < ms; ++u) {
+      int u = 0;
+      for (int s = s0; s < s1; ++s) {
 #pragma unroll
         for (int j = 0; j < EG; ++j) {
           const int e4 = lane + 32 * j;
           if (e4 >= NG) continue;
-          const int h = (4 * e4) / D;
-          const float2 ml = sm.mml[u * kHeadsTile + h];
-          const float4 o = reinterpret_cast<const float4*>(sm.mo + u * G * D)[e4];
-          const float nM = fmaxf(M[j], ml.x);
-          const float a = exp2f(M[j] - nM), f = exp2f(ml.x - nM);
+          float2 m;
+          float4 v;
+          if (s == own) {
+            m = sm.mml[(4 * e4) / D];
+            v = reinterpret_cast<const float4*>(sm.stg)[e4];
+          } else {
+            // u < n <= R: pick the register copy without dynamic indexing
+            m = ml[0][j];
+            v = o[0][j];
+#pragma unroll
+            for (int q = 1; q < R; ++q)
+              if (u == q) {
+                m = ml[q][j];
+                v = o[q][j];
+              }
+          }
+          const float nM = fmaxf(M[j], m.x);
+          const float a = exp2f(M[j] - nM), f = exp2f(m.x - nM);
           M[j] = nM;
-          L[j] = L[j] * a + ml.y * f;
-          acc[j].x = acc[j].x * a + o.x * f;
-          acc[j].y = acc[j].y * a + o.y * f;
-          acc[j].z = acc[j].z * a + o.z * f;
-          acc[j].w = acc[j].w * a + o.w * f;
+          L[j] = L[j] * a + m.y * f;
+          acc[j].x = acc[j].x * a + v.x * f;
+          acc[j].y = acc[j].y * a + v.y * f;
+          acc[j].z = acc[j].z * a + v.z * f;
+          acc[j].w = acc[j].w * a + v.w * f;
         }
+        if (s != own) ++u;
       }
+      s0 = s1;
+      r0 += n;
     }
     const int t = tg / p.num_kv_heads, g = tg % p.num_kv_heads;
 #pragma unroll
@@ -829,6 +879,14 @@ struct Combiner {
       v.y = *reinterpret_cast<const uint32_t*>(&hi);
       *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.num_q_heads + (size_t)g * G) * D + 4 * e4) = v;
     }
+  }
+  // A count issued earlier (acquire-release): lane 0 holds the counter's old value.  The warp that
+  // completes a token's count merges it: returns whether that is this warp.
+  __device__ bool completes_count(int tg, int nsplit, int prev_lane0) {
+    const int prev = __shfl_sync(0xffffffffu, prev_lane0, 0);
+    if (prev != nsplit - 1) return false;
+    if (lane == 0) p.merge_cnt[tg] = 0;  // ready for the next launch on this plan
+    __syncwarp();
     return true;
   }
 
@@ -851,6 +909,10 @@ struct Combiner {
       const int t = rec.x, g = rec.y & 0xFF, s = rec.y >> 8, ctx = rec.w;
       const int nblk = (ctx + kBS - 1) / kBS;
       const int nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
+      const int tg = t * p.num_kv_heads + g;
+      const bool multi = nsplit > 1 && nsplit <= kFusedMergeSplits;
+      int done_lane0 = 0;  // splits of the token counted so far (its result is used after the shares)
+      if (multi && lane == 0) done_lane0 = dev::ld_acquire_gpu(p.merge_cnt + tg);
       // ---- combine the shares in warp order (a fixed order: the result does not depend on timing) ----
       float acc[T::OV];
 #pragma unroll
@@ -902,44 +964,56 @@ struct Combiner {
             frag_coord(lane, r, dim, head);
             if (head < G) sm.stg[head * D + dim] = acc[r];
           }
+          if (lane < T::LG) {
+            sm.mml[2 * lane] = make_float2(M0, L0);
+            sm.mml[2 * lane + 1] = make_float2(M1, L1);
+          }
         }
       }
-      // ---- the count of the partial written one task ago: its stores are long complete, so the release
-      // does not wait; then the count issued one task ago, whose result has arrived: maybe a merge ----
+      // ---- the count of the partial written one task ago (its stores are long complete, so the release
+      // does not wait); then the count issued one task ago, whose result has arrived: maybe a merge ----
       int new_prev = 0;
-      if (wr_tg >= 0 && lane == 0) new_prev = dev::atom_add_release_gpu(p.merge_cnt + wr_tg, 1);
-      if (ct_tg >= 0 && !finish_count(ct_tg, ct_ns, ct_prev)) return;
+      if (wr_tg >= 0 && lane == 0) new_prev = dev::atom_add_acq_rel_gpu(p.merge_cnt + wr_tg, 1);
+      // merges due now: the token whose count completed (all partials in L2), and this task's token if
+      // every other split of it was counted before it started (its own split from shared memory)
+      const bool m1 = ct_tg >= 0 && completes_count(ct_tg, ct_ns, ct_prev);
+      const bool m2 = multi && __shfl_sync(0xffffffffu, done_lane0, 0) == nsplit - 1;
+      if (m2 && lane == 0) p.merge_cnt[tg] = 0;  // nobody else counts this token again in this launch
+      __syncwarp();
+      for (int i = (m1 ? 0 : 1); i < (m2 ? 2 : 1); ++i) {  // one call site keeps the code (and registers) small
+        merge(i == 0 ? ct_tg : tg, i == 0 ? ct_ns : nsplit, i == 0 ? -1 : s);
+      }
       ct_tg = wr_tg;
       ct_ns = wr_ns;
       ct_prev = new_prev;
       wr_tg = -1;
-      // ---- write the output, or the split's partial ----
+      // ---- the output, or the split's partial (unless merged above) ----
       __syncwarp();
       if (nsplit == 1) {
         uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)t * p.num_q_heads + (size_t)g * G) * D);
         for (int c = lane; c < G * D / 8; c += 32) dst[c] = reinterpret_cast<const uint4*>(sm.stg)[c];
+      } else if (m2) {
       } else {
-        const size_t tg = (size_t)t * p.num_kv_heads + g;
-        const size_t pidx = tg * p.max_splits + s;
+        const size_t pidx = (size_t)tg * p.max_splits + s;
         float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * kHeadsTile * D);
         for (int c = lane; c < G * D / 4; c += 32) dst[c] = reinterpret_cast<const float4*>(sm.stg)[c];
         if (real && lane < T::LG) {
           if (2 * lane < G) p.part_ml[pidx * kHeadsTile + 2 * lane] = make_float2(M0, L0);
           if (2 * lane + 1 < G) p.part_ml[pidx * kHeadsTile + 2 * lane + 1] = make_float2(M1, L1);
         }
-        if (nsplit <= kFusedMergeSplits) {
-          wr_tg = (int)tg;
+        if (multi) {
+          wr_tg = tg;
           wr_ns = nsplit;
         }
       }
-      __syncwarp();  // the staging buffer is free again
+      __syncwarp();  // the staging buffers are free again
     }
     // ---- flush: the last partial's count, then the two outstanding results ----
     int new_prev = 0;
-    __syncwarp();
-    if (wr_tg >= 0 && lane == 0) new_prev = dev::atom_add_release_gpu(p.merge_cnt + wr_tg, 1);
-    if (ct_tg >= 0 && !finish_count(ct_tg, ct_ns, ct_prev)) return;
-    if (wr_tg >= 0) finish_count(wr_tg, wr_ns, new_prev);
+    if (wr_tg >= 0 && lane == 0) new_prev = dev::atom_add_acq_rel_gpu(p.merge_cnt + wr_tg, 1);
+    const bool m1 = ct_tg >= 0 && completes_count(ct_tg, ct_ns, ct_prev);
+    const bool m2 = wr_tg >= 0 && completes_count(wr_tg, wr_ns, new_prev);
+    for (int i = (m1 ? 0 : 1); i < (m2 ? 2 : 1); ++i) merge(i == 0 ? ct_tg : wr_tg, i == 0 ? ct_ns : wr_ns, -1);
   }
 };
 
@@ -963,7 +1037,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
       dev::mbar_init(&sm.qfull[i], 1);
       dev::mbar_init(&sm.qempty[i], T::NW + 1);  // the streaming warps and the combiner
     }
-    dev::mbar_init(sm.merge_bar, 1);
+    for (int i = 0; i < T::NW; ++i) dev::mbar_init(&sm.qbar[i], 1);
     *sm.abort = 0;
     dev::fence_mbar_init();
   }
@@ -1008,9 +1082,11 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
 }
 
 // ---------------------------------------------------------------------------------------------------
-// Merge of tokens with more than kFusedMergeSplits splits.  Grid (token, KV head, chunk of partial
-// elements), 256 threads = SG split groups x (256 / SG) element threads; element e of a partial is head
-// e / D, dim e % D.
+// Merge of tokens with more than kFusedMergeSplits splits (long contexts).  Grid (token, KV head, chunk
+// of 32 partial elements of one head); 256 threads = 8 element threads (a float4 each) x 32 split groups.
+// Split group sg folds splits sg, sg + 32, ... into a running (max, sum, o) with four splits' loads in
+// flight; then the 32 groups' results are combined in group order.  A fixed order throughout, so the
+// result depends only on the token's own splits.
 // ---------------------------------------------------------------------------------------------------
 struct MergeParams {
   const float* part_o;
@@ -1024,85 +1100,70 @@ struct MergeParams {
   int max_splits;
 };
 
-template <int D, int SG>
+constexpr int kMergeGroups = 32;  // split groups of the long-context merge
+
+template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
-  constexpr int TE = 256 / SG;                        // threads along the elements
-  constexpr int EPC = SG == 1 ? kHeadsTile * D : TE;  // elements per CTA
-  constexpr int EPT = EPC / TE;              // elements per thread
-  __shared__ float sM[kHeadsTile], sL[kHeadsTile];
-  __shared__ float red[256];
+  __shared__ float4 s_o[kMergeGroups][8];
+  __shared__ float2 s_ml[kMergeGroups];
   dev::griddep_wait();
   dev::griddep_launch_dependents();
   const int t = blockIdx.x, g = blockIdx.y;
   const int ctx = __ldg(p.tok_ctx + t);
-  if (ctx <= 0) return;
+  const int e0 = blockIdx.z * 32;  // the chunk's first element: head e0 / D, dims e0 % D ..
+  if (ctx <= 0 || e0 >= p.group * D) return;
   const int nblk = (ctx + kBS - 1) / kBS;
   const int nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
-  if (nsplit <= kFusedMergeSplits || (int)blockIdx.z * EPC >= p.group * D) return;
+  if (nsplit <= kFusedMergeSplits) return;
+  const int tid = threadIdx.x, e4 = tid & 7, sg = tid >> 3;
+  const int h = e0 / D;
   const size_t sb = ((size_t)t * p.num_kv_heads + g) * p.max_splits;
-  const int tid = threadIdx.x;
-  // per-head max and sum over the splits: thread (head tid % 8, split stride group tid / 8)
-  {
-    const int h = tid & 7;
-    float M = -INFINITY;
-    for (int s = tid >> 3; s < nsplit; s += 32) M = fmaxf(M, p.part_ml[(sb + s) * kHeadsTile + h].x);
-    red[tid] = M;
-    __syncthreads();
-    if (tid < 8) {
-      float x = red[tid];
-      for (int k = 1; k < 32; ++k) x = fmaxf(x, red[tid + 8 * k]);
-      sM[tid] = x;
-    }
-    __syncthreads();
-    M = sM[h];
-    float L = 0.f;
-    for (int s = tid >> 3; s < nsplit; s += 32) {
-      const float2 ml = p.part_ml[(sb + s) * kHeadsTile + h];
-      L += ml.y * exp2f(ml.x - M);
-    }
-    __syncthreads();
-    red[tid] = L;
-    __syncthreads();
-    if (tid < 8) {
-      float x = 0.f;
-      for (int k = 0; k < 32; ++k) x += red[tid + 8 * k];
-      sL[tid] = x;
-    }
-    __syncthreads();
-  }
-  const int te = tid % TE, sg = tid / TE;
-  const int E = p.group * D;  // elements that belong to real query heads
-  float acc[EPT];
-  int heads[EPT];
+  float M = -INFINITY, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto fold = [&](float2 ml, float4 o) {
+    const float nM = fmaxf(M, ml.x);
+    const float a = exp2f(M - nM), f = exp2f(ml.x - nM);
+    M = nM;
+    L = L * a + ml.y * f;
+    acc.x = acc.x * a + o.x * f;
+    acc.y = acc.y * a + o.y * f;
+    acc.z = acc.z * a + o.z * f;
+    acc.w = acc.w * a + o.w * f;
+  };
+  constexpr int U = 4;
+  int s = sg;
+  for (; s + (U - 1) * kMergeGroups < nsplit; s += U * kMergeGroups) {
+    float2 ml[U];
+    float4 o[U];
 #pragma unroll
-  for (int k = 0; k < EPT; ++k) {
-    const int e = blockIdx.z * EPC + te + k * TE;
-    heads[k] = min(e / D, kHeadsTile - 1);
-    acc[k] = 0.f;
-  }
-  for (int s = sg; s < nsplit; s += SG) {
-    const float* po = p.part_o + (sb + s) * kHeadsTile * D;
-    const float2* pml = p.part_ml + (sb + s) * kHeadsTile;
-#pragma unroll
-    for (int k = 0; k < EPT; ++k) {
-      const int e = blockIdx.z * EPC + te + k * TE;
-      if (e < E) acc[k] += po[e] * exp2f(pml[heads[k]].x - sM[heads[k]]);
+    for (int u = 0; u < U; ++u) {
+      const size_t pi = (sb + s + u * kMergeGroups) * kHeadsTile;
+      ml[u] = __ldcg(p.part_ml + pi + h);
+      o[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + pi * D + e0) + e4);
     }
-  }
 #pragma unroll
-  for (int k = 0; k < EPT; ++k) {
-    if constexpr (SG > 1) {
-      __syncthreads();
-      red[tid] = acc[k];
-      __syncthreads();
-      if (sg != 0) continue;
-      for (int j = 1; j < SG; ++j) acc[k] += red[te + j * TE];
-    }
-    const int e = blockIdx.z * EPC + te + k * TE;
-    if (e < E)
-      p.out[((size_t)t * p.num_q_heads + (size_t)g * p.group + heads[k]) * D + e % D] =
-          __float2half_rn(acc[k] / sL[heads[k]]);
+    for (int u = 0; u < U; ++u) fold(ml[u], o[u]);
   }
+  for (; s < nsplit; s += kMergeGroups) {
+    const size_t pi = (sb + s) * kHeadsTile;
+    fold(__ldcg(p.part_ml + pi + h), __ldcg(reinterpret_cast<const float4*>(p.part_o + pi * D + e0) + e4));
+  }
+  s_o[sg][e4] = acc;
+  if (e4 == 0) s_ml[sg] = make_float2(M, L);
+  __syncthreads();
+  if (sg != 0) return;
+  M = -INFINITY;
+  L = 0.f;
+  acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q = 0; q < kMergeGroups; ++q)
+    if (s_ml[q].x != -INFINITY) fold(s_ml[q], s_o[q][e4]);  // groups past nsplit hold nothing
+  const float il = 1.f / L;
+  const __half2 lo = __floats2half2_rn(acc.x * il, acc.y * il);
+  const __half2 hi = __floats2half2_rn(acc.z * il, acc.w * il);
+  uint2 v;
+  v.x = *reinterpret_cast<const uint32_t*>(&lo);
+  v.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.num_q_heads + (size_t)g * p.group) * D + e0 + 4 * e4) = v;
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -1494,11 +1555,11 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
   if (w.max_splits > kFusedMergeSplits) {
     MergeParams m{p.part_o, p.part_ml, reinterpret_cast<const int32_t*>(ws + w.tok_ctx), p.out, c.num_q_heads, c.num_kv_heads, group, c.split_blocks,
                   w.max_splits};
-    const dim3 grid(num_tokens, c.num_kv_heads, (kHeadsTile * c.head_dim) / 64);
+    const dim3 grid(num_tokens, c.num_kv_heads, (group * c.head_dim) / 32);
     switch (c.head_dim) {
-      case 64: e = launch_pdl(merge_kernel<64, 4>, grid, dim3(256), 0, s, m); break;
-      case 128: e = launch_pdl(merge_kernel<128, 4>, grid, dim3(256), 0, s, m); break;
-      default: e = launch_pdl(merge_kernel<256, 4>, grid, dim3(256), 0, s, m); break;
+      case 64: e = launch_pdl(merge_kernel<64>, grid, dim3(256), 0, s, m); break;
+      case 128: e = launch_pdl(merge_kernel<128>, grid, dim3(256), 0, s, m); break;
+      default: e = launch_pdl(merge_kernel<256>, grid, dim3(256), 0, s, m); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
     *launches += 1;
