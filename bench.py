@@ -47,7 +47,7 @@ CONFIGS = {
 # DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
 # source they were taken on; reported as null once the source changes.
-TRAFFIC = {"c6583ba3d0c8": 142.62e6}  # profiles/decode_kernel_qwen_decode.md
+TRAFFIC = {"3499382d1aba": 142.48e6}  # profiles/decode_kernel_qwen_decode.md
 
 FALLBACK_HBM_GBS = 6800.0
 
@@ -459,7 +459,7 @@ def run_pkv(args, rank, world, local):
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
                    "rows": batch.num_seqs, "new_tokens": batch.num_tokens,
                    "context_tokens_per_layer": int(batch.context_lens.sum()), "pool_blocks": batch.num_blocks,
-                   "split_blocks": pool.cfg.split_blocks or 16,
+                   "split_blocks": pool.cfg.split_blocks or pkv.DEFAULT_SPLIT_BLOCKS,
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of K/V per step rotating over "
                          f"{s.num_layers} layer pools", "parallelism": f"replicas x{world}",
                    "launch": "eager" if graph is None else "cuda_graph",

@@ -106,7 +106,7 @@ extern "C" pkv_status pkv_pool_init(const pkv_config* cfg, void* dev_cache, size
     return fail(PKV_ERR_INVALID_ARG, "dev_cache is not device memory");
   pkv_pool* p = new pkv_pool();
   p->cfg = *cfg;
-  if (p->cfg.split_blocks == 0) p->cfg.split_blocks = 16;
+  if (p->cfg.split_blocks == 0) p->cfg.split_blocks = 32;
   p->base = static_cast<char*>(dev_cache);
   p->cache_bytes = cache_bytes_of(cfg);
   p->dev_error = reinterpret_cast<int32_t*>(p->base + p->cache_bytes);

@@ -28,6 +28,8 @@ PKV_DEVERR_ROW_META = 0x4
 PKV_DEVERR_QSL = 0x8
 PKV_DEVERR_WAIT_TIMEOUT = 0x10
 
+DEFAULT_SPLIT_BLOCKS = 32  # pkv_config.split_blocks = 0 selects this many blocks per split-K partition
+
 _p = ctypes.c_void_p
 _i32 = ctypes.c_int32
 _i64 = ctypes.c_int64

@@ -71,7 +71,7 @@ typedef struct {
   int32_t head_dim;
   int32_t block_size;    /* tokens per block; must be 16 */
   int32_t num_blocks;    /* physical blocks per layer    */
-  int32_t split_blocks;  /* blocks per split-K partition of a decode row; 0 = library default (16) */
+  int32_t split_blocks;  /* blocks per split-K partition of a decode row; 0 = library default (32) */
 } pkv_config;
 
 typedef struct pkv_pool pkv_pool;

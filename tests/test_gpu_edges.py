@@ -9,9 +9,10 @@ from helpers_gpu import assert_close, oracle_row, row_slice, run_batch
 
 pytestmark = pytest.mark.gpu
 
-# (cached, q_len) rows around block (16) and split (16 blocks = 256 tokens) boundaries, plus chunks
+# (cached, q_len) rows around block (16 tokens) and split boundaries (the default split of 32 blocks is 512
+# tokens; 16-block splits, 256 tokens, are covered too), plus chunks
 ROWS = [(0, 1), (1, 1), (14, 1), (15, 1), (16, 1), (255, 1), (256, 1), (257, 1), (511, 1), (512, 1), (700, 1),
-        (16, 3), (0, 33), (240, 17), (500, 12), (0, 2)]
+        (1023, 1), (1024, 1), (16, 3), (0, 33), (240, 17), (500, 12), (1020, 6), (0, 2)]
 SHAPES = [(4, 2, 64), (12, 2, 128), (16, 4, 256), (8, 8, 128), (8, 1, 128), (16, 2, 64), (4, 1, 256)]
 
 
