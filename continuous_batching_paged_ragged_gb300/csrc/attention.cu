@@ -50,6 +50,7 @@ constexpr int kMaxSplitBlocks = 32;   // upper bound on split_blocks (a split's 
 constexpr int kSmemPerSM = 228 * 1024;  // shared memory of one SM
 constexpr int kSmemReservedPerCTA = 1024;
 constexpr int kStaticTasks = 2;         // each CTA's first two tasks come without a counter (see Scheduler)
+constexpr int kEagerClaimBlocks = 8;    // past tasks this small, the scheduler claims as early as slots allow
 
 // One task as the scheduler warp hands it to the streaming warps and the combiner warp (shared memory).
 struct TaskEntry {
@@ -240,6 +241,7 @@ struct Streamer {
   int q_seq = -1;        // task whose q was last issued into the buffer
   int q_used = 0;        // q loads taken out of the buffer so far
   bool q_busy = false;   // the buffer holds (or awaits) a q not yet taken
+  bool cur_q_done = false;  // the current task's q is taken (or the task needs none): the buffer may refill
 
   __device__ Streamer(const DecodeParams& p_, const DecodeSmem<D, G>& sm_, int warp_, int lane_)
       : p(p_), sm(sm_), warp(warp_), lane(lane_) {
@@ -297,12 +299,15 @@ struct Streamer {
     q_seq = kk;
     q_busy = true;
   }
+  // Whether the scheduler has published task kk (never waits).
+  __device__ __forceinline__ bool published(int kk) const {
+    return __all_sync(0xffffffffu, dev::mbar_test_wait(&sm.qfull[kk % T::QD], (kk / T::QD) & 1));
+  }
   // The next task's q as soon as its entry is published; never waits for the entry.
   __device__ __forceinline__ void prefetch_q() {
-    if (q_busy || q_seq == k + 1 || cur.t < 0 || !ok) return;
+    if (!cur_q_done || q_busy || q_seq == k + 1 || cur.t < 0 || !ok) return;
     if (!has_nxt) {
-      const bool ready = __all_sync(0xffffffffu, dev::mbar_test_wait(&sm.qfull[(k + 1) % T::QD], ((k + 1) / T::QD) & 1));
-      if (!ready) return;
+      if (!published(k + 1)) return;
       take(k + 1, nxt);
       has_nxt = true;
     }
@@ -328,6 +333,7 @@ struct Streamer {
     }
     ++q_used;
     q_busy = false;
+    cur_q_done = true;
     __syncwarp();  // every lane's reads precede the next copy into the buffer
     prefetch_q();
   }
@@ -335,7 +341,9 @@ struct Streamer {
     issue_slot(v, r, issued % T::NR);
     ++issued;
   }
-  // Issue the next run of the stream (current task, then the next one), if there is one.
+  // Issue the next run of the stream (current task, then the next one), if there is one.  Crossing into
+  // the next task never waits for it to be published: the task in hand comes first, and a later release
+  // tries again.
   __device__ __forceinline__ bool issue_next() {
     if (icur == 0) {
       if (ir < runs(cur)) {
@@ -346,7 +354,7 @@ struct Streamer {
       ir = 0;
     }
     if (!has_nxt) {
-      if (cur.t < 0) return false;
+      if (cur.t < 0 || !published(k + 1)) return false;
       take(k + 1, nxt);
       has_nxt = true;
       prefetch_q();
@@ -382,6 +390,7 @@ struct Streamer {
   __device__ void prologue() {
     take(0, cur);
     if (!ok) return;
+    cur_q_done = cur.nbw == 0;
     while (issued < T::NR && issued < runs(cur)) {
       const int bpos = block_pos(cur, issued >> 1);
       if (!(p.k_in != nullptr || p.late_wait || bpos + kBS <= cur.nst)) break;
@@ -405,6 +414,7 @@ struct Streamer {
     has_nxt = false;
     icur = 0;
     ++k;
+    cur_q_done = cur.nbw == 0;  // a task with no blocks for this warp needs no q
   }
 };
 
@@ -687,6 +697,7 @@ struct Scheduler {
   int filled = 0;        // queue entries published so far (task sequence numbers 0 .. filled-1)
   bool ended = false;    // an end-of-work entry has been published
   int next_dyn = 0;      // lane 0: result of the counter increment for the next dynamic entry
+  int last_nb = 1 << 30; // blocks of the task published last
 
   __device__ Scheduler(const DecodeParams& p_, const DecodeSmem<D, G>& sm_, int lane_) : p(p_), sm(sm_), lane(lane_) {}
 
@@ -741,6 +752,7 @@ struct Scheduler {
       }
       ++filled;
       ended = rec[j].x < 0;
+      last_nb = nb;
     }
     __syncwarp();
     if (lane == 0)
@@ -760,10 +772,12 @@ struct Scheduler {
     static_assert(T::QD == 3, "entry m is claimed after task m - 2, whose slot is (m - 2) % 3");
     while (!ended) {
       // claim entry m once every streaming warp has finished task m - 2 and the combiner has read it (which
-      // also frees entry m's slot, last used by task m - 3)
-      if (filled >= 2 &&
-          !cta_wait(&sm.qempty[(filled - 2) % T::QD], ((filled - 2) / T::QD) & 1, sm.abort, p.err))
-        return;
+      // also frees entry m's slot, last used by task m - 3).  Once the list has reached small tasks (it is
+      // ordered largest first) a CTA can hold one more without unbalancing the launch, and claiming as
+      // soon as the slot is free lets the last tasks' tiles be in flight before a warp reaches them.
+      const bool small = last_nb <= kEagerClaimBlocks;
+      const int gate = small ? filled - T::QD : filled - 2;
+      if (gate >= 0 && !cta_wait(&sm.qempty[gate % T::QD], (gate / T::QD) & 1, sm.abort, p.err)) return;
       const int idx[1] = {kStaticTasks * (int)gridDim.x + __shfl_sync(0xffffffffu, next_dyn, 0)};
       publish(idx);
       if (!ended && lane == 0) next_dyn = atomicAdd(&p.hdr->work, 1);  // used at the next publish
