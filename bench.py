@@ -77,6 +77,13 @@ def measured_peak(key: str = "hbm_gbs", fallback: float = FALLBACK_HBM_GBS):
         return fallback, "fallback"
 
 
+def long_merge(batch: synth.StepBatch, pool) -> bool:
+    """Whether some token of the pass has more than 32 splits (then a merge launch follows each decode)."""
+    split = pool.cfg.split_blocks or pkv.DEFAULT_SPLIT_BLOCKS
+    nblk = (batch.context_lens.astype(np.int64) + 15) // 16
+    return bool((((nblk + split - 1) // split) > 32).any())
+
+
 def prefill_flops(batch: synth.StepBatch) -> int:
     """Per layer: 4 d Hq (causal query-key pairs) over the rows that take the tile kernel."""
     s = batch.shape
@@ -447,7 +454,13 @@ def run_pkv(args, rank, world, local):
         return
     peak, peak_src = measured_peak()
     kernel_bytes = attn_bytes + (append_bytes if step.fused else 0)
-    achieved = kernel_bytes / (attn_ms * 1e-3) / 1e9
+    # The dominant kernel's average launch duration over the timed region: with the fused call a step is
+    # one plan launch plus one attention launch per layer (plus the long-context merge launch where a
+    # token has more than 32 splits), so the step time over the layer count is an upper bound on it (the
+    # plan's share is charged to the attention).  Layers are pipelined through programmatic dependent
+    # launch inside the timed region; `isolated_call_ms` is the same call issued alone, between events.
+    per_call_ms = ms / len(layers) if (step.fused and graph is not None) else attn_ms
+    achieved = kernel_bytes / (per_call_ms * 1e-3) / 1e9
     sh = source_hash()
     value = step_bytes * world / (ms * 1e-3) / 1e9
     line = {
@@ -469,8 +482,13 @@ def run_pkv(args, rank, world, local):
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": TRAFFIC.get(sh),
-                     "kernel": "decode_kernel (split-K decode, fused merge" + (", fused append)" if step.fused else ")"),
-                     "per_launch_bytes": kernel_bytes, "avg_launch_ms": attn_ms, "peak_source": peak_src,
+                     "kernel": "decode_kernel (split-K decode, fused merge" + (", fused append)" if step.fused else ")")
+                               + (" + merge_kernel (tokens with > 32 splits)" if long_merge(batch, pool) else ""),
+                     "per_launch_bytes": kernel_bytes, "avg_launch_ms": per_call_ms,
+                     "avg_launch_over": "timed region (CUDA graph, step time / layers)"
+                                        if per_call_ms is not attn_ms else "per-call CUDA events",
+                     "isolated_call_ms": attn_ms,
+                     "isolated_frac": kernel_bytes / (attn_ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
                      "source": sh},
         "e2e": e2e,
         "clocks": clocks,
@@ -492,6 +510,99 @@ def run_pkv(args, rank, world, local):
                                             "max": max(hbm_ms, tensor_ms), "measured": ms}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(batch)
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------------------
+# Scheduler-driven trace under each allocation policy and unit of scheduling
+# ----------------------------------------------------------------------------------------------------
+
+TRACE_POLICIES = [  # (name, allocation policy, unit of scheduling, declared output / real output, max_num_seqs)
+    ("on_demand/pass", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 256),
+    ("reserve 1x/pass", pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 1.0, 256),
+    ("reserve 4x/pass", pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 4.0, 256),
+    ("on_demand/pass cap 64", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 64),
+    ("on_demand/request cap 64", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_REQUEST, 1.0, 64),
+]
+
+
+def run_sched_trace(args, rank, world, local):
+    """256 trace requests (lognormal prompts, U[50, 781] outputs, token budget 8,192, 20,000 blocks of 16,
+    max_num_seqs 256, or 64 for the comparison of units of scheduling) run to exhaustion under each policy;
+    every pass is the plan + 28 x fused append and attention on the GPU.  Only the GPU work of a pass is timed (CUDA events around it); the host
+    scheduler and the metadata upload run between passes, outside the timed work."""
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    L, Hq, Hkv, d, nblk, cap, budget = 28, 12, 2, 128, 20000, 256, 8192
+    reqs = synth.trace_requests(0)
+    max_w = max((r.prompt_len + r.max_output + 15) // 16 for r in reqs)
+    pool = pkv.Pool(L, Hq, Hkv, d, nblk)
+    q = torch.zeros(budget, Hq, d, dtype=torch.float16, device=dev)
+    k = torch.zeros(budget, Hkv, d, dtype=torch.float16, device=dev)
+    v = torch.zeros_like(k)
+    out = torch.empty_like(q)
+    bt = torch.empty(cap * max_w, dtype=torch.int32, device=dev)
+    ctx = torch.empty(cap, dtype=torch.int32, device=dev)
+    qsl = torch.empty(cap + 1, dtype=torch.int32, device=dev)
+    slots = torch.empty(budget, dtype=torch.int64, device=dev)
+    ws_bytes = pkv.pkv_attention_workspace_bytes(pool.handle, cap, budget, max_w)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    lib = pkv.load()
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    results = []
+    for name, alloc, unit, declared, max_seqs in TRACE_POLICIES:
+        sched = pkv.Scheduler(max_seqs, budget, 16, nblk, synth.block_permutation(nblk, 0), alloc=alloc, unit=unit)
+        for r in reqs:
+            sched.add(r.req_id, r.prompt_len, r.max_output, int(round(declared * r.max_output)))
+        events, steps, launches = [], 0, 0
+        while not sched.done():
+            st = sched.step()
+            B, T, W = len(st["req_ids"]), int(st["query_start_loc"][-1]), st["max_blocks_per_seq"]
+            bt[:B * W].copy_(torch.from_numpy(st["block_tables"].reshape(-1)), non_blocking=False)
+            ctx[:B].copy_(torch.from_numpy(st["context_lens"]))
+            qsl[:B + 1].copy_(torch.from_numpy(st["query_start_loc"]))
+            slots[:T].copy_(torch.from_numpy(st["slot_mapping"]))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            pkv._check(lib.pkv_attention_plan(pool.handle, ctx.data_ptr(), qsl.data_ptr(), B, T, W, ws.data_ptr(),
+                                              ws_bytes, sp), "pkv_attention_plan")
+            launches += lib.pkv_last_launch_count(pool.handle)
+            for layer in range(L):
+                pkv._check(lib.pkv_attention_append(pool.handle, layer, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                    slots.data_ptr(), bt.data_ptr(), W, ctx.data_ptr(),
+                                                    qsl.data_ptr(), B, T, out.data_ptr(), ws.data_ptr(), ws_bytes,
+                                                    sp), "pkv_attention_append")
+                launches += lib.pkv_last_launch_count(pool.handle)
+            b.record(stream)
+            events.append((a, b))
+            steps += 1
+            if len(events) >= 256:  # keep the host from running far ahead of the device
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert pool.check() == 0
+        gpu_s = sum(x.elapsed_time(y) for x, y in events) / 1e3
+        stt = sched.stats()
+        sched.close()
+        outputs = sum(r.max_output for r in reqs)
+        results.append({"policy": name, "max_num_seqs": max_seqs, "output_tokens_per_s": outputs / gpu_s,
+                        "gpu_s": gpu_s, "steps": steps,
+                        "preemptions": stt["preemptions"], "recomputed_tokens": stt["recomputed_tokens"],
+                        "max_batch": stt["max_batch"], "mean_batch": stt["batch_sum"] / max(1, stt["steps"]),
+                        "live_cache": stt["live_tokens"] / max(1, stt["held_slots"]),
+                        "tokens_scheduled": stt["tokens_scheduled"], "gpu_launches": launches})
+    if rank != 0:
+        return
+    head = results[0]
+    line = {"metric": "scheduler-driven trace: output tokens/s over the GPU time of its passes", "value":
+            head["output_tokens_per_s"], "unit": "tokens/s", "n_gpus": world, "steps": head["steps"], "warmup": 0,
+            "ms_per_step": head["gpu_s"] * 1e3 / head["steps"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded trace: 256 requests, lognormal prompts "
+            "median 300 clipped [16, 4096], outputs U[50, 781])",
+            "config": {"workload": "sched_trace", "layers": L, "num_q_heads": Hq, "num_kv_heads": Hkv,
+                       "head_dim": d, "pool_blocks": nblk, "max_num_seqs": cap, "token_budget": budget,
+                       "split_blocks": pkv.DEFAULT_SPLIT_BLOCKS, "launch": "eager (per-pass events)"},
+            "gpu_launches": head["gpu_launches"], "policies": results}
     print(json.dumps(line), flush=True)
 
 
@@ -547,7 +658,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
-    ap.add_argument("--config", default="qwen_decode", choices=sorted(CONFIGS))
+    ap.add_argument("--config", default="qwen_decode", choices=sorted(CONFIGS) + ["sched_trace"])
     ap.add_argument("--split-blocks", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
@@ -559,10 +670,17 @@ def main():
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
     if args.impl == "reference":
+        if args.config == "sched_trace":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the attention workloads; "
+                                  "the scheduler trace's policies are compared on the GPU path only"}), flush=True)
+            return
         return run_reference(args, rank, world)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     try:
+        if args.config == "sched_trace":
+            return run_sched_trace(args, rank, world, local)
         run_pkv(args, rank, world, local)
     finally:
         if world > 1:

@@ -15,6 +15,12 @@
 // Readings where the pages say nothing: FIFO admission with head-of-line blocking; a pass that computes
 // a request's last known token yields one output token; a request with max_output outputs finishes and
 // frees its blocks in the same pass; freed blocks join the tail of the free list in block-table order.
+//
+// Variants (same page, "The allocator is the other half" and "The boundary: when this is worth nothing"):
+// RESERVE admits a request only when its whole reservation, ceil((prompt + declared output) / block_size)
+// blocks, is free, takes it at admission and returns it at finish, and therefore never preempts;
+// UNIT_REQUEST admits only while a batch forms (from a pass that starts with nothing running until the
+// first pass in which a member finishes).  A row's block table lists the blocks its context occupies.
 #include <algorithm>
 #include <cstdint>
 #include <deque>
@@ -38,6 +44,7 @@ struct Req {
   int64_t id;
   int32_t prompt_len;
   int32_t max_output;
+  int32_t declared_output;
   int64_t num_computed = 0;
   int64_t num_output = 0;
   Status status = Status::kWaiting;
@@ -55,6 +62,10 @@ struct Scheduled {
 
 struct pkv_sched {
   pkv_sched_config cfg;
+  int32_t alloc = PKV_ALLOC_ON_DEMAND;
+  int32_t unit = PKV_UNIT_PASS;
+  bool batch_open = false;  // UNIT_REQUEST: the current batch still takes members
+  bool added_any = false;
   std::deque<int32_t> free_list;
   std::vector<Req*> running;       // arrival (admission) order; back = newest
   std::deque<Req*> waiting;        // front = next to admit
@@ -66,6 +77,23 @@ struct pkv_sched {
 
   ~pkv_sched() {
     for (auto& kv : live) delete kv.second;
+  }
+
+  int64_t reservation(const Req* r) const {
+    return ((int64_t)r->prompt_len + r->declared_output + cfg.block_size - 1) / cfg.block_size;
+  }
+  // Blocks at admission: the whole reservation (RESERVE) or those the first tokens need.
+  bool admit_blocks(Req* r, int64_t num_new) {
+    if (alloc == PKV_ALLOC_RESERVE) {
+      const int64_t need = reservation(r);
+      if (need > (int64_t)free_list.size()) return false;
+      for (int64_t i = 0; i < need; ++i) {
+        r->blocks.push_back(free_list.front());
+        free_list.pop_front();
+      }
+      return true;
+    }
+    return allocate(r, num_new);
   }
 
   bool allocate(Req* r, int64_t num_new) {
@@ -117,16 +145,35 @@ extern "C" pkv_status pkv_sched_create(const pkv_sched_config* cfg, const int32_
 
 extern "C" void pkv_sched_destroy(pkv_sched* s) { delete s; }
 
-extern "C" pkv_status pkv_sched_add(pkv_sched* s, int64_t req_id, int32_t prompt_len, int32_t max_output) {
+extern "C" pkv_status pkv_sched_add_declared(pkv_sched* s, int64_t req_id, int32_t prompt_len, int32_t max_output,
+                                             int32_t declared_output) {
   pkv::clear_error();
   if (!s) return fail(PKV_ERR_INVALID_ARG, "scheduler is NULL");
   if (prompt_len < 1 || max_output < 1) return fail(PKV_ERR_INVALID_ARG, "prompt_len and max_output must be >= 1");
+  if (declared_output < max_output) return fail(PKV_ERR_INVALID_ARG, "declared_output must be >= max_output");
   if (s->live.count(req_id)) return fail(PKV_ERR_INVALID_ARG, "duplicate request id");
-  const int64_t worst = ((int64_t)prompt_len + max_output + s->cfg.block_size - 1) / s->cfg.block_size;
+  const int32_t held = s->alloc == PKV_ALLOC_RESERVE ? declared_output : max_output;
+  const int64_t worst = ((int64_t)prompt_len + held + s->cfg.block_size - 1) / s->cfg.block_size;
   if (worst > s->cfg.num_blocks) return fail(PKV_ERR_NO_BLOCKS, "request can never fit the pool");
-  Req* r = new Req{req_id, prompt_len, max_output};
+  Req* r = new Req{req_id, prompt_len, max_output, declared_output};
   s->live[req_id] = r;
   s->waiting.push_back(r);
+  s->added_any = true;
+  return PKV_OK;
+}
+
+extern "C" pkv_status pkv_sched_add(pkv_sched* s, int64_t req_id, int32_t prompt_len, int32_t max_output) {
+  return pkv_sched_add_declared(s, req_id, prompt_len, max_output, max_output);
+}
+
+extern "C" pkv_status pkv_sched_set_policy(pkv_sched* s, int32_t alloc, int32_t unit) {
+  pkv::clear_error();
+  if (!s) return fail(PKV_ERR_INVALID_ARG, "scheduler is NULL");
+  if (alloc != PKV_ALLOC_ON_DEMAND && alloc != PKV_ALLOC_RESERVE) return fail(PKV_ERR_INVALID_ARG, "unknown alloc");
+  if (unit != PKV_UNIT_PASS && unit != PKV_UNIT_REQUEST) return fail(PKV_ERR_INVALID_ARG, "unknown unit");
+  if (s->added_any) return fail(PKV_ERR_INVALID_ARG, "set the policy before adding requests");
+  s->alloc = alloc;
+  s->unit = unit;
   return PKV_OK;
 }
 
@@ -137,6 +184,7 @@ extern "C" pkv_status pkv_sched_step(pkv_sched* s, pkv_step* out) {
   std::vector<Scheduled> sched;
   std::vector<Req*> preempted;
   s->admitted.clear();
+  if (s->unit == PKV_UNIT_REQUEST && s->running.empty()) s->batch_open = true;  // a new batch forms
 
   // phase one: running requests in arrival order
   size_t i = 0;
@@ -165,13 +213,13 @@ extern "C" pkv_status pkv_sched_step(pkv_sched* s, pkv_step* out) {
     ++i;
   }
 
-  // phase two: admission, only if this pass preempted nobody
-  if (preempted.empty()) {
+  // phase two: admission, only if this pass preempted nobody (and, per request, while the batch forms)
+  if (preempted.empty() && (s->unit == PKV_UNIT_PASS || s->batch_open)) {
     while (!s->waiting.empty() && budget > 0) {
       if ((int64_t)s->running.size() >= s->cfg.max_num_seqs) break;
       Req* r = s->waiting.front();
       const int64_t num_new = std::min(r->num_tokens() - r->num_computed, budget);
-      if (!s->allocate(r, num_new)) break;  // head-of-line blocking
+      if (!s->admit_blocks(r, num_new)) break;  // head-of-line blocking
       s->waiting.pop_front();
       r->status = Status::kRunning;
       s->running.push_back(r);
@@ -184,8 +232,8 @@ extern "C" pkv_status pkv_sched_step(pkv_sched* s, pkv_step* out) {
   // the batch handed to the forward pass
   const int64_t bs = s->cfg.block_size;
   const int32_t B = (int32_t)sched.size();
-  int32_t max_blocks = 1;
-  for (auto& x : sched) max_blocks = std::max<int32_t>(max_blocks, (int32_t)x.req->blocks.size());
+  int32_t max_blocks = 1;  // a row's table lists the blocks its context occupies (a reservation may hold more)
+  for (auto& x : sched) max_blocks = std::max<int32_t>(max_blocks, (int32_t)((x.start + x.num_new + bs - 1) / bs));
   s->req_ids.assign(B, 0);
   s->q_lens.assign(B, 0);
   s->context_lens.assign(B, 0);
@@ -198,7 +246,8 @@ extern "C" pkv_status pkv_sched_step(pkv_sched* s, pkv_step* out) {
     s->q_lens[b] = (int32_t)x.num_new;
     s->context_lens[b] = (int32_t)(x.start + x.num_new);
     s->qsl[b + 1] = s->qsl[b] + (int32_t)x.num_new;
-    std::copy(x.req->blocks.begin(), x.req->blocks.end(), s->block_tables.begin() + (size_t)b * max_blocks);
+    const int64_t used = (x.start + x.num_new + bs - 1) / bs;
+    std::copy(x.req->blocks.begin(), x.req->blocks.begin() + used, s->block_tables.begin() + (size_t)b * max_blocks);
     for (int64_t pos = x.start; pos < x.start + x.num_new; ++pos)
       s->slot_mapping.push_back((int64_t)x.req->blocks[pos / bs] * bs + pos % bs);
   }
@@ -223,6 +272,11 @@ extern "C" pkv_status pkv_sched_step(pkv_sched* s, pkv_step* out) {
     }
   }
 
+  if (!s->finished.empty()) s->batch_open = false;  // a member completed: the batch takes no more
+  for (Req* r : s->running) {
+    s->stats.live_tokens += r->num_computed;
+    s->stats.held_slots += (int64_t)r->blocks.size() * bs;
+  }
   s->stats.steps += 1;
   s->stats.preemptions += (int64_t)preempted.size();
   s->stats.max_batch = std::max<int64_t>(s->stats.max_batch, B);

@@ -28,6 +28,11 @@ PKV_DEVERR_ROW_META = 0x4
 PKV_DEVERR_QSL = 0x8
 PKV_DEVERR_WAIT_TIMEOUT = 0x10
 
+PKV_ALLOC_ON_DEMAND = 0
+PKV_ALLOC_RESERVE = 1
+PKV_UNIT_PASS = 0
+PKV_UNIT_REQUEST = 1
+
 DEFAULT_SPLIT_BLOCKS = 32  # pkv_config.split_blocks = 0 selects this many blocks per split-K partition
 
 _p = ctypes.c_void_p
@@ -58,7 +63,8 @@ class pkv_step(ctypes.Structure):
 class pkv_sched_stats(ctypes.Structure):
     _fields_ = [("steps", _i64), ("preemptions", _i64), ("recomputed_tokens", _i64),
                 ("recomputed_prompt_tokens", _i64), ("max_batch", _i64), ("batch_sum", _i64),
-                ("tokens_scheduled", _i64), ("running", _i32), ("waiting", _i32), ("free_blocks", _i32)]
+                ("tokens_scheduled", _i64), ("running", _i32), ("waiting", _i32), ("free_blocks", _i32),
+                ("live_tokens", _i64), ("held_slots", _i64)]
 
 
 # name -> (restype, argtypes); the list every exported symbol of include/pkv.h
@@ -81,6 +87,8 @@ SIGNATURES = {
     "pkv_sched_create": (ctypes.c_int, [ctypes.POINTER(pkv_sched_config), _p, ctypes.POINTER(_p)]),
     "pkv_sched_destroy": (None, [_p]),
     "pkv_sched_add": (ctypes.c_int, [_p, _i64, _i32, _i32]),
+    "pkv_sched_add_declared": (ctypes.c_int, [_p, _i64, _i32, _i32, _i32]),
+    "pkv_sched_set_policy": (ctypes.c_int, [_p, _i32, _i32]),
     "pkv_sched_step": (ctypes.c_int, [_p, ctypes.POINTER(pkv_step)]),
     "pkv_sched_abort": (ctypes.c_int, [_p, _i64]),
     "pkv_sched_set_max_num_seqs": (ctypes.c_int, [_p, _i32]),
@@ -266,7 +274,8 @@ class Pool:
 class Scheduler:
     """The C++ host scheduler (pkv_sched_*), returning numpy copies of each pass's batch."""
 
-    def __init__(self, max_num_seqs: int, token_budget: int, block_size: int, num_blocks: int, free_order=None):
+    def __init__(self, max_num_seqs: int, token_budget: int, block_size: int, num_blocks: int, free_order=None,
+                 alloc: int = 0, unit: int = 0):
         lib = load()
         cfg = pkv_sched_config(max_num_seqs, token_budget, block_size, num_blocks)
         h = _p()
@@ -276,9 +285,15 @@ class Scheduler:
         _check(lib.pkv_sched_create(ctypes.byref(cfg), arr.ctypes.data if arr is not None else None, ctypes.byref(h)),
                "pkv_sched_create")
         self.handle = h.value
+        if alloc or unit:
+            _check(lib.pkv_sched_set_policy(self.handle, alloc, unit), "pkv_sched_set_policy")
 
-    def add(self, req_id: int, prompt_len: int, max_output: int) -> None:
-        _check(load().pkv_sched_add(self.handle, req_id, prompt_len, max_output), "pkv_sched_add")
+    def add(self, req_id: int, prompt_len: int, max_output: int, declared_output: Optional[int] = None) -> None:
+        if declared_output is None:
+            _check(load().pkv_sched_add(self.handle, req_id, prompt_len, max_output), "pkv_sched_add")
+        else:
+            _check(load().pkv_sched_add_declared(self.handle, req_id, prompt_len, max_output, declared_output),
+                   "pkv_sched_add_declared")
 
     def step(self) -> dict:
         st = pkv_step()

@@ -276,7 +276,22 @@ typedef struct {
   int32_t running;
   int32_t waiting;
   int32_t free_blocks;
+  int64_t live_tokens;              /* summed over passes, after each pass: tokens running requests hold */
+  int64_t held_slots;               /* summed over passes: slots of the blocks running requests hold    */
 } pkv_sched_stats;
+
+/* Block allocation policies and units of scheduling (pkv_sched_set_policy).  [CB] "The allocator is
+ * the other half": on demand (the default) allocates a request's blocks as its tokens are computed and
+ * preempts when the pool runs out; RESERVE (Orca) admits a request only if its worst case fits --
+ * ceil((prompt_len + declared_output) / block_size) free blocks, all taken at admission and returned when
+ * it finishes -- so it never preempts, at the price of holding cache for output the client only claimed.
+ * [CB] "The boundary: when this is worth nothing": UNIT_PASS re-decides membership every pass (continuous
+ * batching, the default); UNIT_REQUEST is static batching: a batch forms when nothing runs, takes members
+ * until the first pass in which one of them finishes, and then runs to its slowest member. */
+#define PKV_ALLOC_ON_DEMAND 0
+#define PKV_ALLOC_RESERVE   1
+#define PKV_UNIT_PASS       0
+#define PKV_UNIT_REQUEST    1
 
 /* free_order: the initial free list ([num_blocks] distinct ids in [0, num_blocks)), or NULL for
  * 0..num_blocks-1.  Copied. */
@@ -286,6 +301,12 @@ void pkv_sched_destroy(pkv_sched* s);
  * could never fit the pool (ceil((prompt_len + max_output) / block_size) > num_blocks):
  * PKV_ERR_NO_BLOCKS. */
 pkv_status pkv_sched_add(pkv_sched* s, int64_t req_id, int32_t prompt_len, int32_t max_output);
+/* As pkv_sched_add, with the output the client declares (>= max_output; RESERVE reserves for it).  A
+ * request whose reservation could never fit the pool: PKV_ERR_NO_BLOCKS. */
+pkv_status pkv_sched_add_declared(pkv_sched* s, int64_t req_id, int32_t prompt_len, int32_t max_output,
+                                  int32_t declared_output);
+/* Choose the policies; only before the first request is added (PKV_ERR_INVALID_ARG afterwards). */
+pkv_status pkv_sched_set_policy(pkv_sched* s, int32_t alloc, int32_t unit);
 /* Run one pass; fills *out (num_seqs may be 0 when nothing is left to do). */
 pkv_status pkv_sched_step(pkv_sched* s, pkv_step* out);
 pkv_status pkv_sched_abort(pkv_sched* s, int64_t req_id);

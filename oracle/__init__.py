@@ -26,11 +26,11 @@ routine, a closed form, values the pages print, or brute force); see ``tests/tes
 from .attention import attention_row, attention_batch, round_fp16
 from .paging import (kv_bytes_per_token, kv_bytes_for_window, pool_blocks_for_bytes, blocks_for_tokens,
                      max_resident_sequences, cache_bytes, slot_of, slot_mapping_for_batch, append_reference)
-from .scheduler import Request, Scheduler, StepRows
+from .scheduler import ON_DEMAND, PASS, REQUEST, RESERVE, Request, Scheduler, StepRows
 
 __all__ = [
     "attention_row", "attention_batch", "round_fp16",
     "kv_bytes_per_token", "kv_bytes_for_window", "pool_blocks_for_bytes", "blocks_for_tokens",
     "max_resident_sequences", "cache_bytes", "slot_of", "slot_mapping_for_batch", "append_reference",
-    "Request", "Scheduler", "StepRows",
+    "Request", "Scheduler", "StepRows", "ON_DEMAND", "RESERVE", "PASS", "REQUEST",
 ]

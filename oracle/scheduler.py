@@ -21,6 +21,21 @@ head-of-line blocking (an unallocatable head stops admission for the pass); a pa
 request's last known token yields one output token; a request finishes when its outputs reach its
 budget and frees its blocks the same pass; freed blocks go to the tail of the free list in block-table
 order; the token budget is shared by both phases.
+
+Two variants from the same page, section "The allocator is the other half" and "The boundary: when this
+is worth nothing":
+
+* Allocation RESERVE (Orca): a request is admitted only if its worst case fits -- the page's
+  n_rsrv + max_tokens <= n_slots, here counted in blocks: ceil((prompt + declared output) / block_size)
+  free blocks, all taken at admission and returned when the request finishes.  An admitted request can
+  never run out of cache, so this policy never preempts.  The declared output is what the client claims
+  (at least its real budget).
+* Unit REQUEST (static batching): a batch forms when nothing runs; requests join it while it forms, and
+  it stops taking members at the first pass in which one of them finishes -- from then on it runs to its
+  slowest member.  (Reading: with chunked prefill a batch cannot form in a single pass; "forms the batch
+  once" is read as "admits only until its first member completes".)
+* Reported with both: the share of held cache that holds a token, summed over passes after each pass --
+  tokens whose K/V a running request holds over the slots of the blocks it holds.
 """
 from __future__ import annotations
 
@@ -33,6 +48,8 @@ import numpy as np
 from .paging import slot_of
 
 WAITING, RUNNING, PREEMPTED, FINISHED = "WAITING", "RUNNING", "PREEMPTED", "FINISHED"
+ON_DEMAND, RESERVE = "on_demand", "reserve"   # block allocation policies
+PASS, REQUEST = "pass", "request"             # units of scheduling
 
 
 @dataclasses.dataclass(eq=False)
@@ -40,6 +57,7 @@ class Request:
     req_id: int
     prompt_len: int
     max_output: int
+    declared_output: int = 0      # output the client claims (RESERVE sizes the reservation by it)
     num_computed: int = 0
     num_output: int = 0
     status: str = WAITING
@@ -65,11 +83,17 @@ class StepRows:
 
 
 class Scheduler:
-    def __init__(self, max_num_seqs: int, token_budget: int, block_size: int, free_blocks: Sequence[int]):
+    def __init__(self, max_num_seqs: int, token_budget: int, block_size: int, free_blocks: Sequence[int],
+                 alloc: str = ON_DEMAND, unit: str = PASS):
         if max_num_seqs < 1:
             raise ValueError("max_num_seqs must be at least 1")
         if token_budget < 1 or block_size < 1:
             raise ValueError("token_budget and block_size must be positive")
+        if alloc not in (ON_DEMAND, RESERVE) or unit not in (PASS, REQUEST):
+            raise ValueError("unknown policy")
+        self.alloc = alloc
+        self.unit = unit
+        self.batch_open = False
         self.max_num_seqs = max_num_seqs
         self.token_budget = token_budget
         self.block_size = block_size
@@ -86,8 +110,23 @@ class Scheduler:
         self.max_batch = 0
         self.batch_sum = 0
         self.tokens_scheduled = 0
+        self.live_tokens = 0      # summed over passes: tokens held by running requests after the pass
+        self.held_slots = 0       # summed over passes: slots of the blocks running requests hold
 
     # --- allocator -----------------------------------------------------------------------------------
+    def _reservation(self, req: Request) -> int:
+        return -(-(req.prompt_len + req.declared_output) // self.block_size)
+
+    def _admit_blocks(self, req: Request, num_new: int) -> bool:
+        """Blocks at admission: the whole reservation (RESERVE) or those the first tokens need."""
+        if self.alloc == RESERVE:
+            need = self._reservation(req)
+            if need > len(self.free):
+                return False
+            req.blocks = [self.free.popleft() for _ in range(need)]
+            return True
+        return self._allocate(req, num_new)
+
     def _allocate(self, req: Request, num_new: int) -> bool:
         need = -(-(req.num_computed + num_new) // self.block_size) - len(req.blocks)
         if need > len(self.free):
@@ -101,10 +140,13 @@ class Scheduler:
         req.blocks = []
 
     # --- requests ------------------------------------------------------------------------------------
-    def add(self, req_id: int, prompt_len: int, max_output: int) -> None:
+    def add(self, req_id: int, prompt_len: int, max_output: int, declared_output: Optional[int] = None) -> None:
         if prompt_len < 1 or max_output < 1:
             raise ValueError("prompt_len and max_output must be positive")
-        req = Request(req_id, prompt_len, max_output)
+        declared = max_output if declared_output is None else declared_output
+        if declared < max_output:
+            raise ValueError("the declared output cannot be below the real budget")
+        req = Request(req_id, prompt_len, max_output, declared)
         self.by_id[req_id] = req
         self.waiting.append(req)
 
@@ -133,6 +175,8 @@ class Scheduler:
         scheduled = []          # (request, num_new, num_computed before the pass)
         preempted: List[Request] = []
         admitted: List[int] = []
+        if self.unit == REQUEST and not self.running:
+            self.batch_open = True          # nothing runs: a new batch forms
 
         # phase one: running requests, arrival order
         i = 0
@@ -158,14 +202,14 @@ class Scheduler:
             budget -= num_new
             i += 1
 
-        # phase two: admission, only when nothing was preempted
-        if not preempted:
+        # phase two: admission, only when nothing was preempted (and, per request, while the batch forms)
+        if not preempted and (self.unit == PASS or self.batch_open):
             while self.waiting and budget > 0:
                 if len(self.running) >= self.max_num_seqs:
                     break
                 req = self.waiting[0]
                 num_new = min(req.num_tokens - req.num_computed, budget)
-                if not self._allocate(req, num_new):
+                if not self._admit_blocks(req, num_new):
                     break
                 self.waiting.popleft()
                 req.status = RUNNING
@@ -191,6 +235,10 @@ class Scheduler:
                     req.status = FINISHED
                     finished.append(req.req_id)
         rows.finished = finished
+        if finished:
+            self.batch_open = False             # a member completed: the batch takes no more
+        self.live_tokens += sum(r.num_computed for r in self.running)
+        self.held_slots += sum(len(r.blocks) for r in self.running) * self.block_size
         self.steps += 1
         self.max_batch = max(self.max_batch, len(scheduled))
         self.batch_sum += len(scheduled)
@@ -200,7 +248,9 @@ class Scheduler:
     def _rows(self, scheduled) -> StepRows:
         B = len(scheduled)
         bs = self.block_size
-        max_blocks = max([len(r.blocks) for r, _, _ in scheduled] + [1])
+        # a row's table lists the blocks its context occupies (a reservation may hold more)
+        used = [-(-(start + num_new) // bs) for _, num_new, start in scheduled]
+        max_blocks = max(used + [1])
         req_ids = np.zeros(B, dtype=np.int64)
         q_lens = np.zeros(B, dtype=np.int32)
         ctx = np.zeros(B, dtype=np.int32)
@@ -210,7 +260,7 @@ class Scheduler:
             req_ids[b] = req.req_id
             q_lens[b] = num_new
             ctx[b] = start + num_new
-            bt[b, : len(req.blocks)] = req.blocks
+            bt[b, : used[b]] = req.blocks[: used[b]]
             for p in range(start, start + num_new):
                 slots.append(slot_of(req.blocks, p, bs))
         return StepRows(req_ids, q_lens, ctx, bt, np.asarray(slots, dtype=np.int64), [], [], [])

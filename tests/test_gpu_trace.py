@@ -23,12 +23,18 @@ def _step_batch(shape, num_blocks, st):
                            np.ascontiguousarray(st["block_tables"]), np.zeros(0, dtype=np.int32), SEED, "trace")
 
 
-@pytest.mark.parametrize("num_blocks,cap,steps", [(20000, 256, 24), (5000, 256, 84), (20000, 64, 16)])
-def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps):
+@pytest.mark.parametrize("num_blocks,cap,steps,alloc,unit,declared", [
+    (20000, 256, 24, 0, 0, 1.0), (5000, 256, 84, 0, 0, 1.0), (20000, 64, 16, 0, 0, 1.0),
+    (5000, 256, 40, pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 4.0),
+    (20000, 64, 40, pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_REQUEST, 1.0)])
+def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps, alloc, unit, declared):
+    """The default policy, and the Orca reservation ("The allocator is the other half") and request-level
+    batching ("The boundary: when this is worth nothing") variants of the same page."""
     shape = synth.Shape(len(LAYERS), 12, 2, 128)
-    sched = pkv.Scheduler(cap, 8192, 16, num_blocks, free_order=synth.block_permutation(num_blocks, SEED))
+    sched = pkv.Scheduler(cap, 8192, 16, num_blocks, free_order=synth.block_permutation(num_blocks, SEED),
+                          alloc=alloc, unit=unit)
     for r in synth.trace_requests(SEED):
-        sched.add(r.req_id, r.prompt_len, r.max_output)
+        sched.add(r.req_id, r.prompt_len, r.max_output, int(round(declared * r.max_output)))
     probe = synth.custom_batch(shape, [1], [1], seed=SEED, num_blocks=num_blocks)
     pool = workload.make_pool(probe)
     pool.cache_view().view(torch.int16).fill_(0x7E00)  # fp16 NaN wherever nothing was appended
@@ -61,8 +67,10 @@ def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps):
             assert_close(row_slice(batch, outs[1], b), oracle_row(batch, 1, int(b)),
                          f"step {step} row {b} (req {batch.req_ids[b]}, q_len {ql[b]}, ctx {ctx[b]})")
     stats = sched.stats()
-    if num_blocks == 5000:
+    if num_blocks == 5000 and alloc == pkv.PKV_ALLOC_ON_DEMAND:
         assert stats["preemptions"] > 0 and rechecked > 0, stats
+    if alloc == pkv.PKV_ALLOC_RESERVE:
+        assert stats["preemptions"] == 0
     sched.close()
 
 

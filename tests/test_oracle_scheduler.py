@@ -12,9 +12,10 @@ TRACES = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "sched
 
 
 def _run(trace):
-    s = oracle.Scheduler(trace["max_num_seqs"], trace["token_budget"], trace["block_size"], trace["free_blocks"])
-    for rid, p, o in trace["requests"]:
-        s.add(rid, p, o)
+    s = oracle.Scheduler(trace["max_num_seqs"], trace["token_budget"], trace["block_size"], trace["free_blocks"],
+                         trace.get("alloc", oracle.ON_DEMAND), trace.get("unit", oracle.PASS))
+    for req in trace["requests"]:
+        s.add(*req)
     steps = []
     while not s.done():
         steps.append(s.step())
@@ -36,6 +37,8 @@ def test_hand_worked_trace(trace):
     assert list(s.free) == trace["final_free"]
     assert s.num_preemptions == trace["preemptions"]
     assert s.recomputed_tokens == trace["recomputed"]
+    if "live_tokens" in trace:
+        assert (s.live_tokens, s.held_slots) == (trace["live_tokens"], trace["held_slots"])
 
 
 def _trace_sched(num_blocks, cap, seed=0, n=64):
@@ -131,3 +134,63 @@ def test_no_preemption_when_pool_is_large():
         s.step()
     assert s.num_preemptions == 0
     assert s.max_batch == 256
+
+
+# --- allocation and scheduling-unit variants ("The allocator is the other half", "The boundary: when this
+# is worth nothing"): the orderings the page reports, checked on the trace workload --------------------
+
+def _policy_run(alloc, unit, declared=1.0, num_blocks=5000, cap=256, spread=True):
+    reqs = synth.trace_requests(0) if spread else synth.trace_requests(0, out_lo=256, out_hi=256)
+    s = oracle.Scheduler(cap, 8192, 16, synth.block_permutation(num_blocks, 0), alloc, unit)
+    for r in reqs:
+        s.add(r.req_id, r.prompt_len, r.max_output, int(round(declared * r.max_output)))
+    while not s.done():
+        s.step()
+        assert s.steps < 100000
+    assert all(r.num_output == r.max_output for r in s.by_id.values())
+    return s
+
+
+def test_reservation_never_preempts_and_costs_batch_and_live_cache():
+    on_demand = _policy_run(oracle.ON_DEMAND, oracle.PASS)
+    assert on_demand.num_preemptions > 0                       # this pool is under pressure on demand
+    live = []
+    batches = []
+    for factor in (1.0, 2.0, 4.0, 8.0):
+        r = _policy_run(oracle.RESERVE, oracle.PASS, declared=factor)
+        assert r.num_preemptions == 0 and r.recomputed_tokens == 0
+        live.append(r.live_tokens / r.held_slots)
+        batches.append(r.max_batch)
+    # declaring more than is used lowers the live share of held cache and the largest batch
+    assert all(a > b for a, b in zip(live, live[1:])), live
+    assert all(a >= b for a, b in zip(batches, batches[1:])) and batches[0] > batches[-1], batches
+    # on demand, held cache is live up to the partly filled last block of each request; a reservation holds
+    # a request's whole output from admission, so even an exact declaration (1x) leaves part of it empty
+    # until the outputs arrive -- how much depends on the output/prompt mix (long outputs here)
+    assert on_demand.live_tokens / on_demand.held_slots > 0.95 > live[0] > 0.5
+    assert on_demand.max_batch > batches[0]
+
+
+def test_request_level_scheduling_waits_for_the_slowest_member():
+    for alloc in (oracle.ON_DEMAND, oracle.RESERVE):
+        per_pass = _policy_run(alloc, oracle.PASS, num_blocks=20000, cap=64)
+        per_req = _policy_run(alloc, oracle.REQUEST, num_blocks=20000, cap=64)
+        assert per_req.tokens_scheduled == per_pass.tokens_scheduled   # the same work...
+        assert per_req.steps > 1.3 * per_pass.steps                    # ...in many more passes
+        # with equal outputs the batch ends together and the unit barely matters
+        eq_pass = _policy_run(alloc, oracle.PASS, num_blocks=20000, cap=64, spread=False)
+        eq_req = _policy_run(alloc, oracle.REQUEST, num_blocks=20000, cap=64, spread=False)
+        assert eq_req.steps <= 1.1 * eq_pass.steps
+
+
+def test_request_level_admits_only_while_the_batch_forms():
+    s = oracle.Scheduler(8, 8192, 16, list(range(4000)), oracle.ON_DEMAND, oracle.REQUEST)
+    for r in synth.trace_requests(3, n=40):
+        s.add(r.req_id, r.prompt_len, r.max_output)
+    closed = False
+    while not s.done():
+        running_before = len(s.running)
+        rows = s.step()
+        if running_before and closed:
+            assert rows.admitted == []                # a running batch that has lost a member takes nobody
+        closed = bool(rows.finished) or (closed and bool(s.running))

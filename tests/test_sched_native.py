@@ -33,19 +33,44 @@ def _compare_runs(native, ref, max_steps=100000):
     assert st["recomputed_tokens"] == ref.recomputed_tokens
     assert st["recomputed_prompt_tokens"] == ref.recomputed_prompt_tokens
     assert st["max_batch"] == ref.max_batch and st["batch_sum"] == ref.batch_sum
+    assert (st["live_tokens"], st["held_slots"]) == (ref.live_tokens, ref.held_slots)
     assert native.free_list() == list(ref.free)
     return st
 
 
+_ALLOC = {oracle.ON_DEMAND: 0, oracle.RESERVE: 1}
+_UNIT = {oracle.PASS: 0, oracle.REQUEST: 1}
+
+
 @pytest.mark.parametrize("trace", TRACES, ids=[t["name"] for t in TRACES])
 def test_hand_worked_traces(built, trace):
+    alloc, unit = trace.get("alloc", oracle.ON_DEMAND), trace.get("unit", oracle.PASS)
     native = Scheduler(trace["max_num_seqs"], trace["token_budget"], trace["block_size"], len(trace["free_blocks"]),
-                       trace["free_blocks"])
-    ref = oracle.Scheduler(trace["max_num_seqs"], trace["token_budget"], trace["block_size"], trace["free_blocks"])
-    for rid, p, o in trace["requests"]:
-        native.add(rid, p, o)
-        ref.add(rid, p, o)
+                       trace["free_blocks"], alloc=_ALLOC[alloc], unit=_UNIT[unit])
+    ref = oracle.Scheduler(trace["max_num_seqs"], trace["token_budget"], trace["block_size"], trace["free_blocks"],
+                           alloc, unit)
+    for req in trace["requests"]:
+        native.add(*req)
+        ref.add(*req)
     _compare_runs(native, ref)
+
+
+@pytest.mark.parametrize("alloc,unit,factor,num_blocks,cap", [
+    (oracle.RESERVE, oracle.PASS, 1.0, 5000, 256), (oracle.RESERVE, oracle.PASS, 4.0, 5000, 256),
+    (oracle.ON_DEMAND, oracle.REQUEST, 1.0, 20000, 64), (oracle.RESERVE, oracle.REQUEST, 2.0, 20000, 64),
+    (oracle.ON_DEMAND, oracle.REQUEST, 1.0, 5000, 256)])
+def test_policy_variants_match_oracle(built, alloc, unit, factor, num_blocks, cap):
+    reqs = synth.trace_requests(0)
+    perm = synth.block_permutation(num_blocks, 0)
+    native = Scheduler(cap, 8192, 16, num_blocks, perm, alloc=_ALLOC[alloc], unit=_UNIT[unit])
+    ref = oracle.Scheduler(cap, 8192, 16, perm, alloc, unit)
+    for r in reqs:
+        d = int(round(factor * r.max_output))
+        native.add(r.req_id, r.prompt_len, r.max_output, d)
+        ref.add(r.req_id, r.prompt_len, r.max_output, d)
+    st = _compare_runs(native, ref)
+    if alloc == oracle.RESERVE:
+        assert st["preemptions"] == 0
 
 
 @pytest.mark.parametrize("num_blocks,cap", [(20000, 256), (20000, 64), (5000, 256), (5000, 64), (1500, 512)])
@@ -66,6 +91,14 @@ def test_trace_workload_matches_oracle(built, num_blocks, cap):
 def test_argument_errors(built):
     with pytest.raises(PkvError):
         Scheduler(0, 8192, 16, 100)
+    with pytest.raises(PkvError):
+        Scheduler(4, 8192, 16, 100, alloc=7)
+    r = Scheduler(4, 64, 16, 4, alloc=1)
+    with pytest.raises(PkvError):
+        r.add(1, 10, 2, 1)          # declared below the real output budget
+    with pytest.raises(PkvError):
+        r.add(1, 10, 2, 60)         # a reservation of 5 blocks never fits 4
+    r.add(1, 10, 2, 20)
     with pytest.raises(PkvError):
         Scheduler(4, 8192, 16, 3, [0, 0, 1])
     s = Scheduler(4, 64, 16, 4)
