@@ -21,9 +21,15 @@
 // blocks, is free, takes it at admission and returns it at finish, and therefore never preempts;
 // UNIT_REQUEST admits only while a batch forms (from a pass that starts with nothing running until the
 // first pass in which a member finishes).  A row's block table lists the blocks its context occupies.
+//
+// Prefix caching (same page, same section: the recompute "is partly refundable" when the freed blocks were
+// not evicted): a preempted request's full blocks stay registered while free (returned last block first,
+// so its prefix is evicted last); handing a block out evicts it; on readmission the request takes back the
+// longest registered prefix, leaving at least one token to compute.
 #include <algorithm>
 #include <cstdint>
 #include <deque>
+#include <map>
 #include <new>
 #include <string>
 #include <unordered_map>
@@ -66,6 +72,9 @@ struct pkv_sched {
   int32_t unit = PKV_UNIT_PASS;
   bool batch_open = false;  // UNIT_REQUEST: the current batch still takes members
   bool added_any = false;
+  bool prefix_caching = false;
+  std::map<std::pair<int64_t, int64_t>, int32_t> cached;  // (request, block j) -> free block still holding it
+  std::unordered_map<int32_t, std::pair<int64_t, int64_t>> block_key;  // the reverse map
   std::deque<int32_t> free_list;
   std::vector<Req*> running;       // arrival (admission) order; back = newest
   std::deque<Req*> waiting;        // front = next to admit
@@ -82,18 +91,47 @@ struct pkv_sched {
   int64_t reservation(const Req* r) const {
     return ((int64_t)r->prompt_len + r->declared_output + cfg.block_size - 1) / cfg.block_size;
   }
-  // Blocks at admission: the whole reservation (RESERVE) or those the first tokens need.
-  bool admit_blocks(Req* r, int64_t num_new) {
+  // The free list's head; a block handed out no longer holds what it cached.
+  int32_t take() {
+    const int32_t b = free_list.front();
+    free_list.pop_front();
+    auto it = block_key.find(b);
+    if (it != block_key.end()) {
+      cached.erase(it->second);
+      block_key.erase(it);
+    }
+    return b;
+  }
+  // Blocks at admission: the whole reservation (RESERVE), or the request's cached prefix and those its
+  // first new tokens need.  Returns the pass's new tokens, 0 if the request cannot be admitted.
+  int64_t admit_blocks(Req* r, int64_t budget) {
+    const int64_t bs = cfg.block_size;
     if (alloc == PKV_ALLOC_RESERVE) {
       const int64_t need = reservation(r);
-      if (need > (int64_t)free_list.size()) return false;
-      for (int64_t i = 0; i < need; ++i) {
-        r->blocks.push_back(free_list.front());
-        free_list.pop_front();
-      }
-      return true;
+      if (need > (int64_t)free_list.size()) return 0;
+      for (int64_t i = 0; i < need; ++i) r->blocks.push_back(take());
+      return std::min(r->num_tokens() - r->num_computed, budget);
     }
-    return allocate(r, num_new);
+    std::vector<int32_t> hits;
+    while (prefix_caching && r->num_computed == 0) {
+      auto it = cached.find({r->id, (int64_t)hits.size()});
+      if (it == cached.end() || ((int64_t)hits.size() + 1) * bs > r->num_tokens() - 1) break;
+      hits.push_back(it->second);
+    }
+    const int64_t start = (int64_t)hits.size() * bs;
+    const int64_t num_new = std::min(r->num_tokens() - start, budget);
+    const int64_t need = (start + num_new + bs - 1) / bs - (int64_t)hits.size();
+    if (need > (int64_t)free_list.size() - (int64_t)hits.size()) return 0;
+    for (int32_t b : hits) {
+      free_list.erase(std::find(free_list.begin(), free_list.end(), b));
+      cached.erase(block_key[b]);
+      block_key.erase(b);
+    }
+    r->blocks = hits;
+    r->num_computed = start;
+    stats.prefix_hit_tokens += start;
+    allocate(r, num_new);
+    return num_new;
   }
 
   bool allocate(Req* r, int64_t num_new) {
@@ -101,15 +139,24 @@ struct pkv_sched {
     const int64_t want = (r->num_computed + num_new + bs - 1) / bs;
     const int64_t need = want - (int64_t)r->blocks.size();
     if (need > (int64_t)free_list.size()) return false;
-    for (int64_t i = 0; i < need; ++i) {
-      r->blocks.push_back(free_list.front());
-      free_list.pop_front();
-    }
+    for (int64_t i = 0; i < need; ++i) r->blocks.push_back(take());
     return true;
   }
 
-  void release(Req* r) {
-    for (int32_t b : r->blocks) free_list.push_back(b);
+  // Blocks back to the free list's tail; keep registers a preempted request's full blocks for prefix
+  // caching and returns them last block first.
+  void release(Req* r, bool keep = false) {
+    if (keep && prefix_caching) {
+      for (size_t j = 0; j < r->blocks.size(); ++j) {
+        if ((int64_t)(j + 1) * cfg.block_size <= r->num_computed) {
+          cached[{r->id, (int64_t)j}] = r->blocks[j];
+          block_key[r->blocks[j]] = {r->id, (int64_t)j};
+        }
+      }
+      for (auto it = r->blocks.rbegin(); it != r->blocks.rend(); ++it) free_list.push_back(*it);
+    } else {
+      for (int32_t b : r->blocks) free_list.push_back(b);
+    }
     r->blocks.clear();
   }
 };
@@ -172,8 +219,20 @@ extern "C" pkv_status pkv_sched_set_policy(pkv_sched* s, int32_t alloc, int32_t 
   if (alloc != PKV_ALLOC_ON_DEMAND && alloc != PKV_ALLOC_RESERVE) return fail(PKV_ERR_INVALID_ARG, "unknown alloc");
   if (unit != PKV_UNIT_PASS && unit != PKV_UNIT_REQUEST) return fail(PKV_ERR_INVALID_ARG, "unknown unit");
   if (s->added_any) return fail(PKV_ERR_INVALID_ARG, "set the policy before adding requests");
+  if (alloc == PKV_ALLOC_RESERVE && s->prefix_caching)
+    return fail(PKV_ERR_INVALID_ARG, "prefix caching refunds recompute; a reserving scheduler never preempts");
   s->alloc = alloc;
   s->unit = unit;
+  return PKV_OK;
+}
+
+extern "C" pkv_status pkv_sched_set_prefix_caching(pkv_sched* s, int32_t enable) {
+  pkv::clear_error();
+  if (!s) return fail(PKV_ERR_INVALID_ARG, "scheduler is NULL");
+  if (s->added_any) return fail(PKV_ERR_INVALID_ARG, "set prefix caching before adding requests");
+  if (enable && s->alloc == PKV_ALLOC_RESERVE)
+    return fail(PKV_ERR_INVALID_ARG, "prefix caching refunds recompute; a reserving scheduler never preempts");
+  s->prefix_caching = enable != 0;
   return PKV_OK;
 }
 
@@ -195,7 +254,7 @@ extern "C" pkv_status pkv_sched_step(pkv_sched* s, pkv_step* out) {
     while (!s->allocate(r, num_new)) {
       Req* victim = s->running.back();
       s->running.pop_back();
-      s->release(victim);
+      s->release(victim, /*keep=*/true);
       victim->status = Status::kPreempted;
       s->stats.recomputed_tokens += victim->num_computed;
       s->stats.recomputed_prompt_tokens += std::min<int64_t>(victim->num_computed, victim->prompt_len);
@@ -218,8 +277,8 @@ extern "C" pkv_status pkv_sched_step(pkv_sched* s, pkv_step* out) {
     while (!s->waiting.empty() && budget > 0) {
       if ((int64_t)s->running.size() >= s->cfg.max_num_seqs) break;
       Req* r = s->waiting.front();
-      const int64_t num_new = std::min(r->num_tokens() - r->num_computed, budget);
-      if (!s->admit_blocks(r, num_new)) break;  // head-of-line blocking
+      const int64_t num_new = s->admit_blocks(r, budget);
+      if (num_new == 0) break;  // head-of-line blocking
       s->waiting.pop_front();
       r->status = Status::kRunning;
       s->running.push_back(r);

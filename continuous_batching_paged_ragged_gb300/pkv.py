@@ -64,7 +64,7 @@ class pkv_sched_stats(ctypes.Structure):
     _fields_ = [("steps", _i64), ("preemptions", _i64), ("recomputed_tokens", _i64),
                 ("recomputed_prompt_tokens", _i64), ("max_batch", _i64), ("batch_sum", _i64),
                 ("tokens_scheduled", _i64), ("running", _i32), ("waiting", _i32), ("free_blocks", _i32),
-                ("live_tokens", _i64), ("held_slots", _i64)]
+                ("live_tokens", _i64), ("held_slots", _i64), ("prefix_hit_tokens", _i64)]
 
 
 # name -> (restype, argtypes); the list every exported symbol of include/pkv.h
@@ -89,6 +89,7 @@ SIGNATURES = {
     "pkv_sched_add": (ctypes.c_int, [_p, _i64, _i32, _i32]),
     "pkv_sched_add_declared": (ctypes.c_int, [_p, _i64, _i32, _i32, _i32]),
     "pkv_sched_set_policy": (ctypes.c_int, [_p, _i32, _i32]),
+    "pkv_sched_set_prefix_caching": (ctypes.c_int, [_p, _i32]),
     "pkv_sched_step": (ctypes.c_int, [_p, ctypes.POINTER(pkv_step)]),
     "pkv_sched_abort": (ctypes.c_int, [_p, _i64]),
     "pkv_sched_set_max_num_seqs": (ctypes.c_int, [_p, _i32]),
@@ -275,7 +276,7 @@ class Scheduler:
     """The C++ host scheduler (pkv_sched_*), returning numpy copies of each pass's batch."""
 
     def __init__(self, max_num_seqs: int, token_budget: int, block_size: int, num_blocks: int, free_order=None,
-                 alloc: int = 0, unit: int = 0):
+                 alloc: int = 0, unit: int = 0, prefix_caching: bool = False):
         lib = load()
         cfg = pkv_sched_config(max_num_seqs, token_budget, block_size, num_blocks)
         h = _p()
@@ -287,6 +288,8 @@ class Scheduler:
         self.handle = h.value
         if alloc or unit:
             _check(lib.pkv_sched_set_policy(self.handle, alloc, unit), "pkv_sched_set_policy")
+        if prefix_caching:
+            _check(lib.pkv_sched_set_prefix_caching(self.handle, 1), "pkv_sched_set_prefix_caching")
 
     def add(self, req_id: int, prompt_len: int, max_output: int, declared_output: Optional[int] = None) -> None:
         if declared_output is None:

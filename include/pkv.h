@@ -278,6 +278,7 @@ typedef struct {
   int32_t free_blocks;
   int64_t live_tokens;              /* summed over passes, after each pass: tokens running requests hold */
   int64_t held_slots;               /* summed over passes: slots of the blocks running requests hold    */
+  int64_t prefix_hit_tokens;        /* recompute refunded by prefix caching                            */
 } pkv_sched_stats;
 
 /* Block allocation policies and units of scheduling (pkv_sched_set_policy).  [CB] "The allocator is
@@ -307,6 +308,14 @@ pkv_status pkv_sched_add_declared(pkv_sched* s, int64_t req_id, int32_t prompt_l
                                   int32_t declared_output);
 /* Choose the policies; only before the first request is added (PKV_ERR_INVALID_ARG afterwards). */
 pkv_status pkv_sched_set_policy(pkv_sched* s, int32_t alloc, int32_t unit);
+/* Prefix caching of recompute after preemption ([CB] "What the scheduler does on one step": the recompute
+ * "is partly refundable" when the freed blocks were not evicted by the time the request comes back).  A
+ * preempted request's full blocks stay registered while they sit in the free list (returned last block
+ * first, so its prefix is evicted last); handing a block out evicts it.  On readmission the request takes
+ * back the longest still-registered prefix of its blocks, leaving at least one token to compute, and only
+ * the rest is recomputed (pkv_step rows then start past the reused blocks).  On demand only (a reserving
+ * scheduler never preempts); set before the first request is added. */
+pkv_status pkv_sched_set_prefix_caching(pkv_sched* s, int32_t enable);
 /* Run one pass; fills *out (num_seqs may be 0 when nothing is left to do). */
 pkv_status pkv_sched_step(pkv_sched* s, pkv_step* out);
 pkv_status pkv_sched_abort(pkv_sched* s, int64_t req_id);

@@ -36,6 +36,18 @@ is worth nothing":
   once" is read as "admits only until its first member completes".)
 * Reported with both: the share of held cache that holds a token, summed over passes after each pass --
   tokens whose K/V a running request holds over the slots of the blocks it holds.
+
+And prefix caching for recompute after preemption (same page, "What the scheduler does on one step": the
+recompute "is partly refundable: if prefix caching is on and the freed blocks have not been evicted from
+the cache by the time the request comes back, the recompute is a cache hit instead"):
+
+* When a request is preempted, each of its full blocks (all 16 slots computed) stays registered as holding
+  that request's block j while it sits in the free list; handing the block to any request evicts it.  Its
+  blocks return to the free list last block first, so that its prefix is evicted last (reading).
+* When the request is admitted again, it takes back the longest prefix j = 0, 1, ... of its still
+  registered blocks (leaving at least one token to compute) and counts those tokens as computed; the rest
+  is recomputed.  A hit the remaining allocation cannot accompany is not taken (head-of-line blocking as
+  usual).  On demand only: a reserving scheduler never preempts.
 """
 from __future__ import annotations
 
@@ -84,16 +96,22 @@ class StepRows:
 
 class Scheduler:
     def __init__(self, max_num_seqs: int, token_budget: int, block_size: int, free_blocks: Sequence[int],
-                 alloc: str = ON_DEMAND, unit: str = PASS):
+                 alloc: str = ON_DEMAND, unit: str = PASS, prefix_caching: bool = False):
         if max_num_seqs < 1:
             raise ValueError("max_num_seqs must be at least 1")
         if token_budget < 1 or block_size < 1:
             raise ValueError("token_budget and block_size must be positive")
         if alloc not in (ON_DEMAND, RESERVE) or unit not in (PASS, REQUEST):
             raise ValueError("unknown policy")
+        if prefix_caching and alloc != ON_DEMAND:
+            raise ValueError("prefix caching refunds recompute after preemption; a reserving scheduler never preempts")
         self.alloc = alloc
         self.unit = unit
         self.batch_open = False
+        self.prefix_caching = prefix_caching
+        self.cached = {}          # (req_id, j) -> a free block still holding that request's full block j
+        self.block_key = {}       # block -> (req_id, j) for those blocks
+        self.prefix_hit_tokens = 0
         self.max_num_seqs = max_num_seqs
         self.token_budget = token_budget
         self.block_size = block_size
@@ -117,27 +135,68 @@ class Scheduler:
     def _reservation(self, req: Request) -> int:
         return -(-(req.prompt_len + req.declared_output) // self.block_size)
 
-    def _admit_blocks(self, req: Request, num_new: int) -> bool:
-        """Blocks at admission: the whole reservation (RESERVE) or those the first tokens need."""
+    def _admit_blocks(self, req: Request, budget: int) -> int:
+        """Blocks at admission: the whole reservation (RESERVE), or the request's cached prefix and those its
+        first new tokens need.  Returns the new tokens of the pass, 0 if it cannot be admitted."""
         if self.alloc == RESERVE:
             need = self._reservation(req)
             if need > len(self.free):
-                return False
-            req.blocks = [self.free.popleft() for _ in range(need)]
-            return True
-        return self._allocate(req, num_new)
+                return 0
+            req.blocks = [self._take() for _ in range(need)]
+            return min(req.num_tokens - req.num_computed, budget)
+        hits = self._prefix_hits(req)
+        start = len(hits) * self.block_size
+        num_new = min(req.num_tokens - start, budget)
+        need = -(-(start + num_new) // self.block_size) - len(hits)
+        if need > len(self.free) - len(hits):
+            return 0
+        for b in hits:
+            self.free.remove(b)
+            del self.cached[self.block_key.pop(b)]
+        req.blocks = hits
+        req.num_computed = start
+        self.prefix_hit_tokens += start
+        self._allocate(req, num_new)
+        return num_new
+
+    def _take(self) -> int:
+        """The free list's head; a block handed out no longer holds what it cached."""
+        b = self.free.popleft()
+        key = self.block_key.pop(b, None)
+        if key is not None:
+            del self.cached[key]
+        return b
 
     def _allocate(self, req: Request, num_new: int) -> bool:
         need = -(-(req.num_computed + num_new) // self.block_size) - len(req.blocks)
         if need > len(self.free):
             return False
         for _ in range(max(need, 0)):
-            req.blocks.append(self.free.popleft())
+            req.blocks.append(self._take())
         return True
 
-    def _free(self, req: Request) -> None:
-        self.free.extend(req.blocks)
+    def _free(self, req: Request, keep: bool = False) -> None:
+        """Return the blocks to the free list's tail; keep=True registers the full ones for prefix caching."""
+        if keep and self.prefix_caching:
+            for j, b in enumerate(req.blocks):
+                if (j + 1) * self.block_size <= req.num_computed:
+                    self.cached[(req.req_id, j)] = b
+                    self.block_key[b] = (req.req_id, j)
+            # last block first: the allocator hands out the free list's head, so the request's prefix --
+            # what its readmission can reuse -- is evicted last
+            self.free.extend(reversed(req.blocks))
+        else:
+            self.free.extend(req.blocks)
         req.blocks = []
+
+    def _prefix_hits(self, req: Request) -> List[int]:
+        hits = []
+        while self.prefix_caching and req.num_computed == 0:
+            b = self.cached.get((req.req_id, len(hits)))
+            if b is None or (len(hits) + 1) * self.block_size > req.num_tokens - 1:
+                break
+            hits.append(b)
+        return hits
 
     # --- requests ------------------------------------------------------------------------------------
     def add(self, req_id: int, prompt_len: int, max_output: int, declared_output: Optional[int] = None) -> None:
@@ -186,7 +245,7 @@ class Scheduler:
             schedulable = True
             while not self._allocate(req, num_new):
                 victim = self.running.pop()
-                self._free(victim)
+                self._free(victim, keep=True)
                 victim.status = PREEMPTED
                 self.recomputed_tokens += victim.num_computed
                 self.recomputed_prompt_tokens += min(victim.num_computed, victim.prompt_len)
@@ -208,8 +267,8 @@ class Scheduler:
                 if len(self.running) >= self.max_num_seqs:
                     break
                 req = self.waiting[0]
-                num_new = min(req.num_tokens - req.num_computed, budget)
-                if not self._admit_blocks(req, num_new):
+                num_new = self._admit_blocks(req, budget)
+                if num_new == 0:
                     break
                 self.waiting.popleft()
                 req.status = RUNNING

@@ -23,23 +23,25 @@ def _step_batch(shape, num_blocks, st):
                            np.ascontiguousarray(st["block_tables"]), np.zeros(0, dtype=np.int32), SEED, "trace")
 
 
-@pytest.mark.parametrize("num_blocks,cap,steps,alloc,unit,declared", [
-    (20000, 256, 24, 0, 0, 1.0), (5000, 256, 84, 0, 0, 1.0), (20000, 64, 16, 0, 0, 1.0),
-    (5000, 256, 40, pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 4.0),
-    (20000, 64, 40, pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_REQUEST, 1.0)])
-def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps, alloc, unit, declared):
-    """The default policy, and the Orca reservation ("The allocator is the other half") and request-level
-    batching ("The boundary: when this is worth nothing") variants of the same page."""
+@pytest.mark.parametrize("num_blocks,cap,steps,alloc,unit,declared,prefix", [
+    (20000, 256, 24, 0, 0, 1.0, False), (5000, 256, 84, 0, 0, 1.0, False), (20000, 64, 16, 0, 0, 1.0, False),
+    (5000, 256, 40, pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 4.0, False),
+    (20000, 64, 40, pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_REQUEST, 1.0, False),
+    (5000, 256, 110, 0, 0, 1.0, True)])
+def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps, alloc, unit, declared, prefix):
+    """The default policy, and the Orca reservation ("The allocator is the other half"), request-level
+    batching ("The boundary: when this is worth nothing") and prefix-cached recompute variants of the same
+    page.  With prefix caching a readmitted request reads the blocks it wrote before its preemption."""
     shape = synth.Shape(len(LAYERS), 12, 2, 128)
     sched = pkv.Scheduler(cap, 8192, 16, num_blocks, free_order=synth.block_permutation(num_blocks, SEED),
-                          alloc=alloc, unit=unit)
+                          alloc=alloc, unit=unit, prefix_caching=prefix)
     for r in synth.trace_requests(SEED):
         sched.add(r.req_id, r.prompt_len, r.max_output, int(round(declared * r.max_output)))
     probe = synth.custom_batch(shape, [1], [1], seed=SEED, num_blocks=num_blocks)
     pool = workload.make_pool(probe)
     pool.cache_view().view(torch.int16).fill_(0x7E00)  # fp16 NaN wherever nothing was appended
     rng = np.random.default_rng(7)
-    preempted, rechecked = set(), 0
+    preempted, rechecked, reused = set(), 0, 0
     for step in range(steps):
         st = sched.step()
         preempted.update(st["preempted"])
@@ -61,8 +63,13 @@ def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps, alloc, unit
             sample.append(chunk[0])
         back = [b for b in range(batch.num_seqs) if int(batch.req_ids[b]) in preempted]
         if back:
-            sample.append(back[0])  # a request readmitted after preemption (its cache was recomputed)
+            # a request readmitted after preemption (its cache recomputed, or reused from its own blocks);
+            # prefer one whose first row this is, starting past reused blocks
+            fresh = [b for b in back if int(batch.req_ids[b]) in st["admitted"] and ctx[b] > ql[b]
+                     and int(ql[b]) * int(ctx[b]) <= 2_000_000]
+            sample.append(fresh[0] if fresh else back[0])
             rechecked += 1
+            reused += len(fresh)
         for b in sample:
             assert_close(row_slice(batch, outs[1], b), oracle_row(batch, 1, int(b)),
                          f"step {step} row {b} (req {batch.req_ids[b]}, q_len {ql[b]}, ctx {ctx[b]})")
@@ -71,6 +78,8 @@ def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps, alloc, unit
         assert stats["preemptions"] > 0 and rechecked > 0, stats
     if alloc == pkv.PKV_ALLOC_RESERVE:
         assert stats["preemptions"] == 0
+    if prefix:
+        assert stats["prefix_hit_tokens"] > 0 and reused > 0, stats
     sched.close()
 
 

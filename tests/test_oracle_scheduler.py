@@ -13,7 +13,8 @@ TRACES = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "sched
 
 def _run(trace):
     s = oracle.Scheduler(trace["max_num_seqs"], trace["token_budget"], trace["block_size"], trace["free_blocks"],
-                         trace.get("alloc", oracle.ON_DEMAND), trace.get("unit", oracle.PASS))
+                         trace.get("alloc", oracle.ON_DEMAND), trace.get("unit", oracle.PASS),
+                         trace.get("prefix_caching", False))
     for req in trace["requests"]:
         s.add(*req)
     steps = []
@@ -39,6 +40,8 @@ def test_hand_worked_trace(trace):
     assert s.recomputed_tokens == trace["recomputed"]
     if "live_tokens" in trace:
         assert (s.live_tokens, s.held_slots) == (trace["live_tokens"], trace["held_slots"])
+    if "prefix_hit_tokens" in trace:
+        assert s.prefix_hit_tokens == trace["prefix_hit_tokens"]
 
 
 def _trace_sched(num_blocks, cap, seed=0, n=64):
@@ -194,3 +197,51 @@ def test_request_level_admits_only_while_the_batch_forms():
         if running_before and closed:
             assert rows.admitted == []                # a running batch that has lost a member takes nobody
         closed = bool(rows.finished) or (closed and bool(s.running))
+
+
+# --- prefix caching of recompute after preemption ("What the scheduler does on one step": the recompute is
+# "partly refundable ... a race, not a guarantee") ------------------------------------------------------
+
+def test_prefix_hits_are_the_requests_own_untouched_blocks():
+    reqs = synth.trace_requests(0)
+    s = oracle.Scheduler(256, 8192, 16, synth.block_permutation(5000, 0), prefix_caching=True)
+    for r in reqs:
+        s.add(r.req_id, r.prompt_len, r.max_output)
+    held_at_preemption = {}
+    hits_seen = 0
+    while not s.done():
+        blocks_before = {r.req_id: list(r.blocks) for r in s.running}
+        hits_before = s.prefix_hit_tokens
+        rows = s.step()
+        for rid in rows.preempted:
+            held_at_preemption[rid] = blocks_before[rid]
+        for b, rid in enumerate(rows.req_ids.tolist()):
+            if rid in rows.admitted and rid in held_at_preemption:
+                start = int(rows.context_lens[b] - rows.q_lens[b])
+                assert start % 16 == 0 and start < int(rows.context_lens[b])
+                reused = rows.block_tables[b][: start // 16].tolist()
+                # a prefix of the blocks it held when it was preempted, in the same logical order
+                assert reused == held_at_preemption[rid][: len(reused)]
+                hits_seen += len(reused)
+        assert s.prefix_hit_tokens - hits_before == 16 * sum(
+            int(rows.context_lens[b] - rows.q_lens[b]) // 16 for b, rid in enumerate(rows.req_ids.tolist())
+            if rid in rows.admitted)
+    assert hits_seen > 0 and 0 < s.prefix_hit_tokens <= s.recomputed_tokens
+    assert all(r.num_output == r.max_output for r in s.by_id.values())
+
+
+def test_prefix_caching_only_removes_recompute():
+    """The same workload with and without the cache: the same outputs, fewer prefill tokens."""
+    runs = []
+    for pc in (False, True):
+        s = oracle.Scheduler(256, 8192, 16, synth.block_permutation(5000, 0), prefix_caching=pc)
+        for r in synth.trace_requests(0):
+            s.add(r.req_id, r.prompt_len, r.max_output)
+        while not s.done():
+            s.step()
+        runs.append(s)
+    off, on = runs
+    assert on.prefix_hit_tokens > 0 and off.prefix_hit_tokens == 0
+    assert on.tokens_scheduled < off.tokens_scheduled
+    with pytest.raises(ValueError):
+        oracle.Scheduler(4, 64, 16, list(range(8)), oracle.RESERVE, prefix_caching=True)

@@ -34,6 +34,7 @@ def _compare_runs(native, ref, max_steps=100000):
     assert st["recomputed_prompt_tokens"] == ref.recomputed_prompt_tokens
     assert st["max_batch"] == ref.max_batch and st["batch_sum"] == ref.batch_sum
     assert (st["live_tokens"], st["held_slots"]) == (ref.live_tokens, ref.held_slots)
+    assert st["prefix_hit_tokens"] == ref.prefix_hit_tokens
     assert native.free_list() == list(ref.free)
     return st
 
@@ -45,10 +46,11 @@ _UNIT = {oracle.PASS: 0, oracle.REQUEST: 1}
 @pytest.mark.parametrize("trace", TRACES, ids=[t["name"] for t in TRACES])
 def test_hand_worked_traces(built, trace):
     alloc, unit = trace.get("alloc", oracle.ON_DEMAND), trace.get("unit", oracle.PASS)
+    pc = trace.get("prefix_caching", False)
     native = Scheduler(trace["max_num_seqs"], trace["token_budget"], trace["block_size"], len(trace["free_blocks"]),
-                       trace["free_blocks"], alloc=_ALLOC[alloc], unit=_UNIT[unit])
+                       trace["free_blocks"], alloc=_ALLOC[alloc], unit=_UNIT[unit], prefix_caching=pc)
     ref = oracle.Scheduler(trace["max_num_seqs"], trace["token_budget"], trace["block_size"], trace["free_blocks"],
-                           alloc, unit)
+                           alloc, unit, pc)
     for req in trace["requests"]:
         native.add(*req)
         ref.add(*req)
@@ -130,3 +132,16 @@ def test_abort_and_drain(built):
     while not s.done():
         s.step()
     assert s.stats()["free_blocks"] == 4000
+
+
+@pytest.mark.parametrize("num_blocks,cap", [(5000, 256), (3000, 64), (1500, 512)])
+def test_prefix_caching_matches_oracle(built, num_blocks, cap):
+    reqs = synth.trace_requests(0)
+    perm = synth.block_permutation(num_blocks, 0)
+    native = Scheduler(cap, 8192, 16, num_blocks, perm, prefix_caching=True)
+    ref = oracle.Scheduler(cap, 8192, 16, perm, prefix_caching=True)
+    for r in reqs:
+        native.add(r.req_id, r.prompt_len, r.max_output)
+        ref.add(r.req_id, r.prompt_len, r.max_output)
+    st = _compare_runs(native, ref)
+    assert st["prefix_hit_tokens"] > 0
