@@ -517,12 +517,14 @@ def run_pkv(args, rank, world, local):
 # Scheduler-driven trace under each allocation policy and unit of scheduling
 # ----------------------------------------------------------------------------------------------------
 
-TRACE_POLICIES = [  # (name, allocation policy, unit of scheduling, declared output / real output, max_num_seqs)
-    ("on_demand/pass", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 256),
-    ("reserve 1x/pass", pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 1.0, 256),
-    ("reserve 4x/pass", pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 4.0, 256),
-    ("on_demand/pass cap 64", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 64),
-    ("on_demand/request cap 64", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_REQUEST, 1.0, 64),
+TRACE_POLICIES = [  # (name, allocation, unit, declared output / real output, max_num_seqs, blocks, prefix caching)
+    ("on_demand/pass", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 256, 20000, False),
+    ("reserve 1x/pass", pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 1.0, 256, 20000, False),
+    ("reserve 4x/pass", pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 4.0, 256, 20000, False),
+    ("on_demand/pass cap 64", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 64, 20000, False),
+    ("on_demand/request cap 64", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_REQUEST, 1.0, 64, 20000, False),
+    ("on_demand/pass 5000 blocks", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 256, 5000, False),
+    ("on_demand/pass 5000 blocks prefix-cached", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 256, 5000, True),
 ]
 
 
@@ -551,8 +553,9 @@ def run_sched_trace(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     results = []
-    for name, alloc, unit, declared, max_seqs in TRACE_POLICIES:
-        sched = pkv.Scheduler(max_seqs, budget, 16, nblk, synth.block_permutation(nblk, 0), alloc=alloc, unit=unit)
+    for name, alloc, unit, declared, max_seqs, blocks, prefix in TRACE_POLICIES:
+        sched = pkv.Scheduler(max_seqs, budget, 16, blocks, synth.block_permutation(blocks, 0), alloc=alloc, unit=unit,
+                              prefix_caching=prefix)
         for r in reqs:
             sched.add(r.req_id, r.prompt_len, r.max_output, int(round(declared * r.max_output)))
         events, steps, launches = [], 0, 0
@@ -589,7 +592,8 @@ def run_sched_trace(args, rank, world, local):
                         "gpu_s": gpu_s, "steps": steps,
                         "preemptions": stt["preemptions"], "recomputed_tokens": stt["recomputed_tokens"],
                         "max_batch": stt["max_batch"], "mean_batch": stt["batch_sum"] / max(1, stt["steps"]),
-                        "live_cache": stt["live_tokens"] / max(1, stt["held_slots"]),
+                        "live_cache": stt["live_tokens"] / max(1, stt["held_slots"]), "pool_blocks": blocks,
+                        "prefix_hit_tokens": stt["prefix_hit_tokens"],
                         "tokens_scheduled": stt["tokens_scheduled"], "gpu_launches": launches})
     if rank != 0:
         return
