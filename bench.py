@@ -47,7 +47,7 @@ CONFIGS = {
 # DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
 # source they were taken on; reported as null once the source changes.
-TRAFFIC = {"3499382d1aba": 142.48e6}  # profiles/decode_kernel_qwen_decode.md
+TRAFFIC = {"cbfb3d0ea82d": 142.57e6}  # profiles/decode_kernel_qwen_decode.md
 
 FALLBACK_HBM_GBS = 6800.0
 
