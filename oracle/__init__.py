@@ -19,6 +19,10 @@ Pages it follows (cited by title and section in each function):
   (section "Context math sets the ceiling the fields ignore").
 * "Saturation and Capacity" (inference-lab) -- max_num_seqs gates admission only and must be >= 1
   (section "Runtime capacity control").
+* The 8-bit cache (``oracle.fp8``): quantize the cache when memory is the cap ("Continuous Batching Is
+  Not a Bigger Batch", section "Checking it on a real system"); 8-bit KV halves the raw bytes, scales on
+  top ("An advertised batch limit proves nothing until sampled", section "Context math sets the ceiling
+  the fields ignore").  The E4M3 format is the OCP 8-bit floating point specification's.
 
 Every function here is pinned by a ``-m "not gpu"`` test against something other than itself (a library
 routine, a closed form, values the pages print, or brute force); see ``tests/test_oracle_*.py``.
@@ -26,11 +30,12 @@ routine, a closed form, values the pages print, or brute force); see ``tests/tes
 from .attention import attention_row, attention_batch, round_fp16
 from .paging import (kv_bytes_per_token, kv_bytes_for_window, pool_blocks_for_bytes, blocks_for_tokens,
                      max_resident_sequences, cache_bytes, slot_of, slot_mapping_for_batch, append_reference)
+from . import fp8
 from .scheduler import ON_DEMAND, PASS, REQUEST, RESERVE, Request, Scheduler, StepRows
 
 __all__ = [
     "attention_row", "attention_batch", "round_fp16",
     "kv_bytes_per_token", "kv_bytes_for_window", "pool_blocks_for_bytes", "blocks_for_tokens",
     "max_resident_sequences", "cache_bytes", "slot_of", "slot_mapping_for_batch", "append_reference",
-    "Request", "Scheduler", "StepRows", "ON_DEMAND", "RESERVE", "PASS", "REQUEST",
+    "fp8", "Request", "Scheduler", "StepRows", "ON_DEMAND", "RESERVE", "PASS", "REQUEST",
 ]
