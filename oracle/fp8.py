@@ -72,6 +72,39 @@ def e4m3_encode(x: float) -> int:
     return sign | best_code
 
 
+def e4m3_encode_array(y: np.ndarray) -> np.ndarray:
+    """e4m3_encode on every element of a finite float64 array with |y| <= 448: the same nearest-code rule
+    evaluated for many values at once.  A search of the ascending code values brackets |y| between two
+    neighbours; the nearer one wins, the even code on a tie."""
+    y = np.asarray(y, dtype=np.float64)
+    assert np.all(np.isfinite(y)) and np.all(np.abs(y) <= E4M3_MAX)
+    vals = np.array([v for v, _ in _finite_codes()], dtype=np.float64)   # code c has value vals[c]
+    a = np.abs(y)
+    hi = np.clip(np.searchsorted(vals, a, side="left"), 0, len(vals) - 1)  # vals[hi] >= a (first such)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(a == vals[hi], hi, code)
+    return (code | (np.signbit(y).astype(np.int64) << 7)).astype(np.uint8)
+
+
+def row_exponents(amax: np.ndarray) -> np.ndarray:
+    """row_exponent of every element: a first guess from log2, then exact corrections by the defining
+    inequality (448 * 2^(e-1) < amax <= 448 * 2^e), all comparisons exact in float64."""
+    amax = np.asarray(amax, dtype=np.float64)
+    assert np.all(amax >= 0) and np.all(np.isfinite(amax))
+    pos = amax > 0
+    e = np.zeros(amax.shape, dtype=np.int64)
+    e[pos] = np.ceil(np.log2(amax[pos] / E4M3_MAX)).astype(np.int64)
+    for _ in range(4):
+        up = pos & (amax > E4M3_MAX * np.exp2(e.astype(np.float64)))
+        down = pos & (amax <= E4M3_MAX * np.exp2((e - 1).astype(np.float64)))
+        e = e + up.astype(np.int64) - down.astype(np.int64)
+    assert not np.any(pos & ((amax > E4M3_MAX * np.exp2(e.astype(np.float64))) |
+                             (amax <= E4M3_MAX * np.exp2((e - 1).astype(np.float64)))))
+    return e
+
+
 def row_exponent(amax: float) -> int:
     """Smallest integer e with amax <= 448 * 2^e (0 for amax == 0).  Comparisons are exact in float64."""
     amax = float(amax)
@@ -102,14 +135,14 @@ def dequantize_row(codes: np.ndarray, scale_byte: int) -> np.ndarray:
 
 
 def quantize_rows(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
-    """fp16 [..., d] -> (uint8 codes [..., d], uint8 scale bytes [...]): quantize_row on every row."""
+    """fp16 [..., d] -> (uint8 codes [..., d], uint8 scale bytes [...]): quantize_row on every row, with the
+    exponents from row_exponents and the codes from e4m3_encode_array."""
     x = np.asarray(x)
-    flat = x.reshape(-1, x.shape[-1])
-    codes = np.zeros(flat.shape, dtype=np.uint8)
-    scales = np.zeros(flat.shape[0], dtype=np.uint8)
-    for i in range(flat.shape[0]):
-        codes[i], scales[i] = quantize_row(flat[i])
-    return codes.reshape(x.shape), scales.reshape(x.shape[:-1])
+    flat = x.reshape(-1, x.shape[-1]).astype(np.float64)
+    assert np.all(np.isfinite(flat)), "the 8-bit cache takes finite keys and values"
+    exps = row_exponents(np.max(np.abs(flat), axis=1) if flat.shape[1] else np.zeros(flat.shape[0]))
+    codes = e4m3_encode_array(flat / np.exp2(exps.astype(np.float64))[:, None])
+    return codes.reshape(x.shape), (exps + SCALE_BIAS).astype(np.uint8).reshape(x.shape[:-1])
 
 
 def dequantize_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:

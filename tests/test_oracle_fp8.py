@@ -52,6 +52,22 @@ def test_encode_matches_library_on_codes_midpoints_and_random():
     assert np.array_equal(ours, _torch_encode(xs))
 
 
+def test_array_encoder_matches_scalar_definition():
+    vals = [v for v, _ in fp8._finite_codes()]
+    mids = [(a + b) / 2 for a, b in zip(vals[:-1], vals[1:])]
+    rng = np.random.default_rng(5)
+    y = np.array(vals + mids + [-m for m in mids] + list(rng.uniform(-448, 448, 500)) + [0.0, -0.0])
+    assert np.array_equal(fp8.e4m3_encode_array(y), np.array([fp8.e4m3_encode(v) for v in y], dtype=np.uint8))
+    amax = np.concatenate([np.exp2(rng.uniform(-24, 16, 500)), [0.0, 448.0, 449.0, 224.0, 224.125, 65504.0]])
+    amax = amax.astype(np.float16).astype(np.float64)
+    assert list(fp8.row_exponents(amax)) == [fp8.row_exponent(a) for a in amax]
+    x = _rows(rng, 6, 32)
+    c1, s1 = fp8.quantize_rows(x)
+    for i in range(6):
+        c2, s2 = fp8.quantize_row(x[i])
+        assert np.array_equal(c1[i], c2) and s1[i] == s2
+
+
 def test_encode_ties_go_to_even():
     assert fp8.e4m3_encode(1.0625) == 0x38    # between 1.0 (m=0) and 1.125 (m=1)
     assert fp8.e4m3_encode(1.1875) == 0x3A    # between 1.125 (m=1) and 1.25 (m=2)
