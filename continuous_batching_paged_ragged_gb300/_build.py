@@ -22,7 +22,7 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompil
               "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]
 
 LIBS = {
-    "libpkv.so": ["pool.cu", "attention.cu", "prefill.cu", "sched.cpp"],
+    "libpkv.so": ["pool.cu", "attention.cu", "decode_e4m3.cu", "prefill.cu", "sched.cpp"],
     "libpkv_synth.so": ["synth.cu"],
 }
 

@@ -34,10 +34,14 @@ struct PlanKey {
 }  // namespace pkv
 
 struct pkv_pool {
-  CUtensorMap kv_map;          // 2-D view [rows = L*2*num_blocks*Hkv*16, head_dim] of the cache, 128B swizzle
+  // The cache as the TMA engine sees it, 128-byte swizzle: fp16, rows of head_dim values (one per (layer,
+  // K/V, block, KV head, slot)); 8-bit, rows of 128 code bytes (a (block, KV head) run is 16*head_dim/128
+  // consecutive rows).
+  CUtensorMap kv_map;
   pkv_config cfg;
-  char* base = nullptr;        // device: cache, then the status area
-  size_t cache_bytes = 0;      // bytes of the fp16 cache region
+  char* base = nullptr;        // device: cache (8-bit: codes, then scales), then the status area
+  size_t cache_bytes = 0;      // bytes before the status area
+  size_t scales_off = 0;       // 8-bit cache: offset of the scale bytes
   int32_t* dev_error = nullptr;  // device error word (in the status area)
   int32_t last_launches = 0;
   int num_sms = 0;
@@ -70,6 +74,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // ---- device helpers ------------------------------------------------------------------------------
 #if defined(__CUDACC__)
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 namespace pkv {
 namespace dev {
@@ -378,6 +385,55 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t* addr) {
 
 __device__ __forceinline__ void set_error(int32_t* err, int32_t bits) {
   if (err) atomicOr(err, bits);
+}
+
+// ---- 8-bit cache rows: E4M3 codes with one power-of-two scale per (token, KV head) row ---------------
+// Largest magnitude among 8 fp16 values, as fp16 bits with the sign cleared (for finite values the bit
+// patterns order like the magnitudes).
+__device__ __forceinline__ uint32_t f16x8_amax_bits(const uint4& r) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+  return m;
+}
+// The same over a row spread across LANES consecutive lanes (a lane-aligned group; every lane of the warp
+// takes part).
+template <int LANES>
+__device__ __forceinline__ uint32_t row_amax_bits(uint32_t m) {
+#pragma unroll
+  for (int o = 1; o < LANES; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+// Scale byte e + 127 of a row whose largest magnitude has fp16 bits `amax`: e is the smallest integer with
+// amax <= 448 * 2^e (0 for an all-zero row).  With amax = 1.m * 2^k (a normal fp32 for every fp16 value)
+// and 448 = 1.75 * 2^8: e = k - 8, plus one when 1.m > 1.75.
+__device__ __forceinline__ int e4m3_scale_byte(uint32_t amax) {
+  if (amax == 0) return 127;
+  const uint32_t b = __float_as_uint(__half2float(__ushort_as_half((unsigned short)amax)));
+  const int k = (int)(b >> 23) - 127;
+  return k - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0) + 127;
+}
+// Power of two 2^(sb - 127) as fp32, for scale bytes 1 .. 254.
+__device__ __forceinline__ float scale_of_byte(uint32_t sb) { return __uint_as_float(sb << 23); }
+// E4M3 codes of 8 fp16 values divided by 2^(sb - 127): the division is an exact power-of-two scaling in
+// fp32, then each value is rounded to the nearest E4M3 value, ties to even (saturating, which |x| / 2^e
+// <= 448 never reaches).  Byte i of the result is value i.
+__device__ __forceinline__ uint2 e4m3_encode8(const uint4& r, int sb) {
+  const float inv = __uint_as_float((uint32_t)(254 - sb) << 23);
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    c[i] = __nv_cvt_float2_to_fp8x2(make_float2(f.x * inv, f.y * inv), __NV_SATFINITE, __NV_E4M3);
+  }
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+// Two E4M3 codes (low byte first) as an fp16 pair (low half first); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
 // Row of packed token t: the largest b with query_start_loc[b] <= t (query_start_loc has num_seqs + 1

@@ -2,7 +2,9 @@
 //
 // kv_append follows "Continuous Batching Is Not a Bigger Batch" (opening section and "The allocator is
 // the other half"): every computed token's key and value are kept, one pair per token per layer, in the
-// slot of a 16-token block that was allocated as the token was computed.  It is a pure bit copy.
+// slot of a 16-token block that was allocated as the token was computed.  For an fp16 cache it is a pure
+// bit copy.  For the 8-bit cache (same page, "Checking it on a real system": quantize the cache when it is
+// the limit) each (token, KV head) row is stored as E4M3 codes with one power-of-two scale.
 #include <cuda_fp16.h>
 
 #include <cstring>
@@ -39,6 +41,8 @@ static pkv_status check_config(const pkv_config* c) {
   if (!supported_group(c->num_q_heads / c->num_kv_heads))
     return fail(PKV_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4, 6 or 8");
   if (c->split_blocks < 0) return fail(PKV_ERR_INVALID_ARG, "split_blocks must be >= 0");
+  if (c->kv_dtype != PKV_KV_F16 && c->kv_dtype != PKV_KV_E4M3)
+    return fail(PKV_ERR_UNSUPPORTED, "kv_dtype must be PKV_KV_F16 or PKV_KV_E4M3");
   return PKV_OK;
 }
 
@@ -46,9 +50,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// The cache seen by the TMA engine: rows of head_dim fp16 values, one row per (layer, K/V, block, KV head,
-// slot), boxes of 16 rows x 64 values (128 bytes) with the 128-byte swizzle, so a (block, KV head) run of
-// K or V is head_dim / 64 boxes.
+// The cache seen by the TMA engine, 128-byte swizzle throughout.  fp16: rows of head_dim values, one row per
+// (layer, K/V, block, KV head, slot), boxes of 16 rows x 64 values (128 bytes), so a (block, KV head) run of
+// K or V is head_dim / 64 boxes.  8-bit: the codes as rows of 128 bytes; a run (16 * head_dim bytes) is
+// one box of 16 * head_dim / 128 rows.
 static pkv_status encode_kv_map(pkv_pool* p) {
   static EncodeTiledFn encode = nullptr;
   if (!encode) {
@@ -60,22 +65,31 @@ static pkv_status encode_kv_map(pkv_pool* p) {
     encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
   const pkv_config& c = p->cfg;
-  const uint64_t rows = (uint64_t)c.num_layers * 2 * c.num_blocks * c.num_kv_heads * c.block_size;
+  const bool f8 = c.kv_dtype == PKV_KV_E4M3;
+  const uint64_t toks = (uint64_t)c.num_layers * 2 * c.num_blocks * c.num_kv_heads * c.block_size;
+  const uint64_t rows = f8 ? toks * c.head_dim / 128 : toks;
   if (rows >= (1ull << 31)) return fail(PKV_ERR_UNSUPPORTED, "pool too large for 32-bit TMA row coordinates");
-  cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint64_t dims[2] = {f8 ? 128u : (cuuint64_t)c.head_dim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {f8 ? 128u : (cuuint64_t)c.head_dim * 2};
+  cuuint32_t box[2] = {f8 ? 128u : 64u, f8 ? (cuuint32_t)(c.block_size * c.head_dim / 128) : 16u};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(&p->kv_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->base, dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = encode(&p->kv_map, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->base,
+                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
   return PKV_OK;
 }
 
-static size_t cache_bytes_of(const pkv_config* c) {
+// Bytes of the K/V values (fp16) or codes (8-bit) of every layer.
+static size_t values_bytes_of(const pkv_config* c) {
   return (size_t)2 * c->num_layers * (size_t)c->num_blocks * c->num_kv_heads * c->block_size * c->head_dim *
-         sizeof(__half);
+         (c->kv_dtype == PKV_KV_E4M3 ? 1 : sizeof(__half));
+}
+// Everything before the status area: values, then (8-bit) one scale byte per cached row, padded to 256.
+static size_t cache_bytes_of(const pkv_config* c) {
+  if (c->kv_dtype != PKV_KV_E4M3) return values_bytes_of(c);
+  const size_t scales = (size_t)2 * c->num_layers * (size_t)c->num_blocks * c->num_kv_heads * c->block_size;
+  return (values_bytes_of(c) + scales + 255) / 256 * 256;
 }
 
 }  // namespace pkv
@@ -109,6 +123,7 @@ extern "C" pkv_status pkv_pool_init(const pkv_config* cfg, void* dev_cache, size
   if (p->cfg.split_blocks == 0) p->cfg.split_blocks = 32;
   p->base = static_cast<char*>(dev_cache);
   p->cache_bytes = cache_bytes_of(cfg);
+  p->scales_off = cfg->kv_dtype == PKV_KV_E4M3 ? values_bytes_of(cfg) : 0;
   p->dev_error = reinterpret_cast<int32_t*>(p->base + p->cache_bytes);
   p->device = attr.device;
   e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
@@ -136,8 +151,15 @@ extern "C" void pkv_pool_destroy(pkv_pool* pool) { delete pool; }
 extern "C" void* pkv_pool_layer_ptr(const pkv_pool* pool, int32_t layer, int32_t kv) {
   if (!pool || layer < 0 || layer >= pool->cfg.num_layers || (kv != 0 && kv != 1)) return nullptr;
   const pkv_config& c = pool->cfg;
-  size_t per = (size_t)c.num_blocks * c.num_kv_heads * c.block_size * c.head_dim * sizeof(__half);
+  size_t per = (size_t)c.num_blocks * c.num_kv_heads * c.block_size * c.head_dim *
+               (c.kv_dtype == PKV_KV_E4M3 ? 1 : sizeof(__half));
   return pool->base + ((size_t)layer * 2 + kv) * per;
+}
+
+extern "C" void* pkv_pool_scales_ptr(const pkv_pool* pool, int32_t layer) {
+  if (!pool || pool->cfg.kv_dtype != PKV_KV_E4M3 || layer < 0 || layer >= pool->cfg.num_layers) return nullptr;
+  const pkv_config& c = pool->cfg;
+  return pool->base + pool->scales_off + (size_t)layer * c.num_blocks * c.num_kv_heads * 2 * c.block_size;
 }
 
 extern "C" pkv_status pkv_pool_check(pkv_pool* pool, int32_t* bits, int32_t clear) {
@@ -190,6 +212,53 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
   }
 }
 
+// 8-bit cache: one thread per 16-byte chunk (8 values) of one token's row of one KV head, CPH = head_dim / 8
+// consecutive lanes per row (CPH divides 32, so a row never straddles warps).  The row's largest magnitude
+// is reduced across its lanes; every lane then writes its 8 codes and the row's first lane the scale bytes.
+// The loop runs warp by warp, so every lane of a warp takes part in the reductions.
+template <int CPH>
+__global__ void __launch_bounds__(256) kv_append_e4m3_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                                             const int64_t* __restrict__ slot_mapping, int num_tokens,
+                                                             unsigned char* __restrict__ codes_k,
+                                                             unsigned char* __restrict__ codes_v,
+                                                             unsigned char* __restrict__ scales, int num_kv_heads,
+                                                             int64_t num_slots, int32_t* err) {
+  dev::griddep_wait();
+  dev::griddep_launch_dependents();
+  const int64_t per_token = (int64_t)num_kv_heads * CPH;
+  const int64_t total = (int64_t)num_tokens * per_token;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32; base < total;
+       base += nwarps * 32) {
+    const int64_t i = base + lane;
+    const bool in = i < total;
+    const int64_t t = in ? i / per_token : 0;
+    const int64_t rem = i - t * per_token;
+    const int64_t h = rem / CPH, c = rem % CPH;
+    const int64_t slot = in ? __ldg(slot_mapping + t) : -1;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    const uint4 rk = in ? __ldg(k + i) : zero, rv = in ? __ldg(v + i) : zero;
+    const uint32_t ak = dev::row_amax_bits<CPH>(dev::f16x8_amax_bits(rk));
+    const uint32_t av = dev::row_amax_bits<CPH>(dev::f16x8_amax_bits(rv));
+    if (!in || slot == -1) continue;
+    if (slot < 0 || slot >= num_slots) {
+      if (c == 0 && h == 0) dev::set_error(err, PKV_DEVERR_SLOT_RANGE);
+      continue;
+    }
+    const int sbk = dev::e4m3_scale_byte(ak), sbv = dev::e4m3_scale_byte(av);
+    const int64_t blk = slot >> 4, off = slot & 15;
+    const int64_t row = (blk * num_kv_heads + h) * 16 + off;
+    reinterpret_cast<uint2*>(codes_k + row * (CPH * 8))[c] = dev::e4m3_encode8(rk, sbk);
+    reinterpret_cast<uint2*>(codes_v + row * (CPH * 8))[c] = dev::e4m3_encode8(rv, sbv);
+    if (c == 0) {
+      unsigned char* rec = scales + (blk * num_kv_heads + h) * 32;  // [K: 16 slots][V: 16 slots]
+      rec[off] = (unsigned char)sbk;
+      rec[16 + off] = (unsigned char)sbv;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) slot_mapping_kernel(const int32_t* __restrict__ block_tables, int max_blocks,
                                                            const int32_t* __restrict__ context_lens,
                                                            const int32_t* __restrict__ qsl, int num_seqs,
@@ -234,6 +303,29 @@ extern "C" pkv_status pkv_append(pkv_pool* pool, int32_t layer, const void* k, c
   int64_t blocks = (total + threads - 1) / threads;
   const int64_t cap = (int64_t)pool->num_sms * 8;
   if (blocks > cap) blocks = cap;
+  if (c.kv_dtype == PKV_KV_E4M3) {
+    const uint4* k4 = static_cast<const uint4*>(k);
+    const uint4* v4 = static_cast<const uint4*>(v);
+    unsigned char* ck = static_cast<unsigned char*>(pkv_pool_layer_ptr(pool, layer, 0));
+    unsigned char* cv = static_cast<unsigned char*>(pkv_pool_layer_ptr(pool, layer, 1));
+    unsigned char* sc = static_cast<unsigned char*>(pkv_pool_scales_ptr(pool, layer));
+    const int64_t ns = (int64_t)c.num_blocks * c.block_size;
+    cudaError_t e;
+    switch (chunks) {
+      case 8: e = launch_pdl(kv_append_e4m3_kernel<8>, dim3((unsigned)blocks), dim3(threads), 0, (cudaStream_t)stream, k4,
+                             v4, slot_mapping, (int)num_tokens, ck, cv, sc, (int)c.num_kv_heads, ns, pool->dev_error);
+        break;
+      case 16: e = launch_pdl(kv_append_e4m3_kernel<16>, dim3((unsigned)blocks), dim3(threads), 0, (cudaStream_t)stream, k4,
+                              v4, slot_mapping, (int)num_tokens, ck, cv, sc, (int)c.num_kv_heads, ns, pool->dev_error);
+        break;
+      default: e = launch_pdl(kv_append_e4m3_kernel<32>, dim3((unsigned)blocks), dim3(threads), 0, (cudaStream_t)stream,
+                              k4, v4, slot_mapping, (int)num_tokens, ck, cv, sc, (int)c.num_kv_heads, ns, pool->dev_error);
+        break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    pool->last_launches = 1;
+    return PKV_OK;
+  }
   cudaError_t e = launch_pdl(kv_append_kernel, dim3((unsigned)blocks), dim3(threads), 0, (cudaStream_t)stream,
                              static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, (int)num_tokens,
                              static_cast<uint4*>(pkv_pool_layer_ptr(pool, layer, 0)),

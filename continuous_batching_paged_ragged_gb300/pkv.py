@@ -33,6 +33,9 @@ PKV_ALLOC_RESERVE = 1
 PKV_UNIT_PASS = 0
 PKV_UNIT_REQUEST = 1
 
+PKV_KV_F16 = 0
+PKV_KV_E4M3 = 1
+
 DEFAULT_SPLIT_BLOCKS = 32  # pkv_config.split_blocks = 0 selects this many blocks per split-K partition
 
 _p = ctypes.c_void_p
@@ -43,7 +46,7 @@ _sz = ctypes.c_size_t
 
 class pkv_config(ctypes.Structure):
     _fields_ = [("num_layers", _i32), ("num_q_heads", _i32), ("num_kv_heads", _i32), ("head_dim", _i32),
-                ("block_size", _i32), ("num_blocks", _i32), ("split_blocks", _i32)]
+                ("block_size", _i32), ("num_blocks", _i32), ("split_blocks", _i32), ("kv_dtype", _i32)]
 
 
 class pkv_sched_config(ctypes.Structure):
@@ -73,6 +76,7 @@ SIGNATURES = {
     "pkv_pool_init": (ctypes.c_int, [ctypes.POINTER(pkv_config), _p, _sz, ctypes.POINTER(_p)]),
     "pkv_pool_destroy": (None, [_p]),
     "pkv_pool_layer_ptr": (_p, [_p, _i32, _i32]),
+    "pkv_pool_scales_ptr": (_p, [_p, _i32]),
     "pkv_pool_check": (ctypes.c_int, [_p, ctypes.POINTER(_i32), _i32]),
     "pkv_slot_mapping": (ctypes.c_int, [_p, _p, _i32, _p, _p, _i32, _i32, _p, _p]),
     "pkv_append": (ctypes.c_int, [_p, _i32, _p, _p, _p, _i32, _p]),
@@ -162,6 +166,10 @@ def pkv_pool_layer_ptr(pool: int, layer: int, kv: int) -> int:
     return load().pkv_pool_layer_ptr(pool, layer, kv) or 0
 
 
+def pkv_pool_scales_ptr(pool: int, layer: int) -> int:
+    return load().pkv_pool_scales_ptr(pool, layer) or 0
+
+
 def pkv_pool_check(pool: int, clear: bool = True) -> int:
     bits = _i32(0)
     _check(load().pkv_pool_check(pool, ctypes.byref(bits), 1 if clear else 0), "pkv_pool_check")
@@ -231,31 +239,43 @@ class Pool:
     """A cache pool backed by one torch uint8 device buffer of pkv_pool_bytes(cfg) bytes."""
 
     def __init__(self, num_layers, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size=16, split_blocks=0,
-                 device="cuda"):
+                 device="cuda", kv_dtype=PKV_KV_F16):
         import torch
-        self.cfg = pkv_config(num_layers, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, split_blocks)
+        self.cfg = pkv_config(num_layers, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, split_blocks,
+                              kv_dtype)
         nbytes = pkv_pool_bytes(self.cfg)
         if nbytes == 0:
             raise PkvError(PKV_ERR_INVALID_ARG, "pkv_pool_bytes", pkv_last_error())
         self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.handle = pkv_pool_init(self.cfg, self.buffer, nbytes)
 
+    @property
+    def is_8bit(self) -> bool:
+        return self.cfg.kv_dtype == PKV_KV_E4M3
+
     def layer(self, layer: int, kv: int):
-        """torch view [num_blocks, Hkv, bs, d] (fp16) of one layer's K (kv=0) or V (kv=1) pool."""
-        import torch
-        c = self.cfg
-        per = c.num_blocks * c.num_kv_heads * c.block_size * c.head_dim
-        off = (layer * 2 + kv) * per
-        return self.buffer[: 2 * c.num_layers * per * 2].view(torch.float16)[off:off + per].view(
-            c.num_blocks, c.num_kv_heads, c.block_size, c.head_dim)
+        """torch view [num_blocks, Hkv, bs, d] of one layer's K (kv=0) or V (kv=1) pool: fp16 values, or uint8
+        E4M3 codes for an 8-bit cache."""
+        return self.cache_view()[layer, kv]
 
     def cache_view(self):
-        """torch view [L, 2, num_blocks, Hkv, bs, d] (fp16) of the whole cache."""
+        """torch view [L, 2, num_blocks, Hkv, bs, d] of the whole cache (fp16, or uint8 codes)."""
         import torch
         c = self.cfg
         n = 2 * c.num_layers * c.num_blocks * c.num_kv_heads * c.block_size * c.head_dim
-        return self.buffer[: n * 2].view(torch.float16).view(c.num_layers, 2, c.num_blocks, c.num_kv_heads,
-                                                            c.block_size, c.head_dim)
+        if self.is_8bit:
+            v = self.buffer[:n]
+        else:
+            v = self.buffer[: n * 2].view(torch.float16)
+        return v.view(c.num_layers, 2, c.num_blocks, c.num_kv_heads, c.block_size, c.head_dim)
+
+    def scales_view(self):
+        """8-bit cache: torch uint8 view [L, num_blocks, Hkv, 2 (K, V), bs] of the scale bytes."""
+        c = self.cfg
+        assert self.is_8bit, "an fp16 cache has no scales"
+        off = 2 * c.num_layers * c.num_blocks * c.num_kv_heads * c.block_size * c.head_dim
+        n = 2 * c.num_layers * c.num_blocks * c.num_kv_heads * c.block_size
+        return self.buffer[off:off + n].view(c.num_layers, c.num_blocks, c.num_kv_heads, 2, c.block_size)
 
     def check(self, clear: bool = True) -> int:
         return pkv_pool_check(self.handle, clear)

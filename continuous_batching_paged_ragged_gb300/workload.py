@@ -37,10 +37,11 @@ class DeviceStep:
         return int(self.block_tables.shape[1])
 
 
-def make_pool(batch: synth.StepBatch, num_layers: Optional[int] = None, split_blocks: int = 0) -> pkv.Pool:
+def make_pool(batch: synth.StepBatch, num_layers: Optional[int] = None, split_blocks: int = 0,
+              kv_dtype: int = pkv.PKV_KV_F16) -> pkv.Pool:
     s = batch.shape
     return pkv.Pool(num_layers or s.num_layers, s.num_q_heads, s.num_kv_heads, s.head_dim, batch.num_blocks,
-                    s.block_size, split_blocks)
+                    s.block_size, split_blocks, kv_dtype=kv_dtype)
 
 
 def upload(batch: synth.StepBatch, pool: pkv.Pool, device="cuda") -> DeviceStep:

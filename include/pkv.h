@@ -20,8 +20,9 @@
  *     sync.  Kernels bounds-check every index they derive from them: an out-of-range value is skipped
  *     (never dereferenced) and recorded in the pool's device error word, read by pkv_pool_check().
  *   - No call traps the device, and no kernel waits on another grid.
- *   - Supported shapes: fp16 K/V/Q; head_dim 64, 128 or 256; block_size 16; num_q_heads a multiple of
- *     num_kv_heads with a group of 1, 2, 4, 6 or 8 query heads per KV head.  Others: PKV_ERR_UNSUPPORTED.
+ *   - Supported shapes: fp16 Q and K/V inputs; an fp16 or 8-bit (E4M3) cache; head_dim 64, 128 or 256;
+ *     block_size 16; num_q_heads a multiple of num_kv_heads with a group of 1, 2, 4, 6 or 8 query heads
+ *     per KV head.  Others: PKV_ERR_UNSUPPORTED.
  */
 #ifndef PKV_H
 #define PKV_H
@@ -58,12 +59,28 @@ typedef enum {
  * grouped-query attention keeps num_kv_heads < num_q_heads.  [SB] "Ragged batches": a paged layout
  * stores only real tokens.
  *
- * Layout of the caller's buffer (fp16, row-major):
- *     cache[num_layers][2 (K, V)][num_blocks][num_kv_heads][block_size][head_dim]
+ * Layout of the caller's buffer (row-major), kv_dtype = PKV_KV_F16:
+ *     cache[num_layers][2 (K, V)][num_blocks][num_kv_heads][block_size][head_dim]   fp16
  * followed by a 256-byte status area (the device error word).  One (block, kv head) is a contiguous
  * run of block_size*head_dim*2 bytes, which the kernels move with single bulk copies.
  * Bytes per token of context = 2 * num_layers * num_kv_heads * head_dim * 2 ([CB], same section).
+ *
+ * kv_dtype = PKV_KV_E4M3, the 8-bit cache.  [CB] "Checking it on a real system": when the cache is
+ * what limits the batch, quantize it; [ABL] "Context math sets the ceiling the fields ignore": 8-bit KV
+ * is half the raw bytes of fp16, with scales on top.  Every cached row (one token's head_dim values of
+ * one KV head, K and V separately) is stored as E4M3 codes (OCP 8-bit floating point: bias 7, no
+ * infinities, largest magnitude 448) and one power-of-two scale 2^e, kept as the byte e + 127; e is the
+ * smallest integer with max|x| <= 448 * 2^e (0 for an all-zero row), and each code is x / 2^e rounded to
+ * the nearest E4M3 value, ties to even.  Nothing is clipped; attention reads code * 2^e exactly.
+ *     codes [num_layers][2 (K, V)][num_blocks][num_kv_heads][block_size][head_dim]   uint8
+ *     scales[num_layers][num_blocks][num_kv_heads][2 (K, V)][block_size]              uint8
+ * then the status area (at the next 256-byte boundary).  A (block, kv head) run of codes is
+ * block_size*head_dim bytes; its K and V scales are one 32-byte record.  Bytes per token of context =
+ * 2 * num_layers * num_kv_heads * (head_dim + 1).  K and V inputs must be finite.
  * ---------------------------------------------------------------------------------------------- */
+#define PKV_KV_F16  0
+#define PKV_KV_E4M3 1
+
 typedef struct {
   int32_t num_layers;
   int32_t num_q_heads;
@@ -72,6 +89,7 @@ typedef struct {
   int32_t block_size;    /* tokens per block; must be 16 */
   int32_t num_blocks;    /* physical blocks per layer    */
   int32_t split_blocks;  /* blocks per split-K partition of a decode row; 0 = library default (32) */
+  int32_t kv_dtype;      /* PKV_KV_F16 (0) or PKV_KV_E4M3 */
 } pkv_config;
 
 typedef struct pkv_pool pkv_pool;
@@ -88,9 +106,13 @@ pkv_status pkv_pool_init(const pkv_config* cfg, void* dev_cache, size_t bytes, p
 /* Frees the host handle only; the device buffer stays the caller's. */
 void pkv_pool_destroy(pkv_pool* pool);
 
-/* Device address of layer `layer`'s K (kv = 0) or V (kv = 1) pool [num_blocks][Hkv][bs][d];
- * NULL on a bad argument. */
+/* Device address of layer `layer`'s K (kv = 0) or V (kv = 1) pool [num_blocks][Hkv][bs][d] (fp16 values,
+ * or E4M3 codes for an 8-bit cache); NULL on a bad argument. */
 void* pkv_pool_layer_ptr(const pkv_pool* pool, int32_t layer, int32_t kv);
+
+/* Device address of layer `layer`'s scale bytes [num_blocks][Hkv][2 (K, V)][bs] of an 8-bit cache; NULL
+ * for an fp16 cache or a bad argument. */
+void* pkv_pool_scales_ptr(const pkv_pool* pool, int32_t layer);
 
 /* Synchronously read the device error word (PKV_DEVERR_* bits) into *bits, then clear it if `clear`.
  * Waits for all work on the legacy default stream's device.  While PKV_DEVERR_WAIT_TIMEOUT is set,
@@ -123,8 +145,9 @@ pkv_status pkv_slot_mapping(pkv_pool* pool, const int32_t* block_tables, int32_t
  * are stored in the cache so later passes need not recompute them; storage is the token's slot in a
  * 16-token block.  Copies k[t], v[t] ([num_kv_heads][head_dim] fp16 each) of `layer` into slot
  * slot_mapping[t] for t < num_tokens; a slot of -1 is skipped (padding); any other out-of-range slot
- * is skipped and sets PKV_DEVERR_SLOT_RANGE.  Bit copy, no arithmetic.  Duplicate slots in one call
- * race (last writer unspecified).
+ * is skipped and sets PKV_DEVERR_SLOT_RANGE.  fp16 cache: a bit copy, no arithmetic.  8-bit cache: each
+ * (token, KV head) row of K and of V is quantized as the pool section describes (codes and scale byte,
+ * bit-exact).  Duplicate slots in one call race (last writer unspecified).
  *
  * k, v          fp16 [num_tokens][num_kv_heads][head_dim]   device, 16-byte aligned
  * slot_mapping  int64 [num_tokens]                          device

@@ -45,3 +45,16 @@ def test_host_side_argument_errors(built):
     assert st == pkv.PKV_ERR_INVALID_ARG and b"non-NULL" in built.pkv_last_error()
     assert built.pkv_append(None, 0, None, None, None, 1, None) == pkv.PKV_ERR_INVALID_ARG
     assert built.pkv_attention(None, 0, None, None, 1, None, None, 1, 1, None, None, 0, None) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_8bit_pool_bytes_follow_the_header_layout(built):
+    """Codes (one byte per value), then one scale byte per cached row, padded to 256, then the status area."""
+    for layers, hkv, d, nb in [(1, 2, 64, 64), (3, 4, 128, 10), (2, 1, 256, 7)]:
+        cfg = pkv.pkv_config(layers, 2 * hkv, hkv, d, 16, nb, 0, pkv.PKV_KV_E4M3)
+        codes = 2 * layers * nb * hkv * 16 * d
+        scales = 2 * layers * nb * hkv * 16
+        assert pkv.pkv_pool_bytes(cfg) == (codes + scales + 255) // 256 * 256 + 256
+        f16 = pkv.pkv_config(layers, 2 * hkv, hkv, d, 16, nb, 0, pkv.PKV_KV_F16)
+        assert pkv.pkv_pool_bytes(f16) == 2 * codes + 256
+    assert pkv.pkv_pool_bytes(pkv.pkv_config(1, 4, 2, 64, 16, 64, 0, 2)) == 0   # no such cache format
+    assert built.pkv_pool_scales_ptr(None, 0) is None
