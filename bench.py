@@ -46,21 +46,24 @@ CONFIGS = {
 
 # DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
-# source they were taken on; reported as null once the source changes.
-TRAFFIC = {"cbfb3d0ea82d": 142.57e6}  # profiles/decode_kernel_qwen_decode.md
+# source they were taken on and the cache format; reported as null once the source changes.
+TRAFFIC = {}  # profiles/decode_kernel_qwen_decode.md
 
 FALLBACK_HBM_GBS = 6800.0
 
 
-def algorithmic_bytes(batch: synth.StepBatch):
-    """Per layer: (attention bytes, append bytes) -- each K/V element of a row read once (GQA grouping),
-    q read and output written once, 4 bytes per block-table entry; append reads k/v and writes them."""
+def algorithmic_bytes(batch: synth.StepBatch, kv8: bool = False):
+    """Per layer: (attention bytes, append bytes) -- each cached K/V row of a row read once (GQA grouping):
+    head_dim fp16 values, or head_dim E4M3 codes and one scale byte on the 8-bit cache; q read and output
+    written once (fp16), 4 bytes per block-table entry; append reads the fp16 k/v and writes them in the
+    cache's format, plus the 8-byte slot of each token."""
     s = batch.shape
     ctx = batch.context_lens.astype(np.int64)
     T = int(batch.q_lens.sum())
-    attn = (2 * int(ctx.sum()) * s.num_kv_heads * s.head_dim * 2 + T * s.num_q_heads * s.head_dim * 2 * 2
+    row = s.head_dim + 1 if kv8 else s.head_dim * 2   # bytes of one cached (token, KV head) row of K or V
+    attn = (2 * int(ctx.sum()) * s.num_kv_heads * row + T * s.num_q_heads * s.head_dim * 2 * 2
             + 4 * int(((ctx + 15) // 16).sum()))
-    append = T * s.num_kv_heads * s.head_dim * 2 * 2 * 2 + 8 * T
+    append = T * s.num_kv_heads * (s.head_dim * 2 * 2 + row * 2) + 8 * T
     return attn, append
 
 
@@ -129,7 +132,7 @@ def time_prefill_rows(batch: synth.StepBatch, reps: int = 20):
 
 def source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("attention.cu", "pkv_internal.cuh"):
+    for f in ("attention.cu", "decode.cuh", "decode_e4m3.cu", "pkv_internal.cuh"):
         with open(os.path.join(ROOT, "continuous_batching_paged_ragged_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
@@ -231,11 +234,17 @@ def oracle_bytes(batch, rows):
             + 4 * int(((ctx + 15) // 16).sum())), int(ctx.sum())
 
 
-def cpu_baseline(batch, budget_s: float = 12.0):
+def cpu_baseline(batch, budget_s: float = 12.0, kv8: bool = False):
     import oracle
     rows = list(range(batch.num_seqs))
     items = oracle_inputs(batch, 0, rows)
     nbytes, nctx = oracle_bytes(batch, rows)
+    if kv8:   # attention over the dequantized 8-bit cache (quantized once, outside the timing)
+        from oracle import fp8
+        items = [(q, fp8.dequantize_rows(*fp8.quantize_rows(k)), fp8.dequantize_rows(*fp8.quantize_rows(v)))
+                 for q, k, v in items]
+        s = batch.shape
+        nbytes -= int(batch.context_lens.astype(np.int64).sum()) * 2 * s.num_kv_heads * (s.head_dim - 1)
     reps, t0 = 0, time.perf_counter()
     while True:
         for q, k, v in items:
@@ -365,7 +374,9 @@ def run_pkv(args, rank, world, local):
                                   batch.shape.head_dim, batch.shape.block_size)
     s = batch.shape
     layers = list(range(s.num_layers))
-    pool = workload.make_pool(batch, split_blocks=args.split_blocks)
+    kv8 = args.kv_cache == "e4m3"
+    pool = workload.make_pool(batch, split_blocks=args.split_blocks,
+                              kv_dtype=pkv.PKV_KV_E4M3 if kv8 else pkv.PKV_KV_F16)
     workload.prefill_cache(pool, batch, layers)
     ds = workload.upload(batch, pool)
     qs, ks, vs = workload.step_inputs(ds, layers)
@@ -400,7 +411,7 @@ def run_pkv(args, rank, world, local):
         else:
             step(layers)
 
-    attn_bytes, append_bytes = algorithmic_bytes(batch)
+    attn_bytes, append_bytes = algorithmic_bytes(batch, kv8)
     step_bytes = (attn_bytes + append_bytes) * len(layers)
     ctx_tokens = int(batch.context_lens.astype(np.int64).sum()) * len(layers)
 
@@ -472,6 +483,7 @@ def run_pkv(args, rank, world, local):
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
                    "rows": batch.num_seqs, "new_tokens": batch.num_tokens,
                    "context_tokens_per_layer": int(batch.context_lens.sum()), "pool_blocks": batch.num_blocks,
+                   "kv_cache": "e4m3 codes + power-of-two scale per cached row" if kv8 else "fp16",
                    "split_blocks": pool.cfg.split_blocks or pkv.DEFAULT_SPLIT_BLOCKS,
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of K/V per step rotating over "
                          f"{s.num_layers} layer pools", "parallelism": f"replicas x{world}",
@@ -481,7 +493,7 @@ def run_pkv(args, rank, world, local):
         "ctx_tokens_per_s": ctx_tokens * world / (ms * 1e-3),
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": TRAFFIC.get(sh),
+                     "traffic": TRAFFIC.get(f"{sh}/{args.kv_cache}"),
                      "kernel": "decode_kernel (split-K decode, fused merge" + (", fused append)" if step.fused else ")")
                                + (" + merge_kernel (tokens with > 32 splits)" if long_merge(batch, pool) else ""),
                      "per_launch_bytes": kernel_bytes, "avg_launch_ms": per_call_ms,
@@ -509,7 +521,7 @@ def run_pkv(args, rank, world, local):
         line["lower_bounds_ms_per_step"] = {"hbm": hbm_ms, "tensor": tensor_ms, "sum": hbm_ms + tensor_ms,
                                             "max": max(hbm_ms, tensor_ms), "measured": ms}
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(batch)
+        line["cpu_baseline"] = cpu_baseline(batch, kv8=kv8)
     print(json.dumps(line), flush=True)
 
 
@@ -664,6 +676,8 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--config", default="qwen_decode", choices=sorted(CONFIGS) + ["sched_trace"])
     ap.add_argument("--split-blocks", type=int, default=0)
+    ap.add_argument("--kv-cache", default="fp16", choices=["fp16", "e4m3"],
+                    help="cache format: fp16 values, or E4M3 codes with a power-of-two scale per cached row")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     ap.add_argument("--eager", action="store_true", help="time the calls issued one by one, not a CUDA graph")

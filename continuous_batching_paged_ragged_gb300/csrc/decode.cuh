@@ -17,8 +17,9 @@ constexpr int kFusedMergeSplits = 32;  // tokens with up to this many splits are
 constexpr int kMaxSplitBlocks = 32;   // upper bound on split_blocks (a split's block ids fit one warp)
 
 // Ring slots per streaming warp: runs (a block's K or V for one KV head) in flight; fewer where the shared
-// memory of two CTAs per SM does not hold them.  The 8-bit cache's runs are half as long: twice the slots
-// keep the same bytes in flight.
+// memory of two CTAs per SM does not hold them.  The 8-bit cache's runs are half as long and its warps go
+// through them faster: its rings take every slot that fits (measured on the long-context decode: halving
+// them nearly doubles the time).
 #ifndef PKV_DECODE_RING
 #define PKV_DECODE_RING(D) ((D) == 256 ? 2 : ((D) == 128 ? 5 : 8))
 #endif
@@ -51,14 +52,14 @@ struct DecodeTraits {
   static constexpr int BOXES = F8 ? 1 : D / 64;    // TMA boxes per run: fp16 16 x 64 values, 8-bit one box
   static constexpr int BOXROWS = kBS * D / 128;    // 8-bit: 128-byte rows of a run (its box height)
   static constexpr int SCL = F8 ? 32 : 0;          // 8-bit: scale record per slot (the K and V scales of a block)
-  static constexpr int RING = F8 ? 2 * PKV_DECODE_RING(D) : PKV_DECODE_RING(D);
+  static constexpr int RING = F8 ? 16 : PKV_DECODE_RING(D);  // 8-bit: as many slots as fit, up to 16
   static constexpr int KS = D / 16;                // MMA k-steps over the head dimension (scores)
   static constexpr int MT = D / 16;                // MMA m-tiles over the head dimension (values)
   static constexpr int OV = MT * 4;                // fp32 output values per lane (8-head fragment)
   static constexpr int LG = (G + 1) / 2;           // lanes l with (l & 3) < LG hold real heads
   static constexpr int SHL = 8 * LG;               // such lanes
   static constexpr int QD = 3;                     // task queue depth
-  static constexpr int QB = kHeadsTile * D * 2;    // a streaming warp's q buffer (8 rows; rows >= G unused)
+  static constexpr int QB = G * D * 2;             // a streaming warp's q buffer (the G heads' rows)
   // everything but the rings: q buffers, shares, staging, queue, the other barriers, flag, alignment slack
   static constexpr int REST = NW * QB + NW * OV * SHL * 4 + NW * kHeadsTile * 8 + G * D * 4 + 64 +
                               QD * (int)sizeof(TaskEntry) + (3 * NW + 2 * QD) * 8 + 16 + 1024;
@@ -78,10 +79,13 @@ struct DecodeTraits {
   static constexpr int OFF_SCL = OFF_FLAG + 16;                      // 8-bit: [NW][NR] scale records
   static constexpr int SMEM = OFF_SCL + NW * NR * SCL + 1024;        // + slack to align the rings to 1024 bytes
   static constexpr int FIT = kSmemPerSM / (SMEM + kSmemReservedPerCTA);
-  static constexpr int MINB = FIT < 3 ? FIT : 3;   // CTAs per SM (shared memory bound)
+  // CTAs per SM (shared memory bound).  The 8-bit d = 256 kernel with 8 query heads per KV head holds too
+  // much in registers for two CTAs (it spills); like its fp16 twin, which shared memory limits to one, it
+  // runs one CTA per SM with the whole register file.
+  static constexpr int MINB = (F8 && D == 256 && G > 6) ? 1 : (FIT < 3 ? FIT : 3);
   static_assert(D % 64 == 0 && G >= 1 && G <= kHeadsTile, "shape");
   static_assert(RUN % 1024 == 0, "swizzled boxes need 1024-byte aligned slots");
-  static_assert(8 * D * 2 <= RUN && KS % 2 == 0, "a task's q (8 rows) fits one slot");
+  static_assert(KS % 2 == 0 && QB % 128 == 0, "k-steps in pairs; q buffers stay 16-byte aligned");
   static_assert(OFF_Q % 16 == 0 && OFF_BAR % 8 == 0 && OFF_STG % 16 == 0 && OFF_MML % 16 == 0, "alignment");
   static_assert(NR <= RING && SMEM <= NW * NR * SLOT + REST + 64, "shared-memory budget");
   static_assert(!F8 || (RUN % 1024 == 0 && BOXROWS <= 256), "8-bit runs are whole swizzle atoms, one box each");
@@ -325,9 +329,9 @@ struct Streamer {
     }
     if (ok && nxt.t >= 0 && nxt.nbw > 0) issue_q(nxt, k + 1);
   }
-  // The current task's q as MMA B fragments (Q^T: k = dims, n = heads); rows G..7 of the buffer hold stale
-  // bytes, which only feed score and output columns of heads >= G, never written out.  Then the buffer is
-  // free for the next task's q.
+  // The current task's q as MMA B fragments (Q^T: k = dims, n = heads).  The buffer holds the G heads' rows;
+  // the columns of heads G..7 repeat head 0 (they feed score and output columns that are never written out).
+  // Then the buffer is free for the next task's q.
   __device__ __forceinline__ void load_q(uint32_t (&qb)[T::KS][2]) {
     if (q_seq != k) issue_q(cur, k);  // not prefetched
     const bool got = cta_wait(qbar, q_used & 1, sm.abort, p.err);
@@ -342,12 +346,12 @@ struct Streamer {
       for (int ks = 0; ks < T::KS; ++ks)
         asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
                      : "=r"(qb[ks][0]), "=r"(qb[ks][1])
-                     : "r"(qs + (lane >> 2) * (D * 2) + (16 * ks + 4 * (lane & 3)) * 2));
+                     : "r"(qs + ((lane >> 2) < G ? lane >> 2 : 0) * (D * 2) + (16 * ks + 4 * (lane & 3)) * 2));
     } else {
 #pragma unroll
       for (int k2 = 0; k2 < T::KS / 2; ++k2) {
         uint32_t r4[4];
-        dev::ldsm_x4(qs + (lane & 7) * (D * 2) + (4 * k2 + (lane >> 3)) * 16, r4);
+        dev::ldsm_x4(qs + ((lane & 7) < G ? lane & 7 : 0) * (D * 2) + (4 * k2 + (lane >> 3)) * 16, r4);
         qb[2 * k2][0] = r4[0];
         qb[2 * k2][1] = r4[1];
         qb[2 * k2 + 1][0] = r4[2];
@@ -533,7 +537,8 @@ __device__ __forceinline__ void stream_loop(const DecodeParams& p, const DecodeS
         uint2 ck = make_uint2(0, 0), cv = ck;  // 8-bit, prefetched rows: this lane's codes and its row's scales
         int sbk = 127, sbv = 127;
         // ---- S^T[16 keys x 8 heads] = K Q^T on the tensor cores ----
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        // Two accumulators (even and odd k-steps) halve the chain of dependent MMAs; summed at the end.
+        float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
         float ks0 = p.scale_log2, ks1 = p.scale_log2;  // score scale of keys qh and qh + 8
         uint32_t ev0 = 127, ev1 = 127;                 // 8-bit: scale bytes of their values
         {
@@ -573,12 +578,13 @@ __device__ __forceinline__ void stream_loop(const DecodeParams& p, const DecodeS
             for (int i = 0; i < D / 32; ++i) {
               uint32_t r[4];
               dev::ldsm_x4(ks_base + swz8<D>(kr, 2 * i + (lane >> 4)), r);
-              const uint32_t a0[4] = {dev::e4m3x2_to_f16x2(r[0]), dev::e4m3x2_to_f16x2(r[1]),
-                                      dev::e4m3x2_to_f16x2(r[0] >> 16), dev::e4m3x2_to_f16x2(r[1] >> 16)};
+              uint32_t a0[4], a1[4];  // {key g lo, key g + 8 lo, key g hi, key g + 8 hi}
+              dev::e4m3x4_to_f16x2x2(r[0], a0[0], a0[2]);
+              dev::e4m3x4_to_f16x2x2(r[1], a0[1], a0[3]);
+              dev::e4m3x4_to_f16x2x2(r[2], a1[0], a1[2]);
+              dev::e4m3x4_to_f16x2x2(r[3], a1[1], a1[3]);
               dev::mma_16816(sc, a0, qb[2 * i][0], qb[2 * i][1]);
-              const uint32_t a1[4] = {dev::e4m3x2_to_f16x2(r[2]), dev::e4m3x2_to_f16x2(r[3]),
-                                      dev::e4m3x2_to_f16x2(r[2] >> 16), dev::e4m3x2_to_f16x2(r[3] >> 16)};
-              dev::mma_16816(sc, a1, qb[2 * i + 1][0], qb[2 * i + 1][1]);
+              dev::mma_16816(sd, a1, qb[2 * i + 1][0], qb[2 * i + 1][1]);
             }
           } else {
             if (nov > 0) override_rows(ks_base, p.k_in, pk);
@@ -586,9 +592,11 @@ __device__ __forceinline__ void stream_loop(const DecodeParams& p, const DecodeS
             for (int ks = 0; ks < T::KS; ++ks) {
               uint32_t a[4];
               dev::ldsm_x4(ks_base + swz(kr, 2 * ks + (lane >> 4)), a);
-              dev::mma_16816(sc, a, qb[ks][0], qb[ks][1]);
+              dev::mma_16816((ks & 1) ? sd : sc, a, qb[ks][0], qb[ks][1]);
             }
           }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sc[i] += sd[i];
           if (nov > 0) dev::fence_proxy_async_smem();  // the override precedes the slot's next TMA write
           w.release_run();
         }
@@ -659,14 +667,10 @@ __device__ __forceinline__ void stream_loop(const DecodeParams& p, const DecodeS
             for (int i = 0; i < D / 32; ++i) {
               uint32_t r[4];
               dev::ldsm_x4_t(vs_base + swz8<D>(vr, 2 * i + (mat & 1)), r);
-              uint32_t x[4];
+              uint32_t ae[4], ao[4];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) x[j] = __byte_perm(r[j], 0, 0x3120);
-              const uint32_t ae[4] = {dev::e4m3x2_to_f16x2(x[0]), dev::e4m3x2_to_f16x2(x[1]),
-                                      dev::e4m3x2_to_f16x2(x[2]), dev::e4m3x2_to_f16x2(x[3])};
+              for (int j = 0; j < 4; ++j) dev::e4m3x4_to_f16x2x2(__byte_perm(r[j], 0, 0x3120), ae[j], ao[j]);
               dev::mma_16816(o[2 * i], ae, pb0, pb1);
-              const uint32_t ao[4] = {dev::e4m3x2_to_f16x2(x[0] >> 16), dev::e4m3x2_to_f16x2(x[1] >> 16),
-                                      dev::e4m3x2_to_f16x2(x[2] >> 16), dev::e4m3x2_to_f16x2(x[3] >> 16)};
               dev::mma_16816(o[2 * i + 1], ao, pb0, pb1);
             }
           } else {

@@ -430,10 +430,15 @@ __device__ __forceinline__ uint2 e4m3_encode8(const uint4& r, int sb) {
   }
   return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
-// Two E4M3 codes (low byte first) as an fp16 pair (low half first); exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four E4M3 codes (byte i = code i) as two fp16 pairs: lo = (code 0, code 1), hi = (code 2, code 3), low
+// half first; exact.  The word's two 16-bit halves feed one conversion each, with no repacking.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four));
 }
 
 // Row of packed token t: the largest b with query_start_loc[b] <= t (query_start_loc has num_seqs + 1
