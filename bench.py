@@ -97,9 +97,10 @@ def prefill_flops(batch: synth.StepBatch) -> int:
     return 4 * s.head_dim * s.num_q_heads * pairs
 
 
-def time_prefill_rows(batch: synth.StepBatch, reps: int = 20):
+def time_prefill_rows(batch: synth.StepBatch, reps: int = 20, kv_dtype: int = pkv.PKV_KV_F16):
     """Mean CUDA-event time of one attention call over only the batch's prefill rows (the tile kernel,
-    plus an empty decode launch), rotating over the layers; None if the batch has no such rows."""
+    plus an empty decode launch; on the 8-bit cache also the dequantizing launch), rotating over the layers;
+    None if the batch has no such rows."""
     rows = [b for b in range(batch.num_seqs) if batch.q_lens[b] >= PREFILL_MIN_QLEN]
     if not rows:
         return None
@@ -107,7 +108,7 @@ def time_prefill_rows(batch: synth.StepBatch, reps: int = 20):
     sub = synth.custom_batch(s, batch.cached_lens[rows], batch.q_lens[rows], seed=batch.seed,
                              req_ids=batch.req_ids[rows])
     layers = list(range(s.num_layers))
-    pool = workload.make_pool(sub)
+    pool = workload.make_pool(sub, kv_dtype=kv_dtype)
     workload.prefill_cache(pool, sub, layers)
     ds = workload.upload(sub, pool)
     qs, _, _ = workload.step_inputs(ds, layers)
@@ -459,7 +460,7 @@ def run_pkv(args, rank, world, local):
     # ---- end to end through the public calls with host buffers ----
     e2e = run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_bytes)
 
-    pf_ms = time_prefill_rows(batch) if rank == 0 else None
+    pf_ms = time_prefill_rows(batch, kv_dtype=pool.cfg.kv_dtype) if rank == 0 else None
 
     if rank != 0:
         return

@@ -170,6 +170,8 @@ struct PlanParams {
   int32_t* items_slot;
   int2* pf_sync;
   int max_slots;
+  int32_t* pf_base;  // 8-bit cache: [num_seqs + 1] first fp16 shadow block of each row (rows that are not prefill
+                     // rows hold none), then the total; or null
   WsHeader* hdr;
   int32_t* err;
 };
@@ -300,6 +302,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
       }
     });
 
+  // ---- 8-bit cache: the prefill rows' blocks, numbered row after row in the fp16 shadow ----
+  if (p.pf_base != nullptr) {
+    int nsh = 0;
+    for (int base = 0; base < p.num_seqs; base += blockDim.x) {
+      const int b = base + threadIdx.x;
+      int nb = 0;
+      if (b < p.num_seqs) {
+        const int q_len = __ldg(p.qsl + b + 1) - __ldg(p.qsl + b), ctx = __ldg(p.context_lens + b);
+        if (p.prefill_min_qlen > 0 && q_len >= p.prefill_min_qlen && row_meta_ok(q_len, ctx, p.max_ctx))
+          nb = (ctx + kBS - 1) / kBS;
+      }
+      int total = 0;
+      const int off = nsh + block_exclusive_scan(nb, warp_sums, &total);
+      if (b < p.num_seqs) p.pf_base[b] = off;
+      nsh += total;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) p.pf_base[p.num_seqs] = nsh;
+  }
+
   if (threadIdx.x == 0) {
     p.hdr->n_tasks = n_dec;
     p.hdr->work = 0;
@@ -317,6 +339,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
 // ---------------------------------------------------------------------------------------------------
 struct WsLayout {
   size_t hdr, tok_row, tok_ctx, merge_cnt, tasks, items, items_slot, pf_sync, pf_ml, pf_o, part_ml, part_o, total;
+  // 8-bit cache with prefill rows: the rows' first shadow block, the shadow block tables and the fp16 shadow
+  size_t pf_base = 0, shadow_bt = 0, shadow = 0;
+  int64_t shadow_blocks = 0;
   int max_splits;
   int64_t max_tasks;
   int prefill_min_qlen;  // 0: every row takes the decode path
@@ -331,8 +356,8 @@ static WsLayout ws_layout(const pkv_config& c, int num_seqs, int num_tokens, int
   w.max_splits = (max_blocks + c.split_blocks - 1) / c.split_blocks;
   w.max_tasks = (int64_t)num_tokens * c.num_kv_heads * w.max_splits;
   const int group = c.num_q_heads / c.num_kv_heads;
-  // the tile kernel reads fp16 K/V; on an 8-bit cache every row takes the decode path
-  const bool prefill = prefill_supported(c.head_dim, group) && c.num_kv_heads < 256 && c.kv_dtype == PKV_KV_F16;
+  // the tile kernel reads fp16 K/V: on an 8-bit cache it reads the prefill rows' blocks from an fp16 shadow
+  const bool prefill = prefill_supported(c.head_dim, group) && c.num_kv_heads < 256;
   w.prefill_min_qlen = prefill ? kPrefillMinQlen : 0;
   w.prefill_pos = prefill_item_positions(group);
   // a prefill row has >= prefill_min_qlen tokens, every other row >= 1: at most R such rows, holding at most
@@ -370,6 +395,17 @@ static WsLayout ws_layout(const pkv_config& c, int num_seqs, int num_tokens, int
   off += up256(parts * kHeadsTile * sizeof(float2));
   w.part_o = off;
   off += up256(parts * 32 * (c.head_dim / 4) * sizeof(float));
+  if (c.kv_dtype == PKV_KV_E4M3 && rows > 0) {
+    // the prefill rows hold at most `rows` x max_blocks blocks, and at most the pool's when no two rows
+    // share one; more than that is refused by the dequantizing kernel (reported, never written)
+    w.shadow_blocks = std::min<int64_t>((int64_t)c.num_blocks, rows * (int64_t)max_blocks);
+    w.pf_base = off;
+    off += up256((size_t)(num_seqs + 1) * 4);
+    w.shadow_bt = off;
+    off += up256((size_t)num_seqs * max_blocks * 4);
+    w.shadow = off;
+    off += up256((size_t)2 * w.shadow_blocks * c.num_kv_heads * kBS * c.head_dim * 2);
+  }
   w.total = off;
   return w;
 }
@@ -396,9 +432,91 @@ static cudaError_t launch_plan(pkv_pool* pool, char* ws, const WsLayout& w, cons
   p.items_slot = reinterpret_cast<int32_t*>(ws + w.items_slot);
   p.pf_sync = reinterpret_cast<int2*>(ws + w.pf_sync);
   p.max_slots = (int)w.max_items;
+  p.pf_base = w.shadow_blocks > 0 ? reinterpret_cast<int32_t*>(ws + w.pf_base) : nullptr;
   p.hdr = reinterpret_cast<WsHeader*>(ws + w.hdr);
   p.err = pool->dev_error;
   return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p);
+}
+
+// ---------------------------------------------------------------------------------------------------
+// 8-bit cache, prefill rows: the tile kernel reads fp16 tiles, so every block of a prefill row is first
+// dequantized (exactly) into an fp16 shadow in the workspace, and the row's shadow block table is written
+// alongside.  The plan numbered the prefill rows' blocks row after row (pf_base, monotone, with the total at
+// the end); a CTA takes shadow blocks in turn, finds its row by binary search over pf_base staged in shared
+// memory, and dequantizes the block's Hkv x 16 rows with all its threads.  Keys past the context in a last
+// block are written as zeros.
+// ---------------------------------------------------------------------------------------------------
+struct DequantParams {
+  const unsigned char* codes_k;  // this layer's codes [num_blocks][Hkv][16][D]
+  const unsigned char* codes_v;
+  const unsigned char* scales;   // this layer's scale records [num_blocks][Hkv][2][16]
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* pf_base;        // [num_seqs + 1]
+  int32_t* shadow_bt;            // [num_seqs][max_blocks]
+  uint4* shadow_k;               // [shadow_blocks][Hkv][16][D] fp16
+  uint4* shadow_v;
+  int32_t* err;
+  int64_t shadow_blocks;
+  int num_seqs, max_blocks, num_kv_heads, num_blocks;
+};
+
+constexpr int kDequantMaxRows = 48 * 1024 - 1;  // pf_base staged in shared memory: (rows + 1) x 4 bytes <= 192 KB
+
+template <int D>
+__global__ void __launch_bounds__(256) dequant_prefill_rows_kernel(const DequantParams p) {
+  extern __shared__ int32_t sbase[];  // [num_seqs + 1]
+  dev::griddep_wait();
+  dev::griddep_launch_dependents();
+  constexpr int CPR = D / 8;  // 16-byte fp16 chunks (8 codes) per row
+  for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) sbase[i] = p.pf_base[i];
+  __syncthreads();
+  const int64_t want = sbase[p.num_seqs];
+  // rows sharing blocks can hold more than the shadow: the excess is refused and reported (the tile kernel
+  // then finds an out-of-range id in their tables and reports it too)
+  if (want > p.shadow_blocks && blockIdx.x == 0 && threadIdx.x == 0) dev::set_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+  const int total = (int)min(want, p.shadow_blocks);
+  const int per_block = p.num_kv_heads * kBS * CPR;
+  for (int sb = blockIdx.x; sb < total; sb += gridDim.x) {
+    int lo = 0, hi = p.num_seqs - 1;  // the row: the last b with sbase[b] <= sb (rows before it hold fewer)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sbase[mid] <= sb) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo, j = sb - sbase[b];
+    const int ctx = __ldg(p.context_lens + b);
+    const int id = __ldg(p.block_tables + (int64_t)b * p.max_blocks + j);
+    const bool ok = id >= 0 && id < p.num_blocks;
+    if (threadIdx.x == 0) {
+      p.shadow_bt[(int64_t)b * p.max_blocks + j] = sb;
+      if (!ok) dev::set_error(p.err, PKV_DEVERR_BLOCK_RANGE);
+    }
+    for (int i = threadIdx.x; i < per_block; i += blockDim.x) {
+      const int h = i / (kBS * CPR), r = (i / CPR) % kBS, c = i % CPR;
+      const bool live = ok && j * kBS + r < ctx;
+      const int64_t src = (ok ? (int64_t)id : 0) * p.num_kv_heads + h;
+      const int64_t dst = (((int64_t)sb * p.num_kv_heads + h) * kBS + r) * CPR + c;
+      const unsigned char* rec = p.scales + src * 32;
+      const uint2 zero = make_uint2(0, 0);
+      const uint2 ck = live ? __ldg(reinterpret_cast<const uint2*>(p.codes_k + (src * kBS + r) * D) + c) : zero;
+      const uint2 cv = live ? __ldg(reinterpret_cast<const uint2*>(p.codes_v + (src * kBS + r) * D) + c) : zero;
+      p.shadow_k[dst] = dev::e4m3x8_dequant(ck, live ? __ldg(rec + r) : 127u);
+      p.shadow_v[dst] = dev::e4m3x8_dequant(cv, live ? __ldg(rec + 16 + r) : 127u);
+    }
+  }
+}
+
+template <int D>
+static cudaError_t launch_dequant(const DequantParams& dq, int num_sms, cudaStream_t s) {
+  static bool attr = false;
+  const size_t smem = (size_t)(dq.num_seqs + 1) * 4;
+  if (!attr && smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(dequant_prefill_rows_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (kDequantMaxRows + 1) * 4);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(dequant_prefill_rows_kernel<D>, dim3((unsigned)(num_sms * 2)), dim3(256), smem, s, dq);
 }
 
 // Inputs of an append fused into the decode launch (k == nullptr: not fused).
@@ -410,7 +528,8 @@ struct FusedAppend {
 
 // decode (+ merge of very long tokens) and prefill tiles for one layer on a planned workspace
 static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, const int32_t* block_tables,
-                                   const int32_t* qsl, int max_blocks, int num_seqs, int num_tokens, void* out, char* ws,
+                                   const int32_t* context_lens, const int32_t* qsl, int max_blocks, int num_seqs,
+                                   int num_tokens, void* out, char* ws,
                                    const WsLayout& w, cudaStream_t s, int* launches,
                                    const FusedAppend& fa = FusedAppend()) {
   const pkv_config& c = pool->cfg;
@@ -455,9 +574,48 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
   if (w.prefill_min_qlen > 0 && num_tokens - num_seqs >= w.prefill_min_qlen - 1) {
     PrefillArgs a;
     a.kv_map = &pool->kv_map;
+    a.block_tables = block_tables;
+    a.layer_row0_k = p.layer_row0_k;
+    a.layer_row0_v = p.layer_row0_v;
+    a.num_blocks = c.num_blocks;
+    if (f8) {  // the prefill rows' blocks, dequantized into the workspace's fp16 shadow
+      char* shadow = ws + w.shadow;
+      const uint64_t srows = (uint64_t)2 * w.shadow_blocks * c.num_kv_heads * kBS;
+      if (pool->shadow_base != shadow || pool->shadow_rows != srows) {
+        const pkv_status st = encode_f16_rows(&pool->shadow_map, shadow, srows, c.head_dim);
+        if (st != PKV_OK) return st;
+        pool->shadow_base = shadow;
+        pool->shadow_rows = srows;
+      }
+      DequantParams dq;
+      dq.codes_k = static_cast<const unsigned char*>(pkv_pool_layer_ptr(pool, layer, 0));
+      dq.codes_v = static_cast<const unsigned char*>(pkv_pool_layer_ptr(pool, layer, 1));
+      dq.scales = p.scales;
+      dq.block_tables = block_tables;
+      dq.context_lens = context_lens;
+      dq.pf_base = reinterpret_cast<const int32_t*>(ws + w.pf_base);
+      dq.shadow_bt = reinterpret_cast<int32_t*>(ws + w.shadow_bt);
+      dq.shadow_k = reinterpret_cast<uint4*>(shadow);
+      dq.shadow_v = reinterpret_cast<uint4*>(shadow + srows / 2 * c.head_dim * 2);
+      dq.err = p.err;
+      dq.shadow_blocks = w.shadow_blocks;
+      dq.num_seqs = num_seqs;
+      dq.max_blocks = max_blocks;
+      dq.num_kv_heads = c.num_kv_heads;
+      dq.num_blocks = c.num_blocks;
+      if (num_seqs > kDequantMaxRows)
+        return fail(PKV_ERR_UNSUPPORTED, "8-bit cache: prefill rows in a pass of more than 49151 rows");
+      e = c.head_dim == 64 ? launch_dequant<64>(dq, pool->num_sms, s) : launch_dequant<128>(dq, pool->num_sms, s);
+      if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
+      *launches += 1;
+      a.kv_map = &pool->shadow_map;
+      a.block_tables = dq.shadow_bt;
+      a.layer_row0_k = 0;
+      a.layer_row0_v = (int)(srows / 2);
+      a.num_blocks = (int)w.shadow_blocks;
+    }
     a.q = q;
     a.out = out;
-    a.block_tables = block_tables;
     a.items = reinterpret_cast<const int4*>(ws + w.items);
     a.items_slot = reinterpret_cast<const int32_t*>(ws + w.items_slot);
     a.pf_sync = reinterpret_cast<int2*>(ws + w.pf_sync);
@@ -465,12 +623,9 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
     a.pf_o = reinterpret_cast<float*>(ws + w.pf_o);
     a.hdr = p.hdr;
     a.err = p.err;
-    a.layer_row0_k = p.layer_row0_k;
-    a.layer_row0_v = p.layer_row0_v;
     a.max_blocks = max_blocks;
     a.num_q_heads = c.num_q_heads;
     a.num_kv_heads = c.num_kv_heads;
-    a.num_blocks = c.num_blocks;
     a.head_dim = c.head_dim;
     a.num_sms = pool->num_sms;
     a.max_items = 2 * w.max_items;
@@ -592,7 +747,7 @@ extern "C" pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q
     return fail(PKV_ERR_INVALID_ARG, "no matching plan: call pkv_attention_plan for this workspace and metadata");
   const WsLayout w = ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks_per_seq);
   int launches = 0;
-  st = launch_attention(pool, layer, q, block_tables, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens, out,
+  st = launch_attention(pool, layer, q, block_tables, context_lens, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens, out,
                         static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches);
   pool->last_launches = launches;
   return st;
@@ -635,14 +790,14 @@ extern "C" pkv_status pkv_attention_append(pkv_pool* pool, int32_t layer, const 
     st = pkv_append(pool, layer, k, v, slot_mapping, num_tokens, stream);
     if (st != PKV_OK) return st;
     launches = pool->last_launches;
-    st = launch_attention(pool, layer, q, block_tables, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens,
+    st = launch_attention(pool, layer, q, block_tables, context_lens, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens,
                           out, static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches);
   } else {
     FusedAppend fa;
     fa.k = k;
     fa.v = v;
     fa.slots = slot_mapping;
-    st = launch_attention(pool, layer, q, block_tables, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens,
+    st = launch_attention(pool, layer, q, block_tables, context_lens, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens,
                           out, static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches, fa);
   }
   pool->last_launches = launches;
@@ -714,7 +869,7 @@ extern "C" pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const
   e = launch_plan(pool, ws, w, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq, s);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   int launches = 1;
-  st = launch_attention(pool, layer, q, block_tables, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens, out,
+  st = launch_attention(pool, layer, q, block_tables, context_lens, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens, out,
                         ws, w, s, &launches);
   pool->last_launches = launches;
   return st;

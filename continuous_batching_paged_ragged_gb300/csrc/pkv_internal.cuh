@@ -47,7 +47,18 @@ struct pkv_pool {
   int num_sms = 0;
   int device = 0;
   pkv::PlanKey plan;           // last plan issued through this pool
+  // 8-bit cache: tensor map of the fp16 shadow in the last workspace used for prefill rows (re-encoded when
+  // the workspace or its size changes)
+  CUtensorMap shadow_map;
+  const void* shadow_base = nullptr;
+  uint64_t shadow_rows = 0;
 };
+
+namespace pkv {
+// 2-D TMA map of `rows` rows of head_dim fp16 values at `base`: boxes of 16 rows x 64 values, 128-byte swizzle
+// (the layout of an fp16 pool, and of the 8-bit cache's fp16 shadow).
+pkv_status encode_f16_rows(CUtensorMap* map, void* base, uint64_t rows, int head_dim);
+}  // namespace pkv
 
 namespace pkv {
 
@@ -439,6 +450,23 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, u
       "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
       : "=r"(lo), "=r"(hi)
       : "r"(four));
+}
+
+// Eight E4M3 codes with scale byte sb as eight fp16 values code * 2^(sb - 127): exact wherever the value is an
+// fp16 number, which it is unless within 3 % of the fp16 maximum (there it saturates to +-65504).
+__device__ __forceinline__ uint4 e4m3x8_dequant(const uint2& codes, uint32_t sb) {
+  const float sc = scale_of_byte(sb);
+  uint32_t h[4];
+  e4m3x4_to_f16x2x2(codes.x, h[0], h[1]);
+  e4m3x4_to_f16x2x2(codes.y, h[2], h[3]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+    const __half2 r = __floats2half2_rn(fminf(fmaxf(f.x * sc, -65504.f), 65504.f),
+                                        fminf(fmaxf(f.y * sc, -65504.f), 65504.f));
+    h[i] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+  return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
 // Row of packed token t: the largest b with query_start_loc[b] <= t (query_start_loc has num_seqs + 1

@@ -54,16 +54,35 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 // (layer, K/V, block, KV head, slot), boxes of 16 rows x 64 values (128 bytes), so a (block, KV head) run of
 // K or V is head_dim / 64 boxes.  8-bit: the codes as rows of 128 bytes; a run (16 * head_dim bytes) is
 // one box of 16 * head_dim / 128 rows.
-static pkv_status encode_kv_map(pkv_pool* p) {
+static EncodeTiledFn tensor_map_encoder() {
   static EncodeTiledFn encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-      return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    encode = reinterpret_cast<EncodeTiledFn>(fn);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && fn) encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
+  return encode;
+}
+
+pkv_status encode_f16_rows(CUtensorMap* map, void* base, uint64_t rows, int head_dim) {
+  EncodeTiledFn encode = tensor_map_encoder();
+  if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (rows >= (1ull << 31)) return fail(PKV_ERR_UNSUPPORTED, "too many rows for 32-bit TMA row coordinates");
+  cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+  cuuint32_t box[2] = {64u, 16u};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
+  return PKV_OK;
+}
+
+static pkv_status encode_kv_map(pkv_pool* p) {
+  EncodeTiledFn encode = tensor_map_encoder();
+  if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const pkv_config& c = p->cfg;
   const bool f8 = c.kv_dtype == PKV_KV_E4M3;
   const uint64_t toks = (uint64_t)c.num_layers * 2 * c.num_blocks * c.num_kv_heads * c.block_size;

@@ -186,3 +186,61 @@ def test_qwen_decode_full_size_sampled(cuda, built):
     for layer in (0, 1):
         for b in (0, 77, 255):
             assert_close(row_slice(batch, outs[layer], b), oracle_row_8bit(batch, layer, b), f"layer {layer} row {b}")
+
+
+# chunked-prefill rows: the tile kernel over the fp16 shadow of their blocks (head_dim 64 and 128)
+PREFILL_ROWS = [(0, 16), (0, 21), (0, 128), (0, 129), (5, 43), (127, 16), (1000, 64), (2047, 200), (16, 250)]
+PREFILL_SHAPES = [(12, 2, 128), (8, 8, 64), (8, 1, 128), (16, 4, 128), (4, 2, 64), (8, 8, 128)]
+
+
+@pytest.mark.parametrize("hq,hkv,d", PREFILL_SHAPES)
+def test_prefill_rows_over_8bit_cache(cuda, built, hq, hkv, d):
+    shape = synth.Shape(1, hq, hkv, d)
+    cached, qls = zip(*PREFILL_ROWS)
+    batch = synth.custom_batch(shape, cached, qls, seed=41)
+    pool, ds, outs = run_batch(batch, [0], kv_dtype=E4M3)
+    for b in range(batch.num_seqs):
+        assert_close(row_slice(batch, outs[0], b), oracle_row_8bit(batch, 0, b),
+                     f"{(hq, hkv, d)} row {b} {PREFILL_ROWS[b]}")
+
+
+def test_prefill_and_decode_rows_fused_call(cuda, built):
+    """Decode rows, short chunks and long chunks in one pass through pkv_attention_append, two layers: the
+    cache gets the append's codes, the long chunks read the shadow, the rest the codes."""
+    shape = synth.Shape(2, 12, 2, 128)
+    rows = [(300, 1), (0, 40), (17, 1), (700, 15), (64, 16), (3000, 1), (250, 333), (1, 1)]
+    cached, qls = zip(*rows)
+    batch = synth.custom_batch(shape, cached, qls, seed=8)
+    pa, _, oa = run_batch(batch, [0, 1], kv_dtype=E4M3, fused=False)
+    pb, _, ob = run_batch(batch, [0, 1], kv_dtype=E4M3, fused=True)
+    assert _same(pa.cache_view(), pb.cache_view()) and _same(pa.scales_view(), pb.scales_view())
+    for layer in (0, 1):
+        assert _same(oa[layer], ob[layer])
+        for b in range(batch.num_seqs):
+            assert_close(row_slice(batch, ob[layer], b), oracle_row_8bit(batch, layer, b), f"layer {layer} row {b}")
+
+
+def test_mixed_step_full_size_sampled(cuda, built):
+    """The mixed pass (83 decode rows, chunks of 2048 on 0 and 1024 on 3072) on an 8-bit cache: decode rows
+    and sampled query tokens of the chunks against the oracle, each over its own causal context."""
+    batch = synth.mixed_step(0)
+    batch.shape = synth.Shape(1, batch.shape.num_q_heads, batch.shape.num_kv_heads, batch.shape.head_dim)
+    pool, ds, outs = run_batch(batch, [0], kv_dtype=E4M3)
+    s = batch.shape
+    for b in range(batch.num_seqs):
+        ql, ctx, req = int(batch.q_lens[b]), int(batch.context_lens[b]), int(batch.req_ids[b])
+        got = row_slice(batch, outs[0], b)
+        if ql == 1:
+            if b % 9 == 0:
+                assert_close(got, oracle_row_8bit(batch, 0, b), f"row {b}")
+            continue
+        k, v = synth.sequence_kv(batch.seed, 0, req, ctx, s.num_kv_heads, s.head_dim)
+        kq = fp8.dequantize_rows(*fp8.quantize_rows(k))
+        vq = fp8.dequantize_rows(*fp8.quantize_rows(v))
+        for i in (0, 1, 127, 128, ql // 2, ql - 1):
+            pos = ctx - ql + i
+            q = synth.token_values(synth.KIND_Q, batch.seed, 0, np.array([req]), np.array([pos]), s.num_q_heads,
+                                   s.head_dim)
+            from oracle import attention_row
+            ref = attention_row(q, kq[: pos + 1], vq[: pos + 1])
+            assert_close(got[i:i + 1], ref, f"row {b} token {i}")
