@@ -47,7 +47,8 @@ CONFIGS = {
 # DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
 # source they were taken on and the cache format; reported as null once the source changes.
-TRAFFIC = {}  # profiles/decode_kernel_qwen_decode.md
+TRAFFIC = {"df422b8cbc83/fp16": 142.22e6,   # profiles/decode_kernel_qwen_decode.md
+           "df422b8cbc83/e4m3": 71.76e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
 
 FALLBACK_HBM_GBS = 6800.0
 
