@@ -713,6 +713,8 @@ extern "C" pkv_status pkv_attention_plan(pkv_pool* pool, const int32_t* context_
   clear_error();
   pkv_status st = check_common(pool, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq);
   if (st == PKV_OK) st = check_workspace(pool, workspace, workspace_bytes, num_seqs, num_tokens, max_blocks_per_seq);
+  if (st == PKV_OK) st = validate_metadata(pool, nullptr, max_blocks_per_seq, context_lens, query_start_loc, num_seqs,
+                                           num_tokens, nullptr, stream);
   if (st != PKV_OK) return st;
   pool->last_launches = 0;
   pool->plan = PlanKey{workspace, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq};
@@ -740,6 +742,8 @@ extern "C" pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q
   if (layer < 0 || layer >= pool->cfg.num_layers) return fail(PKV_ERR_OUT_OF_RANGE, "layer out of range");
   if (num_tokens == 0) return PKV_OK;
   st = check_io(q, out, block_tables);
+  if (st == PKV_OK) st = validate_metadata(pool, block_tables, max_blocks_per_seq, context_lens, query_start_loc,
+                                           num_seqs, num_tokens, nullptr, stream);
   if (st != PKV_OK) return st;
   const PlanKey& k = pool->plan;
   if (k.workspace != workspace || k.context_lens != context_lens || k.query_start_loc != query_start_loc ||
@@ -777,6 +781,9 @@ extern "C" pkv_status pkv_attention_append(pkv_pool* pool, int32_t layer, const 
   if (!k || !v || !slot_mapping) return fail(PKV_ERR_INVALID_ARG, "k, v and slot_mapping must be non-NULL");
   if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16 != 0)
     return fail(PKV_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  st = validate_metadata(pool, block_tables, max_blocks_per_seq, context_lens, query_start_loc, num_seqs, num_tokens,
+                         slot_mapping, stream);
+  if (st != PKV_OK) return st;
   const PlanKey& pk = pool->plan;
   if (pk.workspace != workspace || pk.context_lens != context_lens || pk.query_start_loc != query_start_loc ||
       pk.num_seqs != num_seqs || pk.num_tokens != num_tokens || pk.max_blocks_per_seq != max_blocks_per_seq)
@@ -851,6 +858,8 @@ extern "C" pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const
   if (layer < 0 || layer >= pool->cfg.num_layers) return fail(PKV_ERR_OUT_OF_RANGE, "layer out of range");
   if (num_tokens == 0) return PKV_OK;
   st = check_io(q, out, block_tables);
+  if (st == PKV_OK) st = validate_metadata(pool, block_tables, max_blocks_per_seq, context_lens, query_start_loc,
+                                           num_seqs, num_tokens, nullptr, stream);
   if (st != PKV_OK) return st;
   const WsLayout w = ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks_per_seq);
   if (w.total > kNoAllocScratchBytes)

@@ -58,6 +58,10 @@ namespace pkv {
 // 2-D TMA map of `rows` rows of head_dim fp16 values at `base`: boxes of 16 rows x 64 values, 128-byte swizzle
 // (the layout of an fp16 pool, and of the 8-bit cache's fp16 shadow).
 pkv_status encode_f16_rows(CUtensorMap* map, void* base, uint64_t rows, int head_dim);
+// The PKV_VALIDATE=1 host check of a call's device metadata (a no-op otherwise); null pointers are skipped.
+pkv_status validate_metadata(const pkv_pool* pool, const int32_t* block_tables, int32_t max_blocks,
+                             const int32_t* context_lens, const int32_t* qsl, int32_t num_seqs, int32_t num_tokens,
+                             const int64_t* slots, void* stream);
 }  // namespace pkv
 
 namespace pkv {

@@ -7,8 +7,11 @@
 // the limit) each (token, KV head) row is stored as E4M3 codes with one power-of-two scale.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <string>
+#include <vector>
 
 #include "pkv_internal.cuh"
 
@@ -109,6 +112,71 @@ static size_t cache_bytes_of(const pkv_config* c) {
   if (c->kv_dtype != PKV_KV_E4M3) return values_bytes_of(c);
   const size_t scales = (size_t)2 * c->num_layers * (size_t)c->num_blocks * c->num_kv_heads * c->block_size;
   return (values_bytes_of(c) + scales + 255) / 256 * 256;
+}
+
+// PKV_VALIDATE=1 (read at every call): the device metadata of a call are copied to the host and checked
+// before anything is launched -- query_start_loc from 0 to num_tokens without decreasing, 1 <= q_len <=
+// ctx <= max_blocks * block_size per row, every block id a row's context reaches in [0, num_blocks), every
+// slot in [-1, num_slots).  The stream is synchronized first; while it is being captured into a graph nothing
+// is checked (a capture cannot synchronize).  Any pointer may be null (not checked).
+pkv_status validate_metadata(const pkv_pool* pool, const int32_t* block_tables, int32_t max_blocks,
+                             const int32_t* context_lens, const int32_t* qsl, int32_t num_seqs, int32_t num_tokens,
+                             const int64_t* slots, void* stream) {
+  const char* env = std::getenv("PKV_VALIDATE");
+  if (!env || std::strcmp(env, "1") != 0 || num_tokens <= 0) return PKV_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "PKV_VALIDATE: cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone) return PKV_OK;
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "PKV_VALIDATE: cudaStreamSynchronize");
+  auto fetch = [&](const void* src, size_t bytes, void* dst) -> cudaError_t {
+    return cudaMemcpy(dst, src, bytes, cudaMemcpyDefault);
+  };
+  const pkv_config& c = pool->cfg;
+  std::vector<int32_t> q(qsl ? num_seqs + 1 : 0), ctx(context_lens ? num_seqs : 0);
+  if (qsl && (e = fetch(qsl, q.size() * 4, q.data())) != cudaSuccess) return cuda_fail(e, "PKV_VALIDATE: copy");
+  if (context_lens && (e = fetch(context_lens, ctx.size() * 4, ctx.data())) != cudaSuccess)
+    return cuda_fail(e, "PKV_VALIDATE: copy");
+  if (qsl) {
+    if (q[0] != 0 || q[num_seqs] != num_tokens)
+      return fail(PKV_ERR_INVALID_ARG, "PKV_VALIDATE: query_start_loc must run from 0 to num_tokens");
+    for (int b = 0; b < num_seqs; ++b)
+      if (q[b + 1] < q[b]) return fail(PKV_ERR_INVALID_ARG, "PKV_VALIDATE: query_start_loc decreases at row " +
+                                                              std::to_string(b));
+  }
+  if (qsl && context_lens) {
+    for (int b = 0; b < num_seqs; ++b) {
+      const int ql = q[b + 1] - q[b];
+      if (ql < 1 || ctx[b] < ql || (int64_t)ctx[b] > (int64_t)max_blocks * c.block_size)
+        return fail(PKV_ERR_INVALID_ARG, "PKV_VALIDATE: row " + std::to_string(b) + " has q_len " + std::to_string(ql) +
+                                             " and context " + std::to_string(ctx[b]));
+    }
+  }
+  if (block_tables && context_lens) {
+    std::vector<int32_t> bt((size_t)num_seqs * max_blocks);
+    if ((e = fetch(block_tables, bt.size() * 4, bt.data())) != cudaSuccess) return cuda_fail(e, "PKV_VALIDATE: copy");
+    for (int b = 0; b < num_seqs; ++b) {
+      const int64_t nblk = std::min<int64_t>(((int64_t)ctx[b] + c.block_size - 1) / c.block_size, max_blocks);
+      for (int64_t j = 0; j < nblk; ++j) {
+        const int32_t id = bt[(size_t)b * max_blocks + j];
+        if (id < 0 || id >= c.num_blocks)
+          return fail(PKV_ERR_OUT_OF_RANGE, "PKV_VALIDATE: row " + std::to_string(b) + " block " + std::to_string(j) +
+                                                " is " + std::to_string(id));
+      }
+    }
+  }
+  if (slots) {
+    std::vector<int64_t> sl(num_tokens);
+    if ((e = fetch(slots, sl.size() * 8, sl.data())) != cudaSuccess) return cuda_fail(e, "PKV_VALIDATE: copy");
+    const int64_t ns = (int64_t)c.num_blocks * c.block_size;
+    for (int t = 0; t < num_tokens; ++t)
+      if (sl[t] < -1 || sl[t] >= ns)
+        return fail(PKV_ERR_OUT_OF_RANGE, "PKV_VALIDATE: slot of token " + std::to_string(t) + " is " +
+                                              std::to_string(sl[t]));
+  }
+  return PKV_OK;
 }
 
 }  // namespace pkv
@@ -315,6 +383,8 @@ extern "C" pkv_status pkv_append(pkv_pool* pool, int32_t layer, const void* k, c
   if (!k || !v || !slot_mapping) return fail(PKV_ERR_INVALID_ARG, "k, v and slot_mapping must be non-NULL");
   if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16 != 0)
     return fail(PKV_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  pkv_status vst = validate_metadata(pool, nullptr, 0, nullptr, nullptr, 0, num_tokens, slot_mapping, stream);
+  if (vst != PKV_OK) return vst;
   const pkv_config& c = pool->cfg;
   const int chunks = c.head_dim / 8;
   const int64_t total = (int64_t)num_tokens * c.num_kv_heads * chunks;
@@ -367,6 +437,9 @@ extern "C" pkv_status pkv_slot_mapping(pkv_pool* pool, const int32_t* block_tabl
   if (max_blocks_per_seq < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
   if (!block_tables || !context_lens || !query_start_loc || !slot_mapping)
     return fail(PKV_ERR_INVALID_ARG, "metadata pointers must be non-NULL");
+  pkv_status vst = validate_metadata(pool, block_tables, max_blocks_per_seq, context_lens, query_start_loc, num_seqs,
+                                     num_tokens, nullptr, stream);
+  if (vst != PKV_OK) return vst;
   const int threads = 256;
   int blocks = (num_tokens + threads - 1) / threads;
   if (blocks > pool->num_sms * 8) blocks = pool->num_sms * 8;

@@ -19,6 +19,13 @@
  *   - Contents of device metadata (block ids, slots, lengths) cannot be checked on the host without a
  *     sync.  Kernels bounds-check every index they derive from them: an out-of-range value is skipped
  *     (never dereferenced) and recorded in the pool's device error word, read by pkv_pool_check().
+ *   - PKV_VALIDATE=1 in the environment (read at every call): the calls below also copy the device metadata
+ *     they are given (query_start_loc, context_lens, block tables up to each row's context, slots) to the
+ *     host after synchronizing the stream, and refuse a bad pass before launching anything --
+ *     PKV_ERR_INVALID_ARG for rows (query_start_loc not running from 0 to num_tokens without decreasing, or
+ *     not 1 <= q_len <= ctx <= max_blocks_per_seq * block_size), PKV_ERR_OUT_OF_RANGE for block ids and
+ *     slots.  A debugging aid: it costs a synchronization and copies per call, and is skipped while the
+ *     stream is being captured into a graph.
  *   - No call traps the device, and no kernel waits on another grid.
  *   - Supported shapes: fp16 Q and K/V inputs; an fp16 or 8-bit (E4M3) cache; head_dim 64, 128 or 256;
  *     block_size 16; num_q_heads a multiple of num_kv_heads with a group of 1, 2, 4, 6 or 8 query heads
