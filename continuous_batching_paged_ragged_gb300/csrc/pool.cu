@@ -84,20 +84,20 @@ pkv_status encode_f16_rows(CUtensorMap* map, void* base, uint64_t rows, int head
 }
 
 static pkv_status encode_kv_map(pkv_pool* p) {
+  const pkv_config& c = p->cfg;
+  const uint64_t toks = (uint64_t)c.num_layers * 2 * c.num_blocks * c.num_kv_heads * c.block_size;
+  if (c.kv_dtype != PKV_KV_E4M3) return encode_f16_rows(&p->kv_map, p->base, toks, c.head_dim);
   EncodeTiledFn encode = tensor_map_encoder();
   if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const pkv_config& c = p->cfg;
-  const bool f8 = c.kv_dtype == PKV_KV_E4M3;
-  const uint64_t toks = (uint64_t)c.num_layers * 2 * c.num_blocks * c.num_kv_heads * c.block_size;
-  const uint64_t rows = f8 ? toks * c.head_dim / 128 : toks;
+  const uint64_t rows = toks * c.head_dim / 128;
   if (rows >= (1ull << 31)) return fail(PKV_ERR_UNSUPPORTED, "pool too large for 32-bit TMA row coordinates");
-  cuuint64_t dims[2] = {f8 ? 128u : (cuuint64_t)c.head_dim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {f8 ? 128u : (cuuint64_t)c.head_dim * 2};
-  cuuint32_t box[2] = {f8 ? 128u : 64u, f8 ? (cuuint32_t)(c.block_size * c.head_dim / 128) : 16u};
+  cuuint64_t dims[2] = {128u, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {128u};
+  cuuint32_t box[2] = {128u, (cuuint32_t)(c.block_size * c.head_dim / 128)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(&p->kv_map, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->base,
-                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = encode(&p->kv_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p->base, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
   return PKV_OK;
 }
