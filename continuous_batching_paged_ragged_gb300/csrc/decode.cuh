@@ -26,7 +26,7 @@ constexpr int kMaxSplitBlocks = 32;   // upper bound on split_blocks (a split's 
 
 constexpr int kSmemPerSM = 228 * 1024;  // shared memory of one SM
 constexpr int kSmemReservedPerCTA = 1024;
-constexpr int kStaticTasks = 2;         // each CTA's first two tasks come without a counter (see Scheduler)
+constexpr int kStaticTasks = 1;         // each CTA's first task comes without a counter (see Scheduler)
 constexpr int kEagerClaimBlocks = 8;    // past tasks this small, the scheduler claims as early as slots allow
 
 // One task as the scheduler warp hands it to the streaming warps and the combiner warp (shared memory).
@@ -796,11 +796,12 @@ __device__ __forceinline__ void frag_coord(int lane, int r, int& dim, int& head)
 }
 
 // ---------------------------------------------------------------------------------------------------
-// Scheduler warp: publishes the CTA's tasks into the queue.  The first two are static and published before
-// the dependency wait: task blockIdx.x and task 2 * gridDim.x - 1 - blockIdx.x, so that over a task list
-// ordered largest first every CTA starts with a pair of about the same total size.  Every later task is
-// claimed from a global counter once the streaming warps have finished the task two entries back: a CTA
-// then holds one task it has not started, and the launch ends balanced.
+// Scheduler warp: publishes the CTA's tasks into the queue.  The first is static and published before the
+// dependency wait: task blockIdx.x, one of the largest (the list is ordered largest first).  Every later task
+// is claimed from a global counter -- the second at once, each next one once the streaming warps have
+// finished the task two entries back -- so the tasks go out largest first to whichever CTA is ready: a
+// greedy longest-first schedule, which ends the launch more evenly than pairing two static tasks per CTA
+// (2 % on the 256-row decode).  A CTA holds one task it has not started.
 // ---------------------------------------------------------------------------------------------------
 template <int D, int G, int KV>
 struct Scheduler {
@@ -876,8 +877,8 @@ struct Scheduler {
   // Before the dependency wait: the static entries (they touch no counter).
   __device__ void prologue() {
     n_tasks = __ldcg(&p.hdr->n_tasks);
-    static_assert(kStaticTasks == 2, "static pairing");
-    const int idx[kStaticTasks] = {(int)blockIdx.x, 2 * (int)gridDim.x - 1 - (int)blockIdx.x};
+    static_assert(kStaticTasks == 1, "one static task");
+    const int idx[kStaticTasks] = {(int)blockIdx.x};
     publish(idx);
   }
   __device__ void run() {
