@@ -47,8 +47,8 @@ CONFIGS = {
 # DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
 # source they were taken on and the cache format; reported as null once the source changes.
-TRAFFIC = {"df422b8cbc83/fp16": 142.22e6,   # profiles/decode_kernel_qwen_decode.md
-           "df422b8cbc83/e4m3": 71.76e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
+TRAFFIC = {"c346618e19d1/fp16": 142.56e6,   # profiles/decode_kernel_qwen_decode.md
+           "c346618e19d1/e4m3": 72.05e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
 
 FALLBACK_HBM_GBS = 6800.0
 
