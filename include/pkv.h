@@ -184,6 +184,13 @@ pkv_status pkv_append(pkv_pool* pool, int32_t layer, const void* k, const void* 
  * The result is independent of the batch: a row's split-K partition depends only on its own
  * context length, so a row gives bit-identical output alone or in any batch, in any row order.
  *
+ * 8-bit cache: attention reads the dequantized values code * 2^e exactly (scales applied in fp32).  Rows
+ * with 16 or more new tokens (head_dim 64 or 128) first have their blocks dequantized into an fp16 shadow
+ * inside the workspace, read by the tensor-core tile kernel; values within 3 % of the fp16 maximum saturate
+ * there.  pkv_attention_workspace_bytes then includes room for min(num_blocks, R * max_blocks_per_seq)
+ * shadow blocks, R the most rows of 16+ new tokens the pass can hold; prefill rows holding more blocks in
+ * total (rows sharing blocks count each time) are refused and reported (PKV_DEVERR_BLOCK_RANGE).
+ *
  * q                fp16 [num_tokens][num_q_heads][head_dim]   device, 16-byte aligned
  * block_tables     int32 [num_seqs][max_blocks_per_seq]       device
  * context_lens     int32 [num_seqs]                           device
@@ -207,9 +214,11 @@ pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q, const int
  * as pkv_append(pool, layer, k, v, slot_mapping, num_tokens) followed by pkv_attention(...) with the
  * other arguments, under the same plan.  When no row of the pass can take the prefill path (every row
  * has fewer than 16 new tokens; the host checks num_tokens - num_seqs < 15), the append runs inside
- * the decode launch: tiles take this pass's keys and values from k / v directly, and each token is
- * written to the cache by the warp whose block holds its position, so no separate append precedes the
- * attention.  Otherwise this is the append launch followed by the attention launches.  Tokens of rows
+ * the decode launch: tiles take this pass's keys and values from k / v directly (on an 8-bit cache,
+ * quantized exactly as the append would store them), and each token is written to the cache by the warp
+ * whose block holds its position, so no separate append precedes the attention.  Otherwise (and on an
+ * 8-bit cache whenever a row may have 16 or more new tokens) this is the append launch followed by the
+ * attention launches.  Tokens of rows
  * whose metadata is rejected (PKV_DEVERR_ROW_META) are not appended on the fused path.
  *
  * k, v             fp16 [num_tokens][num_kv_heads][head_dim]   device, 16-byte aligned
