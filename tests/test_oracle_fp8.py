@@ -214,3 +214,28 @@ def test_quantizer_mutants_are_caught(kind):
         if not (a <= 448.0 * 2.0 ** e and a > 448.0 * 2.0 ** (e - 1)):
             caught = True
     assert caught, kind
+
+
+def test_quantizing_twice_changes_nothing():
+    """Dequantized rows are fixed points: quantizing them again gives back the same values.  (Not always the
+    same codes and scale: a row whose largest value rounded down to 224 * 2^e is stored again as 448 * 2^(e-1).)"""
+    rng = np.random.default_rng(6)
+    x = _rows(rng, 40, 64)
+    xh = fp8.dequantize_rows(*fp8.quantize_rows(x))
+    xh2 = fp8.dequantize_rows(*fp8.quantize_rows(xh.astype(np.float16)))
+    assert np.array_equal(xh, xh2)
+
+
+def test_values_on_the_grid_come_back_exactly():
+    """A row built from E4M3 values times 2^e (its largest magnitude in (224, 448] * 2^e) is stored exactly."""
+    rng = np.random.default_rng(7)
+    table = fp8.e4m3_table()
+    finite = np.array([c for c in range(256) if not np.isnan(table[c])])
+    for e in (-15, -8, 0, 5):     # from 2^-15 on, every E4M3 value times 2^e is an fp16 number
+        codes = rng.choice(finite, size=32)
+        codes[3] = 0x7E                                   # 448: the row's largest magnitude
+        x = (table[codes] * 2.0 ** e).astype(np.float16)
+        assert np.array_equal(x.astype(np.float64), table[codes] * 2.0 ** e)
+        c, sb = fp8.quantize_row(x)
+        assert sb - fp8.SCALE_BIAS == e
+        assert np.array_equal(fp8.dequantize_row(c, sb), x.astype(np.float64))
