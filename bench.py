@@ -10,7 +10,9 @@ number is the GPU's, not the host's launch rate; `--eager` times the calls issue
 
 Prints one JSON line (rank 0).  `value` is algorithmic HBM bytes per second of the whole step (K/V read
 once per row and layer, q read, output written, block tables, append traffic); `ctx_tokens_per_s` is the
-number of context tokens attended per second.  `--impl reference` times the CPU oracle instead.
+number of context tokens attended per second.  `--kv-cache e4m3` runs the same step on the 8-bit cache (E4M3
+codes and a power-of-two scale per cached row; its bytes counted as stored).  `--impl reference` times the
+CPU oracle instead; `--config sched_trace` runs the scheduler policies' trace.
 """
 from __future__ import annotations
 
@@ -279,6 +281,12 @@ def run_reference(args, rank, world):
     rows = rows_all[:n]
     items = oracle_inputs(batch, 0, rows)
     nbytes, nctx = oracle_bytes(batch, rows)
+    if args.kv_cache == "e4m3":   # attention over the dequantized 8-bit cache (quantized once, untimed)
+        from oracle import fp8
+        items = [(q, fp8.dequantize_rows(*fp8.quantize_rows(k)), fp8.dequantize_rows(*fp8.quantize_rows(v)))
+                 for q, k, v in items]
+        s = batch.shape
+        nbytes -= nctx * 2 * s.num_kv_heads * (s.head_dim - 1)
     for _ in range(args.warmup):
         for q, k, v in items:
             oracle.attention_row(q, k, v)
@@ -293,7 +301,7 @@ def run_reference(args, rank, world):
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": batch.name, "rows_per_step": n, "layers_per_step": 1},
+        "config": {"workload": batch.name, "rows_per_step": n, "layers_per_step": 1, "kv_cache": args.kv_cache},
         "ctx_tokens_per_s": nctx * args.steps / el,
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{n} of {batch.num_seqs} rows of layer 0 per step, fp64 NumPy, 1 thread"},

@@ -28,7 +28,7 @@ def _rank(rank, world, port, results):
         ms = bench.max_over_ranks(1.5 + rank, w)   # rank 1 is the slow one
         out = io.StringIO()
         with contextlib.redirect_stdout(out):
-            args = type("A", (), {"config": "tiny_decode", "steps": 1, "warmup": 3})()
+            args = type("A", (), {"config": "tiny_decode", "steps": 1, "warmup": 3, "kv_cache": "fp16"})()
             if r != 0:
                 bench.run_reference(args, r, w)   # rank 0 alone runs the oracle arm
         results[rank] = (r, w, local, ms, out.getvalue())
