@@ -26,6 +26,7 @@ import ctypes
 import hashlib
 import json
 import math
+import re
 import statistics
 import subprocess
 import sys
@@ -541,14 +542,19 @@ def run_pkv(args, rank, world, local):
 # Scheduler-driven trace under each allocation policy and unit of scheduling
 # ----------------------------------------------------------------------------------------------------
 
-TRACE_POLICIES = [  # (name, allocation, unit, declared output / real output, max_num_seqs, blocks, prefix caching)
-    ("on_demand/pass", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 256, 20000, False),
-    ("reserve 1x/pass", pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 1.0, 256, 20000, False),
-    ("reserve 4x/pass", pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 4.0, 256, 20000, False),
-    ("on_demand/pass cap 64", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 64, 20000, False),
-    ("on_demand/request cap 64", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_REQUEST, 1.0, 64, 20000, False),
-    ("on_demand/pass 5000 blocks", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 256, 5000, False),
-    ("on_demand/pass 5000 blocks prefix-cached", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 256, 5000, True),
+# (name, allocation, unit, declared output / real output, max_num_seqs, blocks, prefix caching, cache format).
+# The last row spends the bytes of the 5,000-block fp16 pool on the 8-bit cache: 2 d / (d + 1) times the blocks.
+TRACE_POLICIES = [
+    ("on_demand/pass", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 256, 20000, False, "fp16"),
+    ("reserve 1x/pass", pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 1.0, 256, 20000, False, "fp16"),
+    ("reserve 4x/pass", pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 4.0, 256, 20000, False, "fp16"),
+    ("on_demand/pass cap 64", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 64, 20000, False, "fp16"),
+    ("on_demand/request cap 64", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_REQUEST, 1.0, 64, 20000, False, "fp16"),
+    ("on_demand/pass 5000 blocks", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 256, 5000, False, "fp16"),
+    ("on_demand/pass 5000 blocks prefix-cached", pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_PASS, 1.0, 256, 5000, True,
+     "fp16"),
+    ("on_demand/pass 8-bit cache, 9922 blocks (the bytes of 5000 fp16 blocks)", pkv.PKV_ALLOC_ON_DEMAND,
+     pkv.PKV_UNIT_PASS, 1.0, 256, 5000 * 2 * 128 // 129, False, "e4m3"),
 ]
 
 
@@ -562,7 +568,9 @@ def run_sched_trace(args, rank, world, local):
     L, Hq, Hkv, d, nblk, cap, budget = 28, 12, 2, 128, 20000, 256, 8192
     reqs = synth.trace_requests(0)
     max_w = max((r.prompt_len + r.max_output + 15) // 16 for r in reqs)
-    pool = pkv.Pool(L, Hq, Hkv, d, nblk)
+    policies = [t for t in TRACE_POLICIES if re.search(args.trace_filter, t[0])]
+    pools = {kv: pkv.Pool(L, Hq, Hkv, d, nblk, kv_dtype=pkv.PKV_KV_E4M3 if kv == "e4m3" else pkv.PKV_KV_F16)
+             for kv in sorted({t[7] for t in policies})}
     q = torch.zeros(budget, Hq, d, dtype=torch.float16, device=dev)
     k = torch.zeros(budget, Hkv, d, dtype=torch.float16, device=dev)
     v = torch.zeros_like(k)
@@ -571,13 +579,14 @@ def run_sched_trace(args, rank, world, local):
     ctx = torch.empty(cap, dtype=torch.int32, device=dev)
     qsl = torch.empty(cap + 1, dtype=torch.int32, device=dev)
     slots = torch.empty(budget, dtype=torch.int64, device=dev)
-    ws_bytes = pkv.pkv_attention_workspace_bytes(pool.handle, cap, budget, max_w)
+    ws_bytes = max(pkv.pkv_attention_workspace_bytes(pl.handle, cap, budget, max_w) for pl in pools.values())
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     lib = pkv.load()
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     results = []
-    for name, alloc, unit, declared, max_seqs, blocks, prefix in TRACE_POLICIES:
+    for name, alloc, unit, declared, max_seqs, blocks, prefix, kv in policies:
+        pool = pools[kv]
         sched = pkv.Scheduler(max_seqs, budget, 16, blocks, synth.block_permutation(blocks, 0), alloc=alloc, unit=unit,
                               prefix_caching=prefix)
         for r in reqs:
@@ -617,7 +626,7 @@ def run_sched_trace(args, rank, world, local):
                         "preemptions": stt["preemptions"], "recomputed_tokens": stt["recomputed_tokens"],
                         "max_batch": stt["max_batch"], "mean_batch": stt["batch_sum"] / max(1, stt["steps"]),
                         "live_cache": stt["live_tokens"] / max(1, stt["held_slots"]), "pool_blocks": blocks,
-                        "prefix_hit_tokens": stt["prefix_hit_tokens"],
+                        "prefix_hit_tokens": stt["prefix_hit_tokens"], "kv_cache": kv,
                         "tokens_scheduled": stt["tokens_scheduled"], "gpu_launches": launches})
     if rank != 0:
         return
@@ -688,6 +697,8 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--config", default="qwen_decode", choices=sorted(CONFIGS) + ["sched_trace"])
     ap.add_argument("--split-blocks", type=int, default=0)
+    ap.add_argument("--trace-filter", default="", help="sched_trace: run the policies whose name matches this "
+                    "regular expression")
     ap.add_argument("--kv-cache", default="fp16", choices=["fp16", "e4m3"],
                     help="cache format: fp16 values, or E4M3 codes with a power-of-two scale per cached row")
     ap.add_argument("--no-cpu-baseline", action="store_true")
