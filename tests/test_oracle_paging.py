@@ -101,3 +101,16 @@ def test_append_reference_scatter_and_skip():
     assert np.array_equal(pk[0, :, 2], k[2]) and np.array_equal(pv[0, :, 2], v[2])
     # exactly 2 tokens' worth of bytes changed (slot -1 skipped)
     assert np.count_nonzero(np.any(pk != 0, axis=-1)) == 2 * hkv
+
+
+def test_bench_byte_counts_match_the_sizing_formula():
+    """The benchmark's algorithmic bytes: K and V once per row and layer at the pages' per-token cost
+    (2 x Hkv x d x bytes, per layer), and on the 8-bit cache d code bytes plus one scale byte per row."""
+    import bench
+    batch = synth.custom_batch(synth.Shape(1, 12, 2, 128), [300, 17], [1, 1], seed=0)
+    ctx = int(batch.context_lens.sum())
+    a16, _ = bench.algorithmic_bytes(batch)
+    a8, _ = bench.algorithmic_bytes(batch, kv8=True)
+    other = 2 * 12 * 128 * 2 * 2 + 4 * int(((batch.context_lens + 15) // 16).sum())   # q in, out, tables
+    assert a16 - other == ctx * oracle.kv_bytes_per_token(1, 2, 128, 2)
+    assert a8 - other == ctx * 2 * 2 * (128 + 1)
