@@ -239,3 +239,18 @@ def test_values_on_the_grid_come_back_exactly():
         c, sb = fp8.quantize_row(x)
         assert sb - fp8.SCALE_BIAS == e
         assert np.array_equal(fp8.dequantize_row(c, sb), x.astype(np.float64))
+
+
+def test_only_the_top_of_the_fp16_range_dequantizes_past_it():
+    """The reading behind the 8-bit prefill shadow: a dequantized value leaves the fp16 range only when the
+    row's exponent is 8 and the value rounds up to 256 * 2^8 = 65536, i.e. |x| >= 63488 (within 3 % of the
+    fp16 maximum 65504)."""
+    c, sb = fp8.quantize_row(np.array([63488.0, 1.0], dtype=np.float16))
+    assert sb - fp8.SCALE_BIAS == 8 and fp8.dequantize_row(c, sb)[0] == 65536.0
+    c, sb = fp8.quantize_row(np.array([63456.0, 1.0], dtype=np.float16))   # the fp16 value just below
+    assert fp8.dequantize_row(c, sb)[0] == 61440.0
+    rng = np.random.default_rng(8)
+    x = (rng.uniform(-1, 1, size=(200, 64)) * np.exp2(rng.uniform(-24, 15.9, size=(200, 1)))).astype(np.float16)
+    x = x[np.abs(x.astype(np.float64)).max(axis=1) < 63488]
+    xh = fp8.dequantize_rows(*fp8.quantize_rows(x))
+    assert np.abs(xh).max() <= 65504 and np.array_equal(xh.astype(np.float16).astype(np.float64), xh)
