@@ -145,3 +145,74 @@ def test_prefix_caching_matches_oracle(built, num_blocks, cap):
         ref.add(r.req_id, r.prompt_len, r.max_output)
     st = _compare_runs(native, ref)
     assert st["prefix_hit_tokens"] > 0
+
+
+def _compare_step(a, b):
+    assert a["req_ids"].tolist() == b.req_ids.tolist()
+    assert np.array_equal(a["q_lens"], b.q_lens) and np.array_equal(a["context_lens"], b.context_lens)
+    assert np.array_equal(a["block_tables"], b.block_tables)
+    assert np.array_equal(a["slot_mapping"], b.slot_mapping)
+    assert a["preempted"] == b.preempted and a["admitted"] == b.admitted
+    assert sorted(a["finished"]) == sorted(b.finished)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_workloads_with_arrivals_aborts_and_cap_changes(built, seed):
+    """Small random pools (heavy preemption), budgets, block sizes and every policy; requests arriving during
+    the run, aborts of live requests and max_num_seqs changes between passes: the C++ scheduler and the oracle
+    agree pass by pass, and at the end every block is back in the same free-list order."""
+    rng = np.random.default_rng(1000 + seed)
+    bs = int(rng.choice([1, 4, 16]))
+    nb = int(rng.integers(8, 200))
+    budget = int(rng.integers(4, 300))
+    cap = int(rng.integers(1, 24))
+    alloc = [oracle.ON_DEMAND, oracle.RESERVE][int(rng.integers(0, 2))]
+    unit = [oracle.PASS, oracle.REQUEST][int(rng.integers(0, 2))]
+    pc = alloc == oracle.ON_DEMAND and bool(rng.integers(0, 2))
+    perm = [int(x) for x in rng.permutation(nb)]
+    native = Scheduler(cap, budget, bs, nb, perm, alloc=_ALLOC[alloc], unit=_UNIT[unit], prefix_caching=pc)
+    ref = oracle.Scheduler(cap, budget, bs, perm, alloc, unit, pc)
+    next_id, live = 0, set()
+
+    def arrive():
+        nonlocal next_id
+        room = nb * bs
+        prompt = int(rng.integers(1, max(2, room // 3)))
+        out = int(rng.integers(1, max(2, room // 4)))
+        declared = out + int(rng.integers(0, 3 * out + 1))
+        worst = prompt + (declared if alloc == oracle.RESERVE else out)
+        if -(-worst // bs) > nb:
+            return
+        native.add(next_id, prompt, out, declared)
+        ref.add(next_id, prompt, out, declared)
+        live.add(next_id)
+        next_id += 1
+
+    for _ in range(int(rng.integers(1, 12))):
+        arrive()
+    for n in range(20000):
+        if ref.done() and n > 60:
+            break
+        if n < 60:
+            r = rng.random()
+            if r < 0.25:
+                arrive()
+            elif r < 0.30 and live:
+                victim = int(rng.choice(sorted(live)))
+                native.abort(victim)
+                ref.abort(victim)
+                live.discard(victim)
+            elif r < 0.35:
+                c = int(rng.integers(1, 24))
+                native.set_max_num_seqs(c)
+                ref.set_max_num_seqs(c)
+        a, b = native.step(), ref.step()
+        _compare_step(a, b)
+        live -= set(a["finished"])
+    assert ref.done() and native.done()
+    st = native.stats()
+    assert (st["steps"], st["preemptions"], st["recomputed_tokens"]) == (ref.steps, ref.num_preemptions,
+                                                                        ref.recomputed_tokens)
+    assert (st["live_tokens"], st["held_slots"], st["prefix_hit_tokens"]) == (ref.live_tokens, ref.held_slots,
+                                                                             ref.prefix_hit_tokens)
+    assert native.free_list() == list(ref.free) and len(ref.free) == nb
