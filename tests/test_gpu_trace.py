@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from continuous_batching_paged_ragged_gb300 import pkv, synth, workload
-from helpers_gpu import assert_close, oracle_row, row_slice
+from helpers_gpu import assert_close, oracle_row, oracle_row_8bit, poison, row_slice
 
 pytestmark = pytest.mark.gpu
 
@@ -23,23 +23,27 @@ def _step_batch(shape, num_blocks, st):
                            np.ascontiguousarray(st["block_tables"]), np.zeros(0, dtype=np.int32), SEED, "trace")
 
 
-@pytest.mark.parametrize("num_blocks,cap,steps,alloc,unit,declared,prefix", [
-    (20000, 256, 24, 0, 0, 1.0, False), (5000, 256, 84, 0, 0, 1.0, False), (20000, 64, 16, 0, 0, 1.0, False),
-    (5000, 256, 40, pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 4.0, False),
-    (20000, 64, 40, pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_REQUEST, 1.0, False),
-    (5000, 256, 110, 0, 0, 1.0, True)])
-def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps, alloc, unit, declared, prefix):
+@pytest.mark.parametrize("num_blocks,cap,steps,alloc,unit,declared,prefix,kv", [
+    (20000, 256, 24, 0, 0, 1.0, False, 0), (5000, 256, 84, 0, 0, 1.0, False, 0), (20000, 64, 16, 0, 0, 1.0, False, 0),
+    (5000, 256, 40, pkv.PKV_ALLOC_RESERVE, pkv.PKV_UNIT_PASS, 4.0, False, 0),
+    (20000, 64, 40, pkv.PKV_ALLOC_ON_DEMAND, pkv.PKV_UNIT_REQUEST, 1.0, False, 0),
+    (5000, 256, 110, 0, 0, 1.0, True, 0),
+    (9922, 256, 60, 0, 0, 1.0, False, pkv.PKV_KV_E4M3)])
+def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps, alloc, unit, declared, prefix, kv):
     """The default policy, and the Orca reservation ("The allocator is the other half"), request-level
     batching ("The boundary: when this is worth nothing") and prefix-cached recompute variants of the same
-    page.  With prefix caching a readmitted request reads the blocks it wrote before its preemption."""
+    page.  With prefix caching a readmitted request reads the blocks it wrote before its preemption.  The last
+    case is the 8-bit cache ("Checking it on a real system": quantize the cache) at the bytes of 5,000 fp16
+    blocks; its rows are checked against the oracle over the dequantized cache."""
     shape = synth.Shape(len(LAYERS), 12, 2, 128)
     sched = pkv.Scheduler(cap, 8192, 16, num_blocks, free_order=synth.block_permutation(num_blocks, SEED),
                           alloc=alloc, unit=unit, prefix_caching=prefix)
     for r in synth.trace_requests(SEED):
         sched.add(r.req_id, r.prompt_len, r.max_output, int(round(declared * r.max_output)))
     probe = synth.custom_batch(shape, [1], [1], seed=SEED, num_blocks=num_blocks)
-    pool = workload.make_pool(probe)
-    pool.cache_view().view(torch.int16).fill_(0x7E00)  # fp16 NaN wherever nothing was appended
+    pool = workload.make_pool(probe, kv_dtype=kv)
+    poison(pool)  # NaN wherever nothing was appended
+    reference = oracle_row_8bit if kv == pkv.PKV_KV_E4M3 else oracle_row
     rng = np.random.default_rng(7)
     preempted, rechecked, reused = set(), 0, 0
     for step in range(steps):
@@ -71,7 +75,7 @@ def test_scheduler_trace_passes(cuda, built, num_blocks, cap, steps, alloc, unit
             rechecked += 1
             reused += len(fresh)
         for b in sample:
-            assert_close(row_slice(batch, outs[1], b), oracle_row(batch, 1, int(b)),
+            assert_close(row_slice(batch, outs[1], b), reference(batch, 1, int(b)),
                          f"step {step} row {b} (req {batch.req_ids[b]}, q_len {ql[b]}, ctx {ctx[b]})")
     stats = sched.stats()
     if num_blocks == 5000 and alloc == pkv.PKV_ALLOC_ON_DEMAND:
