@@ -50,8 +50,8 @@ CONFIGS = {
 # DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
 # source they were taken on and the cache format; reported as null once the source changes.
-TRAFFIC = {"c346618e19d1/fp16": 142.56e6,   # profiles/decode_kernel_qwen_decode.md
-           "c346618e19d1/e4m3": 72.05e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
+TRAFFIC = {"fca057a257e4/fp16": 142.56e6,   # profiles/decode_kernel_qwen_decode.md
+           "fca057a257e4/e4m3": 72.05e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
 
 FALLBACK_HBM_GBS = 6800.0
 
@@ -136,10 +136,16 @@ def time_prefill_rows(batch: synth.StepBatch, reps: int = 20, kv_dtype: int = pk
 
 
 def source_hash() -> str:
+    """sha256 prefix of the kernel sources with comments and blank lines removed: a measurement stays keyed
+    to the code it was taken on, whatever happens to the comments."""
     h = hashlib.sha256()
     for f in ("attention.cu", "decode.cuh", "decode_e4m3.cu", "pkv_internal.cuh"):
-        with open(os.path.join(ROOT, "continuous_batching_paged_ragged_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "continuous_batching_paged_ragged_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(code.encode())
     return h.hexdigest()[:12]
 
 
