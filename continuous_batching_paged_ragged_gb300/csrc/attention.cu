@@ -8,25 +8,24 @@
 //
 // How (GB300 design, not from the pages):
 //  * plan_kernel (once per pass): per packed query token its row and causal context length, and the pass's
-//    task list.  A task is one split of one (token, KV head): `split_blocks` consecutive 16-token blocks.
-//    The split count of a token depends only on its own context, so results are bit-identical whatever
-//    else is in the batch, whatever the row order and wherever the blocks sit physically.
-//  * decode_kernel: persistent; a CTA of 4 warps takes one task at a time from a global counter, and
-//    the task's blocks are dealt round-robin to its warps (block i to warp i % 4).  Every warp streams its
-//    blocks' K and V runs through its own shared-memory ring with 2-D TMA tile copies (128-byte swizzle)
-//    that its lane 0 issues: independent issuers per SM are what keep HBM busy, and sharing a task four
-//    ways keeps all of them busy even when a pass has few tasks.  The KV head's G <= 8 query heads ride
-//    along, so each K/V block is read from HBM exactly once.  Per 16-key block the group contraction runs
-//    on the tensor cores with warp MMAs: S^T[16 keys x 8 heads] = K Q^T and O^T[d x 8 heads] += V^T P^T,
-//    operands fetched from the swizzled ring with ldmatrix; the online softmax (running max and sum in
-//    the log2 domain, fp32) reduces across the lanes that share a head with warp shuffles.  At the end of
-//    a task the four warps' (m, l, o) are combined with log-sum-exp weights through shared memory.
+//    task list, largest first.  A task is one split of one (token, KV head): `split_blocks` consecutive
+//    16-token blocks.  The split count of a token depends only on its own context, so results are
+//    bit-identical whatever else is in the batch, whatever the row order and wherever the blocks sit
+//    physically.  Rows with 16 or more new tokens become prefill work entries instead (longest first).
+//  * decode_kernel (decode.cuh): persistent CTAs of four streaming warps, a combiner warp and a scheduler
+//    warp.  The scheduler warp queues tasks (one static, the rest from a global counter); each task's
+//    blocks are dealt to the streaming warps, which stream K and V through their own TMA rings and run
+//    the G query heads' contraction on warp MMAs with an online softmax; the combiner warp folds the four
+//    warps' shares and finishes the token (fp16 output, or a split partial, or the merge of all of them).
+//    Its fp16-cache instances compile here, the 8-bit ones in decode_e4m3.cu.
 //  * Cross-split merge: a token whose context fits one split gets its fp16 output from the decode
-//    directly.  Otherwise each split leaves an unnormalised partial (m, l, o); the CTA that finishes the
-//    token's last split merges them with log-sum-exp weights, inside the same launch (a separate merge
+//    directly.  Otherwise each split leaves an unnormalised partial (m, l, o), and the CTA that finishes the
+//    token's last split merges them with log-sum-exp weights inside the same launch (a separate merge
 //    launch cost more than the merge: its CTAs cannot start until the decode's have left the SMs).
 //    Tokens with more than 32 splits are merged by merge_kernel, launched behind the decode, which
 //    spreads one token's merge over many CTAs.
+//  * Prefill rows run on the tcgen05 tile kernel (prefill.cu) ahead of the decode; on the 8-bit cache
+//    their blocks are first dequantized into an fp16 shadow in the workspace (dequant_prefill_rows_kernel).
 #include <cuda_fp16.h>
 
 #include <algorithm>
