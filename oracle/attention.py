@@ -32,7 +32,8 @@ def attention_row(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
     """Causal GQA attention of one row's new queries over its whole context.
 
     q: fp16 [q_len, Hq, d] -- this pass's query tokens of the row, in position order.
-    k, v: fp16 [ctx, Hkv, d] -- the row's keys/values in logical (position) order, this pass's included.
+    k, v: [ctx, Hkv, d] -- the row's keys/values in logical (position) order, this pass's included: fp16, or
+    the float64 values an 8-bit cache dequantizes to (oracle.fp8).
     Returns float64 [q_len, Hq, d].
     """
     q_len, num_q_heads, d = q.shape
