@@ -27,6 +27,9 @@
  *     slots.  A debugging aid: it costs a synchronization and copies per call, and is skipped while the
  *     stream is being captured into a graph.
  *   - No call traps the device, and no kernel waits on another grid.
+ *   - A pool handle is used by one host thread at a time: it remembers the last plan issued through it
+ *     and, on an 8-bit cache, the tensor map of the last workspace's fp16 shadow.  Different pools are
+ *     independent; pkv_last_error is per thread.
  *   - Supported shapes: fp16 Q and K/V inputs; an fp16 or 8-bit (E4M3) cache; head_dim 64, 128 or 256;
  *     block_size 16; num_q_heads a multiple of num_kv_heads with a group of 1, 2, 4, 6 or 8 query heads
  *     per KV head.  Others: PKV_ERR_UNSUPPORTED.
