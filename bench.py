@@ -50,8 +50,8 @@ CONFIGS = {
 # DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
 # source they were taken on and the cache format; reported as null once the source changes.
-TRAFFIC = {"fca057a257e4/fp16": 142.56e6,   # profiles/decode_kernel_qwen_decode.md
-           "fca057a257e4/e4m3": 72.05e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
+TRAFFIC = {"fca057a257e4/fp16/qwen_decode": 142.56e6,   # profiles/decode_kernel_qwen_decode.md
+           "fca057a257e4/e4m3/qwen_decode": 72.05e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
 
 FALLBACK_HBM_GBS = 6800.0
 
@@ -321,108 +321,34 @@ def run_reference(args, rank, world):
 # GPU path
 # ----------------------------------------------------------------------------------------------------
 
-class RawStep:
-    """The timed step with every pointer resolved up front: plan + per layer append and attention, as one
-    pkv_attention_append call (fused=True) or pkv_append then pkv_attention."""
-
-    def __init__(self, pool, ds, attn, qs, ks, vs, outs, stream, fused=True):
-        self.fused = fused
-        self.lib = pkv.load()
-        self.pool = pool.handle
-        self.ds = ds
-        self.ws = attn.workspace.data_ptr()
-        self.ws_bytes = attn.ws_bytes
-        self.q = [x.data_ptr() for x in qs]
-        self.k = [x.data_ptr() for x in ks]
-        self.v = [x.data_ptr() for x in vs]
-        self.o = [x.data_ptr() for x in outs]
-        self.stream = stream
-        self.bt = ds.block_tables.data_ptr()
-        self.ctx = ds.context_lens.data_ptr()
-        self.qsl = ds.query_start_loc.data_ptr()
-        self.slots = ds.slot_mapping.data_ptr()
-        self.launches = 0
-
-    def plan(self):
-        d = self.ds
-        st = self.lib.pkv_attention_plan(self.pool, self.ctx, self.qsl, d.num_seqs, d.num_tokens, d.max_blocks,
-                                         self.ws, self.ws_bytes, self.stream)
-        if st:
-            raise pkv.PkvError(st, "pkv_attention_plan", pkv.pkv_last_error())
-        self.launches += self.lib.pkv_last_launch_count(self.pool)
-
-    def append(self, i, layer):
-        st = self.lib.pkv_append(self.pool, layer, self.k[i], self.v[i], self.slots, self.ds.num_tokens, self.stream)
-        if st:
-            raise pkv.PkvError(st, "pkv_append", pkv.pkv_last_error())
-        self.launches += self.lib.pkv_last_launch_count(self.pool)
-
-    def attention(self, i, layer):
-        d = self.ds
-        st = self.lib.pkv_attention(self.pool, layer, self.q[i], self.bt, d.max_blocks, self.ctx, self.qsl,
-                                    d.num_seqs, d.num_tokens, self.o[i], self.ws, self.ws_bytes, self.stream)
-        if st:
-            raise pkv.PkvError(st, "pkv_attention", pkv.pkv_last_error())
-        self.launches += self.lib.pkv_last_launch_count(self.pool)
-
-    def attention_append(self, i, layer):
-        d = self.ds
-        st = self.lib.pkv_attention_append(self.pool, layer, self.q[i], self.k[i], self.v[i], self.slots, self.bt,
-                                           d.max_blocks, self.ctx, self.qsl, d.num_seqs, d.num_tokens, self.o[i],
-                                           self.ws, self.ws_bytes, self.stream)
-        if st:
-            raise pkv.PkvError(st, "pkv_attention_append", pkv.pkv_last_error())
-        self.launches += self.lib.pkv_last_launch_count(self.pool)
-
-    def __call__(self, layers):
-        self.plan()
-        for i, layer in enumerate(layers):
-            if self.fused:
-                self.attention_append(i, layer)
-            else:
-                self.append(i, layer)
-                self.attention(i, layer)
-
-
-def run_pkv(args, rank, world, local):
-    torch.cuda.set_device(local)
+def measure(args, batch, rank, world, local, steps, warmup, cpu_budget_s=12.0, with_e2e=True):
+    """One workload's timed step (plan + every layer's append and attention, as one CUDA graph unless
+    --eager); returns the JSON fields (rank 0) or None."""
     dev = torch.device("cuda", local)
-    batch = CONFIGS[args.config]()
-    if args.layers:
-        batch.shape = synth.Shape(args.layers, batch.shape.num_q_heads, batch.shape.num_kv_heads,
-                                  batch.shape.head_dim, batch.shape.block_size)
     s = batch.shape
     layers = list(range(s.num_layers))
     kv8 = args.kv_cache == "e4m3"
+    fused = not args.unfused
     pool = workload.make_pool(batch, split_blocks=args.split_blocks,
                               kv_dtype=pkv.PKV_KV_E4M3 if kv8 else pkv.PKV_KV_F16)
+    split_blocks = pool.cfg.split_blocks or pkv.DEFAULT_SPLIT_BLOCKS
+    merge_launch = long_merge(batch, pool)
     workload.prefill_cache(pool, batch, layers)
     ds = workload.upload(batch, pool)
     qs, ks, vs = workload.step_inputs(ds, layers)
     outs = [torch.empty_like(q) for q in qs]
     attn = workload.Attention(pool, ds)
     stream = torch.cuda.current_stream(dev)
-    sp = stream.cuda_stream
-    step = RawStep(pool, ds, attn, qs, ks, vs, outs, sp, fused=not args.unfused)
+    step = workload.RawStep(pool, ds, attn, qs, ks, vs, outs, stream.cuda_stream, fused=fused)
     torch.cuda.synchronize()
     assert pool.check() == 0
 
     # the step as one CUDA graph: the same calls, captured on a side stream, replayed on `stream`
     graph = None
     if not args.eager:
-        cap = torch.cuda.Stream(dev)
-        cstep = RawStep(pool, ds, attn, qs, ks, vs, outs, cap.cuda_stream, fused=not args.unfused)
-        cap.wait_stream(stream)
-        with torch.cuda.stream(cap):
-            for _ in range(3):
-                cstep(layers)
-        torch.cuda.synchronize()
-        cstep.launches = 0
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cap):
-            cstep(layers)
-        launches_per_step = cstep.launches
-        torch.cuda.synchronize()
+        graph, launches_per_step = workload.capture_step_graph(pool, ds, attn, qs, ks, vs, outs, layers, fused=fused,
+                                                               device=dev)
+    graphed = graph is not None
 
     def run_step():
         if graph is not None:
@@ -435,7 +361,7 @@ def run_pkv(args, rank, world, local):
     ctx_tokens = int(batch.context_lens.astype(np.int64).sum()) * len(layers)
 
     # ---- device-resident timed region ----
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         run_step()
     torch.cuda.synchronize()
     sampler = ClockSampler(local) if rank == 0 else None
@@ -446,27 +372,27 @@ def run_pkv(args, rank, world, local):
     step.launches = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         run_step()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if sampler else None
-    launches = step.launches if graph is None else launches_per_step * args.steps
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    launches = step.launches if graph is None else launches_per_step * steps
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
     assert pool.check() == 0
 
     # ---- per-kernel timing of the dominant call (pkv_attention), events on its stream ----
     kev = []
-    n_kernel_steps = max(3, min(args.steps, 200))
+    n_kernel_steps = max(3, min(steps, 200))
     for _ in range(n_kernel_steps):
         step.plan()
         for i, layer in enumerate(layers):
-            if not step.fused:
+            if not fused:
                 step.append(i, layer)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            if step.fused:
+            if fused:
                 step.attention_append(i, layer)  # the decode kernel does the append too
             else:
                 step.attention(i, layer)
@@ -476,26 +402,30 @@ def run_pkv(args, rank, world, local):
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
 
     # ---- end to end through the public calls with host buffers ----
-    e2e = run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_bytes)
-
-    pf_ms = time_prefill_rows(batch, kv_dtype=pool.cfg.kv_dtype) if rank == 0 else None
+    e2e = run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_bytes, steps) if with_e2e else None
+    del graph, step, attn, qs, ks, vs, outs, ds
+    pool.close()
+    del pool
+    torch.cuda.empty_cache()
+    pf_ms = time_prefill_rows(batch, kv_dtype=pkv.PKV_KV_E4M3 if kv8 else pkv.PKV_KV_F16) if rank == 0 else None
+    torch.cuda.empty_cache()
 
     if rank != 0:
-        return
+        return None
     peak, peak_src = measured_peak()
-    kernel_bytes = attn_bytes + (append_bytes if step.fused else 0)
+    kernel_bytes = attn_bytes + (append_bytes if fused else 0)
     # The dominant kernel's average launch duration over the timed region: with the fused call a step is
     # one plan launch plus one attention launch per layer (plus the long-context merge launch where a
     # token has more than 32 splits), so the step time over the layer count is an upper bound on it (the
     # plan's share is charged to the attention).  Layers are pipelined through programmatic dependent
     # launch inside the timed region; `isolated_call_ms` is the same call issued alone, between events.
-    per_call_ms = ms / len(layers) if (step.fused and graph is not None) else attn_ms
+    per_call_ms = ms / len(layers) if (fused and graphed) else attn_ms
     achieved = kernel_bytes / (per_call_ms * 1e-3) / 1e9
     sh = source_hash()
     value = step_bytes * world / (ms * 1e-3) / 1e9
     line = {
         "metric": "paged ragged attention: achieved HBM GB/s (% of GB300 peak), ctx tokens/s",
-        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded Philox4x32-10, Irwin-Hall approx N(0,1) fp16)",
         "config": {"workload": batch.name, "layers": s.num_layers, "num_q_heads": s.num_q_heads,
@@ -503,18 +433,18 @@ def run_pkv(args, rank, world, local):
                    "rows": batch.num_seqs, "new_tokens": batch.num_tokens,
                    "context_tokens_per_layer": int(batch.context_lens.sum()), "pool_blocks": batch.num_blocks,
                    "kv_cache": "e4m3 codes + power-of-two scale per cached row" if kv8 else "fp16",
-                   "split_blocks": pool.cfg.split_blocks or pkv.DEFAULT_SPLIT_BLOCKS,
+                   "split_blocks": split_blocks,
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of K/V per step rotating over "
                          f"{s.num_layers} layer pools", "parallelism": f"replicas x{world}",
-                   "launch": "eager" if graph is None else "cuda_graph",
+                   "launch": "eager" if not graphed else "cuda_graph",
                    "layer_call": "pkv_append + pkv_attention" if args.unfused else "pkv_attention_append"},
         "pct_of_peak": 100.0 * value / world / peak,
         "ctx_tokens_per_s": ctx_tokens * world / (ms * 1e-3),
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": TRAFFIC.get(f"{sh}/{args.kv_cache}"),
-                     "kernel": "decode_kernel (split-K decode, fused merge" + (", fused append)" if step.fused else ")")
-                               + (" + merge_kernel (tokens with > 32 splits)" if long_merge(batch, pool) else ""),
+                     "traffic": TRAFFIC.get(f"{sh}/{args.kv_cache}/{batch.name}"),
+                     "kernel": "decode_kernel (split-K decode, fused merge" + (", fused append)" if fused else ")")
+                               + (" + merge_kernel (tokens with > 32 splits)" if merge_launch else ""),
                      "per_launch_bytes": kernel_bytes, "avg_launch_ms": per_call_ms,
                      "avg_launch_over": "timed region (CUDA graph, step time / layers)"
                                         if per_call_ms is not attn_ms else "per-call CUDA events",
@@ -540,8 +470,38 @@ def run_pkv(args, rank, world, local):
         line["lower_bounds_ms_per_step"] = {"hbm": hbm_ms, "tensor": tensor_ms, "sum": hbm_ms + tensor_ms,
                                             "max": max(hbm_ms, tensor_ms), "measured": ms}
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(batch, kv8=kv8)
-    print(json.dumps(line), flush=True)
+        line["cpu_baseline"] = cpu_baseline(batch, budget_s=cpu_budget_s, kv8=kv8)
+    return line
+
+
+def run_pkv(args, rank, world, local):
+    torch.cuda.set_device(local)
+    batch = CONFIGS[args.config]()
+    if args.layers:
+        batch.shape = synth.Shape(args.layers, batch.shape.num_q_heads, batch.shape.num_kv_heads,
+                                  batch.shape.head_dim, batch.shape.block_size)
+    line = measure(args, batch, rank, world, local, args.steps, args.warmup)
+    if args.config == "qwen_decode" and not args.layers and not args.no_configs and world == 1:
+        # the other workloads of the pages, each as its own timed region with its clocks and oracle baseline
+        extra = {}
+        for name, steps in (("mixed_step", min(args.steps, 100)), ("long_gqa", min(args.steps, 20))):
+            t0 = time.perf_counter()
+            sub = measure(args, CONFIGS[name](), rank, world, local, max(steps, 3), args.warmup, cpu_budget_s=4.0)
+            if sub is not None:
+                sub["wall_s"] = time.perf_counter() - t0
+                extra[name] = sub
+        for cap in (256, 64):
+            t0 = time.perf_counter()
+            res = run_trace_policies(args, local, [t for t in TRACE_POLICIES if t[0] in
+                                                   ("on_demand/pass", "on_demand/pass cap 64") and t[4] == cap],
+                                     cpu_baseline_s=4.0 if not args.no_cpu_baseline else 0.0)
+            if rank == 0 and res:
+                res[0]["wall_s"] = time.perf_counter() - t0
+                extra[f"sched_trace_cap{cap}"] = res[0]
+        if rank == 0:
+            line["configs"] = extra
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------------------------------------------
@@ -562,30 +522,63 @@ TRACE_POLICIES = [
     ("on_demand/pass 8-bit cache, 9922 blocks (the bytes of 5000 fp16 blocks)", pkv.PKV_ALLOC_ON_DEMAND,
      pkv.PKV_UNIT_PASS, 1.0, 256, 5000 * 2 * 128 // 129, False, "e4m3"),
 ]
+TRACE_SHAPE = (28, 12, 2, 128)  # layers, q heads, KV heads, head_dim (the Qwen2.5-1.5B cache shape)
+TRACE_BUDGET = 8192             # new tokens per pass
 
 
-def run_sched_trace(args, rank, world, local):
-    """256 trace requests (lognormal prompts, U[50, 781] outputs, token budget 8,192, 20,000 blocks of 16,
-    max_num_seqs 256, or 64 for the comparison of units of scheduling) run to exhaustion under each policy;
-    every pass is the plan + 28 x fused append and attention on the GPU.  Only the GPU work of a pass is timed (CUDA events around it); the host
-    scheduler and the metadata upload run between passes, outside the timed work."""
-    torch.cuda.set_device(local)
+def trace_cpu_baseline(passes, reqs, budget_s: float):
+    """The oracle on a bounded sample of the trace: one layer of the pass with the most decode rows (each row's
+    seeded q/k/v), extrapolated to every pass's context tokens and 28 layers; output tokens per second."""
+    import oracle
+    L, Hq, Hkv, d = TRACE_SHAPE
+    best = max(range(len(passes)), key=lambda i: (passes[i]["decode_rows"], -i))
+    p = passes[best]
+    t0 = time.perf_counter()
+    done_ctx = 0
+    for req, ql, ctx in zip(p["req_ids"], p["q_lens"], p["context_lens"]):
+        ql = min(int(ql), 16)   # a long chunk contributes its last 16 queries (the sample stays bounded)
+        k, v = synth.sequence_kv(0, 0, int(req), int(ctx), Hkv, d)
+        q = synth.token_values(synth.KIND_Q, 0, 0, np.full(ql, int(req)), np.arange(int(ctx) - ql, int(ctx)), Hq, d)
+        oracle.attention_row(q, k, v)
+        done_ctx += int(ctx)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    total_ctx = sum(int(x["ctx_tokens"]) for x in passes) * L
+    est_s = el / max(done_ctx, 1) * total_ctx
+    outputs = sum(r.max_output for r in reqs)
+    return {"value": outputs / est_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done_ctx} context tokens of pass {best} (layer 0, chunks capped at 16 queries), "
+                      f"{el:.1f} s of fp64 NumPy on 1 of {os.cpu_count()} host cores, extrapolated to "
+                      f"{total_ctx} context tokens (all passes, {L} layers)"}
+
+
+def run_trace_policies(args, local, policies, cpu_baseline_s: float = 0.0):
+    """256 trace requests (lognormal prompts, U[50, 781] outputs, token budget 8,192, max_num_seqs and pool as
+    the policy says) run to exhaustion; every pass is the plan + 28 x fused append and attention on the GPU,
+    over the seeded q/k/v of the pass's tokens (generated on the device for every layer before the pass).
+    Only the GPU work of a pass is timed (CUDA events around it); the host scheduler, the metadata upload and
+    the value generation run between passes, outside the timed work."""
     dev = torch.device("cuda", local)
-    L, Hq, Hkv, d, nblk, cap, budget = 28, 12, 2, 128, 20000, 256, 8192
+    L, Hq, Hkv, d = TRACE_SHAPE
+    budget = TRACE_BUDGET
     reqs = synth.trace_requests(0)
     max_w = max((r.prompt_len + r.max_output + 15) // 16 for r in reqs)
-    policies = [t for t in TRACE_POLICIES if re.search(args.trace_filter, t[0])]
+    cap_all = max(t[4] for t in policies)
+    nblk = max(t[5] for t in policies)
     pools = {kv: pkv.Pool(L, Hq, Hkv, d, nblk, kv_dtype=pkv.PKV_KV_E4M3 if kv == "e4m3" else pkv.PKV_KV_F16)
              for kv in sorted({t[7] for t in policies})}
-    q = torch.zeros(budget, Hq, d, dtype=torch.float16, device=dev)
-    k = torch.zeros(budget, Hkv, d, dtype=torch.float16, device=dev)
-    v = torch.zeros_like(k)
-    out = torch.empty_like(q)
-    bt = torch.empty(cap * max_w, dtype=torch.int32, device=dev)
-    ctx = torch.empty(cap, dtype=torch.int32, device=dev)
-    qsl = torch.empty(cap + 1, dtype=torch.int32, device=dev)
+    q = torch.empty(L, budget, Hq, d, dtype=torch.float16, device=dev)
+    k = torch.empty(L, budget, Hkv, d, dtype=torch.float16, device=dev)
+    v = torch.empty_like(k)
+    out = torch.empty(budget, Hq, d, dtype=torch.float16, device=dev)
+    bt = torch.empty(cap_all * max_w, dtype=torch.int32, device=dev)
+    ctx = torch.empty(cap_all, dtype=torch.int32, device=dev)
+    qsl = torch.empty(cap_all + 1, dtype=torch.int32, device=dev)
     slots = torch.empty(budget, dtype=torch.int64, device=dev)
-    ws_bytes = max(pkv.pkv_attention_workspace_bytes(pl.handle, cap, budget, max_w) for pl in pools.values())
+    treq = torch.empty(budget, dtype=torch.int64, device=dev)
+    tpos = torch.empty(budget, dtype=torch.int64, device=dev)
+    ws_bytes = max(pkv.pkv_attention_workspace_bytes(pl.handle, cap_all, budget, max_w) for pl in pools.values())
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     lib = pkv.load()
     stream = torch.cuda.current_stream(dev)
@@ -597,60 +590,97 @@ def run_sched_trace(args, rank, world, local):
                               prefix_caching=prefix)
         for r in reqs:
             sched.add(r.req_id, r.prompt_len, r.max_output, int(round(declared * r.max_output)))
-        events, steps, launches = [], 0, 0
+        events, steps, launches, passes = [], 0, 0, []
+        sampler = ClockSampler(local)
+        sampler.start()
         while not sched.done():
             st = sched.step()
             B, T, W = len(st["req_ids"]), int(st["query_start_loc"][-1]), st["max_blocks_per_seq"]
-            bt[:B * W].copy_(torch.from_numpy(st["block_tables"].reshape(-1)), non_blocking=False)
+            qls = np.diff(st["query_start_loc"]).astype(np.int64)
+            cl = st["context_lens"].astype(np.int64)
+            tok_req = np.repeat(st["req_ids"].astype(np.int64), qls)
+            tok_pos = np.concatenate([np.arange(c - n, c) for c, n in zip(cl, qls)]) if B else np.zeros(0, np.int64)
+            bt[:B * W].copy_(torch.from_numpy(st["block_tables"].reshape(-1)))
             ctx[:B].copy_(torch.from_numpy(st["context_lens"]))
             qsl[:B + 1].copy_(torch.from_numpy(st["query_start_loc"]))
             slots[:T].copy_(torch.from_numpy(st["slot_mapping"]))
+            treq[:T].copy_(torch.from_numpy(tok_req))
+            tpos[:T].copy_(torch.from_numpy(tok_pos))
+            for layer in range(L):   # the pass's seeded values, outside the timed work
+                synth.device_fill(synth.KIND_Q, 0, layer, treq[:T], tpos[:T], Hq, d, q[layer, :T])
+                synth.device_fill(synth.KIND_K, 0, layer, treq[:T], tpos[:T], Hkv, d, k[layer, :T])
+                synth.device_fill(synth.KIND_V, 0, layer, treq[:T], tpos[:T], Hkv, d, v[layer, :T])
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             pkv._check(lib.pkv_attention_plan(pool.handle, ctx.data_ptr(), qsl.data_ptr(), B, T, W, ws.data_ptr(),
                                               ws_bytes, sp), "pkv_attention_plan")
             launches += lib.pkv_last_launch_count(pool.handle)
             for layer in range(L):
-                pkv._check(lib.pkv_attention_append(pool.handle, layer, q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                                    slots.data_ptr(), bt.data_ptr(), W, ctx.data_ptr(),
-                                                    qsl.data_ptr(), B, T, out.data_ptr(), ws.data_ptr(), ws_bytes,
-                                                    sp), "pkv_attention_append")
+                pkv._check(lib.pkv_attention_append(pool.handle, layer, q[layer].data_ptr(), k[layer].data_ptr(),
+                                                    v[layer].data_ptr(), slots.data_ptr(), bt.data_ptr(), W,
+                                                    ctx.data_ptr(), qsl.data_ptr(), B, T, out.data_ptr(),
+                                                    ws.data_ptr(), ws_bytes, sp), "pkv_attention_append")
                 launches += lib.pkv_last_launch_count(pool.handle)
             b.record(stream)
             events.append((a, b))
             steps += 1
-            if len(events) >= 256:  # keep the host from running far ahead of the device
+            passes.append({"req_ids": st["req_ids"].copy(), "q_lens": qls, "context_lens": cl,
+                           "decode_rows": int((qls == 1).sum()), "ctx_tokens": int(cl.sum())})
+            if len(events) % 128 == 0:  # keep the host from running far ahead of the device
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
+        clocks = sampler.stop()
         assert pool.check() == 0
         gpu_s = sum(x.elapsed_time(y) for x, y in events) / 1e3
         stt = sched.stats()
         sched.close()
         outputs = sum(r.max_output for r in reqs)
-        results.append({"policy": name, "max_num_seqs": max_seqs, "output_tokens_per_s": outputs / gpu_s,
-                        "gpu_s": gpu_s, "steps": steps,
-                        "preemptions": stt["preemptions"], "recomputed_tokens": stt["recomputed_tokens"],
-                        "max_batch": stt["max_batch"], "mean_batch": stt["batch_sum"] / max(1, stt["steps"]),
-                        "live_cache": stt["live_tokens"] / max(1, stt["held_slots"]), "pool_blocks": blocks,
-                        "prefix_hit_tokens": stt["prefix_hit_tokens"], "kv_cache": kv,
-                        "tokens_scheduled": stt["tokens_scheduled"], "gpu_launches": launches})
+        res = {"policy": name, "max_num_seqs": max_seqs, "output_tokens_per_s": outputs / gpu_s,
+               "gpu_s": gpu_s, "steps": steps, "ms_per_step": gpu_s * 1e3 / steps,
+               "preemptions": stt["preemptions"], "recomputed_tokens": stt["recomputed_tokens"],
+               "max_batch": stt["max_batch"], "mean_batch": stt["batch_sum"] / max(1, stt["steps"]),
+               "live_cache": stt["live_tokens"] / max(1, stt["held_slots"]), "pool_blocks": blocks,
+               "prefix_hit_tokens": stt["prefix_hit_tokens"], "kv_cache": kv,
+               "tokens_scheduled": stt["tokens_scheduled"], "gpu_launches": launches, "clocks": clocks,
+               "values": "seeded q/k/v of every pass's tokens (device generator, all layers)"}
+        if cpu_baseline_s > 0:
+            res["cpu_baseline"] = trace_cpu_baseline(passes, reqs, cpu_baseline_s)
+        results.append(res)
+    for pl in pools.values():
+        pl.close()
+    del q, k, v, ws
+    torch.cuda.empty_cache()
+    return results
+
+
+def run_sched_trace(args, rank, world, local):
+    torch.cuda.set_device(local)
+    policies = [t for t in TRACE_POLICIES if re.search(args.trace_filter, t[0])]
+    results = run_trace_policies(args, local, policies)
     if rank != 0:
         return
     head = results[0]
+    L, Hq, Hkv, d = TRACE_SHAPE
     line = {"metric": "scheduler-driven trace: output tokens/s over the GPU time of its passes", "value":
             head["output_tokens_per_s"], "unit": "tokens/s", "n_gpus": world, "steps": head["steps"], "warmup": 0,
             "ms_per_step": head["gpu_s"] * 1e3 / head["steps"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded trace: 256 requests, lognormal prompts "
-            "median 300 clipped [16, 4096], outputs U[50, 781])",
+            "median 300 clipped [16, 4096], outputs U[50, 781]; seeded q/k/v)",
             "config": {"workload": "sched_trace", "layers": L, "num_q_heads": Hq, "num_kv_heads": Hkv,
-                       "head_dim": d, "pool_blocks": nblk, "max_num_seqs": cap, "token_budget": budget,
-                       "split_blocks": pkv.DEFAULT_SPLIT_BLOCKS, "launch": "eager (per-pass events)"},
-            "gpu_launches": head["gpu_launches"], "policies": results}
+                       "head_dim": d, "pool_blocks": head["pool_blocks"], "max_num_seqs": head["max_num_seqs"],
+                       "token_budget": TRACE_BUDGET, "split_blocks": pkv.DEFAULT_SPLIT_BLOCKS,
+                       "launch": "eager (per-pass events)"},
+            "gpu_launches": head["gpu_launches"], "clocks": head["clocks"], "policies": results}
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_bytes):
-    """Same metric with the step's inputs copied from pinned host memory and its outputs read back."""
+def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_bytes, steps):
+    """The same metric end to end through the public calls: every step copies the pass's metadata and every
+    layer's q/k/v from pinned host memory and reads every layer's output back.  Layer l + 1's inputs go up on
+    a copy stream while layer l attends, and layer l's output comes down on another while layer l + 1 runs;
+    the step (copies, events and library calls) is captured as one CUDA graph, as the device-resident timing
+    is (--eager: issued call by call)."""
+    dev = stream.device
     L = len(layers)
     h_q = torch.stack([q.cpu() for q in qs]).pin_memory()
     h_k = torch.stack([k.cpu() for k in ks]).pin_memory()
@@ -664,35 +694,73 @@ def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_
     d_k = torch.stack(ks)
     d_v = torch.stack(vs)
     d_out = torch.stack(outs)
-    step = RawStep(pool, ds, attn, list(d_q), list(d_k), list(d_v), list(d_out), stream.cuda_stream,
-                   fused=not args.unfused)
     h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_bt, h_ctx, h_qsl, h_slots))
     d2h = h_out.numel() * h_out.element_size()
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in layers]
+    ev_done = [torch.cuda.Event() for _ in layers]
 
-    def one():
-        ds.block_tables.copy_(h_bt, non_blocking=True)
-        ds.context_lens.copy_(h_ctx, non_blocking=True)
-        ds.query_start_loc.copy_(h_qsl, non_blocking=True)
-        ds.slot_mapping.copy_(h_slots, non_blocking=True)
-        d_q.copy_(h_q, non_blocking=True)
-        d_k.copy_(h_k, non_blocking=True)
-        d_v.copy_(h_v, non_blocking=True)
-        step(layers)
-        h_out.copy_(d_out, non_blocking=True)
+    def one(main, step):
+        with torch.cuda.stream(main):
+            ds.block_tables.copy_(h_bt, non_blocking=True)
+            ds.context_lens.copy_(h_ctx, non_blocking=True)
+            ds.query_start_loc.copy_(h_qsl, non_blocking=True)
+            ds.slot_mapping.copy_(h_slots, non_blocking=True)
+        up.wait_stream(main)      # the previous step has read its inputs
+        down.wait_stream(main)
+        with torch.cuda.stream(up):
+            for i in range(L):
+                d_q[i].copy_(h_q[i], non_blocking=True)
+                d_k[i].copy_(h_k[i], non_blocking=True)
+                d_v[i].copy_(h_v[i], non_blocking=True)
+                ev_in[i].record(up)
+        step.plan()
+        for i, layer in enumerate(layers):
+            main.wait_event(ev_in[i])
+            if step.fused:
+                step.attention_append(i, layer)
+            else:
+                step.append(i, layer)
+                step.attention(i, layer)
+            ev_done[i].record(main)
+            down.wait_event(ev_done[i])
+            with torch.cuda.stream(down):
+                h_out[i].copy_(d_out[i], non_blocking=True)
+        main.wait_stream(up)
+        main.wait_stream(down)
 
-    n = max(3, min(args.steps, 200))
+    n = max(3, min(steps, 200))
+    if args.eager:
+        step = workload.RawStep(pool, ds, attn, list(d_q), list(d_k), list(d_v), list(d_out), stream.cuda_stream,
+                                fused=not args.unfused)
+        run = lambda: one(stream, step)  # noqa: E731
+    else:
+        cap = torch.cuda.Stream(dev)
+        step = workload.RawStep(pool, ds, attn, list(d_q), list(d_k), list(d_v), list(d_out), cap.cuda_stream,
+                                fused=not args.unfused)
+        cap.wait_stream(stream)
+        for _ in range(2):
+            one(cap, step)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            one(cap, step)
+        torch.cuda.synchronize()
+        run = graph.replay
     for _ in range(3):
-        one()
+        run()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(n):
-        one()
+        run()
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n
     return {"value": step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
+            "copies": "per layer on two copy streams, overlapped with the attention of the neighbouring layers"
+                      + ("" if args.eager else "; the step captured as one CUDA graph")}
 
 
 def main():
@@ -708,6 +776,7 @@ def main():
     ap.add_argument("--kv-cache", default="fp16", choices=["fp16", "e4m3"],
                     help="cache format: fp16 values, or E4M3 codes with a power-of-two scale per cached row")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="the default workload alone (no configs object)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     ap.add_argument("--eager", action="store_true", help="time the calls issued one by one, not a CUDA graph")
     ap.add_argument("--unfused", action="store_true", help="pkv_append then pkv_attention per layer, not the "

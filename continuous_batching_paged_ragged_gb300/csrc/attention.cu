@@ -32,6 +32,7 @@
 #include <cmath>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "attn_common.cuh"
 
@@ -577,15 +578,11 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
     a.layer_row0_k = p.layer_row0_k;
     a.layer_row0_v = p.layer_row0_v;
     a.num_blocks = c.num_blocks;
-    if (f8) {  // the prefill rows' blocks, dequantized into the workspace's fp16 shadow
+    if (f8) {  // the prefill rows' blocks, dequantized into the workspace's fp16 shadow (its map is prepared)
       char* shadow = ws + w.shadow;
       const uint64_t srows = (uint64_t)2 * w.shadow_blocks * c.num_kv_heads * kBS;
-      if (pool->shadow_base != shadow || pool->shadow_rows != srows) {
-        const pkv_status st = encode_f16_rows(&pool->shadow_map, shadow, srows, c.head_dim);
-        if (st != PKV_OK) return st;
-        pool->shadow_base = shadow;
-        pool->shadow_rows = srows;
-      }
+      if (pool->shadow_base != shadow || pool->shadow_rows != srows)
+        return fail(PKV_ERR_INVALID_ARG, "8-bit cache: the shadow tensor map was not prepared for this workspace");
       DequantParams dq;
       dq.codes_k = static_cast<const unsigned char*>(pkv_pool_layer_ptr(pool, layer, 0));
       dq.codes_v = static_cast<const unsigned char*>(pkv_pool_layer_ptr(pool, layer, 1));
@@ -602,8 +599,6 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
       dq.max_blocks = max_blocks;
       dq.num_kv_heads = c.num_kv_heads;
       dq.num_blocks = c.num_blocks;
-      if (num_seqs > kDequantMaxRows)
-        return fail(PKV_ERR_UNSUPPORTED, "8-bit cache: prefill rows in a pass of more than 49151 rows");
       e = c.head_dim == 64 ? launch_dequant<64>(dq, pool->num_sms, s) : launch_dequant<128>(dq, pool->num_sms, s);
       if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
       *launches += 1;
@@ -706,25 +701,90 @@ static pkv_status check_io(const void* q, const void* out, const int32_t* block_
   return PKV_OK;
 }
 
+// The plan remembered for `workspace`, or null.
+static const PlanKey* find_plan(const pkv_pool* pool, const void* workspace) {
+  for (auto it = pool->plans.rbegin(); it != pool->plans.rend(); ++it)
+    if (it->workspace == workspace) return &*it;
+  return nullptr;
+}
+
+static void forget_plan(pkv_pool* pool, const void* workspace) {
+  for (auto it = pool->plans.begin(); it != pool->plans.end(); ++it)
+    if (it->workspace == workspace) {
+      pool->plans.erase(it);
+      return;
+    }
+}
+
+static void remember_plan(pkv_pool* pool, const PlanKey& key) {
+  forget_plan(pool, key.workspace);
+  pool->plans.push_back(key);
+  if (pool->plans.size() > kMaxPlans) pool->plans.erase(pool->plans.begin());
+}
+
+// A call on a planned workspace: the plan must have been issued on this workspace with the same metadata
+// pointers and sizes, and (when both the plan and this call ran under PKV_VALIDATE=1) the same
+// context_lens / query_start_loc contents.
+static pkv_status check_plan(const pkv_pool* pool, const void* workspace, const int32_t* context_lens,
+                             const int32_t* qsl, int32_t num_seqs, int32_t num_tokens, int32_t max_blocks,
+                             const MetaCheck& mc) {
+  const PlanKey* k = find_plan(pool, workspace);
+  if (!k || k->context_lens != context_lens || k->query_start_loc != qsl || k->num_seqs != num_seqs ||
+      k->num_tokens != num_tokens || k->max_blocks_per_seq != max_blocks)
+    return fail(PKV_ERR_INVALID_ARG, "no matching plan: call pkv_attention_plan for this workspace and metadata");
+  if (mc.ran && k->summed && mc.sum != k->meta_sum)
+    return fail(PKV_ERR_INVALID_ARG, "PKV_VALIDATE: context_lens / query_start_loc changed since pkv_attention_plan "
+                "on this workspace; plan the pass again");
+  return PKV_OK;
+}
+
+// Host-side refusals of the 8-bit cache's prefill path, made before anything is launched: the dequantizing
+// kernel stages one int per row in shared memory, and the fp16 shadow's tensor map is encoded here (once per
+// workspace placement) so that a failed encode launches nothing either.
+static pkv_status prepare_prefill_shadow(pkv_pool* pool, char* ws, const WsLayout& w, int num_seqs, int num_tokens) {
+  const pkv_config& c = pool->cfg;
+  if (c.kv_dtype != PKV_KV_E4M3 || w.prefill_min_qlen <= 0 || num_tokens - num_seqs < w.prefill_min_qlen - 1)
+    return PKV_OK;
+  if (num_seqs > kDequantMaxRows)
+    return fail(PKV_ERR_UNSUPPORTED, "8-bit cache: prefill rows in a pass of more than 49151 rows");
+  char* shadow = ws + w.shadow;
+  const uint64_t srows = (uint64_t)2 * w.shadow_blocks * c.num_kv_heads * kBS;
+  if (pool->shadow_base != shadow || pool->shadow_rows != srows) {
+    const pkv_status st = encode_f16_rows(&pool->shadow_map, shadow, srows, c.head_dim);
+    if (st != PKV_OK) {
+      pool->shadow_base = nullptr;
+      return st;
+    }
+    pool->shadow_base = shadow;
+    pool->shadow_rows = srows;
+  }
+  return PKV_OK;
+}
+
 extern "C" pkv_status pkv_attention_plan(pkv_pool* pool, const int32_t* context_lens, const int32_t* query_start_loc,
                                          int32_t num_seqs, int32_t num_tokens, int32_t max_blocks_per_seq,
                                          void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
   pkv_status st = check_common(pool, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq);
   if (st == PKV_OK) st = check_workspace(pool, workspace, workspace_bytes, num_seqs, num_tokens, max_blocks_per_seq);
+  MetaCheck mc;
   if (st == PKV_OK) st = validate_metadata(pool, nullptr, max_blocks_per_seq, context_lens, query_start_loc, num_seqs,
-                                           num_tokens, nullptr, stream);
+                                           num_tokens, nullptr, stream, &mc);
   if (st != PKV_OK) return st;
   pool->last_launches = 0;
-  pool->plan = PlanKey{workspace, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq};
-  if (num_tokens == 0) return PKV_OK;
+  forget_plan(pool, workspace);
+  PlanKey key{workspace, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq, mc.ran, mc.sum};
+  if (num_tokens == 0) {
+    remember_plan(pool, key);
+    return PKV_OK;
+  }
   const WsLayout w = ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks_per_seq);
+  st = prepare_prefill_shadow(pool, static_cast<char*>(workspace), w, num_seqs, num_tokens);
+  if (st != PKV_OK) return st;
   cudaError_t e = launch_plan(pool, static_cast<char*>(workspace), w, context_lens, query_start_loc, num_seqs,
                               num_tokens, max_blocks_per_seq, (cudaStream_t)stream);
-  if (e != cudaSuccess) {
-    pool->plan = PlanKey{};
-    return cuda_fail(e, "plan launch");
-  }
+  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+  remember_plan(pool, key);
   pool->last_launches = 1;
   return PKV_OK;
 }
@@ -741,14 +801,15 @@ extern "C" pkv_status pkv_attention(pkv_pool* pool, int32_t layer, const void* q
   if (layer < 0 || layer >= pool->cfg.num_layers) return fail(PKV_ERR_OUT_OF_RANGE, "layer out of range");
   if (num_tokens == 0) return PKV_OK;
   st = check_io(q, out, block_tables);
+  MetaCheck mc;
   if (st == PKV_OK) st = validate_metadata(pool, block_tables, max_blocks_per_seq, context_lens, query_start_loc,
-                                           num_seqs, num_tokens, nullptr, stream);
+                                           num_seqs, num_tokens, nullptr, stream, &mc);
+  if (st == PKV_OK) st = check_plan(pool, workspace, context_lens, query_start_loc, num_seqs, num_tokens,
+                                    max_blocks_per_seq, mc);
   if (st != PKV_OK) return st;
-  const PlanKey& k = pool->plan;
-  if (k.workspace != workspace || k.context_lens != context_lens || k.query_start_loc != query_start_loc ||
-      k.num_seqs != num_seqs || k.num_tokens != num_tokens || k.max_blocks_per_seq != max_blocks_per_seq)
-    return fail(PKV_ERR_INVALID_ARG, "no matching plan: call pkv_attention_plan for this workspace and metadata");
   const WsLayout w = ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks_per_seq);
+  st = prepare_prefill_shadow(pool, static_cast<char*>(workspace), w, num_seqs, num_tokens);
+  if (st != PKV_OK) return st;
   int launches = 0;
   st = launch_attention(pool, layer, q, block_tables, context_lens, query_start_loc, max_blocks_per_seq, num_seqs, num_tokens, out,
                         static_cast<char*>(workspace), w, (cudaStream_t)stream, &launches);
@@ -780,14 +841,15 @@ extern "C" pkv_status pkv_attention_append(pkv_pool* pool, int32_t layer, const 
   if (!k || !v || !slot_mapping) return fail(PKV_ERR_INVALID_ARG, "k, v and slot_mapping must be non-NULL");
   if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16 != 0)
     return fail(PKV_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  MetaCheck mc;
   st = validate_metadata(pool, block_tables, max_blocks_per_seq, context_lens, query_start_loc, num_seqs, num_tokens,
-                         slot_mapping, stream);
+                         slot_mapping, stream, &mc);
+  if (st == PKV_OK) st = check_plan(pool, workspace, context_lens, query_start_loc, num_seqs, num_tokens,
+                                    max_blocks_per_seq, mc);
   if (st != PKV_OK) return st;
-  const PlanKey& pk = pool->plan;
-  if (pk.workspace != workspace || pk.context_lens != context_lens || pk.query_start_loc != query_start_loc ||
-      pk.num_seqs != num_seqs || pk.num_tokens != num_tokens || pk.max_blocks_per_seq != max_blocks_per_seq)
-    return fail(PKV_ERR_INVALID_ARG, "no matching plan: call pkv_attention_plan for this workspace and metadata");
   const WsLayout w = ws_layout(pool->cfg, num_seqs, num_tokens, max_blocks_per_seq);
+  st = prepare_prefill_shadow(pool, static_cast<char*>(workspace), w, num_seqs, num_tokens);
+  if (st != PKV_OK) return st;
   int launches = 0;
   // Prefill rows possible (they read the cache), or on an 8-bit cache a row with 16 or more new tokens
   // (quantizing its rows once beats re-quantizing them in every tile that holds them): append first.
@@ -824,24 +886,63 @@ namespace pkv {
 constexpr size_t kNoAllocScratchBytes = PKV_NOALLOC_SCRATCH_BYTES;  // 16 MiB per device
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// The array's device address, looked up once per device with that device current.  In host code the
-// symbol name itself is only a host-side stand-in and must never reach a kernel.
-static void* noalloc_scratch_ptr(int device, cudaError_t* err) {
+// The array's device address in the current context.  In host code the symbol name itself is only a
+// host-side stand-in and must never reach a kernel.  The address is looked up (cudaGetSymbolAddress, with the
+// device current) the first time a context calls, and cached per (device, context): a context created
+// after cudaDeviceReset loads the library's module again, so it gets its own lookup.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+static CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && f) fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  }
+  return fn;
+}
+
+struct ScratchAddr {
+  int device;
+  CUcontext ctx;
+  void* ptr;
+};
+
+// The cached address for (device, context), or null when that context has not looked it up yet.
+static void* noalloc_scratch_cached(int device, CUcontext ctx, std::vector<ScratchAddr>& cache) {
+  for (const ScratchAddr& a : cache)
+    if (a.device == device && a.ctx == ctx) return a.ptr;
+  return nullptr;
+}
+
+static pkv_status noalloc_scratch_ptr(int device, cudaStream_t stream, void** out) {
   static std::mutex mu;
-  static void* cached[128] = {};
-  *err = cudaSuccess;
-  if (device < 0 || device >= 128) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
+  static std::vector<ScratchAddr> cache;
+  *out = nullptr;
+  // a runtime call on the stream makes the device's context current on this thread (the runtime does this
+  // lazily), and the capture status is needed below anyway
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return fail(PKV_ERR_CUDA, "cuCtxGetCurrent is not available from the driver");
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS || !ctx) return fail(PKV_ERR_CUDA, "cuCtxGetCurrent found no current context");
   std::lock_guard<std::mutex> lock(mu);
-  if (!cached[device]) {
-    void* ptr = nullptr;
-    *err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    cached[device] = ptr;
+  if (void* p = noalloc_scratch_cached(device, ctx, cache)) {
+    *out = p;
+    return PKV_OK;
   }
-  return cached[device];
+  if (cap != cudaStreamCaptureStatusNone)
+    return fail(PKV_ERR_INVALID_ARG, "the first pkv_attention_noalloc call on a device (and context) must come before "
+                "any stream capture: it looks up the built-in scratch array's address");
+  void* ptr = nullptr;
+  e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch array");
+  cache.push_back(ScratchAddr{device, ctx, ptr});
+  *out = ptr;
+  return PKV_OK;
 }
 
 }  // namespace pkv
@@ -868,12 +969,15 @@ extern "C" pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (device != pool->device) return fail(PKV_ERR_INVALID_ARG, "the pool's device must be the current device");
-  void* scratch = noalloc_scratch_ptr(device, &e);
-  if (!scratch) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch array");
+  cudaStream_t s = (cudaStream_t)stream;
+  void* scratch = nullptr;
+  st = noalloc_scratch_ptr(device, s, &scratch);
+  if (st != PKV_OK) return st;
   // What must start at zero -- the task and split counters -- is cleared by the plan kernel on every call;
   // everything else is written before it is read.
   char* ws = static_cast<char*>(scratch);
-  cudaStream_t s = (cudaStream_t)stream;
+  st = prepare_prefill_shadow(pool, ws, w, num_seqs, num_tokens);
+  if (st != PKV_OK) return st;
   e = launch_plan(pool, ws, w, context_lens, query_start_loc, num_seqs, num_tokens, max_blocks_per_seq, s);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   int launches = 1;

@@ -62,7 +62,7 @@ struct DecodeTraits {
   static constexpr int QB = G * D * 2;             // a streaming warp's q buffer (the G heads' rows)
   // everything but the rings: q buffers, shares, staging, queue, the other barriers, flag, alignment slack
   static constexpr int REST = NW * QB + NW * OV * SHL * 4 + NW * kHeadsTile * 8 + G * D * 4 + 64 +
-                              QD * (int)sizeof(TaskEntry) + (3 * NW + 2 * QD) * 8 + 16 + 1024;
+                              QD * (int)sizeof(TaskEntry) + (3 * NW + 3 * QD) * 8 + 8 + 16 + 1024;
   static constexpr int SLOT = RUN + SCL + 8;       // a ring slot with its scale record and its barrier
   static constexpr int NR_FIT = (kSmemPerSM / 2 - kSmemReservedPerCTA - REST) / (NW * SLOT);
   static constexpr int NR = RING < NR_FIT ? RING : (NR_FIT < 2 ? 2 : NR_FIT);
@@ -73,9 +73,10 @@ struct DecodeTraits {
   static constexpr int OFF_MML = OFF_STG + G * D * 4;                // staged split's (m, l): [8] float2
   static constexpr int OFF_Q = OFF_MML + 64;                         // [QD] TaskEntry
   static constexpr int OFF_BAR = OFF_Q + QD * (int)sizeof(TaskEntry);
-  // barriers: ring [NW][NR], share_full [NW], share_empty [NW], queue full [QD], queue empty [QD], q [NW]
-  static constexpr int NBARS = NW * NR + 3 * NW + 2 * QD;
-  static constexpr int OFF_FLAG = OFF_BAR + NBARS * 8;               // the CTA's abort flag
+  // barriers: ring [NW][NR], share_full [NW], share_empty [NW], queue full [QD], queue empty [QD], q [NW],
+  // queue half-done [QD]
+  static constexpr int NBARS = NW * NR + 3 * NW + 3 * QD;
+  static constexpr int OFF_FLAG = OFF_BAR + (NBARS * 8 + 15) / 16 * 16;  // the CTA's abort flag
   static constexpr int OFF_SCL = OFF_FLAG + 16;                      // 8-bit: [NW][NR] scale records
   static constexpr int SMEM = OFF_SCL + NW * NR * SCL + 1024;        // + slack to align the rings to 1024 bytes
   static constexpr int FIT = kSmemPerSM / (SMEM + kSmemReservedPerCTA);
@@ -156,7 +157,7 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, volatil
     if (dev::mbar_try_wait(bar, parity)) return true;
     if ((polls & 31u) == 0) {
       if (*abort) return false;
-      if (polls > (1u << 16) && (int64_t)(dev::globaltimer_ns() - t0) > 1000000000ll) {
+      if (polls > dev::kWaitMinPolls && (int64_t)(dev::globaltimer_ns() - t0) > dev::kWaitLimitNs) {
         dev::set_error(err, PKV_DEVERR_WAIT_TIMEOUT);
         *abort = 1;
         return false;
@@ -182,6 +183,7 @@ struct DecodeSmem {
   uint64_t* qfull;
   uint64_t* qempty;
   uint64_t* qbar;       // [NW] the q buffers' barriers
+  uint64_t* qmid;       // [QD] every streaming warp has consumed half of its runs of the entry's task
   volatile int* abort;
   unsigned char* scl;   // 8-bit: [NW][NR] scale records, 32 bytes each
   __device__ explicit DecodeSmem(unsigned char* s) {
@@ -198,6 +200,7 @@ struct DecodeSmem {
     qfull = share_empty + T::NW;
     qempty = qfull + T::QD;
     qbar = qempty + T::QD;
+    qmid = qbar + T::NW;
     abort = reinterpret_cast<volatile int*>(s + T::OFF_FLAG);
     scl = s + T::OFF_SCL;
   }
@@ -247,6 +250,8 @@ struct Streamer {
   int q_used = 0;        // q loads taken out of the buffer so far
   bool q_busy = false;   // the buffer holds (or awaits) a q not yet taken
   bool cur_q_done = false;  // the current task's q is taken (or the task needs none): the buffer may refill
+  int used_in_task = 0;  // runs of the current task consumed so far
+  bool half_sent = false;  // this warp has told the scheduler it is half-way through the current task
 
   __device__ Streamer(const DecodeParams& p_, const DecodeSmem<D, G, KV>& sm_, int warp_, int lane_)
       : p(p_), sm(sm_), warp(warp_), lane(lane_) {
@@ -407,11 +412,25 @@ struct Streamer {
     ok = __all_sync(0xffffffffu, got) && ok;
     return dev::smem_addr(ring + slot * T::RUN);
   }
+  // Half-way through the current task (half of this warp's runs consumed; at once for a warp with none): the
+  // scheduler warp claims the CTA's next task once every streaming warp is there (see Scheduler).
+  __device__ __forceinline__ void half_way() {
+    if (half_sent || 2 * used_in_task < runs(cur)) return;
+    half_sent = true;
+    if (lane == 0) dev::mbar_arrive(&sm.qmid[k % T::QD]);
+  }
+  __device__ __forceinline__ void task_start() {
+    used_in_task = 0;
+    half_sent = false;
+    half_way();
+  }
   // The warp is done with the oldest run: recycle its slot for the next run of the stream.
   __device__ __forceinline__ void release_run() {
     __syncwarp();
     ++consumed;
+    ++used_in_task;
     if (ok) issue_next();
+    half_way();
   }
   // Before the dependency wait: the first task, and its first K/V runs wherever nothing that the previous
   // kernel writes can be in them (positions the appended tokens never reach, or rows that are replaced
@@ -458,6 +477,7 @@ __device__ __forceinline__ void stream_loop(const DecodeParams& p, const DecodeS
   float2* my_ml = sm.sh_ml + warp * kHeadsTile;
   while (w.ok && w.cur.t >= 0) {
     const TaskView d = w.cur;
+    w.task_start();
     w.fill();
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o[T::MT][4];
@@ -812,7 +832,6 @@ struct Scheduler {
   int n_tasks = 0;
   int filled = 0;        // queue entries published so far (task sequence numbers 0 .. filled-1)
   bool ended = false;    // an end-of-work entry has been published
-  int next_dyn = 0;      // lane 0: result of the counter increment for the next dynamic entry
   int last_nb = 1 << 30; // blocks of the task published last
 
   __device__ Scheduler(const DecodeParams& p_, const DecodeSmem<D, G, KV>& sm_, int lane_) : p(p_), sm(sm_), lane(lane_) {}
@@ -883,20 +902,23 @@ struct Scheduler {
   }
   __device__ void run() {
     static_assert(kStaticTasks < T::QD, "queue");
-    if (ended) return;
-    if (lane == 0) next_dyn = atomicAdd(&p.hdr->work, 1);
-    static_assert(T::QD == 3, "entry m is claimed after task m - 2, whose slot is (m - 2) % 3");
+    static_assert(T::QD == 3, "entry m reuses the slot of task m - 3");
     while (!ended) {
-      // claim entry m once every streaming warp has finished task m - 2 and the combiner has read it (which
-      // also frees entry m's slot, last used by task m - 3).  Once the list has reached small tasks (it is
-      // ordered largest first) a CTA can hold one more without unbalancing the launch, and claiming as
-      // soon as the slot is free lets the last tasks' tiles be in flight before a warp reaches them.
+      // Entry m is claimed once every streaming warp is half-way through task m - 1 (and entry m's slot, last
+      // used by task m - 3, is free): late enough that the next task goes to the CTA that will be free first
+      // (a CTA holding one unstarted task for a whole task's time unbalanced the launch: the busiest CTA held
+      // 1.3x the average), early enough that the claim, the task's record and its first K/V runs arrive
+      // before the warps run dry.  Once the list has reached small tasks (it is ordered largest first) a CTA
+      // can hold one more without unbalancing the launch: those are claimed as soon as the slot is free.
+      const int m = filled;
       const bool small = last_nb <= kEagerClaimBlocks;
-      const int gate = small ? filled - T::QD : filled - 2;
+      if (!small && !cta_wait(&sm.qmid[(m - 1) % T::QD], ((m - 1) / T::QD) & 1, sm.abort, p.err)) return;
+      const int gate = m - T::QD;
       if (gate >= 0 && !cta_wait(&sm.qempty[gate % T::QD], (gate / T::QD) & 1, sm.abort, p.err)) return;
-      const int idx[1] = {kStaticTasks * (int)gridDim.x + __shfl_sync(0xffffffffu, next_dyn, 0)};
+      int c = 0;
+      if (lane == 0) c = atomicAdd(&p.hdr->work, 1);
+      const int idx[1] = {kStaticTasks * (int)gridDim.x + __shfl_sync(0xffffffffu, c, 0)};
       publish(idx);
-      if (!ended && lane == 0) next_dyn = atomicAdd(&p.hdr->work, 1);  // used at the next publish
     }
   }
 };
@@ -1168,6 +1190,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
       dev::mbar_init(&sm.qempty[i], T::NW + 1);  // the streaming warps and the combiner
     }
     for (int i = 0; i < T::NW; ++i) dev::mbar_init(&sm.qbar[i], 1);
+    for (int i = 0; i < T::QD; ++i) dev::mbar_init(&sm.qmid[i], T::NW);  // the streaming warps
     *sm.abort = 0;
     dev::fence_mbar_init();
   }

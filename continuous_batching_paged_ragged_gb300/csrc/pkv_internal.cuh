@@ -9,6 +9,7 @@
 
 #include <string>
 #include <utility>
+#include <vector>
 
 #include "pkv.h"
 
@@ -29,6 +30,20 @@ struct PlanKey {
   int32_t num_seqs = -1;
   int32_t num_tokens = -1;
   int32_t max_blocks_per_seq = -1;
+  // Under PKV_VALIDATE=1: a hash of the context_lens and query_start_loc contents the plan was built from.
+  bool summed = false;
+  uint64_t meta_sum = 0;
+};
+
+// Plans remembered per pool: one per workspace, the most recently planned last.  A plan on a workspace
+// replaces that workspace's earlier plan and nothing else; past kMaxPlans workspaces the oldest is
+// forgotten (its next pkv_attention is refused until it is planned again).
+constexpr size_t kMaxPlans = 32;
+
+// What PKV_VALIDATE=1 learned about a call's metadata (nothing when the check did not run).
+struct MetaCheck {
+  bool ran = false;
+  uint64_t sum = 0;  // hash of the context_lens and query_start_loc contents
 };
 
 }  // namespace pkv
@@ -46,7 +61,7 @@ struct pkv_pool {
   int32_t last_launches = 0;
   int num_sms = 0;
   int device = 0;
-  pkv::PlanKey plan;           // last plan issued through this pool
+  std::vector<pkv::PlanKey> plans;  // the plans issued through this pool, one per workspace (most recent last)
   // 8-bit cache: tensor map of the fp16 shadow in the last workspace used for prefill rows (re-encoded when
   // the workspace or its size changes)
   CUtensorMap shadow_map;
@@ -59,9 +74,10 @@ namespace pkv {
 // (the layout of an fp16 pool, and of the 8-bit cache's fp16 shadow).
 pkv_status encode_f16_rows(CUtensorMap* map, void* base, uint64_t rows, int head_dim);
 // The PKV_VALIDATE=1 host check of a call's device metadata (a no-op otherwise); null pointers are skipped.
+// When `check` is given and the check ran, it receives a hash of the context_lens and query_start_loc contents.
 pkv_status validate_metadata(const pkv_pool* pool, const int32_t* block_tables, int32_t max_blocks,
                              const int32_t* context_lens, const int32_t* qsl, int32_t num_seqs, int32_t num_tokens,
-                             const int64_t* slots, void* stream);
+                             const int64_t* slots, void* stream, MetaCheck* check = nullptr);
 }  // namespace pkv
 
 namespace pkv {
@@ -174,18 +190,24 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Bounded wait: gives up (returns false) only after more than 2^16 polls AND more than ~1 s of
-// %globaltimer time, measured as a signed difference so that an adjustment of the timer can neither
+// Limits of every on-chip wait: it gives up only after more than kWaitMinPolls polls AND more than
+// kWaitLimitNs of %globaltimer time.
+constexpr uint32_t kWaitMinPolls = 1u << 16;
+constexpr int64_t kWaitLimitNs = 1000000000ll;
+
+// Bounded wait: gives up (returns false) only after more than `min_polls` polls AND more than `limit_ns`
+// of %globaltimer time, measured as a signed difference so that an adjustment of the timer can neither
 // wrap the elapsed time nor end the wait early on its own.  Callers record PKV_DEVERR_WAIT_TIMEOUT
 // and unwind without touching the barrier again.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int64_t limit_ns = kWaitLimitNs,
+                                          uint32_t min_polls = kWaitMinPolls) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t polls = 1;; ++polls) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((polls & 255u) == 0 && polls > (1u << 16)) {
+    if ((polls & 255u) == 0 && polls > min_polls) {
       const int64_t dt = (int64_t)(globaltimer_ns() - t0);
-      if (dt > 1000000000ll) return false;
+      if (dt > limit_ns) return false;
     }
   }
 }

@@ -119,9 +119,21 @@ static size_t cache_bytes_of(const pkv_config* c) {
 // ctx <= max_blocks * block_size per row, every block id a row's context reaches in [0, num_blocks), every
 // slot in [-1, num_slots).  The stream is synchronized first; while it is being captured into a graph nothing
 // is checked (a capture cannot synchronize).  Any pointer may be null (not checked).
+// FNV-1a over 32-bit words (a plain change detector, not a security measure).
+static uint64_t fnv1a_words(uint64_t h, const std::vector<int32_t>& words) {
+  for (int32_t w : words) {
+    const uint32_t u = static_cast<uint32_t>(w);
+    for (int i = 0; i < 4; ++i) {
+      h ^= (u >> (8 * i)) & 0xFFu;
+      h *= 1099511628211ull;
+    }
+  }
+  return h;
+}
+
 pkv_status validate_metadata(const pkv_pool* pool, const int32_t* block_tables, int32_t max_blocks,
                              const int32_t* context_lens, const int32_t* qsl, int32_t num_seqs, int32_t num_tokens,
-                             const int64_t* slots, void* stream) {
+                             const int64_t* slots, void* stream, MetaCheck* check) {
   const char* env = std::getenv("PKV_VALIDATE");
   if (!env || std::strcmp(env, "1") != 0 || num_tokens <= 0) return PKV_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -139,6 +151,10 @@ pkv_status validate_metadata(const pkv_pool* pool, const int32_t* block_tables, 
   if (qsl && (e = fetch(qsl, q.size() * 4, q.data())) != cudaSuccess) return cuda_fail(e, "PKV_VALIDATE: copy");
   if (context_lens && (e = fetch(context_lens, ctx.size() * 4, ctx.data())) != cudaSuccess)
     return cuda_fail(e, "PKV_VALIDATE: copy");
+  if (check) {
+    check->ran = true;
+    check->sum = fnv1a_words(fnv1a_words(14695981039346656037ull, ctx), q);
+  }
   if (qsl) {
     if (q[0] != 0 || q[num_seqs] != num_tokens)
       return fail(PKV_ERR_INVALID_ARG, "PKV_VALIDATE: query_start_loc must run from 0 to num_tokens");
@@ -265,6 +281,38 @@ extern "C" pkv_status pkv_pool_check(pkv_pool* pool, int32_t* bits, int32_t clea
 }
 
 extern "C" int32_t pkv_last_launch_count(const pkv_pool* pool) { return pool ? pool->last_launches : 0; }
+
+// ---------------------------------------------------------------------------------------------------
+// Test hook: a bounded on-chip wait that runs out.  One thread waits, through the same bounded wait the
+// attention kernels use, on an mbarrier that nobody arrives at, with the time limit shortened to
+// `limit_ns`; when the wait gives up it records PKV_DEVERR_WAIT_TIMEOUT in the pool's error word and the
+// kernel returns.  Nothing traps and nothing waits without a limit.
+// ---------------------------------------------------------------------------------------------------
+namespace pkv {
+__global__ void expire_wait_kernel(int32_t* err, int64_t limit_ns) {
+  __shared__ uint64_t bar;
+  dev::griddep_wait();
+  if (threadIdx.x != 0) return;
+  dev::mbar_init(&bar, 1);
+  dev::fence_mbar_init();
+  if (!dev::mbar_wait(&bar, 0, limit_ns, 256)) dev::set_error(err, PKV_DEVERR_WAIT_TIMEOUT);
+}
+}  // namespace pkv
+
+extern "C" pkv_status pkv_debug_expire_wait(pkv_pool* pool, int64_t limit_ns, void* stream) {
+  clear_error();
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  pool->last_launches = 0;
+  const char* env = std::getenv("PKV_TEST_HOOKS");
+  if (!env || std::strcmp(env, "1") != 0)
+    return fail(PKV_ERR_UNSUPPORTED, "pkv_debug_expire_wait is a test hook: set PKV_TEST_HOOKS=1 to enable it");
+  if (limit_ns < 1 || limit_ns > 100000000ll) return fail(PKV_ERR_OUT_OF_RANGE, "limit_ns must be in [1, 1e8]");
+  const cudaError_t e = launch_pdl(expire_wait_kernel, dim3(1), dim3(32), 0, (cudaStream_t)stream, pool->dev_error,
+                                   (int64_t)limit_ns);
+  if (e != cudaSuccess) return cuda_fail(e, "expire-wait launch");
+  pool->last_launches = 1;
+  return PKV_OK;
+}
 
 // ---------------------------------------------------------------------------------------------------
 // Kernels

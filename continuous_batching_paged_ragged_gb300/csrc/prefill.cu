@@ -561,7 +561,7 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
           const uint64_t t0 = dev::globaltimer_ns();
           uint32_t polls = 0;
           while (atomicAdd(const_cast<int*>(&sync->y), 0) == 0) {
-            if ((++polls & 255u) == 0 && polls > (1u << 16) && (int64_t)(dev::globaltimer_ns() - t0) > 1000000000ll) {
+            if ((++polls & 255u) == 0 && polls > dev::kWaitMinPolls && (int64_t)(dev::globaltimer_ns() - t0) > dev::kWaitLimitNs) {
               *sh.abort = 1;
               dev::set_error(p.err, PKV_DEVERR_WAIT_TIMEOUT);
               break;

@@ -86,6 +86,7 @@ SIGNATURES = {
     "pkv_attention_noalloc": (ctypes.c_int, [_p, _i32, _p, _p, _i32, _p, _p, _i32, _i32, _p, _p]),
     "pkv_attention_append": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _p, _p, _sz,
                                             _p]),
+    "pkv_debug_expire_wait": (ctypes.c_int, [_p, _i64, _p]),
     "pkv_last_launch_count": (_i32, [_p]),
     "pkv_last_error": (ctypes.c_char_p, []),
     "pkv_sched_create": (ctypes.c_int, [ctypes.POINTER(pkv_sched_config), _p, ctypes.POINTER(_p)]),
@@ -213,6 +214,11 @@ def pkv_attention_append(pool: int, layer: int, q, k, v, slot_mapping, block_tab
                                        max_blocks_per_seq, _ptr(context_lens), _ptr(query_start_loc), num_seqs,
                                        num_tokens, _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)),
            "pkv_attention_append")
+
+
+def pkv_debug_expire_wait(pool: int, limit_ns: int, stream=None) -> None:
+    """Test hook (needs PKV_TEST_HOOKS=1): a bounded on-chip wait that runs out after limit_ns."""
+    _check(load().pkv_debug_expire_wait(pool, limit_ns, _stream(stream)), "pkv_debug_expire_wait")
 
 
 def pkv_attention_noalloc(pool: int, layer: int, q, block_tables, max_blocks_per_seq: int, context_lens,

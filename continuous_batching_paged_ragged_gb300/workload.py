@@ -147,3 +147,88 @@ def run_pass(pool: pkv.Pool, ds: DeviceStep, layers: List[int], qs, ks, vs, outs
             pkv.pkv_append(pool.handle, layer, ks[i], vs[i], ds.slot_mapping, ds.num_tokens)
             attn.run(layer, qs[i], outs[i])
     return attn
+
+
+class RawStep:
+    """One forward pass's hot path with every pointer resolved up front (as a benchmark or a CUDA-graph
+    capture wants it): plan + per layer append and attention, as one pkv_attention_append call (fused=True)
+    or pkv_append then pkv_attention.  `launches` counts the kernels the calls enqueued."""
+
+    def __init__(self, pool, ds, attn, qs, ks, vs, outs, stream, fused=True):
+        self.fused = fused
+        self.lib = pkv.load()
+        self.pool = pool.handle
+        self.ds = ds
+        self.ws = attn.workspace.data_ptr()
+        self.ws_bytes = attn.ws_bytes
+        self.q = [x.data_ptr() for x in qs]
+        self.k = [x.data_ptr() for x in ks]
+        self.v = [x.data_ptr() for x in vs]
+        self.o = [x.data_ptr() for x in outs]
+        self.stream = stream
+        self.bt = ds.block_tables.data_ptr()
+        self.ctx = ds.context_lens.data_ptr()
+        self.qsl = ds.query_start_loc.data_ptr()
+        self.slots = ds.slot_mapping.data_ptr()
+        self.launches = 0
+
+    def plan(self):
+        d = self.ds
+        st = self.lib.pkv_attention_plan(self.pool, self.ctx, self.qsl, d.num_seqs, d.num_tokens, d.max_blocks,
+                                         self.ws, self.ws_bytes, self.stream)
+        if st:
+            raise pkv.PkvError(st, "pkv_attention_plan", pkv.pkv_last_error())
+        self.launches += self.lib.pkv_last_launch_count(self.pool)
+
+    def append(self, i, layer):
+        st = self.lib.pkv_append(self.pool, layer, self.k[i], self.v[i], self.slots, self.ds.num_tokens, self.stream)
+        if st:
+            raise pkv.PkvError(st, "pkv_append", pkv.pkv_last_error())
+        self.launches += self.lib.pkv_last_launch_count(self.pool)
+
+    def attention(self, i, layer):
+        d = self.ds
+        st = self.lib.pkv_attention(self.pool, layer, self.q[i], self.bt, d.max_blocks, self.ctx, self.qsl,
+                                    d.num_seqs, d.num_tokens, self.o[i], self.ws, self.ws_bytes, self.stream)
+        if st:
+            raise pkv.PkvError(st, "pkv_attention", pkv.pkv_last_error())
+        self.launches += self.lib.pkv_last_launch_count(self.pool)
+
+    def attention_append(self, i, layer):
+        d = self.ds
+        st = self.lib.pkv_attention_append(self.pool, layer, self.q[i], self.k[i], self.v[i], self.slots, self.bt,
+                                           d.max_blocks, self.ctx, self.qsl, d.num_seqs, d.num_tokens, self.o[i],
+                                           self.ws, self.ws_bytes, self.stream)
+        if st:
+            raise pkv.PkvError(st, "pkv_attention_append", pkv.pkv_last_error())
+        self.launches += self.lib.pkv_last_launch_count(self.pool)
+
+    def __call__(self, layers):
+        self.plan()
+        for i, layer in enumerate(layers):
+            if self.fused:
+                self.attention_append(i, layer)
+            else:
+                self.append(i, layer)
+                self.attention(i, layer)
+
+
+def capture_step_graph(pool: pkv.Pool, ds: DeviceStep, attn: Attention, qs, ks, vs, outs, layers: List[int],
+                       fused: bool = True, device="cuda", warm: int = 3):
+    """The pass as one CUDA graph: the same library calls (RawStep), run `warm` times on a side stream, then
+    captured there.  Returns (graph, kernel launches per replay).  Replaying it re-runs the plan, the
+    append of this pass's tokens (the same bits to the same slots) and the attention of every layer."""
+    stream = torch.cuda.current_stream(device)
+    cap = torch.cuda.Stream(device)
+    step = RawStep(pool, ds, attn, qs, ks, vs, outs, cap.cuda_stream, fused=fused)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        for _ in range(warm):
+            step(layers)
+    torch.cuda.synchronize()
+    step.launches = 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        step(layers)
+    torch.cuda.synchronize()
+    return graph, step.launches

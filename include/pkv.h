@@ -24,12 +24,15 @@
  *     host after synchronizing the stream, and refuse a bad pass before launching anything --
  *     PKV_ERR_INVALID_ARG for rows (query_start_loc not running from 0 to num_tokens without decreasing, or
  *     not 1 <= q_len <= ctx <= max_blocks_per_seq * block_size), PKV_ERR_OUT_OF_RANGE for block ids and
- *     slots.  A debugging aid: it costs a synchronization and copies per call, and is skipped while the
- *     stream is being captured into a graph.
+ *     slots.  A plan issued under PKV_VALIDATE=1 also remembers a hash of the context_lens and
+ *     query_start_loc contents; a pkv_attention / pkv_attention_append on that workspace whose metadata
+ *     contents differ (same pointers, rewritten in place without a new plan) is refused with
+ *     PKV_ERR_INVALID_ARG.  A debugging aid: it costs a synchronization and copies per call, and is skipped
+ *     while the stream is being captured into a graph.
  *   - No call traps the device, and no kernel waits on another grid.
- *   - A pool handle is used by one host thread at a time: it remembers the last plan issued through it
- *     and, on an 8-bit cache, the tensor map of the last workspace's fp16 shadow.  Different pools are
- *     independent; pkv_last_error is per thread.
+ *   - A pool handle is used by one host thread at a time: it remembers the plan issued on each of its 32
+ *     most recently planned workspaces and, on an 8-bit cache, the tensor map of the last workspace's fp16
+ *     shadow.  Different pools are independent; pkv_last_error is per thread.
  *   - Supported shapes: fp16 Q and K/V inputs; an fp16 or 8-bit (E4M3) cache; head_dim 64, 128 or 256;
  *     block_size 16; num_q_heads a multiple of num_kv_heads with a group of 1, 2, 4, 6 or 8 query heads
  *     per KV head.  Others: PKV_ERR_UNSUPPORTED.
@@ -181,8 +184,11 @@ pkv_status pkv_append(pkv_pool* pool, int32_t layer, const void* k, const void* 
  * for every pkv_attention call with the same workspace and metadata pointers and sizes until the
  * next pkv_attention_plan on that workspace; changing the metadata CONTENTS requires a new plan.
  * pkv_attention refuses (PKV_ERR_INVALID_ARG) a call whose workspace/metadata pointers or sizes
- * differ from the last plan issued on `workspace`.  Plans and calls on one workspace must be
- * ordered on one stream (or synchronised by the caller).
+ * differ from the last plan issued on `workspace` (and, under PKV_VALIDATE=1, one whose metadata
+ * contents changed).  Plans live per workspace: planning one workspace leaves the plans of the
+ * pool's other workspaces valid (double-buffered passes), up to the 32 most recently planned
+ * workspaces per pool.  Plans and calls on one workspace must be ordered on one stream (or
+ * synchronised by the caller).
  *
  * The result is independent of the batch: a row's split-K partition depends only on its own
  * context length, so a row gives bit-identical output alone or in any batch, in any row order.
@@ -244,16 +250,28 @@ pkv_status pkv_attention_append(pkv_pool* pool, int32_t layer, const void* q, co
  * (pkv_attention_workspace_bytes for the same sizes) exceeds that limit is refused with
  * PKV_ERR_OUT_OF_RANGE before anything is launched.
  *
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current -- the pool's device must be the current device -- so make that first call before
- * any stream capture.  Every call shares the one array and leaves its contents behind; nothing in it
- * has to start at zero, but two calls whose kernels can overlap on the GPU (different streams with no
- * ordering between them) race on it. */
+ * The first call in a device's context looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current -- the pool's device must be the current device -- so make that first call
+ * before any stream capture: a first call made while `stream` is capturing is refused with
+ * PKV_ERR_INVALID_ARG.  The address is cached per (device, context), so a context re-created after
+ * cudaDeviceReset looks it up again.  Every call shares the one array and leaves its contents behind;
+ * nothing in it has to start at zero, but two calls whose kernels can overlap on the GPU (different
+ * streams with no ordering between them) race on it.  Every refusal (sizes, the 8-bit cache's prefill
+ * limits, the capture rule) comes before anything is launched. */
 #define PKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 pkv_status pkv_attention_noalloc(pkv_pool* pool, int32_t layer, const void* q, const int32_t* block_tables,
                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
                                  const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens, void* out,
                                  void* stream);
+
+/* Test hook, off by default: refused with PKV_ERR_UNSUPPORTED unless PKV_TEST_HOOKS=1 is in the environment.
+ * The pages have no counterpart; it exercises the failure path of [ABL] "Counting jobs while they run" (a
+ * job must not be left holding the device).  Launches one kernel whose thread waits on an on-chip barrier
+ * that never completes, through the same bounded wait every attention kernel uses, with the time limit
+ * shortened to limit_ns (1 .. 1e8); when the wait gives up it sets PKV_DEVERR_WAIT_TIMEOUT in the pool's
+ * error word and returns.  Afterwards attention launches on the pool do no work until pkv_pool_check
+ * clears the bit and the pass is planned again. */
+pkv_status pkv_debug_expire_wait(pkv_pool* pool, int64_t limit_ns, void* stream);
 
 /* Number of kernel launches the last successful pkv_append / pkv_attention_plan / pkv_attention /
  * pkv_slot_mapping call on `pool` enqueued (for accounting; host-side counter). */

@@ -77,3 +77,47 @@ def test_bad_metadata_refused_before_launch(cuda, built, monkeypatch):
              pkv.PKV_ERR_OUT_OF_RANGE)
     torch.cuda.synchronize()
     assert pool.check() == 0   # nothing ran: the kernels' own range checks never saw the bad values
+
+
+def test_two_workspaces_planned_on_one_pool_both_run(cuda, built):
+    """Plans live per workspace: planning a second workspace leaves the first one's plan valid."""
+    batch, pool, ds, q, k, v = _setup()
+    pkv.pkv_append(pool.handle, 0, k, v, ds.slot_mapping, ds.num_tokens)
+    a, b = workload.Attention(pool, ds), workload.Attention(pool, ds)
+    a.plan()
+    b.plan()
+    out_a, out_b = torch.empty_like(q), torch.empty_like(q)
+    a.run(0, q, out_a)                       # planned before b: still valid
+    b.run(0, q, out_b)
+    a.run(0, q, out_a)
+    torch.cuda.synchronize()
+    assert pool.check() == 0
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+
+
+def test_stale_plan_refused_when_contents_change(cuda, built, monkeypatch):
+    """Under PKV_VALIDATE=1 a pass whose context_lens / query_start_loc were rewritten in place after the plan
+    (same pointers, same sizes) is refused before anything is launched; a new plan makes it run again."""
+    batch, pool, ds, q, k, v = _setup()
+    monkeypatch.setenv("PKV_VALIDATE", "1")
+    attn = workload.Attention(pool, ds)
+    attn.plan()
+    out = torch.empty_like(q)
+    attn.run_append(0, q, k, v, out)
+    torch.cuda.synchronize()
+    saved = ds.context_lens.clone()
+    ds.context_lens[0] -= 1                  # still a valid row, but not the pass the plan was built for
+    torch.cuda.synchronize()
+    with pytest.raises(pkv.PkvError) as e:
+        attn.run(0, q, out)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG and "changed since" in str(e.value)
+    assert pkv.pkv_last_launch_count(pool.handle) == 0
+    with pytest.raises(pkv.PkvError) as e:
+        attn.run_append(0, q, k, v, out)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    ds.context_lens.copy_(saved)
+    attn.run(0, q, out)                      # the contents match the plan again
+    attn.plan()
+    attn.run(0, q, out)
+    torch.cuda.synchronize()
+    assert pool.check() == 0
