@@ -833,6 +833,7 @@ struct Scheduler {
   int filled = 0;        // queue entries published so far (task sequence numbers 0 .. filled-1)
   bool ended = false;    // an end-of-work entry has been published
   int last_nb = 1 << 30; // blocks of the task published last
+  int last_idx = 0;      // list index of the task published last
 
   __device__ Scheduler(const DecodeParams& p_, const DecodeSmem<D, G, KV>& sm_, int lane_) : p(p_), sm(sm_), lane(lane_) {}
 
@@ -842,10 +843,8 @@ struct Scheduler {
   __device__ void publish(const int (&idx)[N]) {
     int4 rec[N];
 #pragma unroll
-    for (int j = 0; j < N; ++j) rec[j] = idx[j] < p.max_tasks ? __ldcg(p.tasks + idx[j]) : make_int4(-1, 0, 0, 0);
-#pragma unroll
-    for (int j = 0; j < N; ++j)  // the count arrives alongside the records: no load waits for it
-      if (idx[j] >= n_tasks) rec[j] = make_int4(-1, 0, 0, 0);
+    for (int j = 0; j < N; ++j)  // past the list: the end of the work, with nothing to load
+      rec[j] = idx[j] < n_tasks && idx[j] < p.max_tasks ? __ldcg(p.tasks + idx[j]) : make_int4(-1, 0, 0, 0);
     int id[N], q0[N];
 #pragma unroll
     for (int j = 0; j < N; ++j) {
@@ -898,6 +897,7 @@ struct Scheduler {
     n_tasks = __ldcg(&p.hdr->n_tasks);
     static_assert(kStaticTasks == 1, "one static task");
     const int idx[kStaticTasks] = {(int)blockIdx.x};
+    last_idx = idx[0];
     publish(idx);
   }
   __device__ void run() {
@@ -912,12 +912,23 @@ struct Scheduler {
       // can hold one more without unbalancing the launch: those are claimed as soon as the slot is free.
       const int m = filled;
       const bool small = last_nb <= kEagerClaimBlocks;
-      if (!small && !cta_wait(&sm.qmid[(m - 1) % T::QD], ((m - 1) / T::QD) & 1, sm.abort, p.err)) return;
+      // Near the end of the list (this CTA's last claim was within two grids of it), the counter is read
+      // before waiting: once every task has been claimed (the counter may lag, never run ahead) the end of
+      // the work is published at once, and the warps finish without waiting for a claim that can only come
+      // back empty.
+      bool out = false;
+      if (last_idx + 2 * (int)gridDim.x >= n_tasks) {
+        int seen = 0;
+        if (lane == 0) seen = dev::ld_relaxed_gpu(&p.hdr->work);
+        out = kStaticTasks * (int)gridDim.x + __shfl_sync(0xffffffffu, seen, 0) >= n_tasks;
+      }
+      if (!out && !small && !cta_wait(&sm.qmid[(m - 1) % T::QD], ((m - 1) / T::QD) & 1, sm.abort, p.err)) return;
       const int gate = m - T::QD;
       if (gate >= 0 && !cta_wait(&sm.qempty[gate % T::QD], (gate / T::QD) & 1, sm.abort, p.err)) return;
       int c = 0;
-      if (lane == 0) c = atomicAdd(&p.hdr->work, 1);
-      const int idx[1] = {kStaticTasks * (int)gridDim.x + __shfl_sync(0xffffffffu, c, 0)};
+      if (lane == 0 && !out) c = atomicAdd(&p.hdr->work, 1);
+      const int idx[1] = {out ? n_tasks : kStaticTasks * (int)gridDim.x + __shfl_sync(0xffffffffu, c, 0)};
+      last_idx = idx[0];
       publish(idx);
     }
   }
@@ -930,9 +941,11 @@ struct Scheduler {
 //    of the token's counter, issued as the task starts): it merges the token at once -- the other splits'
 //    partials from L2, its own from shared memory -- and resets the counter.  Under the largest-first task
 //    order this is the usual case for a token's last, small split.
-//  * otherwise it writes its unnormalised partial and counts it on the token's counter; the count is
-//    issued one task later (its release then waits for no fresh store) and examined one task later still
-//    (its round trip hidden), and the warp that completes the count merges the token.
+//  * otherwise it writes its unnormalised partial and counts it on the token's counter at once (the release
+//    waits for the partial's stores; the combiner has the slack), examines the count's result one task later
+//    (its round trip hidden), and the warp that completes the count merges the token.  Counting at once lets
+//    the count reach the token's other splits while they run, so that near the end of the launch the last
+//    split usually merges at its start, rather than a count and a merge after the last task.
 // Nothing here stalls the streaming warps.
 // ---------------------------------------------------------------------------------------------------
 template <int D, int G, int KV>
@@ -1044,7 +1057,6 @@ struct Combiner {
 
   __device__ void run() {
     uint32_t taken = 0;               // bit w: parity of the shares taken from streaming warp w so far
-    int wr_tg = -1, wr_ns = 0;        // partial written, count not issued yet
     int ct_tg = -1, ct_ns = 0, ct_prev = 0;  // count issued, result not examined yet
     const int hg = lane & 3;
     const bool real = hg < T::LG;     // this lane's fragment columns hold real heads
@@ -1122,12 +1134,9 @@ struct Combiner {
           }
         }
       }
-      // ---- the count of the partial written one task ago (its stores are long complete, so the release
-      // does not wait); then the count issued one task ago, whose result has arrived: maybe a merge ----
-      int new_prev = 0;
-      if (wr_tg >= 0 && lane == 0) new_prev = dev::atom_add_acq_rel_gpu(p.merge_cnt + wr_tg, 1);
-      // merges due now: the token whose count completed (all partials in L2), and this task's token if
-      // every other split of it was counted before it started (its own split from shared memory)
+      // ---- merges due now: the token whose count this warp completed at the end of the previous task (all
+      // partials in L2), and this task's token if every other split of it was counted before it started (its
+      // own split from shared memory) ----
       const bool m1 = ct_tg >= 0 && completes_count(ct_tg, ct_ns, ct_prev);
       const bool m2 = multi && __shfl_sync(0xffffffffu, done_lane0, 0) == nsplit - 1;
       if (m2 && lane == 0) p.merge_cnt[tg] = 0;  // nobody else counts this token again in this launch
@@ -1135,11 +1144,10 @@ struct Combiner {
       for (int i = (m1 ? 0 : 1); i < (m2 ? 2 : 1); ++i) {  // one call site keeps the code (and registers) small
         merge(i == 0 ? ct_tg : tg, i == 0 ? ct_ns : nsplit, i == 0 ? -1 : s);
       }
-      ct_tg = wr_tg;
-      ct_ns = wr_ns;
-      ct_prev = new_prev;
-      wr_tg = -1;
-      // ---- the output, or the split's partial (unless merged above) ----
+      ct_tg = -1;
+      // ---- the output, or the split's partial (unless merged above), counted at once: its count then
+      // reaches the token's other splits while they run, and the one that starts (or finishes) last merges
+      // with no count of its own ----
       __syncwarp();
       if (nsplit == 1) {
         uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)t * p.num_q_heads + (size_t)g * G) * D);
@@ -1154,18 +1162,16 @@ struct Combiner {
           if (2 * lane + 1 < G) p.part_ml[pidx * kHeadsTile + 2 * lane + 1] = make_float2(M1, L1);
         }
         if (multi) {
-          wr_tg = tg;
-          wr_ns = nsplit;
+          __syncwarp();  // every lane's stores precede the release below
+          if (lane == 0) ct_prev = dev::atom_add_acq_rel_gpu(p.merge_cnt + tg, 1);
+          ct_tg = tg;
+          ct_ns = nsplit;
         }
       }
       __syncwarp();  // the staging buffers are free again
     }
-    // ---- flush: the last partial's count, then the two outstanding results ----
-    int new_prev = 0;
-    if (wr_tg >= 0 && lane == 0) new_prev = dev::atom_add_acq_rel_gpu(p.merge_cnt + wr_tg, 1);
-    const bool m1 = ct_tg >= 0 && completes_count(ct_tg, ct_ns, ct_prev);
-    const bool m2 = wr_tg >= 0 && completes_count(wr_tg, wr_ns, new_prev);
-    for (int i = (m1 ? 0 : 1); i < (m2 ? 2 : 1); ++i) merge(i == 0 ? ct_tg : wr_tg, i == 0 ? ct_ns : wr_ns, -1);
+    // ---- flush: the last partial's count (issued with it), maybe a merge ----
+    if (ct_tg >= 0 && completes_count(ct_tg, ct_ns, ct_prev)) merge(ct_tg, ct_ns, -1);
   }
 };
 

@@ -414,6 +414,12 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* addr, int v) {
   return old;
 }
 // GPU-scope load with acquire semantics.
+__device__ __forceinline__ int ld_relaxed_gpu(const int32_t* addr) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int32_t* addr) {
   int v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
