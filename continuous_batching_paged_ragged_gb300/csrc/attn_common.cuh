@@ -57,7 +57,7 @@ struct PrefillArgs {
   const int32_t* items_slot;  // per work entry: the split item's slot, or -1
   int2* pf_sync;              // per slot: {chunks finished, first chunk's partial published}
   float2* pf_ml;              // per slot: [256 rows] (running max, running sum) of the first chunk
-  float* pf_o;                // per slot: [256 rows][head_dim] unnormalised output of the first chunk
+  float* pf_o;                // per slot and Q tile: [head_dim][128 rows] unnormalised output of the first chunk
   WsHeader* hdr;
   int32_t* err;
   int layer_row0_k, layer_row0_v;

@@ -531,6 +531,9 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
       // The chunk that finishes first publishes its unnormalised (m, l, O); the other merges them in
       // chunk order (the result does not depend on which chunk finished first) and writes fp16.
       const size_t prow = (size_t)slot * (2 * kPrefillRows) + wg * kPrefillRows + r;
+      // the partial O of this (slot, Q tile) is stored column by column, [D][128 rows]: a warp's 32 rows of one
+      // column are 32 consecutive floats, so every store and load of the handshake is one coalesced line
+      float* pcol = p.pf_o + ((size_t)slot * 2 + wg) * ((size_t)D * kPrefillRows) + r;
       const int2* sync = p.pf_sync + slot;
       if (threadIdx.x == 0) *sh.order = atomicAdd(const_cast<int*>(&sync->x), 1);
       dev::named_bar_sync(kBarEpi, kSoftmaxThreads);
@@ -544,11 +547,8 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
             uint32_t o[32];
             dev::tmem_ld32(tl + 128 + 32 * k, o);
             dev::tmem_wait_ld();
-            float4* po = reinterpret_cast<float4*>(p.pf_o + prow * D + 32 * k);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              po[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]), __uint_as_float(o[4 * e + 2]),
-                                  __uint_as_float(o[4 * e + 3]));
+            for (int e = 0; e < 32; ++e) pcol[(size_t)(32 * k + e) * kPrefillRows] = __uint_as_float(o[e]);
           }
         }
         dev::named_bar_sync(kBarEpi, kSoftmaxThreads);  // every row published
@@ -588,18 +588,14 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = 0u;
           }
-          float v[32];
-          const float4* po = reinterpret_cast<const float4*>(p.pf_o + prow * D + 32 * k);
+          float v[32], ot[32];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 q4 = other_has && valid ? __ldcg(po + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float ot[4] = {q4.x, q4.y, q4.z, q4.w};
+          for (int e = 0; e < 32; ++e) ot[e] = other_has ? __ldcg(pcol + (size_t)(32 * k + e) * kPrefillRows) : 0.f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float own = __uint_as_float(o[4 * e + i]);
-              const float a0 = it.chunk ? ot[i] : own, a1 = it.chunk ? own : ot[i];
-              v[4 * e + i] = (a0 * f0 + a1 * f1) * il;
-            }
+          for (int e = 0; e < 32; ++e) {
+            const float own = __uint_as_float(o[e]);
+            const float a0 = it.chunk ? ot[e] : own, a1 = it.chunk ? own : ot[e];
+            v[e] = (a0 * f0 + a1 * f1) * il;
           }
           if (valid) store_row(k, v);
         }
