@@ -250,8 +250,7 @@ struct Streamer {
   int q_used = 0;        // q loads taken out of the buffer so far
   bool q_busy = false;   // the buffer holds (or awaits) a q not yet taken
   bool cur_q_done = false;  // the current task's q is taken (or the task needs none): the buffer may refill
-  int used_in_task = 0;  // runs of the current task consumed so far
-  bool half_sent = false;  // this warp has told the scheduler it is half-way through the current task
+  int half_left = 0;     // runs of the current task still to consume before the half-way signal (0: sent)
 
   __device__ Streamer(const DecodeParams& p_, const DecodeSmem<D, G, KV>& sm_, int warp_, int lane_)
       : p(p_), sm(sm_), warp(warp_), lane(lane_) {
@@ -414,23 +413,16 @@ struct Streamer {
   }
   // Half-way through the current task (half of this warp's runs consumed; at once for a warp with none): the
   // scheduler warp claims the CTA's next task once every streaming warp is there (see Scheduler).
-  __device__ __forceinline__ void half_way() {
-    if (half_sent || 2 * used_in_task < runs(cur)) return;
-    half_sent = true;
-    if (lane == 0) dev::mbar_arrive(&sm.qmid[k % T::QD]);
-  }
   __device__ __forceinline__ void task_start() {
-    used_in_task = 0;
-    half_sent = false;
-    half_way();
+    half_left = runs(cur) / 2;
+    if (half_left == 0 && lane == 0) dev::mbar_arrive(&sm.qmid[k % T::QD]);
   }
   // The warp is done with the oldest run: recycle its slot for the next run of the stream.
   __device__ __forceinline__ void release_run() {
     __syncwarp();
     ++consumed;
-    ++used_in_task;
     if (ok) issue_next();
-    half_way();
+    if (half_left > 0 && --half_left == 0 && lane == 0) dev::mbar_arrive(&sm.qmid[k % T::QD]);
   }
   // Before the dependency wait: the first task, and its first K/V runs wherever nothing that the previous
   // kernel writes can be in them (positions the appended tokens never reach, or rows that are replaced
@@ -911,7 +903,9 @@ struct Scheduler {
       // before the warps run dry.  Once the list has reached small tasks (it is ordered largest first) a CTA
       // can hold one more without unbalancing the launch: those are claimed as soon as the slot is free.
       const int m = filled;
-      const bool small = last_nb <= kEagerClaimBlocks;
+      // A long list (many tasks per CTA) balances itself; there the next task is claimed as soon as the
+      // previous one has been handed on, for the deepest look-ahead.
+      const bool small = last_nb <= kEagerClaimBlocks || n_tasks > 4 * (int)gridDim.x;
       // Near the end of the list (this CTA's last claim was within two grids of it), the counter is read
       // before waiting: once every task has been claimed (the counter may lag, never run ahead) the end of
       // the work is published at once, and the warps finish without waiting for a claim that can only come
