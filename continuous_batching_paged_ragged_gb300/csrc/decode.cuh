@@ -84,6 +84,10 @@ struct DecodeTraits {
   // much in registers for two CTAs (it spills); like its fp16 twin, which shared memory limits to one, it
   // runs one CTA per SM with the whole register file.
   static constexpr int MINB = (F8 && D == 256 && G > 6) ? 1 : (FIT < 3 ? FIT : 3);
+  // Lean blocks two at a time (one softmax step and one rescale of O per pair): measured faster for the 8-bit
+  // cache at head_dim 256 (the long-context decode, 7.3 against 8.9 ms a step), whose warps are bound by their
+  // turnaround per block; slower on the 5-slot fp16 rings and the 256-row batch, so only there.
+  static constexpr bool PAIRS = F8 && D == 256;
   static_assert(D % 64 == 0 && G >= 1 && G <= kHeadsTile, "shape");
   static_assert(RUN % 1024 == 0, "swizzled boxes need 1024-byte aligned slots");
   static_assert(KS % 2 == 0 && QB % 128 == 0, "k-steps in pairs; q buffers stay 16-byte aligned");
@@ -211,6 +215,7 @@ struct TaskView {
   int t, g, s, row, ctx, nsplit, nst;
   int nbw;          // blocks of the split dealt to this warp: task-local blocks bw, bw + 4, ...
   int bw;
+  int nlean;        // the warp's leading blocks that are full and hold no row of this pass (see Streamer)
   const int* ids;   // shared memory: the split's block ids
 };
 
@@ -284,16 +289,40 @@ struct Streamer {
     v.bw = (warp - e->rot) & 3;
     v.nbw = v.t >= 0 ? warp_blocks(e->nb, v.bw) : 0;
     v.ids = e->ids;
+    // A block is on the lean path when all its 16 keys are inside the context and none is this pass's (with
+    // the append fused, the pass's rows come from the inputs): blocks below position `from`.  The same rule
+    // holds without the fused append, so both calls pair the same blocks and give the same bits.  Blocks rise
+    // with j, so the lean ones are the warp's first nlean.
+    const int from = min(v.nst, v.ctx);
+    const int first = v.s * p.split_blocks + v.bw;  // absolute index of the warp's block 0
+    const int nfull = from / kBS - first;             // blocks first, first + NW, ... below from / 16
+    v.nlean = (!T::PAIRS || nfull <= 0) ? 0 : min(v.nbw, (nfull + T::NW - 1) / T::NW);
   }
   static __device__ __forceinline__ int runs(const TaskView& v) { return v.t >= 0 ? 2 * v.nbw : 0; }
   __device__ __forceinline__ int block_pos(const TaskView& v, int j) const {
-    return (v.s * p.split_blocks + v.bw + 4 * j) * kBS;
+    return (v.s * p.split_blocks + v.bw + T::NW * j) * kBS;
   }
+  // Run r of the warp's stream within a task: the lean blocks go in pairs, K of both then V of both; the rest
+  // (an odd lean block, then the blocks holding the context's end or this pass's rows) one by one, K then V.
+  static __device__ __forceinline__ void run_of(const TaskView& v, int r, int& j, int& isv) {
+    const int pr = 4 * (v.nlean >> 1);
+    if (r < pr) {
+      j = 2 * (r >> 2) + (r & 1);
+      isv = (r >> 1) & 1;
+    } else {
+      j = 2 * (v.nlean >> 1) + ((r - pr) >> 1);
+      isv = (r - pr) & 1;
+    }
+  }
+
 
   __device__ __forceinline__ void issue_slot(const TaskView& v, int r, int slot) {
     unsigned char* dst = ring + slot * T::RUN;
     if (lane != 0) return;
-    const int id = v.ids[v.bw + 4 * (r >> 1)];
+    int j, isv;
+    run_of(v, r, j, isv);
+    r = isv;  // below, r & 1 tells V from K
+    const int id = v.ids[v.bw + T::NW * j];
     if constexpr (T::F8) {
       // the codes as one box; a K run brings the block's 32-byte scale record (K and V scales) along
       const int row = ((r & 1) ? p.layer_row0_v : p.layer_row0_k) + (id * p.num_kv_heads + v.g) * T::BOXROWS;
@@ -432,7 +461,9 @@ struct Streamer {
     if (!ok) return;
     cur_q_done = cur.nbw == 0;
     while (issued < T::NR && issued < runs(cur)) {
-      const int bpos = block_pos(cur, issued >> 1);
+      int jb, isv;
+      run_of(cur, issued, jb, isv);
+      const int bpos = block_pos(cur, jb);
       if (!(p.k_in != nullptr || p.late_wait || bpos + kBS <= cur.nst)) break;
       issue_slot(cur, issued, issued);
       ++issued;
@@ -467,6 +498,24 @@ __device__ __forceinline__ void stream_loop(const DecodeParams& p, const DecodeS
   int shares = 0;                  // shares this warp has handed to the combiner warp
   float* my_o = sm.sh_o + warp * T::OV * T::SHL;
   float2* my_ml = sm.sh_ml + warp * kHeadsTile;
+  // This lane's ldmatrix row offsets inside a ring slot, hoisted out of the block loop.  fp16: chunk c of a
+  // 64-value box sits at swz(r, c); the chunks 2x + hi of the four k-steps of one box differ only in x, and
+  // the next box adds 2048.  8-bit: one offset per 32 dims of codes.
+  uint32_t koff[4], voff[4];
+  uint32_t k8off[T::F8 ? D / 32 : 1], v8off[T::F8 ? D / 32 : 1];
+  {
+    const int kr = (lane & 7) + ((lane >> 3) & 1) * 8, vmat = lane >> 3, vr = (lane & 7) + ((vmat >> 1) << 3);
+#pragma unroll
+    for (int x4 = 0; x4 < 4; ++x4) {
+      koff[x4] = swz(kr, 2 * x4 + (lane >> 4));
+      voff[x4] = swz(vr, 2 * x4 + (vmat & 1));
+    }
+#pragma unroll
+    for (int i = 0; i < (T::F8 ? D / 32 : 1); ++i) {
+      k8off[i] = T::F8 ? swz8<D>(kr, 2 * i + (lane >> 4)) : 0u;
+      v8off[i] = T::F8 ? swz8<D>(vr, 2 * i + (vmat & 1)) : 0u;
+    }
+  }
   while (w.ok && w.cur.t >= 0) {
     const TaskView d = w.cur;
     w.task_start();
@@ -481,7 +530,122 @@ __device__ __forceinline__ void stream_loop(const DecodeParams& p, const DecodeS
       uint32_t qb[T::KS][2];
       w.load_q(qb);
 
-      for (int j = 0; j < d.nbw && w.ok; ++j) {
+      // ---- the lean blocks, two at a time: both blocks' scores, one softmax step for the pair (one max
+      // reduction, one rescale of O), then both blocks' products.  Their runs sit in the ring in that order. ----
+      int j = 0;
+      if constexpr (T::PAIRS) {
+        for (; j + 1 < d.nlean && w.ok; j += 2) {
+          float x[2][4];            // scaled scores: [block][key qh head h0, key qh h0 + 1, key qh + 8 h0, .. h0 + 1]
+          uint32_t evb[2][2];       // 8-bit: value scale bytes of keys qh, qh + 8
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t kb = w.wait_run();
+            if (!w.ok) break;
+            float ks0 = p.scale_log2, ks1 = p.scale_log2;
+            if constexpr (T::F8) {
+              const unsigned char* rec = w.run_scales();
+              ks0 *= dev::scale_of_byte(rec[qh]);
+              ks1 *= dev::scale_of_byte(rec[qh + 8]);
+              evb[u][0] = rec[16 + qh];
+              evb[u][1] = rec[24 + qh];
+#pragma unroll
+              for (int i = 0; i < D / 32; ++i) {
+                uint32_t r[4];
+                dev::ldsm_x4(kb + k8off[i], r);
+                uint32_t a0[4], a1[4];
+                dev::e4m3x4_to_f16x2x2(r[0], a0[0], a0[2]);
+                dev::e4m3x4_to_f16x2x2(r[1], a0[1], a0[3]);
+                dev::e4m3x4_to_f16x2x2(r[2], a1[0], a1[2]);
+                dev::e4m3x4_to_f16x2x2(r[3], a1[1], a1[3]);
+                dev::mma_16816(sc, a0, qb[2 * i][0], qb[2 * i][1]);
+                dev::mma_16816(sd, a1, qb[2 * i + 1][0], qb[2 * i + 1][1]);
+              }
+            } else {
+#pragma unroll
+              for (int ks = 0; ks < T::KS; ++ks) {
+                uint32_t a[4];
+                dev::ldsm_x4(kb + koff[ks & 3] + (ks >> 2) * 2048, a);
+                dev::mma_16816((ks & 1) ? sd : sc, a, qb[ks][0], qb[ks][1]);
+              }
+            }
+            x[u][0] = (sc[0] + sd[0]) * ks0;
+            x[u][1] = (sc[1] + sd[1]) * ks0;
+            x[u][2] = (sc[2] + sd[2]) * ks1;
+            x[u][3] = (sc[3] + sd[3]) * ks1;
+            w.release_run();
+          }
+          if (!w.ok) break;
+          // ---- one online-softmax step for the pair (log2 domain) ----
+          float b0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
+          float b1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
+#pragma unroll
+          for (int m = 4; m < 32; m <<= 1) {
+            b0 = fmaxf(b0, __shfl_xor_sync(0xffffffffu, b0, m));
+            b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, m));
+          }
+          const float n0 = fmaxf(m0, b0), n1 = fmaxf(m1, b1);
+          const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+          m0 = n0;
+          m1 = n1;
+          float pw[2][4];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            pw[u][0] = exp2f(x[u][0] - n0);
+            pw[u][1] = exp2f(x[u][1] - n1);
+            pw[u][2] = exp2f(x[u][2] - n0);
+            pw[u][3] = exp2f(x[u][3] - n1);
+          }
+          l0 = l0 * a0 + ((pw[0][0] + pw[0][2]) + (pw[1][0] + pw[1][2]));
+          l1 = l1 * a1 + ((pw[0][1] + pw[0][3]) + (pw[1][1] + pw[1][3]));
+#pragma unroll
+          for (int mt = 0; mt < T::MT; ++mt) {
+            o[mt][0] *= a0;
+            o[mt][1] *= a1;
+            o[mt][2] *= a0;
+            o[mt][3] *= a1;
+          }
+          // ---- O^T[d x 8 heads] += V^T P^T for both blocks ----
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            float s0 = 1.f, s1 = 1.f;
+            if constexpr (T::F8) {  // the value scale of each key rides on its weight (an exact power of two)
+              s0 = dev::scale_of_byte(evb[u][0]);
+              s1 = dev::scale_of_byte(evb[u][1]);
+            }
+            const __half2 pk0 = __floats2half2_rn(pw[u][0] * s0, pw[u][1] * s0);
+            const __half2 pk1 = __floats2half2_rn(pw[u][2] * s1, pw[u][3] * s1);
+            const uint32_t pb0 = dev::movmatrix_t(*reinterpret_cast<const uint32_t*>(&pk0));
+            const uint32_t pb1 = dev::movmatrix_t(*reinterpret_cast<const uint32_t*>(&pk1));
+            const uint32_t vb = w.wait_run();
+            if (!w.ok) break;
+            if constexpr (T::F8) {
+#pragma unroll
+              for (int i = 0; i < D / 32; ++i) {
+                uint32_t r[4];
+                dev::ldsm_x4_t(vb + v8off[i], r);
+                uint32_t ae[4], ao[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dev::e4m3x4_to_f16x2x2(__byte_perm(r[q], 0, 0x3120), ae[q], ao[q]);
+                dev::mma_16816(o[2 * i], ae, pb0, pb1);
+                dev::mma_16816(o[2 * i + 1], ao, pb0, pb1);
+              }
+            } else {
+#pragma unroll
+              for (int mt = 0; mt < T::MT; ++mt) {
+                uint32_t a[4];
+                dev::ldsm_x4_t(vb + voff[mt & 3] + (mt >> 2) * 2048, a);
+                dev::mma_16816(o[mt], a, pb0, pb1);
+              }
+            }
+            w.release_run();
+          }
+          w.prefetch_q();  // the next task's q, once the scheduler has published it
+        }
+      }
+      // ---- the rest one by one: an odd lean block, then the blocks holding the context's end or rows of
+      // this pass (masking, the fused append's rows from the inputs, the token's own write to the cache) ----
+      for (; j < d.nbw && w.ok; ++j) {
         const int bpos = w.block_pos(d, j);  // the block's first position
         const int ntok = min(kBS, d.ctx - bpos);
         // fused append: positions ov0 .. bpos + ntok - 1 of the block are this pass's tokens; their rows
