@@ -50,7 +50,7 @@ CONFIGS = {
 # DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
 # source they were taken on and the cache format; reported as null once the source changes.
-TRAFFIC = {"fca057a257e4/fp16/qwen_decode": 142.56e6,   # profiles/decode_kernel_qwen_decode.md
+TRAFFIC = {"fcacad5de686/fp16/qwen_decode": 142.52e6,   # profiles/decode_kernel_qwen_decode.md
            "fca057a257e4/e4m3/qwen_decode": 72.05e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
 
 FALLBACK_HBM_GBS = 6800.0
@@ -676,10 +676,13 @@ def run_sched_trace(args, rank, world, local):
 
 def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_bytes, steps):
     """The same metric end to end through the public calls: every step copies the pass's metadata and every
-    layer's q/k/v from pinned host memory and reads every layer's output back.  Layer l + 1's inputs go up on
-    a copy stream while layer l attends, and layer l's output comes down on another while layer l + 1 runs;
-    the step (copies, events and library calls) is captured as one CUDA graph, as the device-resident timing
-    is (--eager: issued call by call)."""
+    layer's q/k/v from pinned host memory and reads every layer's output back.  The copies run beside the
+    attention on two copy streams and the compute stream waits only twice, so consecutive layers keep their
+    programmatic-dependent-launch overlap: the first layers' inputs go up before the plan, the rest on the
+    upload stream while those layers run (the compute stream waits for them once, before the first layer that
+    needs them); the outputs come down in quarters, each while the next quarter is computed, the last one
+    after the last layer.  The step (copies, events and library calls) is captured as one CUDA graph, as the
+    device-resident timing is (--eager: issued call by call)."""
     dev = stream.device
     L = len(layers)
     h_q = torch.stack([q.cpu() for q in qs]).pin_memory()
@@ -697,8 +700,12 @@ def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_
     h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_bt, h_ctx, h_qsl, h_slots))
     d2h = h_out.numel() * h_out.element_size()
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in layers]
-    ev_done = [torch.cuda.Event() for _ in layers]
+    ev_up = torch.cuda.Event()
+    head = max(1, min(L, (L + 7) // 8))   # layers whose inputs go up before the step starts
+    # outputs come down in quarters: each quarter's copy starts, on the download stream, once its last layer
+    # is done, while the next quarter runs; only the last quarter's copy follows the last layer
+    cuts = sorted({(L * c) // 4 for c in range(1, 4)} - {0, L})
+    ev_cut = [torch.cuda.Event() for _ in cuts]
 
     def one(main, step):
         with torch.cuda.stream(main):
@@ -706,26 +713,35 @@ def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_
             ds.context_lens.copy_(h_ctx, non_blocking=True)
             ds.query_start_loc.copy_(h_qsl, non_blocking=True)
             ds.slot_mapping.copy_(h_slots, non_blocking=True)
+            d_q[:head].copy_(h_q[:head], non_blocking=True)
+            d_k[:head].copy_(h_k[:head], non_blocking=True)
+            d_v[:head].copy_(h_v[:head], non_blocking=True)
         up.wait_stream(main)      # the previous step has read its inputs
         down.wait_stream(main)
         with torch.cuda.stream(up):
-            for i in range(L):
-                d_q[i].copy_(h_q[i], non_blocking=True)
-                d_k[i].copy_(h_k[i], non_blocking=True)
-                d_v[i].copy_(h_v[i], non_blocking=True)
-                ev_in[i].record(up)
+            d_q[head:].copy_(h_q[head:], non_blocking=True)
+            d_k[head:].copy_(h_k[head:], non_blocking=True)
+            d_v[head:].copy_(h_v[head:], non_blocking=True)
+            ev_up.record(up)
         step.plan()
         for i, layer in enumerate(layers):
-            main.wait_event(ev_in[i])
+            if i == head:
+                main.wait_event(ev_up)
+            if i in cuts:
+                c = cuts.index(i)
+                lo = cuts[c - 1] if c else 0
+                ev_cut[c].record(main)
+                down.wait_event(ev_cut[c])
+                with torch.cuda.stream(down):
+                    h_out[lo:i].copy_(d_out[lo:i], non_blocking=True)
             if step.fused:
                 step.attention_append(i, layer)
             else:
                 step.append(i, layer)
                 step.attention(i, layer)
-            ev_done[i].record(main)
-            down.wait_event(ev_done[i])
-            with torch.cuda.stream(down):
-                h_out[i].copy_(d_out[i], non_blocking=True)
+        tail = cuts[-1] if cuts else 0
+        with torch.cuda.stream(main):
+            h_out[tail:].copy_(d_out[tail:], non_blocking=True)
         main.wait_stream(up)
         main.wait_stream(down)
 
@@ -759,8 +775,9 @@ def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_
     ms = e0.elapsed_time(e1) / n
     return {"value": step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
-            "copies": "per layer on two copy streams, overlapped with the attention of the neighbouring layers"
-                      + ("" if args.eager else "; the step captured as one CUDA graph")}
+            "copies": f"inputs of the first {head} layer(s) before the step, the rest on a copy stream beside them; "
+                      "outputs in quarters on a second copy stream, each while the next quarter runs, the last "
+                      "after the last layer" + ("" if args.eager else "; the step captured as one CUDA graph")}
 
 
 def main():
