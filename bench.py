@@ -43,6 +43,7 @@ from continuous_batching_paged_ragged_gb300 import pkv, synth, workload  # noqa:
 CONFIGS = {
     "qwen_decode": lambda: synth.qwen_decode(0),
     "mixed_step": lambda: synth.mixed_step(0),
+    "prefill_8k": lambda: synth.prefill_chunk(0),
     "long_gqa": lambda: synth.long_gqa(0),
     "tiny_decode": lambda: synth.tiny_decode(0),
 }
@@ -226,12 +227,16 @@ def max_over_ranks(x: float, world: int) -> float:
 # CPU oracle legs (cpu_baseline and --impl reference)
 # ----------------------------------------------------------------------------------------------------
 
-def oracle_inputs(batch: synth.StepBatch, layer: int, rows):
+def oracle_inputs(batch: synth.StepBatch, layer: int, rows, max_queries: int = 0):
+    """Per row: (q, k, v) for the oracle; with max_queries > 0 a longer chunk keeps only its last max_queries
+    queries (each still over its whole causal context)."""
     s = batch.shape
     items = []
     for b in rows:
         req, ctx = int(batch.req_ids[b]), int(batch.context_lens[b])
         ql = int(batch.q_lens[b])
+        if max_queries > 0:
+            ql = min(ql, max_queries)
         k, v = synth.sequence_kv(batch.seed, layer, req, ctx, s.num_kv_heads, s.head_dim)
         q = synth.token_values(synth.KIND_Q, batch.seed, layer, np.full(ql, req), np.arange(ctx - ql, ctx),
                                s.num_q_heads, s.head_dim)
@@ -239,19 +244,21 @@ def oracle_inputs(batch: synth.StepBatch, layer: int, rows):
     return items
 
 
-def oracle_bytes(batch, rows):
+def oracle_bytes(batch, rows, max_queries: int = 0):
     s = batch.shape
     ctx = batch.context_lens[rows].astype(np.int64)
     ql = batch.q_lens[rows].astype(np.int64)
+    if max_queries > 0:
+        ql = np.minimum(ql, max_queries)
     return (2 * int(ctx.sum()) * s.num_kv_heads * s.head_dim * 2 + int(ql.sum()) * s.num_q_heads * s.head_dim * 4
             + 4 * int(((ctx + 15) // 16).sum())), int(ctx.sum())
 
 
-def cpu_baseline(batch, budget_s: float = 12.0, kv8: bool = False):
+def cpu_baseline(batch, budget_s: float = 12.0, kv8: bool = False, max_queries: int = 0):
     import oracle
     rows = list(range(batch.num_seqs))
-    items = oracle_inputs(batch, 0, rows)
-    nbytes, nctx = oracle_bytes(batch, rows)
+    items = oracle_inputs(batch, 0, rows, max_queries)
+    nbytes, nctx = oracle_bytes(batch, rows, max_queries)
     if kv8:   # attention over the dequantized 8-bit cache (quantized once, outside the timing)
         from oracle import fp8
         items = [(q, fp8.dequantize_rows(*fp8.quantize_rows(k)), fp8.dequantize_rows(*fp8.quantize_rows(v)))
@@ -268,8 +275,9 @@ def cpu_baseline(batch, budget_s: float = 12.0, kv8: bool = False):
             break
     return {"value": nbytes * reps / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "ctx_tokens_per_s": nctx * reps / el,
-            "sample": f"layer 0 of {batch.shape.num_layers}, all {batch.num_seqs} rows, repeated {reps}x "
-                      f"({el:.1f} s, fp64 NumPy, 1 thread of {os.cpu_count()} host cores)"}
+            "sample": f"layer 0 of {batch.shape.num_layers}, all {batch.num_seqs} rows"
+                      + (f" (a chunk's last {max_queries} queries at most)" if max_queries else "")
+                      + f", repeated {reps}x ({el:.1f} s, fp64 NumPy, 1 thread of {os.cpu_count()} host cores)"}
 
 
 def run_reference(args, rank, world):
@@ -321,7 +329,7 @@ def run_reference(args, rank, world):
 # GPU path
 # ----------------------------------------------------------------------------------------------------
 
-def measure(args, batch, rank, world, local, steps, warmup, cpu_budget_s=12.0, with_e2e=True):
+def measure(args, batch, rank, world, local, steps, warmup, cpu_budget_s=12.0, with_e2e=True, cpu_max_queries=0):
     """One workload's timed step (plan + every layer's append and attention, as one CUDA graph unless
     --eager); returns the JSON fields (rank 0) or None."""
     dev = torch.device("cuda", local)
@@ -470,7 +478,7 @@ def measure(args, batch, rank, world, local, steps, warmup, cpu_budget_s=12.0, w
         line["lower_bounds_ms_per_step"] = {"hbm": hbm_ms, "tensor": tensor_ms, "sum": hbm_ms + tensor_ms,
                                             "max": max(hbm_ms, tensor_ms), "measured": ms}
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(batch, budget_s=cpu_budget_s, kv8=kv8)
+        line["cpu_baseline"] = cpu_baseline(batch, budget_s=cpu_budget_s, kv8=kv8, max_queries=cpu_max_queries)
     return line
 
 
@@ -484,9 +492,11 @@ def run_pkv(args, rank, world, local):
     if args.config == "qwen_decode" and not args.layers and not args.no_configs and world == 1:
         # the other workloads of the pages, each as its own timed region with its clocks and oracle baseline
         extra = {}
-        for name, steps in (("mixed_step", min(args.steps, 100)), ("long_gqa", min(args.steps, 20))):
+        for name, steps, cpu_q in (("mixed_step", min(args.steps, 100), 0), ("prefill_8k", min(args.steps, 20), 256),
+                                   ("long_gqa", min(args.steps, 20), 0)):
             t0 = time.perf_counter()
-            sub = measure(args, CONFIGS[name](), rank, world, local, max(steps, 3), args.warmup, cpu_budget_s=4.0)
+            sub = measure(args, CONFIGS[name](), rank, world, local, max(steps, 3), args.warmup, cpu_budget_s=4.0,
+                          cpu_max_queries=cpu_q)
             if sub is not None:
                 sub["wall_s"] = time.perf_counter() - t0
                 extra[name] = sub

@@ -555,7 +555,8 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
   p.num_slots = (int64_t)c.num_blocks * c.block_size;
   // TMA rows per (layer, K/V) pool: one per token (fp16) or per 128 code bytes (8-bit)
   const int64_t toks_per_pool = (int64_t)c.num_blocks * c.num_kv_heads * c.block_size;
-  const int rows_per_pool = (int)(f8 ? toks_per_pool * c.head_dim / 128 : toks_per_pool);
+  // (the 8-bit d 256 map addresses tokens, with the two halves of a key as its middle dimension)
+  const int rows_per_pool = (int)(f8 && c.head_dim != 256 ? toks_per_pool * c.head_dim / 128 : toks_per_pool);
   p.layer_row0_k = (layer * 2) * rows_per_pool;
   p.layer_row0_v = (layer * 2 + 1) * rows_per_pool;
   p.max_blocks = max_blocks;

@@ -147,6 +147,7 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 // slot (chunk % 8) XOR (R % 8)).
 template <int D>
 __device__ __forceinline__ uint32_t swz8(int r, int c) {
+  if constexpr (D == 256) return swz(r, c);  // one 16-key x 128-byte box per half of the key (fp16's layout)
   const int x = r * D + 16 * c, R = x >> 7;
   return (uint32_t)(R * 128 + ((((x >> 4) & 7) ^ (R & 7)) << 4));
 }
@@ -325,9 +326,15 @@ struct Streamer {
     const int id = v.ids[v.bw + T::NW * j];
     if constexpr (T::F8) {
       // the codes as one box; a K run brings the block's 32-byte scale record (K and V scales) along
-      const int row = ((r & 1) ? p.layer_row0_v : p.layer_row0_k) + (id * p.num_kv_heads + v.g) * T::BOXROWS;
       dev::mbar_arrive_expect_tx(&bars[slot], T::RUN + ((r & 1) ? 0 : T::SCL));
-      dev::tma_load_2d(dst, &p.kv_map, 0, row, &bars[slot], pol);
+      if constexpr (D == 256) {  // two boxes: the keys' first and second 128 code bytes (rows are tokens)
+        const int tok = ((r & 1) ? p.layer_row0_v : p.layer_row0_k) + (id * p.num_kv_heads + v.g) * kBS;
+        dev::tma_load_3d(dst, &p.kv_map, 0, 0, tok, &bars[slot], pol);
+        dev::tma_load_3d(dst + 2048, &p.kv_map, 0, 1, tok, &bars[slot], pol);
+      } else {
+        const int row = ((r & 1) ? p.layer_row0_v : p.layer_row0_k) + (id * p.num_kv_heads + v.g) * T::BOXROWS;
+        dev::tma_load_2d(dst, &p.kv_map, 0, row, &bars[slot], pol);
+      }
       if (!(r & 1))
         dev::bulk_g2s(scl + slot * T::SCL, p.scales + ((size_t)id * p.num_kv_heads + v.g) * T::SCL, T::SCL,
                       &bars[slot], pol);

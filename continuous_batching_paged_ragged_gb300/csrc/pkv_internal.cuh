@@ -51,7 +51,7 @@ struct MetaCheck {
 struct pkv_pool {
   // The cache as the TMA engine sees it, 128-byte swizzle: fp16, rows of head_dim values (one per (layer,
   // K/V, block, KV head, slot)); 8-bit, rows of 128 code bytes (a (block, KV head) run is 16*head_dim/128
-  // consecutive rows).
+  // consecutive rows), at head_dim 256 a 3-D map (128 code bytes, the key's half, the key).
   CUtensorMap kv_map;
   pkv_config cfg;
   char* base = nullptr;        // device: cache (8-bit: codes, then scales), then the status area
@@ -232,6 +232,17 @@ __device__ __forceinline__ void bulk_g2s_plain(void* dst_smem, const void* src_g
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(smem_addr(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
                : "memory");
+}
+
+// 3-D tiled TMA load of a box of `map` at element coordinates (x, y, z) into shared memory.
+__device__ __forceinline__ void tma_load_3d(void* dst_smem, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      ::"r"(smem_addr(dst_smem)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)),
+      "l"(policy)
+      : "memory");
 }
 
 // 2-D tiled TMA load of a box of `map` at element coordinates (x, y) into shared memory.

@@ -56,7 +56,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 // The cache seen by the TMA engine, 128-byte swizzle throughout.  fp16: rows of head_dim values, one row per
 // (layer, K/V, block, KV head, slot), boxes of 16 rows x 64 values (128 bytes), so a (block, KV head) run of
 // K or V is head_dim / 64 boxes.  8-bit: the codes as rows of 128 bytes; a run (16 * head_dim bytes) is
-// one box of 16 * head_dim / 128 rows.
+// one box of 16 * head_dim / 128 rows -- except at head_dim 256, where each half of a key's 256 code bytes is
+// its own box (16 keys x 128 bytes), as fp16 boxes are.
 static EncodeTiledFn tensor_map_encoder() {
   static EncodeTiledFn encode = nullptr;
   if (!encode) {
@@ -89,6 +90,20 @@ static pkv_status encode_kv_map(pkv_pool* p) {
   if (c.kv_dtype != PKV_KV_E4M3) return encode_f16_rows(&p->kv_map, p->base, toks, c.head_dim);
   EncodeTiledFn encode = tensor_map_encoder();
   if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (c.head_dim == 256) {
+    // a key's 256 code bytes as two 128-byte halves: one box per half (16 keys x 128 bytes), so that within
+    // a box key r is swizzle row r (two 128-byte rows per key would repeat the swizzle every four keys)
+    if (toks >= (1ull << 31)) return fail(PKV_ERR_UNSUPPORTED, "pool too large for 32-bit TMA coordinates");
+    cuuint64_t dims3[3] = {128u, 2u, (cuuint64_t)toks};
+    cuuint64_t strides3[2] = {128u, 256u};
+    cuuint32_t box3[3] = {128u, 1u, (cuuint32_t)c.block_size};
+    cuuint32_t estr3[3] = {1, 1, 1};
+    CUresult r = encode(&p->kv_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, p->base, dims3, strides3, box3, estr3,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
+    return PKV_OK;
+  }
   const uint64_t rows = toks * c.head_dim / 128;
   if (rows >= (1ull << 31)) return fail(PKV_ERR_UNSUPPORTED, "pool too large for 32-bit TMA row coordinates");
   cuuint64_t dims[2] = {128u, (cuuint64_t)rows};

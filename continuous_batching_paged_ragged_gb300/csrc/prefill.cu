@@ -28,6 +28,7 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "attn_common.cuh"
 
@@ -367,112 +368,120 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
       pf_wait(sh, &sh.s_done[wg], c & 1, p.err);
       dev::tc_fence_after();
       const int kb = j * kKeys;
-      const bool full = kb + kKeys - 1 <= lim;
-      // masked max of one 64-column half of raw scores (the scale is positive, so it commutes with max)
-      auto half_max = [&](const uint32_t (&s)[2][32], int h) {
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // Whether every valid row of the warp sees the whole tile (warp-uniform): the causal mask costs a
+      // compare and a select per score, so only the tiles that reach a row's diagonal take the masked code.
+      // Then every key of the tile is one of the item's (the TMA wrote it), and the warp's padding rows
+      // (zero q) score 0 on each.  A warp of padding rows alone keeps the mask (key 0 only).
+      const bool full = __any_sync(0xffffffffu, valid) && __all_sync(0xffffffffu, !valid || kb + kKeys - 1 <= lim);
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      auto tile = [&](auto full_tag) {
+        constexpr bool kFull = decltype(full_tag)::value;
+        // masked max of one 64-column half of raw scores (the scale is positive, so it commutes with max)
+        auto half_max = [&](const uint32_t (&s)[2][32], int h) {
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
+          for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float x = __uint_as_float(s[k][e]);
+              mx4[e & 3] = fmaxf(mx4[e & 3], (kFull || kb + 64 * h + 32 * k + e <= lim) ? x : -INFINITY);
+            }
+          return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+        };
+        // P = 2^(s * scale_log2 - m_ref) of one half as packed fp16; one FFMA and one MUFU per score
+        auto half_exp = [&](const uint32_t (&s)[2][32], int h, uint32_t (&pk)[32], float (&sum4)[4]) {
+          const float nm = -m_ref;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float x = __uint_as_float(s[k][e]);
-            mx4[e & 3] = fmaxf(mx4[e & 3], (full || kb + 64 * h + 32 * k + e <= lim) ? x : -INFINITY);
-          }
-        return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
-      };
-      // P = 2^(s * scale_log2 - m_ref) of one half as packed fp16; one FFMA and one MUFU per score
-      auto half_exp = [&](const uint32_t (&s)[2][32], int h, uint32_t (&pk)[32], float (&sum4)[4]) {
-        const float nm = -m_ref;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int k = 2 * e;  // key 64 h + k of the tile
-          float x0 = __uint_as_float(s[k >> 5][k & 31]), x1 = __uint_as_float(s[(k + 1) >> 5][(k + 1) & 31]);
-          if (!full) {
-            if (kb + 64 * h + k > lim) x0 = -INFINITY;
-            if (kb + 64 * h + k + 1 > lim) x1 = -INFINITY;
-          }
-          const float p0 = dev::ex2_approx(fmaf(x0, p.scale_log2, nm));
-          const float p1 = dev::ex2_approx(fmaf(x1, p.scale_log2, nm));
-          sum4[e & 3] += p0 + p1;
-          const __half2 hh = __floats2half2_rn(p0, p1);
-          pk[e] = *reinterpret_cast<const uint32_t*>(&hh);
-        }
-      };
-      auto load_half = [&](int h, uint32_t (&s)[2][32]) {
-        dev::tmem_ld32(tl + 64 * h, s[0]);
-        dev::tmem_ld32(tl + 64 * h + 32, s[1]);
-        dev::tmem_wait_ld();
-      };
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      // Common case (the reference is settled): one pass over S, both halves' P kept in registers and
-      // stored only once neither half moves the row max past the lazy threshold, so S is still intact
-      // for the two-pass path when one does.
-      bool done = false;
-      if (u > 0) {
-        uint32_t pk0[32], pk1[32];
-        bool ok;
-        {
-          uint32_t s[2][32];
-          load_half(0, s);
-          ok = !__any_sync(0xffffffffu, half_max(s, 0) > m_ref + kRescaleLog2);
-          if (ok) half_exp(s, 0, pk0, sum4);
-        }
-        if (ok) {
-          uint32_t s[2][32];
-          load_half(1, s);
-          ok = !__any_sync(0xffffffffu, half_max(s, 1) > m_ref + kRescaleLog2);
-          if (ok) half_exp(s, 1, pk1, sum4);
-        }
-        if (ok) {
-          dev::tmem_st32(tl, pk0);
-          dev::tmem_st32(tl + 32, pk1);
-          done = true;
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) sum4[i] = 0.f;
-        }
-      }
-      if (!done) {
-        // ---- two passes: the row max first (and, past the first tile, the lazy rescale), then P ----
-        float mx;
-        {
-          uint32_t s[2][32];
-          load_half(0, s);
-          mx = half_max(s, 0);
-          load_half(1, s);
-          mx = fmaxf(mx, half_max(s, 1));
-        }
-        if (u == 0) {
-          m_ref = mx;
-        } else {
-          const bool need = mx > m_ref + kRescaleLog2;
-          if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? exp2f(m_ref - mx) : 1.f;
-#pragma unroll
-            for (int k = 0; k < D / 32; ++k) {
-              uint32_t o[32];
-              dev::tmem_ld32(tl + 128 + 32 * k, o);
-              dev::tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              dev::tmem_st32(tl + 128 + 32 * k, o);
+            const int k = 2 * e;  // key 64 h + k of the tile
+            float x0 = __uint_as_float(s[k >> 5][k & 31]), x1 = __uint_as_float(s[(k + 1) >> 5][(k + 1) & 31]);
+            if constexpr (!kFull) {
+              if (kb + 64 * h + k > lim) x0 = -INFINITY;
+              if (kb + 64 * h + k + 1 > lim) x1 = -INFINITY;
             }
-            if (need) {
-              l *= alpha;
-              m_ref = mx;
+            const float p0 = dev::ex2_approx(fmaf(x0, p.scale_log2, nm));
+            const float p1 = dev::ex2_approx(fmaf(x1, p.scale_log2, nm));
+            sum4[e & 3] += p0 + p1;
+            const __half2 hh = __floats2half2_rn(p0, p1);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
+        };
+        auto load_half = [&](int h, uint32_t (&s)[2][32]) {
+          dev::tmem_ld32(tl + 64 * h, s[0]);
+          dev::tmem_ld32(tl + 64 * h + 32, s[1]);
+          dev::tmem_wait_ld();
+        };
+        // Common case (the reference is settled): one pass over S, both halves' P kept in registers and
+        // stored only once neither half moves the row max past the lazy threshold, so S is still intact
+        // for the two-pass path when one does.
+        bool done = false;
+        if (u > 0) {
+          uint32_t pk0[32], pk1[32];
+          bool ok;
+          {
+            uint32_t s[2][32];
+            load_half(0, s);
+            ok = !__any_sync(0xffffffffu, half_max(s, 0) > m_ref + kRescaleLog2);
+            if (ok) half_exp(s, 0, pk0, sum4);
+          }
+          if (ok) {
+            uint32_t s[2][32];
+            load_half(1, s);
+            ok = !__any_sync(0xffffffffu, half_max(s, 1) > m_ref + kRescaleLog2);
+            if (ok) half_exp(s, 1, pk1, sum4);
+          }
+          if (ok) {
+            dev::tmem_st32(tl, pk0);
+            dev::tmem_st32(tl + 32, pk1);
+            done = true;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sum4[i] = 0.f;
+          }
+        }
+        if (!done) {
+          // ---- two passes: the row max first (and, past the first tile, the lazy rescale), then P ----
+          float mx;
+          {
+            uint32_t s[2][32];
+            load_half(0, s);
+            mx = half_max(s, 0);
+            load_half(1, s);
+            mx = fmaxf(mx, half_max(s, 1));
+          }
+          if (u == 0) {
+            m_ref = mx;
+          } else {
+            const bool need = mx > m_ref + kRescaleLog2;
+            if (__any_sync(0xffffffffu, need)) {
+              const float alpha = need ? exp2f(m_ref - mx) : 1.f;
+#pragma unroll
+              for (int k = 0; k < D / 32; ++k) {
+                uint32_t o[32];
+                dev::tmem_ld32(tl + 128 + 32 * k, o);
+                dev::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                dev::tmem_st32(tl + 128 + 32 * k, o);
+              }
+              if (need) {
+                l *= alpha;
+                m_ref = mx;
+              }
             }
           }
-        }
-        // P over the first 64 columns of S: the first half's columns, already read when the second
-        // half is loaded
+          // P over the first 64 columns of S: the first half's columns, already read when the second
+          // half is loaded
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t s[2][32], pk[32];
-          load_half(h, s);
-          half_exp(s, h, pk, sum4);
-          dev::tmem_st32(tl + 32 * h, pk);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t s[2][32], pk[32];
+            load_half(h, s);
+            half_exp(s, h, pk, sum4);
+            dev::tmem_st32(tl + 32 * h, pk);
+          }
         }
-      }
+      };
+      if (full) tile(std::true_type{}); else tile(std::false_type{});
       l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       // ---- the item's last tile: V rows past its keys hold stale bytes; zero them (0 * NaN = NaN) ----
       if (wg == it.zfill_wg && j == it.n_all - 1) {

@@ -239,6 +239,13 @@ def mixed_step(seed: int = 0) -> StepBatch:
     return _make_batch("mixed_step", Shape(28, 12, 2, 128), cached, q_lens, seed)
 
 
+def prefill_chunk(seed: int = 0, q_len: int = 8192, cached: int = 0) -> StepBatch:
+    """Qwen2.5-1.5B shape, one row whose pass is a single chunk of q_len new tokens (the whole per-pass token
+    budget of 8,192 by default) on top of `cached` tokens."""
+    return _make_batch("prefill_8k" if (q_len, cached) == (8192, 0) else "prefill_chunk", Shape(28, 12, 2, 128),
+                       [cached], [q_len], seed)
+
+
 def long_gqa(seed: int = 0, cached_len: int = 262144, num_seqs: int = 4, num_layers: int = 16) -> StepBatch:
     """16 KV layers, 16 q / 4 KV heads, d=256; 4 rows of 262,144 cached tokens, one query each."""
     return _make_batch("long_gqa", Shape(num_layers, 16, 4, 256), [cached_len] * num_seqs,

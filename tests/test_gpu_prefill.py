@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from continuous_batching_paged_ragged_gb300 import synth
 from helpers_gpu import assert_close, oracle_row, row_slice, run_batch
 
@@ -83,3 +84,24 @@ def test_prefill_split_items_many_entries_per_cta(cuda, built):
     for layer in (0, 1):
         for b in range(batch.num_seqs):
             assert_close(row_slice(batch, outs[layer], b), oracle_row(batch, layer, b), f"layer {layer} row {b}")
+
+
+def test_prefill_8k_chunk_sampled_positions(cuda, built):
+    """One row whose pass is a whole 8,192-token chunk (the per-pass token budget) on an empty cache: 392 work
+    items, the longer ones split in two key ranges.  The oracle runs query by query at sampled positions (tile
+    and item boundaries, both split halves, the last position), each over its own causal prefix."""
+    batch = synth.prefill_chunk(0)
+    batch.shape = synth.Shape(1, batch.shape.num_q_heads, batch.shape.num_kv_heads, batch.shape.head_dim)
+    s = batch.shape
+    pool, ds, outs = run_batch(batch, [0])
+    out = row_slice(batch, outs[0], 0)
+    req, ctx = int(batch.req_ids[0]), int(batch.context_lens[0])
+    k, v = synth.sequence_kv(batch.seed, 0, req, ctx, s.num_kv_heads, s.head_dim)
+    rng = np.random.Generator(np.random.PCG64(88))
+    picks = {0, 1, 20, 21, 41, 42, 127, 128, 129, 1023, 1024, 4095, 4096, 6000, 8150, 8190, 8191}
+    picks |= set(int(x) for x in rng.integers(0, ctx, size=12))
+    for i in sorted(picks):
+        q = synth.token_values(synth.KIND_Q, batch.seed, 0, np.array([req]), np.array([i]), s.num_q_heads,
+                               s.head_dim)
+        ref = oracle.attention_row(q, k[: i + 1], v[: i + 1])
+        assert_close(out[i : i + 1], ref, f"position {i}")
