@@ -162,6 +162,7 @@ struct PlanParams {
   int num_seqs, num_tokens, max_ctx, split_blocks, num_kv_heads;
   int prefill_min_qlen;  // rows with at least this many new tokens become prefill items (0: none)
   int prefill_pos;       // query positions per prefill item
+  int prefill_ctas;      // CTAs of the prefill tile kernel at most (the SM count)
   int32_t* tok_row;
   int32_t* tok_ctx;
   int32_t* merge_cnt;
@@ -196,6 +197,21 @@ __device__ __forceinline__ void for_row_items(const PlanParams& p, int b, F fn) 
 
 // K/V tiles of the two chunks of an item of n tiles (the first chunk takes the extra tile).
 __device__ __forceinline__ int split_first(int n) { return (n + 1) / 2; }
+
+// K/V tiles of all of row b's prefill items, over every KV head.
+__device__ __forceinline__ int64_t row_prefill_tiles(const PlanParams& p, int b) {
+  int64_t t = 0;
+  for_row_items(p, b, [&](int n, int, int, int) { t += n; });
+  return t * p.num_kv_heads;
+}
+
+// An item runs as two chunks of keys when it is long (more than kPrefillSplitTiles tiles) and its row alone
+// cannot keep every CTA busy for as long as the item takes (row tiles / CTAs < the item's tiles): a long
+// chunk on a short prompt splits, the items of a chunk that fills the GPU by itself do not (no handshake).
+// It depends on the row and the device alone, so a row's result does not depend on the rest of the batch.
+__device__ __forceinline__ bool split_item(const PlanParams& p, int n, int64_t row_tiles) {
+  return n > kPrefillSplitTiles && (int64_t)n * p.prefill_ctas > row_tiles;
+}
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) {
   __shared__ int warp_sums[32];
@@ -267,15 +283,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
 
   // ---- prefill work entries, bucketed by K/V tile count, longest first; long items in two chunks ----
   auto bucket_of = [](int cost) { return kPrefillBuckets - 1 - min(cost, kPrefillBuckets - 1); };
-  for (int b = threadIdx.x; b < p.num_seqs; b += blockDim.x)
+  for (int b = threadIdx.x; b < p.num_seqs; b += blockDim.x) {
+    const int64_t row_tiles = row_prefill_tiles(p, b);
     for_row_items(p, b, [&](int n, int, int, int) {
-      if (n > kPrefillSplitTiles) {
+      if (split_item(p, n, row_tiles)) {
         atomicAdd(&hist[bucket_of(split_first(n))], p.num_kv_heads);
         atomicAdd(&hist[bucket_of(n - split_first(n))], p.num_kv_heads);
       } else {
         atomicAdd(&hist[bucket_of(n)], p.num_kv_heads);
       }
     });
+  }
   __syncthreads();
   int n_items = 0;
   for (int base = 0; base < kPrefillBuckets; base += blockDim.x) {
@@ -288,9 +306,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     n_items += total;
     __syncthreads();
   }
-  for (int b = threadIdx.x; b < p.num_seqs; b += blockDim.x)
+  for (int b = threadIdx.x; b < p.num_seqs; b += blockDim.x) {
+    const int64_t row_tiles = row_prefill_tiles(p, b);
     for_row_items(p, b, [&](int n, int npos, int t0, int w) {
-      const bool split = n > kPrefillSplitTiles;
+      const bool split = split_item(p, n, row_tiles);
       const int slot = split ? atomicAdd(&n_slots, p.num_kv_heads) : -1;
       for (int chunk = 0; chunk < (split ? 2 : 1); ++chunk) {
         const int cost = split ? (chunk == 0 ? split_first(n) : n - split_first(n)) : n;
@@ -301,6 +320,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
         }
       }
     });
+  }
 
   // ---- 8-bit cache: the prefill rows' blocks, numbered row after row in the fp16 shadow ----
   if (p.pf_base != nullptr) {
@@ -424,6 +444,7 @@ static cudaError_t launch_plan(pkv_pool* pool, char* ws, const WsLayout& w, cons
   p.num_kv_heads = c.num_kv_heads;
   p.prefill_min_qlen = w.prefill_min_qlen;
   p.prefill_pos = w.prefill_pos;
+  p.prefill_ctas = pool->num_sms;
   p.tok_row = reinterpret_cast<int32_t*>(ws + w.tok_row);
   p.tok_ctx = reinterpret_cast<int32_t*>(ws + w.tok_ctx);
   p.merge_cnt = reinterpret_cast<int32_t*>(ws + w.merge_cnt);
@@ -534,7 +555,7 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
                                    const FusedAppend& fa = FusedAppend()) {
   const pkv_config& c = pool->cfg;
   DecodeParams p;
-  p.kv_map = pool->kv_map;
+  p.kv_map = c.kv_dtype == PKV_KV_E4M3 ? pool->kv_map : pool->run_map;  // fp16: one copy per run
   p.q = static_cast<const __half*>(q);
   p.block_tables = block_tables;
   p.qsl = qsl;

@@ -20,7 +20,8 @@ constexpr int kPrefillRows = 128;  // MMA rows of a prefill Q tile: (query posit
 constexpr int kPrefillKeys = 128;  // keys per K/V tile
 constexpr int kPrefillBuckets = 1024;
 // An item whose keys span more K/V tiles than this runs as two chunks of keys (split-KV) that the
-// second chunk to finish merges; the split depends on the row alone.
+// second chunk to finish merges, when its row alone cannot keep every CTA busy for the item's length; the
+// split depends on the row (and the SM count) alone.
 constexpr int kPrefillSplitTiles = 24;
 
 // Query positions per prefill Q tile: the G query heads of a KV head are packed into the MMA rows.

@@ -49,7 +49,6 @@ struct DecodeTraits {
   static constexpr int NTHREADS = (NW + 2) * 32;
   static constexpr bool F8 = KV == kKvE4M3;
   static constexpr int RUN = kBS * D * (F8 ? 1 : 2);  // one (block, KV head) run of K or V
-  static constexpr int BOXES = F8 ? 1 : D / 64;    // TMA boxes per run: fp16 16 x 64 values, 8-bit one box
   static constexpr int BOXROWS = kBS * D / 128;    // 8-bit: 128-byte rows of a run (its box height)
   static constexpr int SCL = F8 ? 32 : 0;          // 8-bit: scale record per slot (the K and V scales of a block)
   static constexpr int RING = F8 ? 16 : PKV_DECODE_RING(D);  // 8-bit: as many slots as fit, up to 16
@@ -99,7 +98,7 @@ struct DecodeTraits {
 };
 
 struct DecodeParams {
-  CUtensorMap kv_map;  // the pool as TMA rows (64-byte aligned: first member)
+  CUtensorMap kv_map;  // fp16: the pool as whole runs; 8-bit: as rows of codes (64-byte aligned: first member)
   const __half* q;
   const int32_t* block_tables;
   const int32_t* qsl;  // query_start_loc
@@ -341,8 +340,7 @@ struct Streamer {
     } else {
       const int row = ((r & 1) ? p.layer_row0_v : p.layer_row0_k) + (id * p.num_kv_heads + v.g) * kBS;
       dev::mbar_arrive_expect_tx(&bars[slot], T::RUN);
-#pragma unroll
-      for (int b = 0; b < T::BOXES; ++b) dev::tma_load_2d(dst + b * 2048, &p.kv_map, b * 64, row, &bars[slot], pol);
+      dev::tma_load_3d(dst, &p.kv_map, 0, row, 0, &bars[slot], pol);  // the run's D / 64 sub-tiles, one copy
     }
   }
   // Task kk's q into the warp's q buffer (which must be free).

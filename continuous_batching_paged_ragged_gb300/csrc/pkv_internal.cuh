@@ -53,6 +53,9 @@ struct pkv_pool {
   // K/V, block, KV head, slot)); 8-bit, rows of 128 code bytes (a (block, KV head) run is 16*head_dim/128
   // consecutive rows), at head_dim 256 a 3-D map (128 code bytes, the key's half, the key).
   CUtensorMap kv_map;
+  // fp16: the same cache as whole (block, KV head) runs of K or V, one box of 16 rows x head_dim values laid
+  // out as head_dim / 64 swizzled 2 KB sub-tiles (the 2-D map's boxes side by side): one copy per run
+  CUtensorMap run_map;
   pkv_config cfg;
   char* base = nullptr;        // device: cache (8-bit: codes, then scales), then the status area
   size_t cache_bytes = 0;      // bytes before the status area
@@ -73,6 +76,10 @@ namespace pkv {
 // 2-D TMA map of `rows` rows of head_dim fp16 values at `base`: boxes of 16 rows x 64 values, 128-byte swizzle
 // (the layout of an fp16 pool, and of the 8-bit cache's fp16 shadow).
 pkv_status encode_f16_rows(CUtensorMap* map, void* base, uint64_t rows, int head_dim);
+// 3-D TMA map of the same rows whose box is a whole run: 16 rows x head_dim values, stored as head_dim / 64
+// sub-tiles of 16 rows x 64 values (128-byte swizzle), sub-tile h at 2048 h bytes -- the layout of head_dim / 64
+// boxes of the 2-D map side by side, in one copy.
+pkv_status encode_f16_runs(CUtensorMap* map, void* base, uint64_t rows, int head_dim);
 // The PKV_VALIDATE=1 host check of a call's device metadata (a no-op otherwise); null pointers are skipped.
 // When `check` is given and the check ran, it receives a hash of the context_lens and query_start_loc contents.
 pkv_status validate_metadata(const pkv_pool* pool, const int32_t* block_tables, int32_t max_blocks,

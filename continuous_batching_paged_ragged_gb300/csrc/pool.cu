@@ -84,10 +84,32 @@ pkv_status encode_f16_rows(CUtensorMap* map, void* base, uint64_t rows, int head
   return PKV_OK;
 }
 
+pkv_status encode_f16_runs(CUtensorMap* map, void* base, uint64_t rows, int head_dim) {
+  EncodeTiledFn encode = tensor_map_encoder();
+  if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (rows >= (1ull << 31)) return fail(PKV_ERR_UNSUPPORTED, "too many rows for 32-bit TMA row coordinates");
+  // dimensions: 64 values of a 64-value column group, the row, the column group (its stride is 128 bytes,
+  // below the row's: the box walks a group's 16 rows before the next group, as the 2-D boxes do)
+  cuuint64_t dims[3] = {64u, (cuuint64_t)rows, (cuuint64_t)(head_dim / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, 128u};
+  cuuint32_t box[3] = {64u, 16u, (cuuint32_t)(head_dim / 64)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the run map: " + std::to_string((int)r));
+  return PKV_OK;
+}
+
 static pkv_status encode_kv_map(pkv_pool* p) {
   const pkv_config& c = p->cfg;
   const uint64_t toks = (uint64_t)c.num_layers * 2 * c.num_blocks * c.num_kv_heads * c.block_size;
-  if (c.kv_dtype != PKV_KV_E4M3) return encode_f16_rows(&p->kv_map, p->base, toks, c.head_dim);
+  if (c.kv_dtype != PKV_KV_E4M3) {
+    const pkv_status st = encode_f16_rows(&p->kv_map, p->base, toks, c.head_dim);
+    if (st != PKV_OK) return st;
+    return encode_f16_runs(&p->run_map, p->base, toks, c.head_dim);
+  }
   EncodeTiledFn encode = tensor_map_encoder();
   if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   if (c.head_dim == 256) {

@@ -39,11 +39,12 @@ namespace {
 constexpr int kKSlots = 3;             // K ring depth
 constexpr int kVSlots = 2;             // V ring depth
 constexpr int kWG = 2;                 // softmax warpgroups = Q tiles per item
-constexpr int kMmaWarp = 4 * kWG;      // issues the MMAs and hands out items
+constexpr int kMmaWarp = 4 * kWG;      // issues group 0's MMAs and hands out items
 constexpr int kTmaWarp = 4 * kWG + 1;  // streams K/V tiles
-constexpr int kThreads = (4 * kWG + 2) * 32;
+constexpr int kMmaWarp1 = 4 * kWG + 2; // issues group 1's MMAs
+constexpr int kThreads = (4 * kWG + 3) * 32;
 constexpr int kBarItem = 1, kBarQ = 2, kBarEpi = 3;  // named barriers (0 is __syncthreads)
-constexpr int kBarQThreads = (4 * kWG + 1) * 32;  // softmax groups + the MMA warp
+constexpr int kBarQThreads = (4 * kWG + 2) * 32;  // softmax groups + the two MMA warps
 constexpr int kSoftmaxThreads = 4 * kWG * 32;
 constexpr float kRescaleLog2 = 8.f;    // lazy rescale threshold (log2 units)
 constexpr int kKeys = kPrefillKeys;    // keys per K/V tile
@@ -94,6 +95,8 @@ struct Bars {
   uint64_t* s_done;   // [kWG]      S of the group's current tile written (and every earlier MMA done)
   uint64_t* p_ready;  // [kWG]      P written over S, O rescaled (128 arrivals)
   uint64_t* pv_done;  // [kWG]      the group's product of its current tile completed
+  uint64_t* zfill;    // [1]        the last tile's V rows past the item's keys zeroed (128 arrivals; one phase per
+                      //            entry that holds an item's partial last tile)
   uint32_t* tmem_base;
   int4* item;
   volatile int* abort;
@@ -221,47 +224,60 @@ __device__ void tma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
   }
 }
 
-// ---- MMA warp: hands out items, issues every MMA from one thread ----------------------------------
-template <int D, int G>
+// ---- MMA warps: one per Q-tile group, each issuing its group's MMAs from one thread ------------------
+// Measured on GB300: one issuing thread sustains one 128 x 128 x 16 MMA per ~113 cycles, two issuing warps
+// together one per ~64 (the tensor core's rate).  So each group's scores and products come from its own warp;
+// the K and V ring slots are released once both warps' MMAs that read them have completed (two arrivals).
+// The first MMA warp also hands out the items.
+template <int D, int G, int w>
 __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh, int lane, int n_items) {
   using T = PfTraits<D, G>;
   const uint32_t sbase = dev::smem_addr(smem);
   const uint32_t tmem = *sh.tmem_base;
-  // base descriptors (Q tile 0, K slot 0, V slot 0): the others differ only in the start-address field
-  const uint64_t dq0 = dev::umma_desc_sw128(sbase + T::OFF_Q, 16, 1024);
+  // base descriptors (this group's Q tile, K slot 0, V slot 0): the others differ only in the start address
+  const uint64_t dq = dev::umma_desc_sw128(sbase + T::OFF_Q + w * T::QTILE, 16, 1024);
   const uint64_t dk0 = dev::umma_desc_sw128(sbase + T::OFF_K, 16, 1024);
   const uint64_t dv0 = dev::umma_desc_sw128(sbase + T::OFF_V, kKeys * 128, 1024);
   int gt = 0;            // CTA-wide index of the next K/V tile
   int cw[kWG] = {0, 0};  // per Q-tile group: tiles processed so far (barrier phases)
+  int nz = 0;            // entries so far whose item's partial last tile was zero-filled (zfill phases)
   bool first = true;
   while (true) {
     int4 rec = make_int4(-1, 0, 0, 0);
-    if (lane == 0) {
-      const int idx = first ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&p.hdr->pwork, 1);
-      int slot = -1;
-      if (idx < n_items) {
-        rec = __ldg(p.items + idx);
-        slot = __ldg(p.items_slot + idx);
+    if constexpr (w == 0) {
+      if (lane == 0) {
+        const int idx = first ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&p.hdr->pwork, 1);
+        int slot = -1;
+        if (idx < n_items) {
+          rec = __ldg(p.items + idx);
+          slot = __ldg(p.items_slot + idx);
+        }
+        *sh.item = rec;
+        *sh.slot = slot;
       }
-      *sh.item = rec;
-      *sh.slot = slot;
+      first = false;
+      rec.x = __shfl_sync(0xffffffffu, rec.x, 0);
+      rec.y = __shfl_sync(0xffffffffu, rec.y, 0);
+      rec.z = __shfl_sync(0xffffffffu, rec.z, 0);
+      rec.w = __shfl_sync(0xffffffffu, rec.w, 0);
+      __syncwarp();
+      dev::named_bar_arrive(kBarItem, kThreads);
+    } else {
+      dev::named_bar_sync(kBarItem, kThreads);
+      const volatile int* vi = reinterpret_cast<volatile int*>(sh.item);
+      rec = make_int4(vi[0], vi[1], vi[2], vi[3]);
     }
-    first = false;
-    rec.x = __shfl_sync(0xffffffffu, rec.x, 0);
-    rec.y = __shfl_sync(0xffffffffu, rec.y, 0);
-    rec.z = __shfl_sync(0xffffffffu, rec.z, 0);
-    rec.w = __shfl_sync(0xffffffffu, rec.w, 0);
-    __syncwarp();
-    dev::named_bar_arrive(kBarItem, kThreads);
     if (rec.x < 0) break;
     const ItemGeo it = item_geo<T::P>(rec);
     const int n = it.te - it.tb;  // tiles of this entry; u below is the entry's tile, tb + u the item's
     int ne[kWG];                  // tiles of this entry per group
 #pragma unroll
-    for (int w = 0; w < kWG; ++w) ne[w] = max(0, min(it.te, it.n[w]) - it.tb);
+    for (int g = 0; g < kWG; ++g) ne[g] = max(0, min(it.te, it.n[g]) - it.tb);
+    const int zf = it.zfill_wg;
+    // this entry holds the item's last tile and it is partial: group zf zeroes its V rows past the keys
+    const bool zfe = it.te == it.n_all && it.kend_all - (it.n_all - 1) * kKeys < kKeys;
 
-    auto issue_s = [&](int w, int j) {  // S_w(u = j) = Q_w K^T; commits every earlier MMA too
-      const uint64_t dq = dq0 + (uint64_t)((w * T::QTILE) >> 4);
+    auto issue_s = [&](int j) {  // S_w(u = j) = Q_w K^T; commits every earlier MMA of this warp too
       const uint64_t dk = dk0 + (uint64_t)((((gt + j) % kKSlots) * T::KVTILE) >> 4);
       if (lane == 0) {
 #pragma unroll
@@ -272,7 +288,7 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
       }
       __syncwarp();
     };
-    auto issue_pv = [&](int w, int j) {  // O_w (+)= P_w(j) V(j), P from tensor memory
+    auto issue_pv = [&](int j) {  // O_w (+)= P_w(j) V(j), P from tensor memory
       const uint64_t dv = dv0 + (uint64_t)((((gt + j) % kVSlots) * T::KVTILE) >> 4);
       if (lane == 0) {
 #pragma unroll
@@ -291,35 +307,31 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
     dev::named_bar_sync(kBarQ, kBarQThreads);  // both Q tiles are in shared memory
     dev::tc_fence_after();
     pf_wait(sh, &sh.kfull[gt % kKSlots], (gt / kKSlots) & 1, p.err);
-#pragma unroll
-    for (int w = 0; w < kWG; ++w)
-      if (ne[w] > 0) issue_s(w, 0);
+    if (ne[w] > 0) issue_s(0);
     commit(&sh.kfree[gt % kKSlots]);
     for (int j = 0; j < n; ++j) {
       const int gi = gt + j;
       const bool last = j == n - 1;
       pf_wait(sh, &sh.vfull[gi % kVSlots], (gi / kVSlots) & 1, p.err);
       if (!last) pf_wait(sh, &sh.kfull[(gi + 1) % kKSlots], ((gi + 1) / kKSlots) & 1, p.err);
-      if (last) {  // one group zero-fills the last tile's V rows past the item's keys: wait for all
-#pragma unroll
-        for (int w = 0; w < kWG; ++w)
-          if (j < ne[w]) pf_wait(sh, &sh.p_ready[w], (cw[w] + j) & 1, p.err);
-      }
-      // per group: its product of tile j, then (P has been read) its scores of tile j + 1 over the same S
-#pragma unroll
-      for (int w = 0; w < kWG; ++w) {
-        if (j >= ne[w]) continue;
-        if (!last) pf_wait(sh, &sh.p_ready[w], (cw[w] + j) & 1, p.err);
+      if (j < ne[w]) {
+        pf_wait(sh, &sh.p_ready[w], (cw[w] + j) & 1, p.err);
+        // the last tile: the other group zeroes V rows past the item's keys (its own P is ready after that).  A
+        // barrier of its own, one phase per such entry, since this warp does not follow the other group tile by
+        // tile (a parity wait on its P barrier could match a phase two tiles old).
+        if (last && zfe && zf != w) pf_wait(sh, sh.zfill, nz & 1, p.err);
         dev::tc_fence_after();
-        issue_pv(w, j);
-        if (j + 1 < ne[w]) issue_s(w, j + 1);
+        // this group's product of tile j, then (P has been read) its scores of tile j + 1 over the same S
+        issue_pv(j);
+        if (j + 1 < ne[w]) issue_s(j + 1);
       }
       if (!last) commit(&sh.kfree[(gi + 1) % kKSlots]);
       commit(&sh.vfree[gi % kVSlots]);
     }
     gt += n;
 #pragma unroll
-    for (int w = 0; w < kWG; ++w) cw[w] += ne[w];
+    for (int g = 0; g < kWG; ++g) cw[g] += ne[g];
+    if (zfe) ++nz;
   }
 }
 
@@ -497,6 +509,8 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
                          "r"(0)
                          : "memory");
           }
+          dev::fence_proxy_async_smem();
+          dev::mbar_arrive(sh.zfill);  // the other group's product of this tile waits for it
         }
       }
       dev::fence_proxy_async_smem();
@@ -633,6 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   sh.s_done = sh.vfree + kVSlots;
   sh.p_ready = sh.s_done + kWG;
   sh.pv_done = sh.p_ready + kWG;
+  sh.zfill = sh.pv_done + kWG;
   sh.tmem_base = reinterpret_cast<uint32_t*>(smem + T::OFF_MISC);
   sh.item = reinterpret_cast<int4*>(smem + T::OFF_MISC + 16);
   sh.abort = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 32);
@@ -640,12 +655,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   sh.order = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 40);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2 * (kKSlots + kVSlots); ++i) dev::mbar_init(&bars[i], 1);
+    for (int i = 0; i < kKSlots; ++i) {
+      dev::mbar_init(&sh.kfull[i], 1);
+      dev::mbar_init(&sh.kfree[i], kWG);  // one commit per MMA warp
+    }
+    for (int i = 0; i < kVSlots; ++i) {
+      dev::mbar_init(&sh.vfull[i], 1);
+      dev::mbar_init(&sh.vfree[i], kWG);
+    }
     for (int w = 0; w < kWG; ++w) {
       dev::mbar_init(&sh.s_done[w], 1);
       dev::mbar_init(&sh.p_ready[w], 128);
       dev::mbar_init(&sh.pv_done[w], 1);
     }
+    dev::mbar_init(sh.zfill, 128);
     dev::fence_mbar_init();
     *sh.abort = 0;
   }
@@ -659,7 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const bool poisoned = __syncthreads_or(threadIdx.x == 0 && dev::pool_poisoned(p.err));
   dev::tc_fence_after();
   const int n_items = poisoned ? 0 : p.hdr->n_items;
-  if (warp == kMmaWarp) mma_warp<D, G>(p, smem, sh, lane, n_items);
+  if (warp == kMmaWarp) mma_warp<D, G, 0>(p, smem, sh, lane, n_items);
+  else if (warp == kMmaWarp1) mma_warp<D, G, 1>(p, smem, sh, lane, n_items);
   else if (warp == kTmaWarp) tma_warp<D, G>(p, smem, sh, lane);
   else softmax_group<D, G>(p, smem, sh, warp >> 2, warp, lane);
   dev::tc_fence_before();
