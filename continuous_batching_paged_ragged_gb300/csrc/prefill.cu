@@ -11,17 +11,18 @@
 //    head (row r = position r / G, head r % G): every K/V tile is read once for the whole group, and
 //    the causal diagonal wastes at most P keys per tile.  A work item is two adjacent Q tiles of one row
 //    and KV head; they share every 128-key K/V tile.
-//  * Persistent CTAs of 10 warps.  Warp 9 streams K and V tiles from the paged pool with 2-D TMA copies
-//    (128-byte swizzle) into rings of 3 K and 2 V slots, block ids fetched a tile ahead.  Warp 8 issues,
-//    from one thread, the MMAs S = Q K^T (M 128, N 128, K d) and O += P V (M 128, N d, K 128) of both
-//    Q tiles, fp32 accumulators in tensor memory (per Q tile: S and O, 256 columns; 512 in all).
+//  * Persistent CTAs of 11 warps.  Warp 9 streams K and V tiles from the paged pool with 2-D TMA copies
+//    (128-byte swizzle) into rings of 3 K and 2 V slots, block ids fetched a tile ahead.  Warps 8 and 10
+//    each issue, from one thread, one Q tile's MMAs S = Q K^T (M 128, N 128, K d) and O += P V (M 128,
+//    N d, K 128), fp32 accumulators in tensor memory (per Q tile: S and O, 256 columns; 512 in all).
 //    Warpgroups 0 and 1 (softmax) each own one Q tile, one S/O row per thread (TMEM lane = thread):
 //    they load S with tcgen05.ld, apply the causal mask and an online softmax in the log2 domain, and
 //    store P as fp16 over the S they just read (tcgen05.st); the product takes P straight from tensor
-//    memory.  The MMA order S_0(j), S_1(j), P_0(j)V, S_0(j+1), P_1(j)V, S_1(j+1), ... keeps the tensor
-//    core on one group's products and scores while the other group runs its softmax.
-//  * Measured on GB300: one thread issues a tcgen05.mma about every 96 cycles whatever N up to 128, so
-//    128-wide score tiles (not 64) are what lets the tensor core, not the issue, set the pace.
+//    memory.  Per group the order is S(j), P(j)V, S(j + 1), P(j + 1)V, ...: while one group runs its
+//    softmax the tensor core works on the other group's products and scores.
+//  * Measured on GB300: one thread issues a 128 x 128 x 16 tcgen05.mma about every 113 cycles whatever N up
+//    to 128, two issuing warps one every ~64 (the tensor core's rate).  Hence one issuing warp per Q tile,
+//    and 128-wide score tiles (not 64).
 //  * The running max is lazy: O (in TMEM) and the running sum are rescaled only when a row's max grows
 //    by more than 8 (a factor 256), which keeps P <= 256 and the arithmetic exact up to rounding.
 //  * Items are taken longest first (the plan sorts them by K/V tile count) from a global counter.
