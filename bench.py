@@ -51,8 +51,8 @@ CONFIGS = {
 # DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
 # source they were taken on and the cache format; reported as null once the source changes.
-TRAFFIC = {"fcacad5de686/fp16/qwen_decode": 142.52e6,   # profiles/decode_kernel_qwen_decode.md
-           "fca057a257e4/e4m3/qwen_decode": 72.05e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
+TRAFFIC = {"a3a98270e14c/fp16/qwen_decode": 142.55e6,   # profiles/decode_kernel_qwen_decode.md
+           "a3a98270e14c/e4m3/qwen_decode": 71.75e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
 
 FALLBACK_HBM_GBS = 6800.0
 
