@@ -687,12 +687,12 @@ def run_sched_trace(args, rank, world, local):
 def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_bytes, steps):
     """The same metric end to end through the public calls: every step copies the pass's metadata and every
     layer's q/k/v from pinned host memory and reads every layer's output back.  The copies run beside the
-    attention on two copy streams and the compute stream waits only twice, so consecutive layers keep their
-    programmatic-dependent-launch overlap: the first layers' inputs go up before the plan, the rest on the
-    upload stream while those layers run (the compute stream waits for them once, before the first layer that
-    needs them); the outputs come down in quarters, each while the next quarter is computed, the last one
-    after the last layer.  The step (copies, events and library calls) is captured as one CUDA graph, as the
-    device-resident timing is (--eager: issued call by call)."""
+    attention on two copy streams in chunks that double in size, so that only a layer's worth is exposed at
+    each end: layer 0's inputs go up before the plan, layers [1, 2), [2, 4), [4, 8), ... on the upload stream
+    (the compute stream waits for each chunk before its first layer, by then long landed: a layer's inputs
+    take a fraction of its attention time); the outputs come down in chunks that halve toward the end, each
+    as soon as its last layer is done, the last layer's after it.  The step (copies, events and library calls)
+    is captured as one CUDA graph, as the device-resident timing is (--eager: issued call by call)."""
     dev = stream.device
     L = len(layers)
     h_q = torch.stack([q.cpu() for q in qs]).pin_memory()
@@ -710,11 +710,9 @@ def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_
     h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_bt, h_ctx, h_qsl, h_slots))
     d2h = h_out.numel() * h_out.element_size()
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_up = torch.cuda.Event()
-    head = max(1, min(L, (L + 7) // 8))   # layers whose inputs go up before the step starts
-    # outputs come down in quarters: each quarter's copy starts, on the download stream, once its last layer
-    # is done, while the next quarter runs; only the last quarter's copy follows the last layer
-    cuts = sorted({(L * c) // 4 for c in range(1, 4)} - {0, L})
+    ups = [b for b in (1 << k for k in range(32)) if b < L]          # upload chunks start at these layers
+    ev_up = [torch.cuda.Event() for _ in ups]
+    cuts = sorted({L - (1 << k) for k in range(32) if 0 < L - (1 << k) < L})  # download chunks end here
     ev_cut = [torch.cuda.Event() for _ in cuts]
 
     def one(main, step):
@@ -723,20 +721,22 @@ def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_
             ds.context_lens.copy_(h_ctx, non_blocking=True)
             ds.query_start_loc.copy_(h_qsl, non_blocking=True)
             ds.slot_mapping.copy_(h_slots, non_blocking=True)
-            d_q[:head].copy_(h_q[:head], non_blocking=True)
-            d_k[:head].copy_(h_k[:head], non_blocking=True)
-            d_v[:head].copy_(h_v[:head], non_blocking=True)
+            d_q[:1].copy_(h_q[:1], non_blocking=True)
+            d_k[:1].copy_(h_k[:1], non_blocking=True)
+            d_v[:1].copy_(h_v[:1], non_blocking=True)
         up.wait_stream(main)      # the previous step has read its inputs
         down.wait_stream(main)
         with torch.cuda.stream(up):
-            d_q[head:].copy_(h_q[head:], non_blocking=True)
-            d_k[head:].copy_(h_k[head:], non_blocking=True)
-            d_v[head:].copy_(h_v[head:], non_blocking=True)
-            ev_up.record(up)
+            for c, lo in enumerate(ups):
+                hi = ups[c + 1] if c + 1 < len(ups) else L
+                d_q[lo:hi].copy_(h_q[lo:hi], non_blocking=True)
+                d_k[lo:hi].copy_(h_k[lo:hi], non_blocking=True)
+                d_v[lo:hi].copy_(h_v[lo:hi], non_blocking=True)
+                ev_up[c].record(up)
         step.plan()
         for i, layer in enumerate(layers):
-            if i == head:
-                main.wait_event(ev_up)
+            if i in ups:
+                main.wait_event(ev_up[ups.index(i)])
             if i in cuts:
                 c = cuts.index(i)
                 lo = cuts[c - 1] if c else 0
@@ -785,9 +785,9 @@ def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_
     ms = e0.elapsed_time(e1) / n
     return {"value": step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
-            "copies": f"inputs of the first {head} layer(s) before the step, the rest on a copy stream beside them; "
-                      "outputs in quarters on a second copy stream, each while the next quarter runs, the last "
-                      "after the last layer" + ("" if args.eager else "; the step captured as one CUDA graph")}
+            "copies": "layer 0's inputs before the step, the rest on a copy stream in chunks starting at layers "
+                      f"{ups}; outputs on a second copy stream in chunks ending at layers {cuts}, the last layer's "
+                      "after it" + ("" if args.eager else "; the step captured as one CUDA graph")}
 
 
 def main():
