@@ -179,12 +179,13 @@ def test_many_launches_on_one_plan(cuda, built):
 
 
 def test_qwen_decode_full_size_sampled(cuda, built):
-    """The benchmark's workload on an 8-bit cache through the fused call: 256 rows, sampled rows."""
+    """The benchmark's workload on an 8-bit cache through the fused call: 256 rows, every row on both layers
+    of a 2-layer pool."""
     batch = synth.qwen_decode(0)
     batch.shape = synth.Shape(2, 12, 2, 128)
     pool, ds, outs = run_batch(batch, [0, 1], kv_dtype=E4M3, fused=True)
     for layer in (0, 1):
-        for b in (0, 77, 255):
+        for b in range(batch.num_seqs):
             assert_close(row_slice(batch, outs[layer], b), oracle_row_8bit(batch, layer, b), f"layer {layer} row {b}")
 
 

@@ -66,14 +66,16 @@ def test_tiny_decode_parity(cuda, built):
 
 
 def test_qwen_decode_full_size_sampled(cuda, built):
-    """All 28 layers, 256 rows, in the benchmark's launch configuration; rows sampled per layer."""
+    """All 28 layers, 256 rows, in the benchmark's launch configuration: every row on the first and the last
+    layer, and on every other layer the shortest and longest contexts and three fixed rows."""
     batch = synth.qwen_decode(0)
     layers = list(range(28))
     pool, ds, outs = run_batch(batch, layers, poison=False)
     order = np.argsort(batch.context_lens)
     sample = sorted(set(order[:3].tolist() + order[-3:].tolist() + [17, 100, 201]))
-    for layer in (0, 13, 27):
-        for b in sample:
+    for layer in layers:
+        rows = range(batch.num_seqs) if layer in (0, 27) else sample
+        for b in rows:
             assert_close(row_slice(batch, outs[layer], b), oracle_row(batch, layer, b), f"layer {layer} row {b}")
 
 
