@@ -162,6 +162,7 @@ struct PlanParams {
   int num_seqs, num_tokens, max_ctx, split_blocks, num_kv_heads;
   int prefill_min_qlen;  // rows with at least this many new tokens become prefill items (0: none)
   int prefill_pos;       // query positions per prefill item
+  int prefill_keys;      // keys per prefill K/V tile
   int prefill_ctas;      // CTAs of the prefill tile kernel at most (the SM count)
   int32_t* tok_row;
   int32_t* tok_ctx;
@@ -191,7 +192,7 @@ __device__ __forceinline__ void for_row_items(const PlanParams& p, int b, F fn) 
   for (int qb = 0; qb * p.prefill_pos < q_len; ++qb) {
     const int npos = min(p.prefill_pos, q_len - qb * p.prefill_pos);
     const int w = ctx - q_len + qb * p.prefill_pos;
-    fn((w + npos + kPrefillKeys - 1) / kPrefillKeys, npos, q0 + qb * p.prefill_pos, w);
+    fn((w + npos + p.prefill_keys - 1) / p.prefill_keys, npos, q0 + qb * p.prefill_pos, w);
   }
 }
 
@@ -379,7 +380,7 @@ static WsLayout ws_layout(const pkv_config& c, int num_seqs, int num_tokens, int
   // the tile kernel reads fp16 K/V: on an 8-bit cache it reads the prefill rows' blocks from an fp16 shadow
   const bool prefill = prefill_supported(c.head_dim, group) && c.num_kv_heads < 256;
   w.prefill_min_qlen = prefill ? kPrefillMinQlen : 0;
-  w.prefill_pos = prefill_item_positions(group);
+  w.prefill_pos = prefill_item_positions(group, c.head_dim);
   // a prefill row has >= prefill_min_qlen tokens, every other row >= 1: at most R such rows, holding at most
   // num_tokens - (num_seqs - R) tokens
   int64_t rows = 0, toks = 0;
@@ -444,6 +445,7 @@ static cudaError_t launch_plan(pkv_pool* pool, char* ws, const WsLayout& w, cons
   p.num_kv_heads = c.num_kv_heads;
   p.prefill_min_qlen = w.prefill_min_qlen;
   p.prefill_pos = w.prefill_pos;
+  p.prefill_keys = prefill_tile_keys(c.head_dim);
   p.prefill_ctas = pool->num_sms;
   p.tok_row = reinterpret_cast<int32_t*>(ws + w.tok_row);
   p.tok_ctx = reinterpret_cast<int32_t*>(ws + w.tok_ctx);
@@ -621,7 +623,9 @@ static pkv_status launch_attention(pkv_pool* pool, int layer, const void* q, con
       dq.max_blocks = max_blocks;
       dq.num_kv_heads = c.num_kv_heads;
       dq.num_blocks = c.num_blocks;
-      e = c.head_dim == 64 ? launch_dequant<64>(dq, pool->num_sms, s) : launch_dequant<128>(dq, pool->num_sms, s);
+      e = c.head_dim == 64    ? launch_dequant<64>(dq, pool->num_sms, s)
+          : c.head_dim == 128 ? launch_dequant<128>(dq, pool->num_sms, s)
+                              : launch_dequant<256>(dq, pool->num_sms, s);
       if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
       *launches += 1;
       a.kv_map = &pool->shadow_map;

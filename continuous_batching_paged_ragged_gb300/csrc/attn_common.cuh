@@ -17,7 +17,7 @@ constexpr int kHeadsTile = 8;    // query heads per KV head handled by one decod
 // row's result does not depend on the rest of the batch.
 constexpr int kPrefillMinQlen = 16;
 constexpr int kPrefillRows = 128;  // MMA rows of a prefill Q tile: (query position, query head) pairs
-constexpr int kPrefillKeys = 128;  // keys per K/V tile
+constexpr int kPrefillKeys = 128;  // keys per K/V tile (64 at head_dim 256, prefill_tile_keys)
 constexpr int kPrefillBuckets = 1024;
 // An item whose keys span more K/V tiles than this runs as two chunks of keys (split-KV) that the
 // second chunk to finish merges, when its row alone cannot keep every CTA busy for the item's length; the
@@ -26,6 +26,9 @@ constexpr int kPrefillSplitTiles = 24;
 
 // Query positions per prefill Q tile: the G query heads of a KV head are packed into the MMA rows.
 __host__ __device__ constexpr int prefill_positions(int group) { return kPrefillRows / group; }
+// Keys per prefill K/V tile: at head_dim 256 a Q tile's output takes 256 tensor memory columns, its scores the
+// next 64 (a 128-key tile's would not fit beside them), and 64-key tiles keep the K/V rings in shared memory.
+__host__ __device__ constexpr int prefill_tile_keys(int head_dim) { return head_dim == 256 ? 64 : kPrefillKeys; }
 
 struct WsHeader {
   int32_t n_tasks;   // decode tasks of the pass
@@ -38,7 +41,7 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
-// A prefill work entry: one KV head, up to prefill_item_positions(G) consecutive query positions of one
+// A prefill work entry: one KV head, up to prefill_item_positions(G, d) consecutive query positions of one
 // row, all of its keys or one of two chunks of them.
 //   x: row (block-table row)
 //   y: KV head | positions << 8 | chunk << 20 | split << 21
@@ -72,6 +75,6 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 // Whether the tile kernel serves this head shape (otherwise every row takes the decode path).
 bool prefill_supported(int head_dim, int group);
 // Query positions per prefill item (the Q tiles of one item share their K/V tiles).
-int prefill_item_positions(int group);
+int prefill_item_positions(int group, int head_dim);
 
 }  // namespace pkv

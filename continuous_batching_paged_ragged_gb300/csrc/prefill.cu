@@ -39,35 +39,42 @@ namespace {
 
 constexpr int kKSlots = 3;             // K ring depth
 constexpr int kVSlots = 2;             // V ring depth
-constexpr int kWG = 2;                 // softmax warpgroups = Q tiles per item
-constexpr int kMmaWarp = 4 * kWG;      // issues group 0's MMAs and hands out items
-constexpr int kTmaWarp = 4 * kWG + 1;  // streams K/V tiles
-constexpr int kMmaWarp1 = 4 * kWG + 2; // issues group 1's MMAs
-constexpr int kThreads = (4 * kWG + 3) * 32;
+constexpr int kWG = 2;                 // softmax warpgroups (Q tiles per item) at most
 constexpr int kBarItem = 1, kBarQ = 2, kBarEpi = 3;  // named barriers (0 is __syncthreads)
-constexpr int kBarQThreads = (4 * kWG + 2) * 32;  // softmax groups + the two MMA warps
-constexpr int kSoftmaxThreads = 4 * kWG * 32;
 constexpr float kRescaleLog2 = 8.f;    // lazy rescale threshold (log2 units)
-constexpr int kKeys = kPrefillKeys;    // keys per K/V tile
-static_assert(kKeys == 128, "S of a tile fills 128 TMEM columns; its P (fp16) the first 64");
 
+// Per head dim: d <= 128 runs two Q tiles per item on 128-key K/V tiles (per Q tile S 128 + O 128 tensor
+// memory columns: 512 in all); d = 256 runs one Q tile on 64-key tiles (S 64 + O 256 columns), which also
+// keeps the Q tile (64 KB) and the K/V rings within shared memory.
 template <int D, int G>
 struct PfTraits {
+  static constexpr int WG = D == 256 ? 1 : 2;         // softmax warpgroups = Q tiles per item
+  static constexpr int KEYS = prefill_tile_keys(D);   // keys per K/V tile
+  static constexpr int NH = KEYS / 64;                // 64-key halves of a row of scores
+  static constexpr int MMA0 = 4 * WG;                 // issues group 0's MMAs and hands out items
+  static constexpr int TMA = 4 * WG + 1;              // streams K/V tiles
+  static constexpr int MMA1 = 4 * WG + 2;             // issues group 1's MMAs (two groups only)
+  static constexpr int THREADS = (5 * WG + 1) * 32;   // softmax groups, the TMA warp, an MMA warp per group
+  static constexpr int Q_THREADS = 5 * WG * 32;       // the Q-tile barrier: softmax groups + MMA warps
+  static constexpr int SOFTMAX_THREADS = 4 * WG * 32;
   static constexpr int DH = D / 64;                   // 64-column halves of a row (128-byte swizzle atoms)
   static constexpr int P = prefill_positions(G);      // query positions per Q tile
   static constexpr int QTILE = DH * 128 * 128;        // 128 rows x D fp16
-  static constexpr int KVTILE = DH * kKeys * 128;     // 128 keys x D fp16
-  static constexpr int OFF_Q = 0;                     // [kWG]
-  static constexpr int OFF_K = OFF_Q + kWG * QTILE;   // [kKSlots]
+  static constexpr int KVTILE = DH * KEYS * 128;      // KEYS keys x D fp16
+  static constexpr int OFF_Q = 0;                     // [WG]
+  static constexpr int OFF_K = OFF_Q + WG * QTILE;    // [kKSlots]
   static constexpr int OFF_V = OFF_K + kKSlots * KVTILE;  // [kVSlots]
   static constexpr int OFF_BAR = OFF_V + kVSlots * KVTILE;
   static constexpr int OFF_MISC = OFF_BAR + 256;      // TMEM base, item record, abort flag, slot, merge order
   static constexpr int SMEM = OFF_MISC + 64 + 1024;   // + slack to align to 1024 bytes
-  // group w: S at 256 w (128 columns; P, as fp16, overwrites its first 64), O at 256 w + 128
+  // tensor memory of group w: S (KEYS columns; P, as fp16, overwrites its first KEYS / 2), then O (D columns)
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t IDESC_S = dev::umma_idesc_f16(128, kKeys, false, false);
+  static constexpr uint32_t SO = D == 256 ? 256 : 128;  // O's first column, past S's
+  __host__ __device__ static constexpr uint32_t s_col(int w) { return 256u * (uint32_t)w; }
+  static constexpr uint32_t IDESC_S = dev::umma_idesc_f16(128, KEYS, false, false);
   static constexpr uint32_t IDESC_PV = dev::umma_idesc_f16(128, D, false, true);
-  static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(D == 64 || D == 128 || D == 256, "head_dim");
+  static_assert(WG * 256 <= (int)TMEM_COLS && SO + D <= 256u * (3 - WG), "tensor memory");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -133,8 +140,9 @@ struct ItemGeo {
   int tb, te;           // K/V tiles [tb, te) of the item that this entry processes
 };
 
-template <int P>
+template <class T>
 __device__ __forceinline__ ItemGeo item_geo(const int4 rec) {
+  constexpr int P = T::P;
   ItemGeo it;
   it.row = rec.x;
   it.g = rec.y & 0xFF;
@@ -148,9 +156,9 @@ __device__ __forceinline__ ItemGeo item_geo(const int4 rec) {
   it.zfill_wg = 0;
 #pragma unroll
   for (int w = 0; w < kWG; ++w) {
-    it.npos[w] = max(0, min(P, npos - w * P));
+    it.npos[w] = w < T::WG ? max(0, min(P, npos - w * P)) : 0;
     const int kend = it.w0 + w * P + it.npos[w];
-    it.n[w] = it.npos[w] > 0 ? (kend + kKeys - 1) / kKeys : 0;
+    it.n[w] = it.npos[w] > 0 ? (kend + T::KEYS - 1) / T::KEYS : 0;
     if (it.npos[w] > 0) {
       it.n_all = it.n[w];
       it.kend_all = kend;
@@ -167,16 +175,16 @@ __device__ __forceinline__ ItemGeo item_geo(const int4 rec) {
 template <int D, int G>
 __device__ void tma_warp(const PfParams& p, unsigned char* smem, const Bars& sh, int lane) {
   using T = PfTraits<D, G>;
-  constexpr int BPT = kKeys / kBS;  // blocks per K/V tile
+  constexpr int BPT = T::KEYS / kBS;  // blocks per K/V tile
   static_assert(BPT * T::DH <= 32, "one box per lane");
   const uint64_t pol = dev::l2_policy_evict_last();
   int gt = 0;  // CTA-wide index of the next K/V tile
   while (true) {
-    dev::named_bar_sync(kBarItem, kThreads);
+    dev::named_bar_sync(kBarItem, T::THREADS);
     const volatile int* vi = reinterpret_cast<volatile int*>(sh.item);
     const int4 rec = make_int4(vi[0], vi[1], vi[2], vi[3]);
     if (rec.x < 0) break;
-    const ItemGeo it = item_geo<T::P>(rec);
+    const ItemGeo it = item_geo<T>(rec);
     const int n = it.te - it.tb;  // tiles of this entry: item tiles tb .. te - 1
     const int nblk = (it.kend_all + kBS - 1) / kBS;
     const int32_t* bt = p.block_tables + (int64_t)it.row * p.max_blocks;
@@ -209,7 +217,7 @@ __device__ void tma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
       const int blk = lane / T::DH, h = lane % T::DH;
       const int bid = __shfl_sync(0xffffffffu, id, blk & 31);
       if (lane < nb * T::DH)
-        dev::tma_load_2d(dst + h * (kKeys * 128) + blk * 2048, &p.kv_map, h * 64,
+        dev::tma_load_2d(dst + h * (T::KEYS * 128) + blk * 2048, &p.kv_map, h * 64,
                          row0 + (bid * p.num_kv_heads + it.g) * kBS, full, pol);
     };
     // K runs one tile ahead of V: a K slot is released by the scores, earlier than a V slot by the products
@@ -238,7 +246,7 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
   // base descriptors (this group's Q tile, K slot 0, V slot 0): the others differ only in the start address
   const uint64_t dq = dev::umma_desc_sw128(sbase + T::OFF_Q + w * T::QTILE, 16, 1024);
   const uint64_t dk0 = dev::umma_desc_sw128(sbase + T::OFF_K, 16, 1024);
-  const uint64_t dv0 = dev::umma_desc_sw128(sbase + T::OFF_V, kKeys * 128, 1024);
+  const uint64_t dv0 = dev::umma_desc_sw128(sbase + T::OFF_V, T::KEYS * 128, 1024);
   int gt = 0;            // CTA-wide index of the next K/V tile
   int cw[kWG] = {0, 0};  // per Q-tile group: tiles processed so far (barrier phases)
   int nz = 0;            // entries so far whose item's partial last tile was zero-filled (zfill phases)
@@ -262,29 +270,29 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
       rec.z = __shfl_sync(0xffffffffu, rec.z, 0);
       rec.w = __shfl_sync(0xffffffffu, rec.w, 0);
       __syncwarp();
-      dev::named_bar_arrive(kBarItem, kThreads);
+      dev::named_bar_arrive(kBarItem, T::THREADS);
     } else {
-      dev::named_bar_sync(kBarItem, kThreads);
+      dev::named_bar_sync(kBarItem, T::THREADS);
       const volatile int* vi = reinterpret_cast<volatile int*>(sh.item);
       rec = make_int4(vi[0], vi[1], vi[2], vi[3]);
     }
     if (rec.x < 0) break;
-    const ItemGeo it = item_geo<T::P>(rec);
+    const ItemGeo it = item_geo<T>(rec);
     const int n = it.te - it.tb;  // tiles of this entry; u below is the entry's tile, tb + u the item's
     int ne[kWG];                  // tiles of this entry per group
 #pragma unroll
-    for (int g = 0; g < kWG; ++g) ne[g] = max(0, min(it.te, it.n[g]) - it.tb);
+    for (int g = 0; g < kWG; ++g) ne[g] = g < T::WG ? max(0, min(it.te, it.n[g]) - it.tb) : 0;
     const int zf = it.zfill_wg;
     // this entry holds the item's last tile and it is partial: group zf zeroes its V rows past the keys
-    const bool zfe = it.te == it.n_all && it.kend_all - (it.n_all - 1) * kKeys < kKeys;
+    const bool zfe = it.te == it.n_all && it.kend_all - (it.n_all - 1) * T::KEYS < T::KEYS;
 
     auto issue_s = [&](int j) {  // S_w(u = j) = Q_w K^T; commits every earlier MMA of this warp too
       const uint64_t dk = dk0 + (uint64_t)((((gt + j) % kKSlots) * T::KVTILE) >> 4);
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          dev::umma_f16_ss(tmem + 256 * w, dq + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
-                           dk + (uint64_t)(((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4), T::IDESC_S, kk > 0);
+          dev::umma_f16_ss(tmem + T::s_col(w), dq + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+                           dk + (uint64_t)(((kk >> 2) * (T::KEYS * 128) + (kk & 3) * 32) >> 4), T::IDESC_S, kk > 0);
         dev::umma_commit(&sh.s_done[w]);
       }
       __syncwarp();
@@ -293,8 +301,8 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
       const uint64_t dv = dv0 + (uint64_t)((((gt + j) % kVSlots) * T::KVTILE) >> 4);
       if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)
-          dev::umma_f16_ts(tmem + 256 * w + 128, tmem + 256 * w + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4),
+        for (int kk = 0; kk < T::KEYS / 16; ++kk)
+          dev::umma_f16_ts(tmem + T::s_col(w) + T::SO, tmem + T::s_col(w) + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4),
                            T::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
         dev::umma_commit(&sh.pv_done[w]);
       }
@@ -305,7 +313,7 @@ __device__ void mma_warp(const PfParams& p, unsigned char* smem, const Bars& sh,
       __syncwarp();
     };
 
-    dev::named_bar_sync(kBarQ, kBarQThreads);  // both Q tiles are in shared memory
+    dev::named_bar_sync(kBarQ, T::Q_THREADS);  // the Q tiles are in shared memory
     dev::tc_fence_after();
     pf_wait(sh, &sh.kfull[gt % kKSlots], (gt / kKSlots) & 1, p.err);
     if (ne[w] > 0) issue_s(0);
@@ -341,16 +349,16 @@ template <int D, int G>
 __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars& sh, int wg, int warp, int lane) {
   using T = PfTraits<D, G>;
   const int r = (warp & 3) * 32 + lane;  // this thread's tile row and TMEM lane
-  const uint32_t tl = *sh.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + 256 * wg;  // lane, group columns
+  const uint32_t tl = *sh.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + T::s_col(wg);  // lane, group columns
   const uint32_t sQa = dev::smem_addr(smem + T::OFF_Q + wg * T::QTILE);
   int cw = 0;  // tiles processed by this group so far (barrier phases)
   int gt = 0;  // K/V tiles of the CTA so far (V slot / phase of the zero-fill wait)
   while (true) {
-    dev::named_bar_sync(kBarItem, kThreads);
+    dev::named_bar_sync(kBarItem, T::THREADS);
     const volatile int* vi = reinterpret_cast<volatile int*>(sh.item);
     const int4 rec = make_int4(vi[0], vi[1], vi[2], vi[3]);
     if (rec.x < 0) break;
-    const ItemGeo it = item_geo<T::P>(rec);
+    const ItemGeo it = item_geo<T>(rec);
     const int slot = *sh.slot;
     const int n = max(0, min(it.te, wg ? it.n[1] : it.n[0]) - it.tb);  // this group's tiles of the entry
     const int pos = r / G, hq = r % G;
@@ -372,7 +380,7 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
       }
       dev::fence_proxy_async_smem();
     }
-    dev::named_bar_arrive(kBarQ, kBarQThreads);
+    dev::named_bar_arrive(kBarQ, T::Q_THREADS);
 
     float m_ref = -INFINITY, l = 0.f;
     for (int u = 0; u < n; ++u) {
@@ -380,12 +388,12 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
       // S(j) written; its commit also covers the product of tile j - 1, so O is settled
       pf_wait(sh, &sh.s_done[wg], c & 1, p.err);
       dev::tc_fence_after();
-      const int kb = j * kKeys;
+      const int kb = j * T::KEYS;
       // Whether every valid row of the warp sees the whole tile (warp-uniform): the causal mask costs a
       // compare and a select per score, so only the tiles that reach a row's diagonal take the masked code.
       // Then every key of the tile is one of the item's (the TMA wrote it), and the warp's padding rows
       // (zero q) score 0 on each.  A warp of padding rows alone keeps the mask (key 0 only).
-      const bool full = __any_sync(0xffffffffu, valid) && __all_sync(0xffffffffu, !valid || kb + kKeys - 1 <= lim);
+      const bool full = __any_sync(0xffffffffu, valid) && __all_sync(0xffffffffu, !valid || kb + T::KEYS - 1 <= lim);
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
       auto tile = [&](auto full_tag) {
         constexpr bool kFull = decltype(full_tag)::value;
@@ -429,23 +437,20 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
         // for the two-pass path when one does.
         bool done = false;
         if (u > 0) {
-          uint32_t pk0[32], pk1[32];
-          bool ok;
-          {
-            uint32_t s[2][32];
-            load_half(0, s);
-            ok = !__any_sync(0xffffffffu, half_max(s, 0) > m_ref + kRescaleLog2);
-            if (ok) half_exp(s, 0, pk0, sum4);
+          uint32_t pk[T::NH][32];
+          bool ok = true;
+#pragma unroll
+          for (int h = 0; h < T::NH; ++h) {
+            if (ok) {
+              uint32_t s[2][32];
+              load_half(h, s);
+              ok = !__any_sync(0xffffffffu, half_max(s, h) > m_ref + kRescaleLog2);
+              if (ok) half_exp(s, h, pk[h], sum4);
+            }
           }
           if (ok) {
-            uint32_t s[2][32];
-            load_half(1, s);
-            ok = !__any_sync(0xffffffffu, half_max(s, 1) > m_ref + kRescaleLog2);
-            if (ok) half_exp(s, 1, pk1, sum4);
-          }
-          if (ok) {
-            dev::tmem_st32(tl, pk0);
-            dev::tmem_st32(tl + 32, pk1);
+#pragma unroll
+            for (int h = 0; h < T::NH; ++h) dev::tmem_st32(tl + 32 * h, pk[h]);
             done = true;
           } else {
 #pragma unroll
@@ -454,13 +459,12 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
         }
         if (!done) {
           // ---- two passes: the row max first (and, past the first tile, the lazy rescale), then P ----
-          float mx;
-          {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int h = 0; h < T::NH; ++h) {
             uint32_t s[2][32];
-            load_half(0, s);
-            mx = half_max(s, 0);
-            load_half(1, s);
-            mx = fmaxf(mx, half_max(s, 1));
+            load_half(h, s);
+            mx = fmaxf(mx, half_max(s, h));
           }
           if (u == 0) {
             m_ref = mx;
@@ -471,11 +475,11 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
 #pragma unroll
               for (int k = 0; k < D / 32; ++k) {
                 uint32_t o[32];
-                dev::tmem_ld32(tl + 128 + 32 * k, o);
+                dev::tmem_ld32(tl + T::SO + 32 * k, o);
                 dev::tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                dev::tmem_st32(tl + 128 + 32 * k, o);
+                dev::tmem_st32(tl + T::SO + 32 * k, o);
               }
               if (need) {
                 l *= alpha;
@@ -486,7 +490,7 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
           // P over the first 64 columns of S: the first half's columns, already read when the second
           // half is loaded
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < T::NH; ++h) {
             uint32_t s[2][32], pk[32];
             load_half(h, s);
             half_exp(s, h, pk, sum4);
@@ -499,13 +503,13 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
       // ---- the item's last tile: V rows past its keys hold stale bytes; zero them (0 * NaN = NaN) ----
       if (wg == it.zfill_wg && j == it.n_all - 1) {
         const int kl = it.kend_all - kb;
-        if (kl < kKeys) {
+        if (kl < T::KEYS) {
           const int gi = gt + u, vs = gi % kVSlots;
           pf_wait(sh, &sh.vfull[vs], (gi / kVSlots) & 1, p.err);
           const uint32_t sv = dev::smem_addr(smem + T::OFF_V + vs * T::KVTILE);
-          for (int idx = r; idx < (kKeys - kl) * T::DH * 8; idx += 128) {
+          for (int idx = r; idx < (T::KEYS - kl) * T::DH * 8; idx += 128) {
             const int kr = kl + idx / (T::DH * 8), rest = idx % (T::DH * 8);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sv + (rest >> 3) * (kKeys * 128) + kr * 128 +
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sv + (rest >> 3) * (T::KEYS * 128) + kr * 128 +
                                                                             (rest & 7) * 16),
                          "r"(0)
                          : "memory");
@@ -543,7 +547,7 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
 #pragma unroll
         for (int k = 0; k < D / 32; ++k) {
           uint32_t o[32];
-          dev::tmem_ld32(tl + 128 + 32 * k, o);
+          dev::tmem_ld32(tl + T::SO + 32 * k, o);
           dev::tmem_wait_ld();
           float v[32];
 #pragma unroll
@@ -560,7 +564,7 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
       float* pcol = p.pf_o + ((size_t)slot * 2 + wg) * ((size_t)D * kPrefillRows) + r;
       const int2* sync = p.pf_sync + slot;
       if (threadIdx.x == 0) *sh.order = atomicAdd(const_cast<int*>(&sync->x), 1);
-      dev::named_bar_sync(kBarEpi, kSoftmaxThreads);
+      dev::named_bar_sync(kBarEpi, T::SOFTMAX_THREADS);
       const int order = *sh.order;
       const float m_own = n > 0 ? m_ref : -INFINITY, l_own = n > 0 ? l : 0.f;
       if (order == 0) {
@@ -569,13 +573,13 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
 #pragma unroll
           for (int k = 0; k < D / 32; ++k) {
             uint32_t o[32];
-            dev::tmem_ld32(tl + 128 + 32 * k, o);
+            dev::tmem_ld32(tl + T::SO + 32 * k, o);
             dev::tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) pcol[(size_t)(32 * k + e) * kPrefillRows] = __uint_as_float(o[e]);
           }
         }
-        dev::named_bar_sync(kBarEpi, kSoftmaxThreads);  // every row published
+        dev::named_bar_sync(kBarEpi, T::SOFTMAX_THREADS);  // every row published
         if (threadIdx.x == 0) {
           __threadfence();
           atomicExch(const_cast<int*>(&sync->y), 1);
@@ -593,7 +597,7 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
           }
           __threadfence();
         }
-        dev::named_bar_sync(kBarEpi, kSoftmaxThreads);
+        dev::named_bar_sync(kBarEpi, T::SOFTMAX_THREADS);
         const float2 mlo = __ldcg(p.pf_ml + prow);
         // chunk 0 first, whichever of the two this is
         const float m0 = it.chunk ? mlo.x : m_own, l0 = it.chunk ? mlo.y : l_own;
@@ -606,7 +610,7 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
         for (int k = 0; k < D / 32; ++k) {
           uint32_t o[32];
           if (n > 0) {
-            dev::tmem_ld32(tl + 128 + 32 * k, o);
+            dev::tmem_ld32(tl + T::SO + 32 * k, o);
             dev::tmem_wait_ld();
           } else {
 #pragma unroll
@@ -623,7 +627,7 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
           }
           if (valid) store_row(k, v);
         }
-        dev::named_bar_sync(kBarEpi, kSoftmaxThreads);
+        dev::named_bar_sync(kBarEpi, T::SOFTMAX_THREADS);
         if (threadIdx.x == 0) *const_cast<int2*>(sync) = make_int2(0, 0);  // ready for the next launch
       }
     }
@@ -634,7 +638,7 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PfParams p) {
+__global__ void __launch_bounds__(PfTraits<D, G>::THREADS, 1) prefill_kernel(const __grid_constant__ PfParams p) {
   using T = PfTraits<D, G>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
@@ -658,11 +662,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKSlots; ++i) {
       dev::mbar_init(&sh.kfull[i], 1);
-      dev::mbar_init(&sh.kfree[i], kWG);  // one commit per MMA warp
+      dev::mbar_init(&sh.kfree[i], T::WG);  // one commit per MMA warp
     }
     for (int i = 0; i < kVSlots; ++i) {
       dev::mbar_init(&sh.vfull[i], 1);
-      dev::mbar_init(&sh.vfree[i], kWG);
+      dev::mbar_init(&sh.vfree[i], T::WG);
     }
     for (int w = 0; w < kWG; ++w) {
       dev::mbar_init(&sh.s_done[w], 1);
@@ -683,9 +687,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const bool poisoned = __syncthreads_or(threadIdx.x == 0 && dev::pool_poisoned(p.err));
   dev::tc_fence_after();
   const int n_items = poisoned ? 0 : p.hdr->n_items;
-  if (warp == kMmaWarp) mma_warp<D, G, 0>(p, smem, sh, lane, n_items);
-  else if (warp == kMmaWarp1) mma_warp<D, G, 1>(p, smem, sh, lane, n_items);
-  else if (warp == kTmaWarp) tma_warp<D, G>(p, smem, sh, lane);
+  if (warp == T::MMA0) mma_warp<D, G, 0>(p, smem, sh, lane, n_items);
+  else if (warp == T::MMA1) mma_warp<D, G, T::WG - 1>(p, smem, sh, lane, n_items);  // only with two groups
+  else if (warp == T::TMA) tma_warp<D, G>(p, smem, sh, lane);
   else softmax_group<D, G>(p, smem, sh, warp >> 2, warp, lane);
   dev::tc_fence_before();
   __syncthreads();
@@ -714,7 +718,7 @@ cudaError_t launch_t(const PfParams& p, int num_sms, int64_t max_items, cudaStre
   int64_t grid = num_sms;  // one CTA per SM (shared memory and tensor memory bound)
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
-  return launch_pdl(prefill_kernel<D, G>, dim3((unsigned)grid), dim3(kThreads), T::SMEM, stream, p);
+  return launch_pdl(prefill_kernel<D, G>, dim3((unsigned)grid), dim3(T::THREADS), T::SMEM, stream, p);
 }
 
 template <int D>
@@ -732,10 +736,11 @@ cudaError_t launch_d(int group, const PfParams& p, int num_sms, int64_t max_item
 }  // namespace
 
 bool prefill_supported(int head_dim, int group) {
-  return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4 || group == 6 || group == 8);
+  return (head_dim == 64 || head_dim == 128 || head_dim == 256) &&
+         (group == 1 || group == 2 || group == 4 || group == 6 || group == 8);
 }
 
-int prefill_item_positions(int group) { return kWG * prefill_positions(group); }
+int prefill_item_positions(int group, int head_dim) { return (head_dim == 256 ? 1 : kWG) * prefill_positions(group); }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   PfParams p;
@@ -761,6 +766,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   switch (a.head_dim) {
     case 64: return launch_d<64>(group, p, a.num_sms, a.max_items, stream);
     case 128: return launch_d<128>(group, p, a.num_sms, a.max_items, stream);
+    case 256: return launch_d<256>(group, p, a.num_sms, a.max_items, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -189,9 +189,9 @@ def test_qwen_decode_full_size_sampled(cuda, built):
             assert_close(row_slice(batch, outs[layer], b), oracle_row_8bit(batch, layer, b), f"layer {layer} row {b}")
 
 
-# chunked-prefill rows: the tile kernel over the fp16 shadow of their blocks (head_dim 64 and 128)
+# chunked-prefill rows: the tile kernel over the fp16 shadow of their blocks (head_dim 64, 128 and 256)
 PREFILL_ROWS = [(0, 16), (0, 21), (0, 128), (0, 129), (5, 43), (127, 16), (1000, 64), (2047, 200), (16, 250)]
-PREFILL_SHAPES = [(12, 2, 128), (8, 8, 64), (8, 1, 128), (16, 4, 128), (4, 2, 64), (8, 8, 128)]
+PREFILL_SHAPES = [(12, 2, 128), (8, 8, 64), (8, 1, 128), (16, 4, 128), (4, 2, 64), (8, 8, 128), (16, 4, 256)]
 
 
 @pytest.mark.parametrize("hq,hkv,d", PREFILL_SHAPES)

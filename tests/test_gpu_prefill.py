@@ -1,4 +1,4 @@
-"""GPU parity of the chunked-prefill tile path (rows with >= 16 new tokens, head_dim 64 or 128) against the
+"""GPU parity of the chunked-prefill tile path (rows with >= 16 new tokens, head_dim 64, 128 or 256) against the
 fp64 oracle: chunks over zero, short and long cached prefixes, chunk lengths around the tile sizes
 (positions per tile = 128 / G, 128 keys per K/V tile, 16-token blocks), every supported head grouping,
 and the same rows mixed with decode rows in one pass."""
@@ -15,7 +15,8 @@ pytestmark = pytest.mark.gpu
 # (cached, q_len): chunk boundaries against P = 128 / G positions per tile and 128-key K/V tiles
 PREFILL_ROWS = [(0, 16), (0, 21), (0, 22), (0, 127), (0, 128), (0, 129), (0, 300), (5, 43), (127, 16),
                 (128, 17), (1000, 64), (2047, 200), (16, 250)]
-SHAPES = [(12, 2, 128), (8, 8, 64), (8, 1, 128), (16, 4, 128), (4, 2, 64), (8, 8, 128), (16, 16, 64)]
+SHAPES = [(12, 2, 128), (8, 8, 64), (8, 1, 128), (16, 4, 128), (4, 2, 64), (8, 8, 128), (16, 16, 64),
+          (16, 4, 256), (12, 2, 256), (8, 8, 256), (16, 2, 256)]
 
 
 @pytest.mark.parametrize("hq,hkv,d", SHAPES)
@@ -105,3 +106,16 @@ def test_prefill_8k_chunk_sampled_positions(cuda, built):
                                s.head_dim)
         ref = oracle.attention_row(q, k[: i + 1], v[: i + 1])
         assert_close(out[i : i + 1], ref, f"position {i}")
+
+
+def test_prefill_d256_long_prefix_split(cuda, built):
+    """head_dim 256 (one Q tile per item, 64-key tiles): chunks on long cached prefixes, so items span more than
+    24 tiles and run as two key chunks, mixed with decode rows; two layers reuse the merge slots."""
+    shape = synth.Shape(2, 16, 4, 256)
+    rows = [(3000, 100), (17, 1), (1500, 64), (5000, 33), (9, 40)]
+    cached, qls = zip(*rows)
+    batch = synth.custom_batch(shape, cached, qls, seed=41)
+    pool, ds, outs = run_batch(batch, [0, 1])
+    for layer in (0, 1):
+        for b in range(batch.num_seqs):
+            assert_close(row_slice(batch, outs[layer], b), oracle_row(batch, layer, b), f"layer {layer} row {b}")
