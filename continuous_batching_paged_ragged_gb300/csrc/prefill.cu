@@ -10,7 +10,8 @@
 //  * A Q tile is 128 MMA rows = P = 128 / G consecutive query positions x the G query heads of one KV
 //    head (row r = position r / G, head r % G): every K/V tile is read once for the whole group, and
 //    the causal diagonal wastes at most P keys per tile.  A work item is two adjacent Q tiles of one row
-//    and KV head; they share every 128-key K/V tile.
+//    and KV head; they share every 128-key K/V tile.  (At head_dim 256 an item is one Q tile on 64-key
+//    tiles, PfTraits below: the warps, columns and shared memory of one group.)
 //  * Persistent CTAs of 11 warps.  Warp 9 streams K and V tiles from the paged pool with 2-D TMA copies
 //    (128-byte swizzle) into rings of 3 K and 2 V slots, block ids fetched a tile ahead.  Warps 8 and 10
 //    each issue, from one thread, one Q tile's MMAs S = Q K^T (M 128, N 128, K d) and O += P V (M 128,

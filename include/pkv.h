@@ -194,7 +194,7 @@ pkv_status pkv_append(pkv_pool* pool, int32_t layer, const void* k, const void* 
  * context length, so a row gives bit-identical output alone or in any batch, in any row order.
  *
  * 8-bit cache: attention reads the dequantized values code * 2^e exactly (scales applied in fp32).  Rows
- * with 16 or more new tokens (head_dim 64 or 128) first have their blocks dequantized into an fp16 shadow
+ * with 16 or more new tokens first have their blocks dequantized into an fp16 shadow
  * inside the workspace, read by the tensor-core tile kernel; values within 3 % of the fp16 maximum saturate
  * there.  pkv_attention_workspace_bytes then includes room for min(num_blocks, R * max_blocks_per_seq)
  * shadow blocks, R the most rows of 16+ new tokens the pass can hold; prefill rows holding more blocks in
