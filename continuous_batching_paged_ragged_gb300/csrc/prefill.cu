@@ -438,20 +438,36 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
         // for the two-pass path when one does.
         bool done = false;
         if (u > 0) {
-          uint32_t pk[T::NH][32];
-          bool ok = true;
-#pragma unroll
-          for (int h = 0; h < T::NH; ++h) {
+          bool ok;
+          if constexpr (T::NH == 2) {
+            uint32_t pk0[32], pk1[32];
+            {
+              uint32_t s[2][32];
+              load_half(0, s);
+              ok = !__any_sync(0xffffffffu, half_max(s, 0) > m_ref + kRescaleLog2);
+              if (ok) half_exp(s, 0, pk0, sum4);
+            }
             if (ok) {
               uint32_t s[2][32];
-              load_half(h, s);
-              ok = !__any_sync(0xffffffffu, half_max(s, h) > m_ref + kRescaleLog2);
-              if (ok) half_exp(s, h, pk[h], sum4);
+              load_half(1, s);
+              ok = !__any_sync(0xffffffffu, half_max(s, 1) > m_ref + kRescaleLog2);
+              if (ok) half_exp(s, 1, pk1, sum4);
+            }
+            if (ok) {
+              dev::tmem_st32(tl, pk0);
+              dev::tmem_st32(tl + 32, pk1);
+            }
+          } else {  // one 64-key half
+            uint32_t pk0[32];
+            uint32_t s[2][32];
+            load_half(0, s);
+            ok = !__any_sync(0xffffffffu, half_max(s, 0) > m_ref + kRescaleLog2);
+            if (ok) {
+              half_exp(s, 0, pk0, sum4);
+              dev::tmem_st32(tl, pk0);
             }
           }
           if (ok) {
-#pragma unroll
-            for (int h = 0; h < T::NH; ++h) dev::tmem_st32(tl + 32 * h, pk[h]);
             done = true;
           } else {
 #pragma unroll
@@ -460,12 +476,15 @@ __device__ void softmax_group(const PfParams& p, unsigned char* smem, const Bars
         }
         if (!done) {
           // ---- two passes: the row max first (and, past the first tile, the lazy rescale), then P ----
-          float mx = -INFINITY;
-#pragma unroll
-          for (int h = 0; h < T::NH; ++h) {
+          float mx;
+          {
             uint32_t s[2][32];
-            load_half(h, s);
-            mx = fmaxf(mx, half_max(s, h));
+            load_half(0, s);
+            mx = half_max(s, 0);
+            if constexpr (T::NH == 2) {
+              load_half(1, s);
+              mx = fmaxf(mx, half_max(s, 1));
+            }
           }
           if (u == 0) {
             m_ref = mx;
