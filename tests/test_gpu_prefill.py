@@ -89,12 +89,22 @@ def test_prefill_split_items_many_entries_per_cta(cuda, built):
 
 def test_prefill_8k_chunk_sampled_positions(cuda, built):
     """One row whose pass is a whole 8,192-token chunk (the per-pass token budget) on an empty cache: 392 work
-    items, the longer ones split in two key ranges.  The oracle runs query by query at sampled positions (tile
-    and item boundaries, both split halves, the last position), each over its own causal prefix."""
+    entries, ~2.6 per CTA.  Every output row is written (a NaN sentinel everywhere before the pass), and the
+    oracle runs query by query at sampled positions (tile and item boundaries, the last position), each over
+    its own causal prefix."""
+    from continuous_batching_paged_ragged_gb300 import workload
     batch = synth.prefill_chunk(0)
     batch.shape = synth.Shape(1, batch.shape.num_q_heads, batch.shape.num_kv_heads, batch.shape.head_dim)
     s = batch.shape
-    pool, ds, outs = run_batch(batch, [0])
+    pool = workload.make_pool(batch)
+    workload.prefill_cache(pool, batch, [0])
+    ds = workload.upload(batch, pool)
+    qs, ks, vs = workload.step_inputs(ds, [0])
+    outs = [torch.full_like(qs[0], float("nan"))]
+    workload.run_pass(pool, ds, [0], qs, ks, vs, outs)
+    torch.cuda.synchronize()
+    assert pool.check() == 0
+    assert bool(torch.isfinite(outs[0]).all()), "some output rows were never written"
     out = row_slice(batch, outs[0], 0)
     req, ctx = int(batch.req_ids[0]), int(batch.context_lens[0])
     k, v = synth.sequence_kv(batch.seed, 0, req, ctx, s.num_kv_heads, s.head_dim)
