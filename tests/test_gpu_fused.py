@@ -56,8 +56,9 @@ def test_fused_skips_slot_minus_one(cuda, built):
     assert _same(pa.cache_view(), pb.cache_view())
 
 
-def test_fused_falls_back_when_a_prefill_row_is_possible(cuda, built):
-    shape = synth.Shape(1, 12, 2, 128)
+@pytest.mark.parametrize("hq,hkv,d", [(12, 2, 128), (16, 4, 256)])
+def test_fused_falls_back_when_a_prefill_row_is_possible(cuda, built, hq, hkv, d):
+    shape = synth.Shape(1, hq, hkv, d)
     batch = synth.custom_batch(shape, [200, 0, 50], [1, 40, 1], seed=5)
     pa, oa = _pass(batch, [0], fused=False)
     pb, ob = _pass(batch, [0], fused=True)
