@@ -61,7 +61,7 @@ struct DecodeTraits {
   static constexpr int QB = G * D * 2;             // a streaming warp's q buffer (the G heads' rows)
   // everything but the rings: q buffers, shares, staging, queue, the other barriers, flag, alignment slack
   static constexpr int REST = NW * QB + NW * OV * SHL * 4 + NW * kHeadsTile * 8 + G * D * 4 + 64 +
-                              QD * (int)sizeof(TaskEntry) + (3 * NW + 3 * QD) * 8 + 8 + 16 + 1024;
+                              QD * (int)sizeof(TaskEntry) + (3 * NW + 3 * QD + 1) * 8 + 8 + 16 + 1024;
   static constexpr int SLOT = RUN + SCL + 8;       // a ring slot with its scale record and its barrier
   static constexpr int NR_FIT = (kSmemPerSM / 2 - kSmemReservedPerCTA - REST) / (NW * SLOT);
   static constexpr int NR = RING < NR_FIT ? RING : (NR_FIT < 2 ? 2 : NR_FIT);
@@ -73,8 +73,8 @@ struct DecodeTraits {
   static constexpr int OFF_Q = OFF_MML + 64;                         // [QD] TaskEntry
   static constexpr int OFF_BAR = OFF_Q + QD * (int)sizeof(TaskEntry);
   // barriers: ring [NW][NR], share_full [NW], share_empty [NW], queue full [QD], queue empty [QD], q [NW],
-  // queue half-done [QD]
-  static constexpr int NBARS = NW * NR + 3 * NW + 3 * QD;
+  // queue half-done [QD], the combiner's partial copy
+  static constexpr int NBARS = NW * NR + 3 * NW + 3 * QD + 1;
   static constexpr int OFF_FLAG = OFF_BAR + (NBARS * 8 + 15) / 16 * 16;  // the CTA's abort flag
   static constexpr int OFF_SCL = OFF_FLAG + 16;                      // 8-bit: [NW][NR] scale records
   static constexpr int SMEM = OFF_SCL + NW * NR * SCL + 1024;        // + slack to align the rings to 1024 bytes
@@ -188,6 +188,7 @@ struct DecodeSmem {
   uint64_t* qempty;
   uint64_t* qbar;       // [NW] the q buffers' barriers
   uint64_t* qmid;       // [QD] every streaming warp has consumed half of its runs of the entry's task
+  uint64_t* pbar;       // the combiner's copy of another split's partial into stg / mml
   volatile int* abort;
   unsigned char* scl;   // 8-bit: [NW][NR] scale records, 32 bytes each
   __device__ explicit DecodeSmem(unsigned char* s) {
@@ -205,6 +206,7 @@ struct DecodeSmem {
     qempty = qfull + T::QD;
     qbar = qempty + T::QD;
     qmid = qbar + T::NW;
+    pbar = qmid + T::QD;
     abort = reinterpret_cast<volatile int*>(s + T::OFF_FLAG);
     scl = s + T::OFF_SCL;
   }
@@ -1101,16 +1103,30 @@ struct Scheduler {
 // Combiner warp: combines the streaming warps' shares of every task with log-sum-exp weights and writes a
 // one-split token's fp16 output.  A split of a multi-split token is finished one of two ways:
 //  * every other split of the token was already counted when the combiner took the task (an acquire load
-//    of the token's counter, issued as the task starts): it merges the token at once -- the other splits'
-//    partials from L2, its own from shared memory -- and resets the counter.  Under the largest-first task
-//    order this is the usual case for a token's last, small split.
+//    of the token's counter as the task starts): it merges the token at the task's end -- the other splits'
+//    partials from L2 (with one other split, loaded while the task streams), its own from shared memory --
+//    and resets the counter.  Under the largest-first task order this is the usual case for a token's last,
+//    small split.
 //  * otherwise it writes its unnormalised partial and counts it on the token's counter at once (the release
-//    waits for the partial's stores; the combiner has the slack), examines the count's result one task later
-//    (its round trip hidden), and the warp that completes the count merges the token.  Counting at once lets
-//    the count reach the token's other splits while they run, so that near the end of the launch the last
-//    split usually merges at its start, rather than a count and a merge after the last task.
+//    waits for the partial's stores; the combiner has the slack), examines the count's result when it takes
+//    the next task (or the end of the work), and the warp that completes the count merges the token there,
+//    while the next task streams.  Counting at once lets the count reach the token's other splits while they
+//    run, so that near the end of the launch the last split usually merges at its end with nothing to load.
+// Traces of a 256-row decode layer showed the last CTAs spending ~4 us after their last block on merges whose
+// loads (and a count's round trip) came after the shares; both are now off that path.
 // Nothing here stalls the streaming warps.
 // ---------------------------------------------------------------------------------------------------
+// One step of the split fold (log-sum-exp): the running (M, L) take split (m, l) in; a scales what was
+// accumulated, f the split's values.  Shared by every merge path so their bits agree.
+__device__ __forceinline__ void fold_weights(float& M, float& L, float2 ml, float& a, float& f) {
+  const float nM = fmaxf(M, ml.x);
+  a = exp2f(M - nM);
+  f = exp2f(ml.x - nM);
+  M = nM;
+  L = fmaf(ml.y, f, L * a);
+}
+__device__ __forceinline__ float fold_value(float acc, float a, float v, float f) { return fmaf(v, f, acc * a); }
+
 template <int D, int G, int KV>
 struct Combiner {
   using T = DecodeTraits<D, G, KV>;
@@ -1127,6 +1143,8 @@ struct Combiner {
   // split order, so the result does not depend on which CTA merges or how.  Split `own` (-1: none) is this
   // warp's and was never written out: its o is in the staging buffer ([G][D] fp32), its (m, l) in own_ml.
   // The others are read from L2 (.cg): they were written by other CTAs during this launch.
+  // Fold every split of token tg in split order and write its fp16 output.  Split `own` (if >= 0) is this warp's,
+  // staged in shared memory; the others come from L2.
   __device__ void merge(int tg, int nsplit, int own) {
     const size_t sb = (size_t)tg * p.max_splits;
     float M[EG], L[EG];
@@ -1180,14 +1198,12 @@ struct Combiner {
                 v = o[q][j];
               }
           }
-          const float nM = fmaxf(M[j], m.x);
-          const float a = exp2f(M[j] - nM), f = exp2f(m.x - nM);
-          M[j] = nM;
-          L[j] = L[j] * a + m.y * f;
-          acc[j].x = acc[j].x * a + v.x * f;
-          acc[j].y = acc[j].y * a + v.y * f;
-          acc[j].z = acc[j].z * a + v.z * f;
-          acc[j].w = acc[j].w * a + v.w * f;
+          float a, f;
+          fold_weights(M[j], L[j], m, a, f);
+          acc[j].x = fold_value(acc[j].x, a, v.x, f);
+          acc[j].y = fold_value(acc[j].y, a, v.y, f);
+          acc[j].z = fold_value(acc[j].z, a, v.z, f);
+          acc[j].w = fold_value(acc[j].w, a, v.w, f);
         }
         if (s != own) ++u;
       }
@@ -1208,6 +1224,45 @@ struct Combiner {
       *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.num_q_heads + (size_t)g * G) * D + 4 * e4) = v;
     }
   }
+  // A two-split token, merged at the end of its split `own`: this warp's result in registers (acc in fragment
+  // order, (M0, L0) / (M1, L1) for the lane's two heads), the other split's partial copied into the staging
+  // buffers (stg [G][D] fp32, mml [8]) while the task streamed.  The same fold as merge, element by element,
+  // in split order, so the bits do not depend on which path merged.  The fp16 result is staged over stg and
+  // written out coalesced.
+  __device__ void merge_two(int tg, int own, float (&acc)[T::OV], float M0, float L0, float M1, float L1) {
+    const bool real = (lane & 3) < T::LG;
+    if (real) {
+#pragma unroll
+      for (int r = 0; r < T::OV; ++r) {
+        int dim, head;
+        frag_coord<KV>(lane, r, dim, head);
+        if (head >= G) continue;
+        const float2 mo = (r & 1) ? make_float2(M1, L1) : make_float2(M0, L0), mp = sm.mml[head];
+        const float vo = acc[r], vp = sm.stg[head * D + dim];
+        float M = -INFINITY, L = 0.f, x = 0.f;
+        float a, f;
+        fold_weights(M, L, own == 0 ? mo : mp, a, f);
+        x = fold_value(x, a, own == 0 ? vo : vp, f);
+        fold_weights(M, L, own == 0 ? mp : mo, a, f);
+        x = fold_value(x, a, own == 0 ? vp : vo, f);
+        acc[r] = x * (1.f / L);
+      }
+    }
+    __syncwarp();  // every lane has read the partial before the fp16 result goes over it
+    if (real) {
+      __half* sh = reinterpret_cast<__half*>(sm.stg);
+#pragma unroll
+      for (int r = 0; r < T::OV; ++r) {
+        int dim, head;
+        frag_coord<KV>(lane, r, dim, head);
+        if (head < G) sh[head * D + dim] = __float2half_rn(acc[r]);
+      }
+    }
+    __syncwarp();
+    const int t = tg / p.num_kv_heads, g = tg % p.num_kv_heads;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)t * p.num_q_heads + (size_t)g * G) * D);
+    for (int c = lane; c < G * D / 8; c += 32) dst[c] = reinterpret_cast<const uint4*>(sm.stg)[c];
+  }
   // A count issued earlier (acquire-release): lane 0 holds the counter's old value.  The warp that
   // completes a token's count merges it: returns whether that is this warp.
   __device__ bool completes_count(int tg, int nsplit, int prev_lane0) {
@@ -1220,7 +1275,11 @@ struct Combiner {
 
   __device__ void run() {
     uint32_t taken = 0;               // bit w: parity of the shares taken from streaming warp w so far
-    int ct_tg = -1, ct_ns = 0, ct_prev = 0;  // count issued, result not examined yet
+    // the merge due when the next task (or the end of the work) is in hand: token pm_tg's, with this warp's split
+    // pm_own staged in shared memory (or -1), and (pm_cnt) only if the count issued for it completes the token
+    int pm_tg = -1, pm_ns = 0, pm_own = -1, ct_prev = 0;
+    bool pm_cnt = false;
+    uint32_t pcopies = 0;  // partial copies into the staging buffers so far (pbar phases)
     const int hg = lane & 3;
     const bool real = hg < T::LG;     // this lane's fragment columns hold real heads
     const int ci = (lane >> 2) * T::LG + hg;
@@ -1231,6 +1290,11 @@ struct Combiner {
       const int4 rec = e->rec;
       const int nb = e->nb, rot = e->rot;
       __syncwarp();
+      // ---- the merge left by the previous task (its count examined now): it runs while this task streams ----
+      if (pm_tg >= 0) {
+        if (!pm_cnt || completes_count(pm_tg, pm_ns, ct_prev)) merge(pm_tg, pm_ns, pm_own);
+        pm_tg = -1;
+      }
       if (rec.x < 0) break;
       if (lane == 0) dev::mbar_arrive(&sm.qempty[k % T::QD]);
       const int t = rec.x, g = rec.y & 0xFF, s = rec.y >> 8, ctx = rec.w;
@@ -1238,8 +1302,28 @@ struct Combiner {
       const int nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
       const int tg = t * p.num_kv_heads + g;
       const bool multi = nsplit > 1 && nsplit <= kFusedMergeSplits;
-      int done_lane0 = 0;  // splits of the token counted so far (its result is used after the shares)
+      int done_lane0 = 0;  // splits of the token counted so far
       if (multi && lane == 0) done_lane0 = dev::ld_acquire_gpu(p.merge_cnt + tg);
+      // Every other split already counted: this task merges the token at its end.  With one other split (the
+      // usual case: a token's last, small split, under the largest-first order) its partial is loaded now, while
+      // the task streams.
+      const bool m2 = multi && __shfl_sync(0xffffffffu, done_lane0, 0) == nsplit - 1;
+      const bool pre = m2 && nsplit == 2;
+      if (pre) {
+        __syncwarp();  // every read of the staging buffers (the merge above) precedes the copy over them
+        if (lane == 0) {
+          const size_t pidx = (size_t)tg * p.max_splits + (1 - s);
+          dev::fence_proxy_async_smem();
+          dev::fence_proxy_async_global();  // the counts' acquire precedes the copy's reads
+          dev::mbar_arrive_expect_tx(sm.pbar, G * D * 4 + kHeadsTile * 8);
+          dev::bulk_g2s_plain(sm.stg, p.part_o + pidx * kHeadsTile * D, G * D * 4, sm.pbar);
+          dev::bulk_g2s_plain(sm.mml, p.part_ml + pidx * kHeadsTile, kHeadsTile * 8, sm.pbar);
+        }
+      }
+      // an abort below must not leave the CTA with the copy in flight
+      auto bail = [&]() {
+        if (pre) dev::mbar_wait(sm.pbar, pcopies & 1);
+      };
       // ---- combine the shares in warp order (a fixed order: the result does not depend on timing) ----
       float acc[T::OV];
 #pragma unroll
@@ -1247,7 +1331,10 @@ struct Combiner {
       float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
       for (int w = 0; w < T::NW; ++w) {
         if (warp_blocks(nb, (w - rot) & 3) == 0) continue;
-        if (!cta_wait(&sm.share_full[w], (taken >> w) & 1, sm.abort, p.err)) return;
+        if (!cta_wait(&sm.share_full[w], (taken >> w) & 1, sm.abort, p.err)) {
+          bail();
+          return;
+        }
         taken ^= 1u << w;
         if (real) {
           const float2 ma = sm.sh_ml[w * kHeadsTile + 2 * hg], mb = sm.sh_ml[w * kHeadsTile + 2 * hg + 1];
@@ -1284,7 +1371,7 @@ struct Combiner {
             frag_coord<KV>(lane, r, dim, head);
             if (head < G) sh[head * D + dim] = __float2half_rn(acc[r] * ((r & 1) ? i1 : i0));
           }
-        } else {
+        } else if (!pre) {
 #pragma unroll
           for (int r = 0; r < T::OV; ++r) {
             int dim, head;
@@ -1297,17 +1384,24 @@ struct Combiner {
           }
         }
       }
-      // ---- merges due now: the token whose count this warp completed at the end of the previous task (all
-      // partials in L2), and this task's token if every other split of it was counted before it started (its
-      // own split from shared memory) ----
-      const bool m1 = ct_tg >= 0 && completes_count(ct_tg, ct_ns, ct_prev);
-      const bool m2 = multi && __shfl_sync(0xffffffffu, done_lane0, 0) == nsplit - 1;
+      // ---- this task's token, if every other split of it was counted before it started (its own split from
+      // shared memory): with two splits now (nothing left to load), otherwise when the next task is in hand ----
       if (m2 && lane == 0) p.merge_cnt[tg] = 0;  // nobody else counts this token again in this launch
       __syncwarp();
-      for (int i = (m1 ? 0 : 1); i < (m2 ? 2 : 1); ++i) {  // one call site keeps the code (and registers) small
-        merge(i == 0 ? ct_tg : tg, i == 0 ? ct_ns : nsplit, i == 0 ? -1 : s);
+      if (pre) {
+        const bool got = cta_wait(sm.pbar, pcopies & 1, sm.abort, p.err);
+        ++pcopies;
+        if (!__all_sync(0xffffffffu, got)) {
+          dev::mbar_wait(sm.pbar, (pcopies - 1) & 1);
+          return;
+        }
+        merge_two(tg, s, acc, M0, L0, M1, L1);
+      } else if (m2) {
+        pm_tg = tg;
+        pm_ns = nsplit;
+        pm_own = s;
+        pm_cnt = false;
       }
-      ct_tg = -1;
       // ---- the output, or the split's partial (unless merged above), counted at once: its count then
       // reaches the token's other splits while they run, and the one that starts (or finishes) last merges
       // with no count of its own ----
@@ -1327,14 +1421,14 @@ struct Combiner {
         if (multi) {
           __syncwarp();  // every lane's stores precede the release below
           if (lane == 0) ct_prev = dev::atom_add_acq_rel_gpu(p.merge_cnt + tg, 1);
-          ct_tg = tg;
-          ct_ns = nsplit;
+          pm_tg = tg;
+          pm_ns = nsplit;
+          pm_own = -1;
+          pm_cnt = true;
         }
       }
       __syncwarp();  // the staging buffers are free again
     }
-    // ---- flush: the last partial's count (issued with it), maybe a merge ----
-    if (ct_tg >= 0 && completes_count(ct_tg, ct_ns, ct_prev)) merge(ct_tg, ct_ns, -1);
   }
 };
 
@@ -1360,6 +1454,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     }
     for (int i = 0; i < T::NW; ++i) dev::mbar_init(&sm.qbar[i], 1);
     for (int i = 0; i < T::QD; ++i) dev::mbar_init(&sm.qmid[i], T::NW);  // the streaming warps
+    dev::mbar_init(sm.pbar, 1);
     *sm.abort = 0;
     dev::fence_mbar_init();
   }
