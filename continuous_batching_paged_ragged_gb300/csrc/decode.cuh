@@ -1047,6 +1047,17 @@ struct Scheduler {
         e->nb = nb;
         e->rot = rot;
       }
+      // Append fused: the split holding the token's own position reads its key and value rows from the
+      // inputs (and its slot) in the middle of its last block, where the load's latency is exposed; bring
+      // them into L2 now, a task or more before they are needed.
+      if (p.k_in != nullptr && rec[j].x >= 0 && nb > 0 &&
+          (rec[j].y >> 8) == ((rec[j].w + kBS - 1) / kBS - 1) / p.split_blocks) {
+        constexpr int LINES = D * 2 / 128;  // 128-byte lines of one row
+        const size_t row = ((size_t)rec[j].x * p.num_kv_heads + (rec[j].y & 0xFF)) * D;
+        if (lane < LINES) dev::prefetch_l2(p.k_in + row + lane * 64);
+        else if (lane < 2 * LINES) dev::prefetch_l2(p.v_in + row + (lane - LINES) * 64);
+        else if (lane == 2 * LINES) dev::prefetch_l2(p.slots + rec[j].x);
+      }
       ++filled;
       ended = rec[j].x < 0;
       last_nb = nb;
