@@ -1495,15 +1495,16 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     if (warp == T::NW) Combiner<D, G, KV>(p, sm, lane).run();
     else sch.run();
   }
-  // the last CTA out resets the task counter for the next launch on this plan
+  // The last CTA out resets the task counter for the next launch on this plan.  No fence on either side: a
+  // CTA's claims are atomics whose results it has used before this barrier (performed at L2 before its count
+  // below is issued), and the next launch reads the counters only after its dependency wait, which sees every
+  // write of this grid.  This sits on the critical path of every launch (the last CTA's exit).
   __syncwarp();
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
     if (atomicAdd(&p.hdr->done, 1) == (int)gridDim.x - 1) {
       p.hdr->work = 0;
       p.hdr->done = 0;
-      __threadfence();
     }
   }
   if (p.late_wait) dev::griddep_wait();  // complete only after the prefill kernel ahead of it

@@ -715,13 +715,13 @@ __global__ void __launch_bounds__(PfTraits<D, G>::THREADS, 1) prefill_kernel(con
   __syncthreads();
   dev::tc_fence_after();
   if (warp == 0) dev::tmem_dealloc(*sh.tmem_base, T::TMEM_COLS);
-  // the last CTA out resets the item counter for the next launch on this plan
+  // The last CTA out resets the item counter for the next launch on this plan.  No fence on either side (as
+  // in the decode kernel): the CTA's claims were used before the barrier above, and the next launch reads
+  // the counters only after its dependency wait, which sees every write of this grid.
   if (threadIdx.x == 0) {
-    __threadfence();
     if (atomicAdd(&p.hdr->pdone, 1) == (int)gridDim.x - 1) {
       p.hdr->pwork = 0;
       p.hdr->pdone = 0;
-      __threadfence();
     }
   }
 }
