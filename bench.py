@@ -51,8 +51,8 @@ CONFIGS = {
 # DRAM bytes per pkv_attention call measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the call's kernels) on the qwen_decode workload, keyed by the sha256 prefix of the kernel
 # source they were taken on and the cache format; reported as null once the source changes.
-TRAFFIC = {"12e66aa2477b/fp16/qwen_decode": 142.48e6,   # profiles/decode_kernel_qwen_decode.md
-           "12e66aa2477b/e4m3/qwen_decode": 71.73e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
+TRAFFIC = {"68f5e3fd9c44/fp16/qwen_decode": 142.34e6,   # profiles/decode_kernel_qwen_decode.md
+           "68f5e3fd9c44/e4m3/qwen_decode": 71.68e6}    # profiles/decode_kernel_qwen_decode_e4m3.md
 
 FALLBACK_HBM_GBS = 6800.0
 
