@@ -1316,8 +1316,8 @@ struct Combiner {
       int done_lane0 = 0;  // splits of the token counted so far
       if (multi && lane == 0) done_lane0 = dev::ld_acquire_gpu(p.merge_cnt + tg);
       // Every other split already counted: this task merges the token at its end.  With one other split (the
-      // usual case: a token's last, small split, under the largest-first order) its partial is loaded now, while
-      // the task streams.
+      // usual case: a token's last, small split, under the largest-first order) that split's partial is copied
+      // into the staging buffers now, while the task streams.
       const bool m2 = multi && __shfl_sync(0xffffffffu, done_lane0, 0) == nsplit - 1;
       const bool pre = m2 && nsplit == 2;
       if (pre) {
