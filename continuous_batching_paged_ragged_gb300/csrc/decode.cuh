@@ -1115,8 +1115,8 @@ struct Scheduler {
 // one-split token's fp16 output.  A split of a multi-split token is finished one of two ways:
 //  * every other split of the token was already counted when the combiner took the task (an acquire load
 //    of the token's counter as the task starts): it merges the token at the task's end -- the other splits'
-//    partials from L2 (with one other split, loaded while the task streams), its own from shared memory --
-//    and resets the counter.  Under the largest-first task order this is the usual case for a token's last,
+//    partials from L2 (with one other split, copied into shared memory while the task streams), its own
+//    from shared memory or registers -- and resets the counter.  Under the largest-first task order this is the usual case for a token's last,
 //    small split.
 //  * otherwise it writes its unnormalised partial and counts it on the token's counter at once (the release
 //    waits for the partial's stores; the combiner has the slack), examines the count's result when it takes
@@ -1154,8 +1154,6 @@ struct Combiner {
   // split order, so the result does not depend on which CTA merges or how.  Split `own` (-1: none) is this
   // warp's and was never written out: its o is in the staging buffer ([G][D] fp32), its (m, l) in own_ml.
   // The others are read from L2 (.cg): they were written by other CTAs during this launch.
-  // Fold every split of token tg in split order and write its fp16 output.  Split `own` (if >= 0) is this warp's,
-  // staged in shared memory; the others come from L2.
   __device__ void merge(int tg, int nsplit, int own) {
     const size_t sb = (size_t)tg * p.max_splits;
     float M[EG], L[EG];
