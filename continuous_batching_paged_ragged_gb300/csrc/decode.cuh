@@ -1152,7 +1152,7 @@ struct Combiner {
 
   // Merge the nsplit partials of token-head tg (all final) into its fp16 output with log-sum-exp weights in
   // split order, so the result does not depend on which CTA merges or how.  Split `own` (-1: none) is this
-  // warp's and was never written out: its o is in the staging buffer ([G][D] fp32), its (m, l) in own_ml.
+  // warp's and was never written out: its o is in the staging buffer stg ([G][D] fp32), its (m, l) in mml.
   // The others are read from L2 (.cg): they were written by other CTAs during this launch.
   __device__ void merge(int tg, int nsplit, int own) {
     const size_t sb = (size_t)tg * p.max_splits;
