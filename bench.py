@@ -684,6 +684,16 @@ def run_sched_trace(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def e2e_chunks(L: int):
+    """The end-to-end step's copy chunks over L layers: `ups`, the first layer of each upload chunk after layer 0
+    (chunk c is layers [ups[c], ups[c + 1]) , the last one up to L), and `cuts`, the layer before which each
+    download chunk goes down (chunk c is layers [cuts[c - 1], cuts[c]), the first from 0; the layers from the
+    last cut on go down after the step).  Uploads double in size, downloads halve toward the end."""
+    ups = [b for b in (1 << k for k in range(32)) if b < L]
+    cuts = sorted({L - (1 << k) for k in range(32) if 0 < L - (1 << k) < L})
+    return ups, cuts
+
+
 def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_bytes, steps):
     """The same metric end to end through the public calls: every step copies the pass's metadata and every
     layer's q/k/v from pinned host memory and reads every layer's output back.  The copies run beside the
@@ -710,9 +720,8 @@ def run_e2e(args, batch, pool, ds, attn, qs, ks, vs, outs, stream, layers, step_
     h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_bt, h_ctx, h_qsl, h_slots))
     d2h = h_out.numel() * h_out.element_size()
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ups = [b for b in (1 << k for k in range(32)) if b < L]          # upload chunks start at these layers
+    ups, cuts = e2e_chunks(L)
     ev_up = [torch.cuda.Event() for _ in ups]
-    cuts = sorted({L - (1 << k) for k in range(32) if 0 < L - (1 << k) < L})  # download chunks end here
     ev_cut = [torch.cuda.Event() for _ in cuts]
 
     def one(main, step):
