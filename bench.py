@@ -686,7 +686,7 @@ def run_sched_trace(args, rank, world, local):
 
 def e2e_chunks(L: int):
     """The end-to-end step's copy chunks over L layers: `ups`, the first layer of each upload chunk after layer 0
-    (chunk c is layers [ups[c], ups[c + 1]) , the last one up to L), and `cuts`, the layer before which each
+    (chunk c is layers [ups[c], ups[c + 1]), the last one up to L), and `cuts`, the layer before which each
     download chunk goes down (chunk c is layers [cuts[c - 1], cuts[c]), the first from 0; the layers from the
     last cut on go down after the step).  Uploads double in size, downloads halve toward the end."""
     ups = [b for b in (1 << k for k in range(32)) if b < L]
